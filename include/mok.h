@@ -1,0 +1,192 @@
+/*
+ * mok.h -- C ABI of the single-GPU MoE layer (GB300, sm_103a).
+ *
+ * The layer (Mixture-of-Kittens blog, "Overlapping computation and
+ * communication in MoE", the MoE(x, s) equation):
+ *
+ *   MoE(x, s) = E_shared(x) + sum_{i in topk(s)} g_i E_i(x),
+ *   E_i(x)    = W_down_i (SiLU(W_gate_i x) * (W_up_i x)),
+ *   g_i       = s_i / sum_{j in topk(s)} s_j.
+ *
+ * Notation: T tokens, D model dim, I expert intermediate dim, E routed
+ * experts, K experts per token, I_shared shared-expert intermediate dim,
+ * R = T*K routes.  A route is a (token t, slot k) pair, numbered t*K + k.
+ *
+ * Conventions for every entry point:
+ *  - All matrices are row-major and densely packed (leading dim = row width).
+ *    bf16 buffers are IEEE bfloat16 bit patterns; fp32 buffers are IEEE
+ *    binary32.  Device pointers unless stated otherwise.
+ *  - The caller owns every buffer.  The library never allocates device
+ *    memory, never frees, and never synchronises the host, except
+ *    mok_get_error(), which synchronises the given stream.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued on it in order; results are valid once the
+ *    stream reaches that point.
+ *  - Argument errors (null pointers, misalignment, unsupported sizes,
+ *    workspace too small) are detected on the host and returned at once;
+ *    nothing is enqueued then.  Errors the GPU detects (an expert index
+ *    outside [0, E), a pipeline wait that timed out) set a device status
+ *    word that mok_get_error() reads and clears.  MOK_ERR_CUDA means a launch
+ *    or CUDA runtime call failed.
+ *  - Results are bitwise deterministic: every reduction runs in a fixed
+ *    order and no floating-point atomics are used.
+ *  - Pointers must be 16-byte aligned.  Size rules: D % 256 == 0,
+ *    I % 128 == 0, I_shared % 128 == 0, 1 <= K <= min(E, 32), E <= 1024,
+ *    T*K < 2^31.
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOK_OK = 0,
+  MOK_ERR_INVALID_ARG = 1,
+  MOK_ERR_UNSUPPORTED = 2,
+  MOK_ERR_WORKSPACE = 3,
+  MOK_ERR_CUDA = 4,
+  MOK_ERR_TIMEOUT = 5,
+  MOK_ERR_BAD_ROUTE = 6
+} mok_status;
+
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_dtype;
+
+/* Operation codes for mok_workspace_bytes(). */
+typedef enum {
+  MOK_OP_PLAN = 0,
+  MOK_OP_EXPERT_FFN = 1,
+  MOK_OP_SHARED_FFN = 2,
+  MOK_OP_FWD = 3,
+  MOK_OP_BWD = 4
+} mok_op;
+
+/* Layer shape.  I_shared = 0 means no shared expert.  dtype selects the
+ * arithmetic of the routed experts (the shared expert is always BF16).
+ * chunk_rows: routed rows per dispatch chunk (0 = whole batch; else
+ * 512..32768, the overlap granularity b of the Mixture-of-Kittens paper
+ * note, "Granularity as a tunable").  producer_sms: reserved, must be 0. */
+typedef struct {
+  int32_t T, D, I, E, K, I_shared;
+  int32_t dtype;
+  int32_t chunk_rows;
+  int32_t producer_sms;
+} mok_shape;
+
+/* Weights (device, bf16 unless noted).  Routed: w_gate, w_up [E][I][D];
+ * w_down [E][D][I].  MXFP8 copies (nullable for BF16): q_* E4M3 bytes of the
+ * same shapes, sc_* E8M0 bytes, one per 32 elements along the last dim
+ * ([E][I][D/32], [E][I][D/32], [E][D][I/32]).  Shared expert: ws_gate,
+ * ws_up [I_shared][D]; ws_down [D][I_shared] (null when I_shared = 0). */
+typedef struct {
+  const void *w_gate, *w_up, *w_down;
+  const void *q_gate, *q_up, *q_down;
+  const uint8_t *sc_gate, *sc_up, *sc_down;
+  const void *ws_gate, *ws_up, *ws_down;
+} mok_weights;
+
+/* Routing and plan state saved by the forward for the backward.
+ * topk_idx int32 [T][K]; g fp32 [T][K]; counts int32 [E]; offsets int32
+ * [E+1]; table int32 [R][3]; route_dst int32 [R]. */
+typedef struct {
+  int32_t *topk_idx;
+  float *g;
+  int32_t *counts, *offsets, *table, *route_dst;
+} mok_plan_buf;
+
+/* Bytes of caller-provided device workspace `op` needs for `shape`
+ * (0 for an invalid shape).  The workspace needs 256-byte alignment. */
+size_t mok_workspace_bytes(const mok_shape *shape, int op);
+
+/* Top-K routing (blog, "Overlapping computation and communication in MoE":
+ * the router selects the top-k routed experts and their weights).
+ * s: fp32 [T][E] router weights.  Writes topk_idx int32 [T][K] (descending
+ * s, lowest expert index first among equal s) and g fp32 [T][K]
+ * (g_k = s_k / (((s_0 + s_1) + s_2) + ...), fp32 sum in k order, IEEE
+ * division).  Scores must be finite. */
+mok_status mok_route(const float *s, int32_t T, int32_t E, int32_t K,
+                     int32_t *topk_idx, float *g, void *stream);
+
+/* Device-side plan (blog, "Scheduling": the pull schedule with one source
+ * rank).  From topk_idx int32 [T][K] writes counts int32 [E] (routes per
+ * expert), offsets int32 [E+1] (exclusive scan, offsets[E] = R), table
+ * int32 [R][3] (row dst = {src_index = t*K + k, expert, dst}; an expert's
+ * routes are contiguous and in ascending t*K + k order) and route_dst int32
+ * [R] (route_dst[t*K + k] = dst).  ws: mok_workspace_bytes(MOK_OP_PLAN)
+ * bytes of scratch.  An index outside [0, E) sets MOK_ERR_BAD_ROUTE in the
+ * device status word; the outputs are then unspecified. */
+mok_status mok_plan(const int32_t *topk_idx, int32_t T, int32_t E, int32_t K,
+                    int32_t *counts, int32_t *offsets, int32_t *table,
+                    int32_t *route_dst, void *ws, size_t ws_bytes, void *stream);
+
+/* Gather (blog, "Scheduling": tokens land expert-contiguous, zero local
+ * copies).  xg[p] = x[table[p].src_index / K] for p < R; x bf16 [T][D],
+ * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives E4M3 codes [R][D] and
+ * xg_scale E8M0 bytes [R][D/32] (quantisation fused into the dispatch);
+ * xg_scale is ignored for BF16. */
+mok_status mok_dispatch(const mok_shape *shape, const void *x, const int32_t *table,
+                        void *xg, uint8_t *xg_scale, void *stream);
+
+/* Grouped expert FFN over expert-contiguous rows: expert e owns rows
+ * [offsets[e], offsets[e+1]) of xg.  a = bf16(SiLU(xg W_gate^T) * (xg W_up^T))
+ * [R][I] (written to a_out when non-null, else to the workspace), then
+ * yg = bf16(a W_down^T) [R][D].  fp32 accumulation on the tensor cores. */
+mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const void *xg,
+                          const uint8_t *xg_scale, const int32_t *offsets, void *a_out,
+                          void *yg, void *ws, size_t ws_bytes, void *stream);
+
+/* Shared expert (paper note, "The production details": kept in BF16).
+ * ys = bf16(W_sd bf16(SiLU(W_sg x) * (W_su x))) [T][D]. */
+mok_status mok_shared_ffn(const mok_shape *shape, const mok_weights *w, const void *x,
+                          void *ys, void *ws, size_t ws_bytes, void *stream);
+
+/* Combine (blog layer equation; paper note "The production details":
+ * fixed-order reduction).  out[t] = bf16(ys[t] + sum_{k=0..K-1}
+ * g[t,k] * yg[route_dst[t*K+k]]), fp32 accumulation in that order.  ys may
+ * be NULL (no shared expert); g may be NULL (all weights 1). */
+mok_status mok_combine(const mok_shape *shape, const void *yg, const void *ys, const float *g,
+                       const int32_t *route_dst, void *out, void *stream);
+
+/* Whole forward: route -> plan -> dispatch -> shared FFN -> grouped FFN ->
+ * combine.  x bf16 [T][D]; s fp32 [T][E]; out bf16 [T][D].  `saved`
+ * (nullable) receives the routing and plan for mok_moe_bwd. */
+mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void *x,
+                       const float *s, void *out, mok_plan_buf *saved, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Backward of L = <dy, MoE(x, s)> (BF16).  saved: the forward's routing and
+ * plan.  dy bf16 [T][D].  Writes dx bf16 [T][D]; dw_gate, dw_up bf16
+ * [E][I][D]; dw_down bf16 [E][D][I]; dws_* the shared expert's (ignored
+ * when I_shared = 0); ds fp32 [T][E] (zero outside the top-k);
+ * dg fp32 [T][K] (nullable) = <t, a> per route with t = W_down^T dy (paper
+ * note, "The production details": the router-gradient inner product; the
+ * down-projection output is not formed).  h and u are recomputed.  Weight
+ * gradients of experts with no routes are written as zeros. */
+mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void *x,
+                       const float *s, const mok_plan_buf *saved, const void *dy, void *dx,
+                       void *dw_gate, void *dw_up, void *dw_down, void *dws_gate,
+                       void *dws_up, void *dws_down, float *ds, float *dg, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* MXFP8 quantiser: src bf16 [rows][cols] (cols % 32 == 0) -> q E4M3 bytes
+ * [rows][cols] and scale E8M0 bytes [rows][cols/32]; per 1x32 block the
+ * scale is 2^e with e the smallest integer such that amax <= 448 * 2^e
+ * (all-zero block: byte 0), codes round to nearest even. */
+mok_status mok_quantize_mxfp8(const void *src, int64_t rows, int64_t cols, void *q,
+                              uint8_t *scale, void *stream);
+
+/* Synchronises `stream`, returns the device status word of the current
+ * device (MOK_OK, MOK_ERR_BAD_ROUTE or MOK_ERR_TIMEOUT) and clears it. */
+mok_status mok_get_error(void *stream);
+
+/* Static description of a status code. */
+const char *mok_status_string(mok_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOK_H */

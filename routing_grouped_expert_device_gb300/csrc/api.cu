@@ -1,0 +1,224 @@
+// C ABI entry points: argument checks, workspace carving and the ordered
+// launch sequence of the layer.  No entry point allocates, frees or
+// synchronises (mok_get_error excepted, see status.cu).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mok {
+
+bool shape_ok(const mok_shape* s) {
+  if (!s) return false;
+  if (s->T < 0 || s->D <= 0 || s->I <= 0 || s->E < 1 || s->E > 1024 || s->K < 1 || s->K > 32 ||
+      s->K > s->E || s->I_shared < 0)
+    return false;
+  if (s->D % 256 || s->I % 128 || s->I_shared % 128) return false;
+  if (static_cast<int64_t>(s->T) * s->K >= (int64_t(1) << 31)) return false;
+  if (s->dtype != MOK_BF16 && s->dtype != MOK_MXFP8) return false;
+  if (s->chunk_rows != 0 && (s->chunk_rows < 512 || s->chunk_rows > 32768)) return false;
+  if (s->producer_sms != 0) return false;
+  return true;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// Workspace carving: a bump allocator over the caller's buffer.
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += round_up(bytes);
+    return o;
+  }
+};
+
+struct FwdLayout {
+  size_t topk, g, counts, offsets, table, route_dst, hist, xg, xg_scale, a, yg, as, ys, total;
+};
+
+FwdLayout fwd_layout(const mok_shape& s) {
+  const size_t T = s.T, D = s.D, I = s.I, E = s.E, K = s.K, Is = s.I_shared, R = T * K;
+  Carve c;
+  FwdLayout L;
+  L.topk = c.take(R * 4);
+  L.g = c.take(R * 4);
+  L.counts = c.take(E * 4);
+  L.offsets = c.take((E + 1) * 4);
+  L.table = c.take(R * 12);
+  L.route_dst = c.take(R * 4);
+  L.hist = c.take(plan_scratch_bytes(static_cast<int64_t>(R), s.E));
+  L.xg = c.take(R * D * 2);
+  L.xg_scale = c.take(s.dtype == MOK_MXFP8 ? R * D / 32 : 0);
+  L.a = c.take(R * I * 2);
+  L.yg = c.take(R * D * 2);
+  L.as = c.take(T * Is * 2);
+  L.ys = c.take(Is ? T * D * 2 : 0);
+  L.total = c.off;
+  return L;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+}  // namespace
+}  // namespace mok
+
+using namespace mok;
+
+extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
+  if (!shape_ok(shape)) return 0;
+  const mok_shape& s = *shape;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  switch (op) {
+    case MOK_OP_PLAN: return round_up(plan_scratch_bytes(R, s.E));
+    case MOK_OP_EXPERT_FFN: return round_up(static_cast<size_t>(R) * s.I * 2);
+    case MOK_OP_SHARED_FFN: return round_up(static_cast<size_t>(s.T) * (s.I_shared ? s.I_shared : 1) * 2);
+    case MOK_OP_FWD: return fwd_layout(s).total;
+    case MOK_OP_BWD: return 0;
+  }
+  return 0;
+}
+
+extern "C" mok_status mok_dispatch(const mok_shape* shape, const void* x, const int32_t* table,
+                                   void* xg, uint8_t* xg_scale, void* stream) {
+  if (!shape_ok(shape)) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  if (R == 0) return MOK_OK;
+  if (!x || !table || !xg || !aligned16(x) || !aligned16(xg)) return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s.dtype == MOK_MXFP8) {
+    if (!xg_scale) return MOK_ERR_INVALID_ARG;
+    return launch_dispatch_mxfp8(x, table, R, s.K, s.D, xg, xg_scale, st);
+  }
+  return launch_dispatch_bf16(x, table, R, s.K, s.D, xg, nullptr, nullptr, st);
+}
+
+extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* w, const void* xg,
+                                     const uint8_t* xg_scale, const int32_t* offsets, void* a_out,
+                                     void* yg, void* ws, size_t ws_bytes, void* stream) {
+  (void)xg_scale;
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  if (R == 0) return MOK_OK;
+  if (!xg || !offsets || !yg || !w->w_gate || !w->w_up || !w->w_down) return MOK_ERR_INVALID_ARG;
+  if (!aligned16(xg) || !aligned16(yg) || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
+      !aligned16(w->w_down) || (a_out && !aligned16(a_out)))
+    return MOK_ERR_INVALID_ARG;
+  void* a = a_out;
+  if (!a) {
+    if (!ws || ws_bytes < static_cast<size_t>(R) * s.I * 2) return MOK_ERR_WORKSPACE;
+    a = ws;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mok_status r = launch_upgate(xg, R, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a, st);
+  if (r != MOK_OK) return r;
+  return launch_down(a, R, w->w_down, offsets, s.E, R, s.D, s.I, yg, st);
+}
+
+extern "C" mok_status mok_shared_ffn(const mok_shape* shape, const mok_weights* w, const void* x,
+                                     void* ys, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.I_shared == 0 || s.T == 0) return MOK_OK;
+  if (!x || !ys || !w->ws_gate || !w->ws_up || !w->ws_down || !aligned16(x) || !aligned16(ys))
+    return MOK_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < static_cast<size_t>(s.T) * s.I_shared * 2) return MOK_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mok_status r =
+      launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, ws, st);
+  if (r != MOK_OK) return r;
+  return launch_down(ws, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st);
+}
+
+extern "C" mok_status mok_combine(const mok_shape* shape, const void* yg, const void* ys,
+                                  const float* g, const int32_t* route_dst, void* out,
+                                  void* stream) {
+  if (!shape_ok(shape)) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.T == 0) return MOK_OK;
+  if (!yg || !route_dst || !out || !aligned16(yg) || !aligned16(out) || (ys && !aligned16(ys)))
+    return MOK_ERR_INVALID_ARG;
+  return launch_combine(yg, ys, g, route_dst, s.T, s.K, s.D, out,
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, const void* x,
+                                  const float* s_in, void* out, mok_plan_buf* saved, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (s.T == 0) return MOK_OK;
+  if (!x || !s_in || !out || !aligned16(x) || !aligned16(out) || !w->w_gate || !w->w_up ||
+      !w->w_down)
+    return MOK_ERR_INVALID_ARG;
+  if (s.I_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOK_ERR_INVALID_ARG;
+  const FwdLayout L = fwd_layout(s);
+  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOK_ERR_WORKSPACE;
+  mok_plan_buf pb;
+  if (saved) {
+    pb = *saved;
+    if (!pb.topk_idx || !pb.g || !pb.counts || !pb.offsets || !pb.table || !pb.route_dst)
+      return MOK_ERR_INVALID_ARG;
+  } else {
+    pb.topk_idx = at<int32_t>(ws, L.topk);
+    pb.g = at<float>(ws, L.g);
+    pb.counts = at<int32_t>(ws, L.counts);
+    pb.offsets = at<int32_t>(ws, L.offsets);
+    pb.table = at<int32_t>(ws, L.table);
+    pb.route_dst = at<int32_t>(ws, L.route_dst);
+  }
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mok_status r;
+  if ((r = launch_route(s_in, s.T, s.E, s.K, pb.topk_idx, pb.g, st)) != MOK_OK) return r;
+  if ((r = launch_plan(pb.topk_idx, R, s.E, pb.counts, pb.offsets, pb.table, pb.route_dst,
+                       at<int>(ws, L.hist), st)) != MOK_OK)
+    return r;
+  void* xg = at<void>(ws, L.xg);
+  void* a = at<void>(ws, L.a);
+  void* yg = at<void>(ws, L.yg);
+  void* ys = nullptr;
+  if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
+    return r;
+  if (s.I_shared) {
+    ys = at<void>(ws, L.ys);
+    void* as = at<void>(ws, L.as);
+    if ((r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as,
+                           st)) != MOK_OK)
+      return r;
+    if ((r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st)) != MOK_OK)
+      return r;
+  }
+  if ((r = launch_upgate(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st)) != MOK_OK)
+    return r;
+  if ((r = launch_down(a, R, w->w_down, pb.offsets, s.E, R, s.D, s.I, yg, st)) != MOK_OK) return r;
+  return launch_combine(yg, ys, pb.g, pb.route_dst, s.T, s.K, s.D, out, st);
+}
+
+extern "C" mok_status mok_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
+                                         uint8_t* scale, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 32) return MOK_ERR_INVALID_ARG;
+  if (rows == 0) return MOK_OK;
+  if (!src || !q || !scale || !aligned16(src) || !aligned16(q)) return MOK_ERR_INVALID_ARG;
+  return launch_quantize_mxfp8(src, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, const void* x,
+                                  const float* s_in, const mok_plan_buf* saved, const void* dy,
+                                  void* dx, void* dw_gate, void* dw_up, void* dw_down,
+                                  void* dws_gate, void* dws_up, void* dws_down, float* ds,
+                                  float* dg, void* ws, size_t ws_bytes, void* stream) {
+  (void)shape; (void)w; (void)x; (void)s_in; (void)saved; (void)dy; (void)dx; (void)dw_gate;
+  (void)dw_up; (void)dw_down; (void)dws_gate; (void)dws_up; (void)dws_down; (void)ds; (void)dg;
+  (void)ws; (void)ws_bytes; (void)stream;
+  return MOK_ERR_UNSUPPORTED;
+}

@@ -1,0 +1,217 @@
+// Memory-bound kernels: gather (dispatch), MXFP8 quantisation and the
+// fixed-order weighted combine.  All accesses are 16-byte vectors.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mok {
+namespace {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Gather (Mixture-of-Kittens blog, "Scheduling": rows land expert-contiguous,
+// read once, written once).  One warp per destination row; 4 vectors in
+// flight per lane.
+__global__ void __launch_bounds__(256) dispatch_bf16_kernel(const uint4* __restrict__ x,
+                                                            const int32_t* __restrict__ table,
+                                                            int64_t R, int K, int D8,
+                                                            uint4* __restrict__ xg,
+                                                            const float* __restrict__ g,
+                                                            float* __restrict__ g_route) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; p < R;
+       p += nwarps) {
+    const int src = __ldg(table + p * 3);
+    const uint4* in = x + static_cast<int64_t>(src / K) * D8;
+    uint4* out = xg + p * D8;
+    int i = lane;
+    for (; i + 96 < D8; i += 128) {
+      const uint4 a = ld_nc_v4(in + i), b = ld_nc_v4(in + i + 32), c = ld_nc_v4(in + i + 64),
+                  d = ld_nc_v4(in + i + 96);
+      out[i] = a;
+      out[i + 32] = b;
+      out[i + 64] = c;
+      out[i + 96] = d;
+    }
+    for (; i < D8; i += 32) out[i] = ld_nc_v4(in + i);
+    if (g_route && lane == 0) g_route[p] = g[src];
+  }
+}
+
+// Smallest e with amax <= 448 * 2^e for a finite amax >= 0: with
+// amax = 1.f * 2^E, 448 = 1.75 * 2^8, e = E - 8 if 1.f <= 1.75 else E - 7.
+// Zero and subnormal amax give the E8M0 minimum, -127.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  const int eb = static_cast<int>((b >> 23) & 0xFFu);
+  if (eb == 0) return -127;
+  const int e = eb - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// Quantise 32 bf16 values (4 x uint4) to E4M3 with one E8M0 scale.
+__device__ __forceinline__ void quant_block(const uint4 (&v)[4], uint4 (&q)[2], uint8_t& sc) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[i * 8 + 2 * j] = bf16lo(w[j]);
+      f[i * 8 + 2 * j + 1] = bf16hi(w[j]);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const int e = mx_exponent(amax);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+  uint32_t packed[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(f[4 * i] * inv, f[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+    packed[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  q[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  q[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  sc = static_cast<uint8_t>(e + 127);
+}
+
+// One thread per 1x32 block.  row_map == nullptr: identity rows (plain
+// quantiser); else source row = table[p].src / K (dispatch with fused
+// quantisation).
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ src,
+                                                         const int32_t* __restrict__ table, int K,
+                                                         int64_t rows, int64_t cols,
+                                                         uint4* __restrict__ q,
+                                                         uint8_t* __restrict__ scale) {
+  const int64_t nb = cols / 32;
+  const int64_t total = rows * nb;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / nb, blk = i - row * nb;
+    const int64_t srow = table ? static_cast<int64_t>(__ldg(table + row * 3) / K) : row;
+    const uint4* in = src + (srow * cols + blk * 32) / 8;
+    uint4 v[4] = {ld_nc_v4(in), ld_nc_v4(in + 1), ld_nc_v4(in + 2), ld_nc_v4(in + 3)};
+    uint4 o[2];
+    uint8_t sc;
+    quant_block(v, o, sc);
+    uint4* out = q + (row * cols + blk * 32) / 16;
+    out[0] = o[0];
+    out[1] = o[1];
+    scale[i] = sc;
+  }
+}
+
+// Fixed-order combine (paper note, "The production details": a fixed
+// reduction order makes the layer bitwise deterministic).  One CTA per token;
+// fp32 accumulation base -> k = 0 .. K-1, one rounding to bf16 at the end.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ rows,
+                                                      const uint4* __restrict__ base,
+                                                      const float* __restrict__ w,
+                                                      const int32_t* __restrict__ route_dst, int T,
+                                                      int K, int D8, uint4* __restrict__ out) {
+  __shared__ int dst[32];
+  __shared__ float wk[32];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (threadIdx.x < K) {
+      dst[threadIdx.x] = route_dst[static_cast<int64_t>(t) * K + threadIdx.x];
+      wk[threadIdx.x] = w ? w[static_cast<int64_t>(t) * K + threadIdx.x] : 1.0f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < D8; i += blockDim.x) {
+      float acc[8];
+      if (base) {
+        const uint4 b = ld_nc_v4(base + static_cast<int64_t>(t) * D8 + i);
+        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = bf16lo(bw[j]);
+          acc[2 * j + 1] = bf16hi(bw[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      }
+      for (int k = 0; k < K; ++k) {
+        const uint4 v = ld_nc_v4(rows + static_cast<int64_t>(dst[k]) * D8 + i);
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        const float gk = wk[k];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[2 * j] = __fmaf_rn(gk, bf16lo(vw[j]), acc[2 * j]);
+          acc[2 * j + 1] = __fmaf_rn(gk, bf16hi(vw[j]), acc[2 * j + 1]);
+        }
+      }
+      out[static_cast<int64_t>(t) * D8 + i] =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+    __syncthreads();
+  }
+}
+
+int grid_for(int64_t work_items, int per_block) {
+  int64_t b = (work_items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (b > cap) b = cap;
+  return b < 1 ? 1 : static_cast<int>(b);
+}
+
+}  // namespace
+
+mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, int K, int D,
+                                void* xg, const float* g, float* g_route, cudaStream_t st) {
+  if (R == 0) return MOK_OK;
+  dispatch_bf16_kernel<<<grid_for(R, 8), 256, 0, st>>>(static_cast<const uint4*>(x), table, R, K,
+                                                        D / 8, static_cast<uint4*>(xg), g, g_route);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, int64_t R, int K, int D,
+                                 void* xg_q, uint8_t* xg_scale, cudaStream_t st) {
+  if (R == 0) return MOK_OK;
+  quant_rows_kernel<<<grid_for(R * (D / 32), 256), 256, 0, st>>>(
+      static_cast<const uint4*>(x), table, K, R, D, static_cast<uint4*>(xg_q), xg_scale);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
+                                 uint8_t* scale, cudaStream_t st) {
+  if (rows == 0) return MOK_OK;
+  quant_rows_kernel<<<grid_for(rows * (cols / 32), 256), 256, 0, st>>>(
+      static_cast<const uint4*>(src), nullptr, 1, rows, cols, static_cast<uint4*>(q), scale);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_combine(const void* rows, const void* base, const float* w,
+                          const int32_t* route_dst, int T, int K, int D, void* out,
+                          cudaStream_t st) {
+  if (T == 0) return MOK_OK;
+  int blocks = T;
+  const int cap = num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  const int D8 = D / 8;
+  const int threads = D8 >= 256 ? 256 : ((D8 + 31) / 32) * 32;
+  combine_kernel<<<blocks, threads, 0, st>>>(static_cast<const uint4*>(rows),
+                                             static_cast<const uint4*>(base), w, route_dst, T, K,
+                                             D8, static_cast<uint4*>(out));
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+}  // namespace mok

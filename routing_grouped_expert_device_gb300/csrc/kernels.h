@@ -1,0 +1,48 @@
+// Host-side launchers shared between the translation units of libmok.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mok.h"
+
+namespace mok {
+
+// Routes per plan chunk (one CTA of the count / place kernels).
+constexpr int kPlanChunk = 1024;
+
+int plan_chunks(int64_t R);
+size_t plan_scratch_bytes(int64_t R, int E);
+
+mok_status launch_route(const float* s, int T, int E, int K, int32_t* topk, float* g,
+                        cudaStream_t st);
+mok_status launch_plan(const int32_t* topk, int64_t R, int E, int32_t* counts, int32_t* offsets,
+                       int32_t* table, int32_t* route_dst, int* hist, cudaStream_t st);
+
+// xg[p] = x[table[p].src / K]; when g_route is non-null also
+// g_route[p] = g[table[p].src].
+mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, int K, int D,
+                                void* xg, const float* g, float* g_route, cudaStream_t st);
+mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, int64_t R, int K, int D,
+                                 void* xg_q, uint8_t* xg_scale, cudaStream_t st);
+mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
+                                 uint8_t* scale, cudaStream_t st);
+// out[t] = bf16(base[t] + sum_k w[t,k] * rows[route_dst[t*K+k]]); base and w
+// nullable (0 and 1).
+mok_status launch_combine(const void* rows, const void* base, const float* w,
+                          const int32_t* route_dst, int T, int K, int D, void* out,
+                          cudaStream_t st);
+
+// Forward grouped GEMMs.  offsets == nullptr: one group of m_total rows.
+//  up/gate: a[rows][I] = bf16(SiLU(A W_gate^T) * (A W_up^T)), A [rows][D]
+//  down   : y[rows][D] = bf16(a W_down^T)
+mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
+                         const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
+                         cudaStream_t st);
+mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
+                       int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
+
+bool shape_ok(const mok_shape* s);
+
+}  // namespace mok

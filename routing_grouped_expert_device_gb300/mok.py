@@ -1,0 +1,206 @@
+"""ctypes binding of libmok (include/mok.h).
+
+Argument marshalling only: every function takes torch tensors (or None),
+passes their device pointers, sizes and the current CUDA stream to the C ABI,
+and raises MokError on any status other than MOK_OK.  There is no fallback:
+if libmok.so is missing the import of the library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Dict, Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmok.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "mok.h")
+
+MOK_OK, MOK_ERR_INVALID_ARG, MOK_ERR_UNSUPPORTED, MOK_ERR_WORKSPACE, MOK_ERR_CUDA, \
+    MOK_ERR_TIMEOUT, MOK_ERR_BAD_ROUTE = range(7)
+MOK_BF16, MOK_MXFP8 = 0, 1
+OP_PLAN, OP_EXPERT_FFN, OP_SHARED_FFN, OP_FWD, OP_BWD = range(5)
+
+
+class MokError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib_handle().mok_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "D", "I", "E", "K", "I_shared", "dtype", "chunk_rows", "producer_sms")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_gate", "w_up", "w_down", "q_gate", "q_up", "q_down",
+                 "sc_gate", "sc_up", "sc_down", "ws_gate", "ws_up", "ws_down")]
+
+
+class PlanBuf(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst")]
+
+
+_LIB: Optional[ctypes.CDLL] = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "mok_workspace_bytes": (_SZ, [ctypes.POINTER(Shape), ctypes.c_int]),
+    "mok_route": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
+    "mok_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
+    "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
+                                      _P, _SZ, _P]),
+    "mok_shared_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _SZ, _P]),
+    "mok_combine": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
+    "mok_moe_fwd": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P,
+                                   ctypes.POINTER(PlanBuf), _P, _SZ, _P]),
+    "mok_moe_bwd": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P,
+                                   ctypes.POINTER(PlanBuf), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                   _P, _SZ, _P]),
+    "mok_quantize_mxfp8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "mok_get_error": (ctypes.c_int, [_P]),
+    "mok_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def _lib_handle() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libmok.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def header_symbols():
+    """Every entry point declared in include/mok.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(mok_[a-z0-9_]+)\s*\(", text)))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != MOK_OK:
+        raise MokError(status, where)
+
+
+def make_shape(T, D, I, E, K, I_shared=0, dtype=MOK_BF16, chunk_rows=0, producer_sms=0) -> Shape:
+    return Shape(T, D, I, E, K, I_shared, dtype, chunk_rows, producer_sms)
+
+
+def shape_of(cfg, dtype=None, chunk_rows=0) -> Shape:
+    dt = MOK_MXFP8 if (dtype or cfg.dtype) == "mxfp8" else MOK_BF16
+    return make_shape(cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, dt, chunk_rows)
+
+
+def make_weights(t: Dict[str, object]) -> Weights:
+    w = Weights()
+    for name in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down",
+                 "q_gate", "q_up", "q_down", "sc_gate", "sc_up", "sc_down"):
+        if t.get(name) is not None:
+            setattr(w, name, _ptr(t[name]))
+    return w
+
+
+def make_plan_buf(t: Dict[str, object]) -> PlanBuf:
+    return PlanBuf(*(_ptr(t[n]) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst")))
+
+
+def workspace_bytes(shape: Shape, op: int) -> int:
+    return int(_lib_handle().mok_workspace_bytes(ctypes.byref(shape), op))
+
+
+def route(s, K, topk_idx, g, stream=None):
+    T, E = s.shape
+    _check(_lib_handle().mok_route(_ptr(s), T, E, K, _ptr(topk_idx), _ptr(g), _stream(stream)), "mok_route")
+
+
+def plan(topk_idx, E, counts, offsets, table, route_dst, ws, stream=None):
+    T, K = topk_idx.shape
+    _check(_lib_handle().mok_plan(_ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets), _ptr(table),
+                                  _ptr(route_dst), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "mok_plan")
+
+
+def dispatch(shape: Shape, x, table, xg, xg_scale=None, stream=None):
+    _check(_lib_handle().mok_dispatch(ctypes.byref(shape), _ptr(x), _ptr(table), _ptr(xg), _ptr(xg_scale),
+                                      _stream(stream)), "mok_dispatch")
+
+
+def expert_ffn(shape: Shape, weights: Weights, xg, offsets, yg, a_out=None, ws=None, xg_scale=None, stream=None):
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(_lib_handle().mok_expert_ffn(ctypes.byref(shape), ctypes.byref(weights), _ptr(xg), _ptr(xg_scale),
+                                        _ptr(offsets), _ptr(a_out), _ptr(yg), _ptr(ws), nbytes,
+                                        _stream(stream)), "mok_expert_ffn")
+
+
+def shared_ffn(shape: Shape, weights: Weights, x, ys, ws, stream=None):
+    _check(_lib_handle().mok_shared_ffn(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(ys), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)), "mok_shared_ffn")
+
+
+def combine(shape: Shape, yg, ys, g, route_dst, out, stream=None):
+    _check(_lib_handle().mok_combine(ctypes.byref(shape), _ptr(yg), _ptr(ys), _ptr(g), _ptr(route_dst),
+                                     _ptr(out), _stream(stream)), "mok_combine")
+
+
+def moe_fwd(shape: Shape, weights: Weights, x, s, out, ws, saved: Optional[PlanBuf] = None, stream=None):
+    _check(_lib_handle().mok_moe_fwd(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(s), _ptr(out),
+                                     ctypes.byref(saved) if saved is not None else None, _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)), "mok_moe_fwd")
+
+
+def moe_bwd(shape: Shape, weights: Weights, x, s, saved: PlanBuf, dy, dx, dw_gate, dw_up, dw_down,
+            dws_gate, dws_up, dws_down, ds, dg, ws, stream=None):
+    _check(_lib_handle().mok_moe_bwd(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(s),
+                                     ctypes.byref(saved), _ptr(dy), _ptr(dx), _ptr(dw_gate), _ptr(dw_up),
+                                     _ptr(dw_down), _ptr(dws_gate), _ptr(dws_up), _ptr(dws_down), _ptr(ds),
+                                     _ptr(dg), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "mok_moe_bwd")
+
+
+def quantize_mxfp8(src, q, scale, stream=None):
+    rows, cols = src.shape
+    _check(_lib_handle().mok_quantize_mxfp8(_ptr(src), rows, cols, _ptr(q), _ptr(scale), _stream(stream)),
+           "mok_quantize_mxfp8")
+
+
+def get_error(stream=None) -> int:
+    return int(_lib_handle().mok_get_error(_stream(stream)))
+
+
+def check_device_status(stream=None):
+    st = get_error(stream)
+    _check(st, "device status")
+
+
+def status_string(status: int) -> str:
+    return _lib_handle().mok_status_string(status).decode()

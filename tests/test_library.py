@@ -1,0 +1,47 @@
+"""Host-side checks of libmok.so: it builds for sm_103a, loads without a GPU,
+exports every entry point include/mok.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+
+import pytest
+
+from helpers import mok
+
+
+@pytest.fixture(scope="module")
+def m():
+    return mok()
+
+
+def test_exports_every_header_symbol(m):
+    lib = ctypes.CDLL(m.LIB_PATH)
+    syms = m.header_symbols()
+    assert len(syms) >= 12
+    for name in syms:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(m):
+    for st in range(7):
+        assert m.status_string(st)
+
+
+def test_workspace_bytes_host_only(m):
+    good = m.make_shape(T=7168, D=7168, I=2048, E=256, K=8, I_shared=2048)
+    fwd = m.workspace_bytes(good, m.OP_FWD)
+    R = 7168 * 8
+    assert fwd >= R * 7168 * 2 * 2 + R * 2048 * 2
+    assert m.workspace_bytes(good, m.OP_PLAN) > 0
+    assert m.workspace_bytes(m.make_shape(T=16, D=200, I=128, E=8, K=2), m.OP_FWD) == 0
+    assert m.workspace_bytes(m.make_shape(T=16, D=256, I=128, E=8, K=9), m.OP_FWD) == 0
+
+
+def test_bad_arguments_rejected_on_host(m):
+    lib = m._lib_handle()
+    assert lib.mok_route(None, 16, 8, 9, None, None, None) == m.MOK_ERR_INVALID_ARG
+    assert lib.mok_route(None, 16, 8, 2, None, None, None) == m.MOK_ERR_INVALID_ARG
+    assert lib.mok_plan(None, 16, 8, 2, None, None, None, None, None, 0, None) == m.MOK_ERR_INVALID_ARG
+    sh = m.make_shape(T=16, D=256, I=128, E=8, K=2)
+    assert lib.mok_moe_fwd(ctypes.byref(sh), ctypes.byref(m.Weights()), None, None, None, None, None, 0,
+                           None) == m.MOK_ERR_INVALID_ARG
+    assert lib.mok_quantize_mxfp8(None, 4, 33, None, None, None) == m.MOK_ERR_INVALID_ARG

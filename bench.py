@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Throughput of the single-GPU MoE layer (tokens/s, TFLOP/s, % of peak).
+
+One step = one forward pass of the whole layer over one batch of synthetic
+tokens: route -> plan -> dispatch -> shared expert -> grouped up/gate +
+SwiGLU -> grouped down -> combine, every kernel launched through the C ABI of
+libmok.so on the current stream (the same kernels, in the same order, as one
+mok_moe_fwd call).  The default workload is the DSV3-shaped BF16 forward
+(T 7168, D 7168, I 2048, 256 experts top-8 + one shared expert, I 2048).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config NAME]
+
+N > 1 runs under torch.distributed (one process per GPU, NCCL barrier and a
+MAX reduction of the timed region): independent replicas, each on its own
+tokens, no collective on the data path ("scaling": "weak").
+
+--impl reference times the CPU oracle (oracle/, numpy) on the host cores on
+a bounded sample of the same workload and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from routing_grouped_expert_device_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE layer fwd/bwd tokens/s and TFLOP/s (% dense tensor peak), 1×GB300"
+KERNEL_SOURCES = ["common.cuh", "gemm_core.cuh", "gemm_fwd.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "upgate_gemm_dsv3_bf16_fwd_traffic.txt")
+
+
+# ---------------------------------------------------------------------------
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=30)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="dsv3_bf16_fwd")
+    p.add_argument("--cpu-sample-tokens", type=int, default=4)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "routing_grouped_expert_device_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(cfg_name: str):
+    """DRAM bytes per launch of the up/gate kernel from the committed ncu
+    summary, if it was taken on the current kernel source and workload."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != source_hash() or kv.get("workload") != cfg_name:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------------------
+def oracle_tokens_per_s(cfg, d, n_tokens: int, first: int = 0):
+    """Time the CPU oracle on n_tokens tokens of the workload (host cores).
+
+    The timed work is what the oracle does per token as it stands: top-k
+    routing of the token, then for each selected expert and the shared expert
+    the bf16 -> fp32 conversion of the weights and the SwiGLU FFN, then the
+    combine.  The expert weights are copied to host memory beforehand."""
+    import oracle as O
+    s_host = d["s"].cpu().numpy()
+    toks = [(first + 997 * i) % cfg.T for i in range(n_tokens)]
+    idx, _, _ = O.route(s_host[toks], cfg.K)
+    need = sorted(set(int(e) for e in idx.reshape(-1)))
+    cache = {e: (W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e])) for e in need}
+    shared = None
+    if cfg.I_shared:
+        shared = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
+    weights = O.HostWeights(lambda e: cache[e], shared)
+    x_rows = W.bf16_bits(d["x"][toks])
+    t0 = time.perf_counter()
+    O.moe_forward_tokens(toks, x_rows, s_host[toks], weights, cfg.K)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from routing_grouped_expert_device_gb300 import mok as M
+    M._lib_handle()
+    cfg = W.CONFIGS[args.config]
+    if cfg.backward or cfg.dtype != "bf16":
+        raise SystemExit(f"config {cfg.name}: bench covers the BF16 forward workloads")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = W.make_inputs(cfg, dev, seed=rank)
+    T, D, I, E, K, Is, R = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, cfg.R
+    shape = M.shape_of(cfg)
+    w = M.make_weights(d)
+    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+    topk = torch.empty(T, K, dtype=i32, device=dev)
+    g = torch.empty(T, K, dtype=f32, device=dev)
+    counts = torch.empty(E, dtype=i32, device=dev)
+    offsets = torch.empty(E + 1, dtype=i32, device=dev)
+    table = torch.empty(R, 3, dtype=i32, device=dev)
+    route_dst = torch.empty(R, dtype=i32, device=dev)
+    pws = torch.empty(M.workspace_bytes(shape, M.OP_PLAN), dtype=torch.uint8, device=dev)
+    xg = torch.empty(R, D, dtype=bf, device=dev)
+    a = torch.empty(R, I, dtype=bf, device=dev)
+    yg = torch.empty(R, D, dtype=bf, device=dev)
+    ys = torch.empty(T, D, dtype=bf, device=dev) if Is else None
+    sws = torch.empty(M.workspace_bytes(shape, M.OP_SHARED_FFN), dtype=torch.uint8, device=dev)
+    out = torch.empty(T, D, dtype=bf, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 1 + 3 + 1 + (2 if Is else 0) + 1 + 1 + 1
+
+    def step(ev0=None, ev1=None):
+        M.route(d["s"], K, topk, g)
+        M.plan(topk, E, counts, offsets, table, route_dst, pws)
+        M.dispatch(shape, d["x"], table, xg)
+        if Is:
+            M.shared_ffn(shape, w, d["x"], ys, sws)
+        if ev0 is not None:
+            ev0.record(stream)
+        M.expert_upgate(shape, w, xg, offsets, a)
+        if ev1 is not None:
+            ev1.record(stream)
+        M.expert_down(shape, w, a, offsets, yg)
+        M.combine(shape, yg, ys, g, route_dst, out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    M.check_device_status()
+    nonempty = int((counts > 0).sum().item())
+
+    K_steps = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K_steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start.record(stream)
+    for i in range(K_steps):
+        step(*evs[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    M.check_device_status()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world)
+    upgate_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    ms_step = total_ms / K_steps
+    value = world * T * K_steps / (total_ms / 1e3)
+    flops = cfg.fwd_flops()
+    tflops = flops / (ms_step / 1e3) / 1e12
+    peaks = measured_peaks()
+
+    # roofline of the dominant kernel: grouped up/gate + SwiGLU (HBM-bound:
+    # each expert's W_gate/W_up tile is read once per 128..256 routed rows)
+    w_bytes = nonempty * 2 * I * D * 2
+    alg_bytes = w_bytes + R * D * 2 + R * I * 2
+    achieved = alg_bytes / (upgate_ms / 1e3) / 1e9
+    traffic = recorded_traffic(cfg.name)
+    roofline = {"kernel": "grouped up/gate + SwiGLU GEMM (tcgen05)", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "algorithmic_bytes": alg_bytes, "avg_launch_ms": round(upgate_ms, 4),
+                "peak_source": peaks["source"],
+                "tflops": round(6 * R * D * I * 2 / 3 / (upgate_ms / 1e3) / 1e12, 1)}
+
+    # end to end through mok_moe_fwd with host buffers (pinned), copies timed
+    x_h = d["x"].cpu().pin_memory()
+    s_h = d["s"].cpu().pin_memory()
+    out_h = torch.empty(T, D, dtype=bf, pin_memory=True)
+    ws = torch.empty(M.workspace_bytes(shape, M.OP_FWD), dtype=torch.uint8, device=dev)
+    x_d = torch.empty_like(d["x"])
+    s_d = torch.empty_like(d["s"])
+    e2e_steps = max(3, min(K_steps, 100))
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        s_d.copy_(s_h, non_blocking=True)
+        M.moe_fwd(shape, w, x_d, s_d, out, ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    M.check_device_status()
+    e2e = {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * D * 2 + T * E * 4, "d2h_bytes_per_step": T * D * 2,
+           "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, dt = oracle_tokens_per_s(cfg, d, args.cpu_sample_tokens)
+        cpu = {"value": round(tps, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{args.cpu_sample_tokens} tokens of {cfg.name} (route, {K} routed + shared "
+                         f"SwiGLU experts incl. bf16->fp32 weight conversion, combine), {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), logits~N(0,1) softmax; bf16)",
+            "config": {"workload": cfg.name, "T": T, "D": D, "I": I, "E": E, "K": K, "I_shared": Is,
+                       "global_batch": world * T, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: every step streams all expert weights "
+                             f"({(nonempty * 3 * I * D + 3 * Is * D) * 2 / 1e9:.1f} GB)"},
+            "tflops": round(tflops, 1), "tensor_frac": round(tflops / peaks["bf16"], 4),
+            "tensor_peak": peaks["bf16"], "tensor_peak_source": peaks["source"] + " burst bf16",
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_step * K_steps, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, world, rank, local):
+    """The CPU oracle as the reference arm.  Each step is one of the K + 1
+    expert FFN evaluations of one token (its top-k routing, the bf16 -> fp32
+    conversion of that expert's weights, the SwiGLU FFN), cycling over the
+    token's routed experts and the shared expert, so a step counts as
+    1 / (K + 1) token.  Only rank 0 works; other ranks exit."""
+    if rank != 0:
+        return
+    import oracle as O
+    cfg = W.CONFIGS[args.config]
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    d = W.make_inputs(cfg, dev, seed=0)
+    s_host = d["s"].cpu().numpy()
+    parts = cfg.K + (1 if cfg.I_shared else 0)
+
+    def one(i):
+        t = (997 * (i // parts)) % cfg.T
+        j = i % parts
+        x_row = W.bf16_bits(d["x"][t:t + 1])
+        idx, _, _ = O.route(s_host[t:t + 1], cfg.K)
+        if j < cfg.K:
+            e = int(idx[0, j])
+            wts = (W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e]))
+        else:
+            wts = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
+        t0 = time.perf_counter()
+        O.route(s_host[t:t + 1], cfg.K)
+        O.expert_ffn_rows(x_row, *wts)
+        return time.perf_counter() - t0
+
+    for i in range(args.warmup):
+        one(i)
+    total = sum(one(args.warmup + i) for i in range(args.steps))
+    tokens = args.steps / parts
+    value = tokens / total
+    line = {
+        "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)", "config": {"workload": cfg.name, "T": cfg.T, "D": cfg.D, "I": cfg.I,
+                                                 "E": cfg.E, "K": cfg.K, "I_shared": cfg.I_shared},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"one of the {parts} expert FFNs of one {cfg.name} token per step"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank, local)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -139,6 +139,17 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
                           const uint8_t *xg_scale, const int32_t *offsets, void *a_out,
                           void *yg, void *ws, size_t ws_bytes, void *stream);
 
+/* The two halves of mok_expert_ffn, for callers that schedule them apart.
+ * mok_expert_upgate: a = bf16(SiLU(xg W_gate^T) * (xg W_up^T)) [R][I].
+ * mok_expert_down: yg = bf16(a W_down^T) [R][D].  Same rules as
+ * mok_expert_ffn; xg_scale / a_scale are reserved for MXFP8 (NULL). */
+mok_status mok_expert_upgate(const mok_shape *shape, const mok_weights *w, const void *xg,
+                             const uint8_t *xg_scale, const int32_t *offsets, void *a,
+                             void *stream);
+mok_status mok_expert_down(const mok_shape *shape, const mok_weights *w, const void *a,
+                           const uint8_t *a_scale, const int32_t *offsets, void *yg,
+                           void *stream);
+
 /* Shared expert (paper note, "The production details": kept in BF16).
  * ys = bf16(W_sd bf16(SiLU(W_sg x) * (W_su x))) [T][D]. */
 mok_status mok_shared_ffn(const mok_shape *shape, const mok_weights *w, const void *x,

@@ -123,6 +123,38 @@ extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* 
   return launch_down(a, R, w->w_down, offsets, s.E, R, s.D, s.I, yg, st);
 }
 
+extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weights* w,
+                                        const void* xg, const uint8_t* xg_scale,
+                                        const int32_t* offsets, void* a, void* stream) {
+  (void)xg_scale;
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  if (R == 0) return MOK_OK;
+  if (!xg || !offsets || !a || !w->w_gate || !w->w_up || !aligned16(xg) || !aligned16(a) ||
+      !aligned16(w->w_gate) || !aligned16(w->w_up))
+    return MOK_ERR_INVALID_ARG;
+  return launch_upgate(xg, R, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a,
+                       static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mok_status mok_expert_down(const mok_shape* shape, const mok_weights* w, const void* a,
+                                      const uint8_t* a_scale, const int32_t* offsets, void* yg,
+                                      void* stream) {
+  (void)a_scale;
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  if (R == 0) return MOK_OK;
+  if (!a || !offsets || !yg || !w->w_down || !aligned16(a) || !aligned16(yg) ||
+      !aligned16(w->w_down))
+    return MOK_ERR_INVALID_ARG;
+  return launch_down(a, R, w->w_down, offsets, s.E, R, s.D, s.I, yg,
+                     static_cast<cudaStream_t>(stream));
+}
+
 extern "C" mok_status mok_shared_ffn(const mok_shape* shape, const mok_weights* w, const void* x,
                                      void* ys, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;

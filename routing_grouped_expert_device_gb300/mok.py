@@ -57,6 +57,8 @@ _SIGS = {
     "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
+    "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P]),
+    "mok_expert_down": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P]),
     "mok_shared_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _SZ, _P]),
     "mok_combine": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
     "mok_moe_fwd": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P,
@@ -160,6 +162,16 @@ def expert_ffn(shape: Shape, weights: Weights, xg, offsets, yg, a_out=None, ws=N
     _check(_lib_handle().mok_expert_ffn(ctypes.byref(shape), ctypes.byref(weights), _ptr(xg), _ptr(xg_scale),
                                         _ptr(offsets), _ptr(a_out), _ptr(yg), _ptr(ws), nbytes,
                                         _stream(stream)), "mok_expert_ffn")
+
+
+def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None, stream=None):
+    _check(_lib_handle().mok_expert_upgate(ctypes.byref(shape), ctypes.byref(weights), _ptr(xg), _ptr(xg_scale),
+                                           _ptr(offsets), _ptr(a), _stream(stream)), "mok_expert_upgate")
+
+
+def expert_down(shape: Shape, weights: Weights, a, offsets, yg, a_scale=None, stream=None):
+    _check(_lib_handle().mok_expert_down(ctypes.byref(shape), ctypes.byref(weights), _ptr(a), _ptr(a_scale),
+                                         _ptr(offsets), _ptr(yg), _stream(stream)), "mok_expert_down")
 
 
 def shared_ffn(shape: Shape, weights: Weights, x, ys, ws, stream=None):

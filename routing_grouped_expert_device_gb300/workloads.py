@@ -71,6 +71,9 @@ CONFIGS: Dict[str, MoEConfig] = {
                                  skew=2.0, chunks=(512, 2048, 8192, 32768)),
     "dsv3_mxfp8_fwd": MoEConfig("dsv3_mxfp8_fwd", T=7168, D=7168, I=2048, E=256, K=8, I_shared=2048,
                                 dtype="mxfp8"),
+    # 1/8 of the DSV3 layer (32 experts, same rows per expert): a profiling
+    # case for the same kernels that still exceeds L2
+    "dsv3_slice_bf16_fwd": MoEConfig("dsv3_slice_bf16_fwd", T=896, D=7168, I=2048, E=32, K=8, I_shared=2048),
     "dsv3_bf16_fwdbwd": MoEConfig("dsv3_bf16_fwdbwd", T=4096, D=7168, I=2048, E=256, K=8, I_shared=2048,
                                   backward=True),
 }

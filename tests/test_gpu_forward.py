@@ -263,3 +263,22 @@ def test_invalid_shapes_rejected(m):
         sh = m.make_shape(**kw)
         assert lib.mok_moe_fwd(ctypes.byref(sh), ctypes.byref(m.Weights()), None, None, None, None, None, 0,
                                None) == m.MOK_ERR_INVALID_ARG
+
+
+def test_split_expert_entry_points_match_expert_ffn(m):
+    cfg = SMALL["ragged"]
+    inp = W.make_inputs(cfg, "cpu")
+    ref = O.moe_forward(host(inp), cfg.K)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    shape = m.shape_of(cfg)
+    xg = torch.from_numpy(O.f32_to_bf16_bits(ref["xg"]).view(np.int16)).view(torch.bfloat16).to(DEV)
+    off = torch.from_numpy(ref["offsets"]).to(DEV)
+    a1 = torch.empty(cfg.R, cfg.I, dtype=torch.bfloat16, device=DEV)
+    y1 = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
+    m.expert_ffn(shape, m.make_weights(d), xg, off, y1, a_out=a1)
+    a2 = torch.empty_like(a1)
+    y2 = torch.empty_like(y1)
+    m.expert_upgate(shape, m.make_weights(d), xg, off, a2)
+    m.expert_down(shape, m.make_weights(d), a2, off, y2)
+    assert torch.equal(a1.view(torch.int16), a2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))

@@ -123,6 +123,24 @@ mok_status mok_plan(const int32_t *topk_idx, int32_t T, int32_t E, int32_t K,
                     int32_t *counts, int32_t *offsets, int32_t *table,
                     int32_t *route_dst, void *ws, size_t ws_bytes, void *stream);
 
+/* mok_plan without caller-provided scratch: the same outputs, computed by
+ * the same kernels, for callers that cannot hand over device memory as
+ * workspace (their device memory belongs to another allocator they may not
+ * call from here, or the code path must not allocate).  The pages have no
+ * counterpart to this entry point.
+ * The scratch is a fixed 1 MiB array inside the library's device image
+ * (held on every GPU that loads the library until the process exits); it
+ * allows ceil(T*K / 1024) * E <= 262144, else MOK_ERR_WORKSPACE and nothing
+ * is enqueued.  Nothing is allocated.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  All calls share the one array, so
+ * calls that overlap on the GPU (different streams, no ordering between
+ * them) race and give wrong plans; order them.  Arguments and errors
+ * otherwise as mok_plan. */
+mok_status mok_plan_static(const int32_t *topk_idx, int32_t T, int32_t E, int32_t K,
+                           int32_t *counts, int32_t *offsets, int32_t *table,
+                           int32_t *route_dst, void *stream);
+
 /* Gather (blog, "Scheduling": tokens land expert-contiguous, zero local
  * copies).  xg[p] = x[table[p].src_index / K] for p < R; x bf16 [T][D],
  * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives E4M3 codes [R][D] and

@@ -54,6 +54,7 @@ _SIGS = {
     "mok_workspace_bytes": (_SZ, [ctypes.POINTER(Shape), ctypes.c_int]),
     "mok_route": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "mok_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "mok_plan_static": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
     "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
@@ -150,6 +151,13 @@ def plan(topk_idx, E, counts, offsets, table, route_dst, ws, stream=None):
     _check(_lib_handle().mok_plan(_ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets), _ptr(table),
                                   _ptr(route_dst), _ptr(ws), ws.numel() * ws.element_size(),
                                   _stream(stream)), "mok_plan")
+
+
+def plan_static(topk_idx, E, counts, offsets, table, route_dst, stream=None):
+    """mok_plan with the library's own fixed scratch (no workspace argument)."""
+    T, K = topk_idx.shape
+    _check(_lib_handle().mok_plan_static(_ptr(topk_idx), T, E, K, _ptr(counts), _ptr(offsets), _ptr(table),
+                                         _ptr(route_dst), _stream(stream)), "mok_plan_static")
 
 
 def dispatch(shape: Shape, x, table, xg, xg_scale=None, stream=None):

@@ -47,11 +47,11 @@ import numpy as np
 
 __all__ = [
     "Numerics", "FP32", "FP64_SHADOW",
-    "bf16_to_f32", "round_bf16", "f32_to_bf16_bits",
+    "bf16_to_f32", "round_bf16", "f32_to_bf16_bits", "bf16_flip_ulp",
     "silu", "route", "pull_schedule", "plan", "gather",
     "expert_ffn_rows", "expert_ffn", "shared_ffn", "combine", "moe_forward",
     "HostWeights", "moe_forward_tokens",
-    "route_backward_rows", "moe_backward", "router_grad",
+    "route_backward_rows", "moe_backward", "router_grad", "router_grad_slack",
     "e4m3_code_values", "e4m3_encode", "mx_scale_exponent", "mxfp8_quantize",
     "mxfp8_dequantize", "moe_forward_mxfp8",
 ]
@@ -76,6 +76,20 @@ def round_bf16(v) -> np.ndarray:
     keep_lsb = (u >> np.uint32(16)) & np.uint32(1)
     r = (u + np.uint32(0x7FFF) + keep_lsb) & np.uint32(0xFFFF0000)
     return r.view(np.float32)
+
+
+def bf16_flip_ulp(v, rel: float = 2.0 ** -14) -> np.ndarray:
+    """Where a bf16 rounding decision is not fixed by fp32 arithmetic.
+
+    An fp32 value that is the sum of many products differs between two
+    correct evaluations (other summation orders) by far less than 2^-14 of
+    its size.  If rounding v * (1 - rel) and v * (1 + rel) to bf16 gives
+    different values, either rounding of v is a correct result; return that
+    one-ulp difference there and 0 elsewhere."""
+    v = np.asarray(v, dtype=np.float64)
+    lo = round_bf16((v * (1.0 - rel)).astype(np.float32))
+    hi = round_bf16((v * (1.0 + rel)).astype(np.float32))
+    return np.abs(hi.astype(np.float64) - lo.astype(np.float64))
 
 
 def f32_to_bf16_bits(v) -> np.ndarray:
@@ -345,25 +359,54 @@ def route_backward_rows(xrows, dyrows, g, Wg, Wu, Wd, num: Numerics = FP32):
     SiLU'(h) = sig(h) (1 + h (1 - sig(h))):
         dh = bf16(da * u * SiLU'(h)),  du = bf16(da * SiLU(h)),
         a_g = bf16(g * a),  dx = bf16(dh W_gate + du W_up).
-    Returns dict(h, u, a, t, dg, dh, du, a_g, dx)."""
+    Returns dict(h, u, a, t, dg, dh, du, a_g, dx) and, under the fp32
+    numerics, flip_dh / flip_du / flip_ag: bf16_flip_ulp of each rounding
+    point (a_g also inherits g times the flip of a)."""
     X = num.w(xrows)
     dY = num.w(dyrows)
     gcol = np.asarray(g, dtype=num.dtype).reshape(-1, 1)
     Wg_, Wu_, Wd_ = num.w(Wg), num.w(Wu), num.w(Wd)
     h = X @ Wg_.T
     u = X @ Wu_.T
-    a = num.rnd(silu(h) * u).astype(num.dtype)
+    a_pre = silu(h) * u
+    a = num.rnd(a_pre).astype(num.dtype)
     t = dY @ Wd_
     dg = np.sum(t * a, axis=1)
     da = gcol * t
     one = num.dtype(1)
     with np.errstate(over="ignore"):
         sig = one / (one + np.exp(-h))
-    dh = num.rnd(da * u * sig * (one + h * (one - sig))).astype(num.dtype)
-    du = num.rnd(da * h * sig).astype(num.dtype)
-    a_g = num.rnd(gcol * a).astype(num.dtype)
-    dx = num.rnd(dh @ Wg_ + du @ Wu_).astype(num.dtype)
-    return dict(h=h, u=u, a=a, t=t, dg=dg, dh=dh, du=du, a_g=a_g, dx=dx)
+    dh_pre = da * u * sig * (one + h * (one - sig))
+    du_pre = da * h * sig
+    ag_pre = gcol * a
+    dh = num.rnd(dh_pre).astype(num.dtype)
+    du = num.rnd(du_pre).astype(num.dtype)
+    a_g = num.rnd(ag_pre).astype(num.dtype)
+    dx_pre = dh @ Wg_ + du @ Wu_
+    dx = num.rnd(dx_pre).astype(num.dtype)
+    out = dict(h=h, u=u, a=a, t=t, dg=dg, dh=dh, du=du, a_g=a_g, dx=dx)
+    if num.round_points:
+        flip_a = bf16_flip_ulp(a_pre)
+        out["flip_dh"] = bf16_flip_ulp(dh_pre)
+        out["flip_du"] = bf16_flip_ulp(du_pre)
+        out["flip_ag"] = bf16_flip_ulp(ag_pre) + np.abs(gcol) * flip_a
+        out["flip_dg"] = np.sum(flip_a * np.abs(t), axis=1)
+        out["flip_dx"] = (bf16_flip_ulp(dx_pre) + out["flip_dh"] @ np.abs(Wg_.astype(np.float64))
+                          + out["flip_du"] @ np.abs(Wu_.astype(np.float64)))
+    return out
+
+
+def router_grad_slack(flip_dg, g, den, topk_idx, E):
+    """Bound on ds from ambiguous roundings inside dg (see router_grad):
+    (flip_dg_k + sum_k' |g_k'| flip_dg_k') / den at the selected experts."""
+    flip_dg = np.asarray(flip_dg, dtype=np.float64)
+    gg = np.abs(np.asarray(g, dtype=np.float64))
+    T, K = gg.shape
+    dot = np.sum(gg * flip_dg, axis=1)
+    out = np.zeros((T, E))
+    val = (flip_dg + dot[:, None]) / np.abs(np.asarray(den, dtype=np.float64))[:, None]
+    np.put_along_axis(out, np.asarray(topk_idx, dtype=np.int64), val, axis=1)
+    return out
 
 
 def router_grad(dg, g, den, topk_idx, E, num: Numerics = FP32):
@@ -383,7 +426,8 @@ def router_grad(dg, g, den, topk_idx, E, num: Numerics = FP32):
 
 
 def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
-                 fwd: Optional[Dict[str, np.ndarray]] = None) -> Dict[str, np.ndarray]:
+                 fwd: Optional[Dict[str, np.ndarray]] = None,
+                 with_slack: bool = False) -> Dict[str, np.ndarray]:
     """Gradients of L = <dY, MoE(x, s)> w.r.t. x, every weight and s.
 
     Routing is recomputed (or taken from ``fwd``); gradients do not flow
@@ -391,7 +435,13 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
       dW_down[e] = bf16(sum_p dY_p (x) a_g_p), dW_gate[e] = bf16(sum_p dh_p (x) x_p),
       dW_up[e] = bf16(sum_p du_p (x) x_p);
     the shared expert likewise with g = 1 over all tokens;
-    dX[t] = bf16(dx_shared[t] + sum_k dx[route_dst[t,k]]) in k order."""
+    dX[t] = bf16(dx_shared[t] + sum_k dx[route_dst[t,k]]) in k order.
+
+    with_slack (fp32 numerics): also return out["slack"][name], per weight
+    gradient element the sum over rows of |other operand| times the
+    bf16_flip_ulp of the rounded factor (dh, du or a_g): how far another
+    correct evaluation, which may round those ambiguous factors the other
+    way, can land from this one."""
     if fwd is None:
         s = inp["s"]
         topk_idx, g, den = route(s, K, num)
@@ -410,9 +460,14 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
     g_route = np.asarray(g, dtype=num.dtype)[src_tok, src_k]
     dx_r = np.zeros((R, D), dtype=num.dtype)
     dg_route = np.zeros(R, dtype=num.dtype)
+    flip_dg_route = np.zeros(R)
+    flip_dx_r = np.zeros((R, D)) if with_slack else None
     dW_gate = np.zeros((E, I, D), dtype=num.dtype)
     dW_up = np.zeros((E, I, D), dtype=num.dtype)
     dW_down = np.zeros((E, D, I), dtype=num.dtype)
+    slack = {}
+    if with_slack:
+        slack = dict(dW_gate=np.zeros((E, I, D)), dW_up=np.zeros((E, I, D)), dW_down=np.zeros((E, D, I)))
     for e in range(E):
         p0, p1 = int(offsets[e]), int(offsets[e + 1])
         if p0 == p1:
@@ -425,8 +480,16 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
         dW_down[e] = num.rnd(dY[rows].T @ b["a_g"])
         dW_gate[e] = num.rnd(b["dh"].T @ x[rows])
         dW_up[e] = num.rnd(b["du"].T @ x[rows])
+        if with_slack:
+            flip_dg_route[p0:p1] = b["flip_dg"]
+            flip_dx_r[p0:p1] = b["flip_dx"]
+            ax, ady = np.abs(x[rows]).astype(np.float64), np.abs(dY[rows]).astype(np.float64)
+            slack["dW_down"][e] = ady.T @ b["flip_ag"]
+            slack["dW_gate"][e] = b["flip_dh"].T @ ax
+            slack["dW_up"][e] = b["flip_du"].T @ ax
     out = dict(dW_gate=dW_gate, dW_up=dW_up, dW_down=dW_down, dx_r=dx_r)
     acc = np.zeros((T, D), dtype=num.dtype)
+    slack_dx = np.zeros((T, D)) if with_slack else None
     if inp.get("ws_gate") is not None:
         bs = route_backward_rows(x, dY, np.ones(T, dtype=num.dtype),
                                  inp["ws_gate"], inp["ws_up"], inp["ws_down"], num)
@@ -434,14 +497,29 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
         out["dWs_down"] = num.rnd(dY.T @ bs["a_g"]).astype(num.dtype)
         out["dWs_gate"] = num.rnd(bs["dh"].T @ x).astype(num.dtype)
         out["dWs_up"] = num.rnd(bs["du"].T @ x).astype(num.dtype)
+        if with_slack:
+            slack_dx += bs["flip_dx"]
+            ax, ady = np.abs(x).astype(np.float64), np.abs(dY).astype(np.float64)
+            slack["dWs_down"] = ady.T @ bs["flip_ag"]
+            slack["dWs_gate"] = bs["flip_dh"].T @ ax
+            slack["dWs_up"] = bs["flip_du"].T @ ax
     rd = np.asarray(route_dst).reshape(T, K)
     for k in range(K):
         acc = acc + dx_r[rd[:, k]]
+        if with_slack:
+            slack_dx += flip_dx_r[rd[:, k]]
     out["dX"] = num.rnd(acc).astype(num.dtype)
     dg = np.zeros((T, K), dtype=num.dtype)
     dg[src_tok, src_k] = dg_route
     out["dg"] = dg
     out["ds"] = router_grad(dg, g, den, topk_idx, E, num)
+    if with_slack:
+        fdg = np.zeros((T, K))
+        fdg[src_tok, src_k] = flip_dg_route
+        slack["dX"] = slack_dx + bf16_flip_ulp(acc)
+        slack["dg"] = fdg
+        slack["ds"] = router_grad_slack(fdg, g, den, topk_idx, E)
+        out["slack"] = slack
     return out
 
 

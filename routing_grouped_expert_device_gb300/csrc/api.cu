@@ -60,6 +60,30 @@ FwdLayout fwd_layout(const mok_shape& s) {
   return L;
 }
 
+struct BwdLayout {
+  size_t xg, dyg, g_route, dh, du, ag, dgp, dxr, dhs, dus, ags, dxs, total;
+};
+
+BwdLayout bwd_layout(const mok_shape& s) {
+  const size_t T = s.T, D = s.D, I = s.I, K = s.K, Is = s.I_shared, R = T * K;
+  Carve c;
+  BwdLayout L;
+  L.xg = c.take(R * D * 2);
+  L.dyg = c.take(R * D * 2);
+  L.g_route = c.take(R * 4);
+  L.dh = c.take(R * I * 2);
+  L.du = c.take(R * I * 2);
+  L.ag = c.take(R * I * 2);
+  L.dgp = c.take(R * (I / 128) * 4);
+  L.dxr = c.take(R * D * 2);
+  L.dhs = c.take(T * Is * 2);
+  L.dus = c.take(T * Is * 2);
+  L.ags = c.take(T * Is * 2);
+  L.dxs = c.take(Is ? T * D * 2 : 0);
+  L.total = c.off;
+  return L;
+}
+
 template <class T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -79,7 +103,7 @@ extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
     case MOK_OP_EXPERT_FFN: return round_up(static_cast<size_t>(R) * s.I * 2);
     case MOK_OP_SHARED_FFN: return round_up(static_cast<size_t>(s.T) * (s.I_shared ? s.I_shared : 1) * 2);
     case MOK_OP_FWD: return fwd_layout(s).total;
-    case MOK_OP_BWD: return 0;
+    case MOK_OP_BWD: return bwd_layout(s).total;
   }
   return 0;
 }
@@ -249,8 +273,65 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
                                   void* dx, void* dw_gate, void* dw_up, void* dw_down,
                                   void* dws_gate, void* dws_up, void* dws_down, float* ds,
                                   float* dg, void* ws, size_t ws_bytes, void* stream) {
-  (void)shape; (void)w; (void)x; (void)s_in; (void)saved; (void)dy; (void)dx; (void)dw_gate;
-  (void)dw_up; (void)dw_down; (void)dws_gate; (void)dws_up; (void)dws_down; (void)ds; (void)dg;
-  (void)ws; (void)ws_bytes; (void)stream;
-  return MOK_ERR_UNSUPPORTED;
+  if (!shape_ok(shape) || !w || !saved) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  if (s.T == 0) return MOK_OK;
+  const mok_plan_buf& pb = *saved;
+  if (!x || !s_in || !dy || !dx || !dw_gate || !dw_up || !dw_down || !ds || !pb.topk_idx ||
+      !pb.g || !pb.offsets || !pb.table || !pb.route_dst || !w->w_gate || !w->w_up || !w->w_down)
+    return MOK_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(dw_gate) ||
+      !aligned16(dw_up) || !aligned16(dw_down) || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
+      !aligned16(w->w_down))
+    return MOK_ERR_INVALID_ARG;
+  if (s.I_shared && (!w->ws_gate || !w->ws_up || !w->ws_down || !dws_gate || !dws_up || !dws_down))
+    return MOK_ERR_INVALID_ARG;
+  const BwdLayout L = bwd_layout(s);
+  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOK_ERR_WORKSPACE;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* xg = at<void>(ws, L.xg);
+  void* dyg = at<void>(ws, L.dyg);
+  float* g_route = at<float>(ws, L.g_route);
+  void* dh = at<void>(ws, L.dh);
+  void* du = at<void>(ws, L.du);
+  void* ag = at<void>(ws, L.ag);
+  float* dgp = at<float>(ws, L.dgp);
+  void* dxr = at<void>(ws, L.dxr);
+  mok_status r;
+  // gather x, dY and the route weights into expert order (the forward's plan)
+  if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, pb.g, g_route, st)) != MOK_OK) return r;
+  if ((r = launch_dispatch_bf16(dy, pb.table, R, s.K, s.D, dyg, nullptr, nullptr, st)) != MOK_OK)
+    return r;
+  // replay h, u; t = dY W_down; dh, du, g*a, <t, a> partials
+  if ((r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,
+                            g_route, dh, du, ag, dgp, st)) != MOK_OK)
+    return r;
+  if ((r = launch_bwd_dx(dh, du, R, w->w_gate, w->w_up, pb.offsets, s.E, s.D, s.I, dxr, st)) != MOK_OK)
+    return r;
+  void* dxs = nullptr;
+  if (s.I_shared) {
+    void* dhs = at<void>(ws, L.dhs);
+    void* dus = at<void>(ws, L.dus);
+    void* ags = at<void>(ws, L.ags);
+    dxs = at<void>(ws, L.dxs);
+    if ((r = launch_bwd_dgrad(x, dy, s.T, w->ws_gate, w->ws_up, w->ws_down, nullptr, 1, s.D,
+                              s.I_shared, nullptr, dhs, dus, ags, nullptr, st)) != MOK_OK)
+      return r;
+    if ((r = launch_bwd_dx(dhs, dus, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.D, s.I_shared, dxs,
+                           st)) != MOK_OK)
+      return r;
+    if ((r = launch_wgrad(dy, ags, s.T, nullptr, 1, s.D, s.I_shared, dws_down, st)) != MOK_OK) return r;
+    if ((r = launch_wgrad(dhs, x, s.T, nullptr, 1, s.I_shared, s.D, dws_gate, st)) != MOK_OK) return r;
+    if ((r = launch_wgrad(dus, x, s.T, nullptr, 1, s.I_shared, s.D, dws_up, st)) != MOK_OK) return r;
+  }
+  // reverse combine in fixed k order
+  if ((r = launch_combine(dxr, dxs, nullptr, pb.route_dst, s.T, s.K, s.D, dx, st)) != MOK_OK) return r;
+  // per-expert weight gradients, K over the expert's rows
+  if ((r = launch_wgrad(dyg, ag, R, pb.offsets, s.E, s.D, s.I, dw_down, st)) != MOK_OK) return r;
+  if ((r = launch_wgrad(dh, xg, R, pb.offsets, s.E, s.I, s.D, dw_gate, st)) != MOK_OK) return r;
+  if ((r = launch_wgrad(du, xg, R, pb.offsets, s.E, s.I, s.D, dw_up, st)) != MOK_OK) return r;
+  return launch_router_grad(dgp, s.I / 128, pb.route_dst, pb.topk_idx, pb.g, s_in, s.T, s.E, s.K,
+                            ds, dg, st);
 }

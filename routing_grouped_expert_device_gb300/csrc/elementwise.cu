@@ -162,6 +162,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
   }
 }
 
+// Router-weight gradient (g_k = s_k / den, den the fp32 sum of the top-k s
+// in k order): dg_k = sum of the route's partials in order,
+// ds[t, topk_k] = (dg_k - sum_k' g_k' dg_k') / den, zero elsewhere.
+// One warp per token.
+__global__ void __launch_bounds__(256) router_grad_kernel(
+    const float* __restrict__ dgp, int nI, const int32_t* __restrict__ route_dst,
+    const int32_t* __restrict__ topk, const float* __restrict__ g, const float* __restrict__ s,
+    int T, int E, int K, float* __restrict__ ds, float* __restrict__ dg_out) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+    float dgk = 0.0f, gk = 0.0f, sk = 0.0f;
+    int ek = 0;
+    if (lane < K) {
+      const int64_t r = static_cast<int64_t>(t) * K + lane;
+      const int64_t dst = route_dst[r];
+      for (int j = 0; j < nI; ++j) dgk = __fadd_rn(dgk, dgp[dst * nI + j]);
+      gk = g[r];
+      ek = topk[r];
+      sk = s[static_cast<int64_t>(t) * E + ek];
+    }
+    float den = __shfl_sync(0xffffffffu, sk, 0);
+    float dot = __fmul_rn(__shfl_sync(0xffffffffu, gk, 0), __shfl_sync(0xffffffffu, dgk, 0));
+    for (int k = 1; k < K; ++k) {
+      den = __fadd_rn(den, __shfl_sync(0xffffffffu, sk, k));
+      dot = __fadd_rn(dot, __fmul_rn(__shfl_sync(0xffffffffu, gk, k), __shfl_sync(0xffffffffu, dgk, k)));
+    }
+    float* row = ds + static_cast<int64_t>(t) * E;
+    for (int e = lane; e < E; e += 32) row[e] = 0.0f;
+    __syncwarp();
+    if (lane < K) {
+      row[ek] = __fdiv_rn(__fsub_rn(dgk, dot), den);
+      if (dg_out) dg_out[static_cast<int64_t>(t) * K + lane] = dgk;
+    }
+    __syncwarp();
+  }
+}
+
 int grid_for(int64_t work_items, int per_block) {
   int64_t b = (work_items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
@@ -194,6 +232,16 @@ mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, vo
   if (rows == 0) return MOK_OK;
   quant_rows_kernel<<<grid_for(rows * (cols / 32), 256), 256, 0, st>>>(
       static_cast<const uint4*>(src), nullptr, 1, rows, cols, static_cast<uint4*>(q), scale);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_router_grad(const float* dgp, int nI, const int32_t* route_dst,
+                              const int32_t* topk, const float* g, const float* s, int T, int E,
+                              int K, float* ds, float* dg, cudaStream_t st) {
+  if (T == 0) return MOK_OK;
+  router_grad_kernel<<<grid_for(T, 8), 256, 0, st>>>(dgp, nI, route_dst, topk, g, s, T, E, K, ds,
+                                                      dg);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

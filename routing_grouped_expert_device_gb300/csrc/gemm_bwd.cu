@@ -1,0 +1,386 @@
+// Backward grouped GEMMs on tcgen05 / TMEM.
+//
+//  dgrad+replay : per (expert, 128 rows, 128 cols of I) one CTA accumulates
+//                 h = xg W_gate^T, u = xg W_up^T (the forward replay) and
+//                 t = dYg W_down (W_down read MN-major) in three TMEM
+//                 accumulators over K = D.  The epilogue forms, per row,
+//                 a = bf16(SiLU(h) u), the router-gradient partial <t, a>
+//                 (paper note "The production details": the down-projection
+//                 output is never formed), da = g t,
+//                 dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)), a_g = bf16(g a).
+//  dx           : dx = bf16(dh W_gate + du W_up), K = 2I, weights MN-major.
+//  wgrad        : dW[e] = bf16(sum over the expert's rows of P^T Q) with both
+//                 operands MN-major and K running over rows; the last K block
+//                 of an expert is masked by zeroing the rows past its end.
+#include "gemm_core.cuh"
+#include "kernels.h"
+
+namespace mok {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int KTILE = BM * BK * 2;  // 16 KB: 128 x 64 bf16, K-major
+constexpr int MNCHUNK = 64 * 128;   // 8 KB: 64 K-rows x 64 MN elements, MN-major
+
+// 128-byte swizzled descriptors: K-major (SBO 1024) and MN-major (LBO = one
+// 64-wide MN chunk = 8 KB, SBO 1024).
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
+__device__ __forceinline__ uint64_t mndesc(uint32_t a) { return sdesc_sw128(a, MNCHUNK, 1024); }
+
+// ---------------------------------------------------------------------------
+struct DgradCfg {
+  static constexpr int STAGES = 2;
+  static constexpr int STAGE_BYTES = 4 * KTILE + 2 * MNCHUNK;  // 80 KB
+  static constexpr int NUM_ACC = 1;
+  static constexpr int ACC_COLS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t ID_KK = idesc_bf16(128, 128, false, false);
+  static constexpr uint32_t ID_KMN = idesc_bf16(128, 128, false, true);
+
+  struct Params {
+    SchedArgs sched;
+    int* status;
+    CUtensorMap tmX, tmDy;   // [rows][D], K-major boxes 128 x 64
+    CUtensorMap tmWg, tmWu;  // [G*I][D], K-major boxes 128 x 64
+    CUtensorMap tmWd;        // [G*D][I], MN-major boxes 64 x 64
+    int32_t I, D;
+    const float* g_route;    // [rows] or null (weight 1)
+    __nv_bfloat16 *dh, *du, *ag;  // [rows][I]
+    float* dgp;              // [rows][I/128] or null
+  };
+
+  __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
+                              uint64_t* bar) {
+    const int k0 = kb * BK;
+    const int r = c.row0 + c.mt * BM;
+    const int wrow = c.g * P.I + c.nt * 128;
+    tma_load_2d(st, &P.tmX, k0, r, bar);
+    tma_load_2d(st + KTILE, &P.tmDy, k0, r, bar);
+    tma_load_2d(st + 2 * KTILE, &P.tmWg, k0, wrow, bar);
+    tma_load_2d(st + 3 * KTILE, &P.tmWu, k0, wrow, bar);
+    const int drow = c.g * P.D + k0;
+    tma_load_2d(st + 4 * KTILE, &P.tmWd, c.nt * 128, drow, bar);
+    tma_load_2d(st + 4 * KTILE + MNCHUNK, &P.tmWd, c.nt * 128 + 64, drow, bar);
+  }
+
+  __device__ static void fixup(const Params&, const TileCoord&, int, uint8_t*, int) {}
+
+  __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
+    const uint32_t s = smem_u32(st);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      const uint32_t acc = (kb | k) != 0;
+      const uint64_t ax = kdesc(s + k * 32), ay = kdesc(s + KTILE + k * 32);
+      mma_bf16(d, ax, kdesc(s + 2 * KTILE + k * 32), ID_KK, acc);
+      mma_bf16(d + 128, ax, kdesc(s + 3 * KTILE + k * 32), ID_KK, acc);
+      mma_bf16(d + 256, ay, mndesc(s + 4 * KTILE + k * 2048), ID_KMN, acc);
+    }
+  }
+
+  __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
+                                  int lane, bool) {
+    const int r = ew * 32 + lane;
+    const bool valid = c.mt * BM + r < c.rows;
+    const int64_t row = c.row0 + c.mt * BM + r;
+    const float g = (valid && P.g_route) ? P.g_route[row] : 1.0f;
+    const size_t o = static_cast<size_t>(row) * P.I + c.nt * 128;
+    float dot = 0.0f;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t hv[32], uv[32], tv[32];
+      tmem_ld32(taddr + ch * 32, hv);
+      tmem_ld32(taddr + 128 + ch * 32, uv);
+      tmem_ld32(taddr + 256 + ch * 32, tv);
+      tmem_ld_wait();
+      uint32_t pdh[16], pdu[16], pag[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float dhv[2], duv[2], agv[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float h = __uint_as_float(hv[2 * j + q]);
+          const float u = __uint_as_float(uv[2 * j + q]);
+          const float t = __uint_as_float(tv[2 * j + q]);
+          const float sig = 1.0f / (1.0f + __expf(-h));
+          const float a = __bfloat162float(__float2bfloat16_rn(silu_f(h) * u));
+          dot = __fmaf_rn(t, a, dot);
+          const float da = g * t;
+          dhv[q] = da * u * sig * (1.0f + h * (1.0f - sig));
+          duv[q] = da * h * sig;
+          agv[q] = g * a;
+        }
+        pdh[j] = pack_bf16x2(dhv[0], dhv[1]);
+        pdu[j] = pack_bf16x2(duv[0], duv[1]);
+        pag[j] = pack_bf16x2(agv[0], agv[1]);
+      }
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          st_global_v4(P.dh + o + ch * 32 + q * 8, pdh[4 * q], pdh[4 * q + 1], pdh[4 * q + 2], pdh[4 * q + 3]);
+          st_global_v4(P.du + o + ch * 32 + q * 8, pdu[4 * q], pdu[4 * q + 1], pdu[4 * q + 2], pdu[4 * q + 3]);
+          st_global_v4(P.ag + o + ch * 32 + q * 8, pag[4 * q], pag[4 * q + 1], pag[4 * q + 2], pag[4 * q + 3]);
+        }
+      }
+    }
+    if (valid && P.dgp) P.dgp[row * (P.I / 128) + c.nt] = dot;
+  }
+};
+
+// ---------------------------------------------------------------------------
+struct DxCfg {
+  static constexpr int STAGES = 4;
+  static constexpr int STAGE_BYTES = KTILE + 4 * MNCHUNK;  // 48 KB
+  static constexpr int NUM_ACC = 2;
+  static constexpr int ACC_COLS = 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t IDESC = idesc_bf16(128, 256, false, true);
+
+  struct Params {
+    SchedArgs sched;
+    int* status;
+    CUtensorMap tmDh, tmDu;  // [rows][I], K-major boxes 128 x 64
+    CUtensorMap tmWg, tmWu;  // [G*I][D], MN-major boxes 64 x 64
+    int32_t I, half_kb;
+    __nv_bfloat16* out;      // [rows][D]
+    int32_t out_ld;
+  };
+
+  __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
+                              uint64_t* bar) {
+    const bool up = kb >= P.half_kb;
+    const int k0 = (up ? kb - P.half_kb : kb) * BK;
+    tma_load_2d(st, up ? &P.tmDu : &P.tmDh, k0, c.row0 + c.mt * BM, bar);
+    const CUtensorMap* w = up ? &P.tmWu : &P.tmWg;
+    const int wrow = c.g * P.I + k0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d(st + KTILE + j * MNCHUNK, w, c.nt * 256 + 64 * j, wrow, bar);
+  }
+
+  __device__ static void fixup(const Params&, const TileCoord&, int, uint8_t*, int) {}
+
+  __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
+    const uint32_t s = smem_u32(st);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k)
+      mma_bf16(d, kdesc(s + k * 32), mndesc(s + KTILE + k * 2048), IDESC, (kb | k) != 0);
+  }
+
+  __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
+                                  int lane, bool) {
+    const int r = ew * 32 + lane;
+    const bool valid = c.mt * BM + r < c.rows;
+    __nv_bfloat16* orow =
+        P.out + static_cast<size_t>(c.row0 + c.mt * BM + r) * P.out_ld + c.nt * 256;
+#pragma unroll 1
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// dW[g][m][n] = sum_{p in group g} Pm[p][m] * Qn[p][n]: A = Pm^T, B = Qn^T,
+// both MN-major in their [rows][...] storage.  M tile 128, N tile BN.
+template <int BN>
+struct WgradCfg {
+  static constexpr int NB = BN / 64;  // 64-wide MN chunks of B
+  static constexpr int STAGES = 4;
+  static constexpr int STAGE_BYTES = (2 + NB) * MNCHUNK;
+  static constexpr int NUM_ACC = 2;
+  static constexpr int ACC_COLS = BN;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr uint32_t IDESC = idesc_bf16(128, BN, true, true);
+
+  struct Params {
+    SchedArgs sched;
+    int* status;
+    CUtensorMap tmA;  // [rows][M], MN-major boxes 64 x 64
+    CUtensorMap tmB;  // [rows][N], MN-major boxes 64 x 64
+    int32_t M, N;
+    __nv_bfloat16* out;  // [G][M][N]
+  };
+
+  __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
+                              uint64_t* bar) {
+    const int rk = c.row0 + kb * BK;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tma_load_2d(st + j * MNCHUNK, &P.tmA, c.mt * 128 + 64 * j, rk, bar);
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+      tma_load_2d(st + (2 + j) * MNCHUNK, &P.tmB, c.nt * BN + 64 * j, rk, bar);
+  }
+
+  // Rows past the group's end in its last K block belong to the next group
+  // (or lie past the tensor and are zero-filled): zero them in A.
+  __device__ static void fixup(const Params&, const TileCoord& c, int kb, uint8_t* st, int lane) {
+    const int valid = c.rows - kb * BK;
+    if (valid >= BK) return;
+    const int nrows = BK - valid;
+    const int units = 2 * nrows * 8;  // 16-byte units: 2 chunks x rows x 128 B
+    for (int u = lane; u < units; u += 32) {
+      const int chunk = u / (nrows * 8);
+      const int rem = u - chunk * nrows * 8;
+      const int rrow = valid + rem / 8;
+      uint4* p = reinterpret_cast<uint4*>(st + chunk * MNCHUNK + rrow * 128 + (rem % 8) * 16);
+      *p = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+
+  __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
+    const uint32_t s = smem_u32(st);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k)
+      mma_bf16(d, mndesc(s + k * 2048), mndesc(s + 2 * MNCHUNK + k * 2048), IDESC, (kb | k) != 0);
+  }
+
+  __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
+                                  int lane, bool has_acc) {
+    const int r = ew * 32 + lane;
+    __nv_bfloat16* orow = P.out + static_cast<size_t>(c.g) * P.M * P.N +
+                          static_cast<size_t>(c.mt * 128 + r) * P.N + c.nt * BN;
+#pragma unroll 1
+    for (int ch = 0; ch < BN / 32; ++ch) {
+      uint32_t pk[16];
+      if (has_acc) {
+        uint32_t v[32];
+        tmem_ld32(taddr + ch * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+};
+
+template <class Cfg>
+mok_status run(const typename Cfg::Params& P, cudaStream_t st) {
+  const size_t smem = gemm_smem_bytes<Cfg>(P.sched.G);
+  if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(gemm_persistent<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  gemm_persistent<Cfg><<<num_sms(), 256, smem, st>>>(P);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+SchedArgs sched_rows(const int32_t* offsets, int G, int64_t m_total, int n_tiles, int k_blocks) {
+  SchedArgs s;
+  s.offsets = offsets;
+  s.G = offsets ? G : 1;
+  s.m_total = static_cast<int32_t>(m_total);
+  s.n_tiles = n_tiles;
+  s.m_tiles_fixed = 0;
+  s.k_blocks_fixed = k_blocks;
+  s.bm = BM;
+  s.bk_rows = BK;
+  return s;
+}
+
+constexpr auto kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+bool kmap(CUtensorMap* m, const void* p, int64_t rows, int cols) {
+  return make_tmap_2d(m, p, kBF16, rows, cols, static_cast<uint64_t>(cols) * 2, 128, BK, true);
+}
+bool mnmap(CUtensorMap* m, const void* p, int64_t rows, int cols) {
+  return make_tmap_2d(m, p, kBF16, rows, cols, static_cast<uint64_t>(cols) * 2, BK, 64, true);
+}
+
+}  // namespace
+
+mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
+                            const void* w_up, const void* w_down, const int32_t* offsets, int G,
+                            int D, int I, const float* g_route, void* dh, void* du, void* ag,
+                            float* dgp, cudaStream_t st) {
+  if (rows == 0) return MOK_OK;
+  DgradCfg::Params P;
+  P.sched = sched_rows(offsets, G, rows, I / 128, D / BK);
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const int groups = offsets ? G : 1;
+  if (!kmap(&P.tmX, xg, rows, D) || !kmap(&P.tmDy, dyg, rows, D) ||
+      !kmap(&P.tmWg, w_gate, static_cast<int64_t>(groups) * I, D) ||
+      !kmap(&P.tmWu, w_up, static_cast<int64_t>(groups) * I, D) ||
+      !mnmap(&P.tmWd, w_down, static_cast<int64_t>(groups) * D, I))
+    return MOK_ERR_CUDA;
+  P.I = I;
+  P.D = D;
+  P.g_route = g_route;
+  P.dh = static_cast<__nv_bfloat16*>(dh);
+  P.du = static_cast<__nv_bfloat16*>(du);
+  P.ag = static_cast<__nv_bfloat16*>(ag);
+  P.dgp = dgp;
+  return run<DgradCfg>(P, st);
+}
+
+mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,
+                         const void* w_up, const int32_t* offsets, int G, int D, int I, void* dx,
+                         cudaStream_t st) {
+  if (rows == 0) return MOK_OK;
+  DxCfg::Params P;
+  P.sched = sched_rows(offsets, G, rows, D / 256, 2 * (I / BK));
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const int groups = offsets ? G : 1;
+  if (!kmap(&P.tmDh, dh, rows, I) || !kmap(&P.tmDu, du, rows, I) ||
+      !mnmap(&P.tmWg, w_gate, static_cast<int64_t>(groups) * I, D) ||
+      !mnmap(&P.tmWu, w_up, static_cast<int64_t>(groups) * I, D))
+    return MOK_ERR_CUDA;
+  P.I = I;
+  P.half_kb = I / BK;
+  P.out = static_cast<__nv_bfloat16*>(dx);
+  P.out_ld = D;
+  return run<DxCfg>(P, st);
+}
+
+template <int BN>
+mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t* offsets, int G,
+                    int M, int N, void* dw, cudaStream_t st) {
+  typename WgradCfg<BN>::Params P;
+  SchedArgs s;
+  s.offsets = offsets;
+  s.G = offsets ? G : 1;
+  s.m_total = static_cast<int32_t>(rows);
+  s.n_tiles = N / BN;
+  s.m_tiles_fixed = M / 128;
+  s.k_blocks_fixed = 0;
+  s.bm = BM;
+  s.bk_rows = BK;
+  P.sched = s;
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const int64_t map_rows = rows > 0 ? rows : 1;
+  if (!mnmap(&P.tmA, pm, map_rows, M) || !mnmap(&P.tmB, qn, map_rows, N)) return MOK_ERR_CUDA;
+  P.M = M;
+  P.N = N;
+  P.out = static_cast<__nv_bfloat16*>(dw);
+  return run<WgradCfg<BN>>(P, st);
+}
+
+mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
+                        int G, int M, int N, void* dw, cudaStream_t st) {
+  if (N % 256 == 0) return wgrad_bn<256>(pm, qn, rows, offsets, G, M, N, dw, st);
+  return wgrad_bn<128>(pm, qn, rows, offsets, G, M, N, dw, st);
+}
+
+}  // namespace mok

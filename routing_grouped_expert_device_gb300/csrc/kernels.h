@@ -43,6 +43,24 @@ mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, cons
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
 
+// Backward.  dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
+// non-null, dgp [rows][I/128] partial <t, a>; g_route null = weight 1.
+mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
+                            const void* w_up, const void* w_down, const int32_t* offsets, int G,
+                            int D, int I, const float* g_route, void* dh, void* du, void* ag,
+                            float* dgp, cudaStream_t st);
+// dx [rows][D] = bf16(dh W_gate + du W_up)
+mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,
+                         const void* w_up, const int32_t* offsets, int G, int D, int I, void* dx,
+                         cudaStream_t st);
+// dw [G][M][N] = bf16(sum over each group's rows of pm[p][m] qn[p][n])
+mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
+                        int G, int M, int N, void* dw, cudaStream_t st);
+// ds [T][E], dg [T][K] (nullable) from the partials dgp [R][nI]
+mok_status launch_router_grad(const float* dgp, int nI, const int32_t* route_dst,
+                              const int32_t* topk, const float* g, const float* s, int T, int E,
+                              int K, float* ds, float* dg, cudaStream_t st);
+
 bool shape_ok(const mok_shape* s);
 
 }  // namespace mok

@@ -118,3 +118,20 @@ def test_mxfp8_zero_block_and_signed_zero():
     assert sc[0, 0] == 0
     assert np.all(q[0, :32] == 0)
     assert q[0, 40] == 0x80
+
+
+def test_bf16_flip_ulp_marks_only_near_midpoints():
+    one = np.float32(1.0)
+    ulp = 2.0 ** -7  # bf16 spacing in [1, 2)
+    mid = np.float32(1.0 + ulp / 2)  # exact rounding midpoint
+    assert O.bf16_flip_ulp(mid) == ulp
+    assert O.bf16_flip_ulp(np.nextafter(mid, np.float32(2))) == ulp
+    assert O.bf16_flip_ulp(one) == 0.0
+    assert O.bf16_flip_ulp(np.float32(1.0 + ulp / 4)) == 0.0
+    rng = np.random.default_rng(7)
+    v = rng.standard_normal(100000).astype(np.float32)
+    f = O.bf16_flip_ulp(v)
+    frac = np.mean(f > 0)
+    assert 0.001 < frac < 0.05  # ~ 2 * 2^-14 / 2^-8 of values sit near a midpoint
+    nz = f > 0
+    assert np.allclose(f[nz], np.abs(O.round_bf16(v[nz] * (1 + 2.0 ** -14)) - O.round_bf16(v[nz] * (1 - 2.0 ** -14))))

@@ -77,11 +77,21 @@ typedef struct {
   int32_t producer_sms;
 } mok_shape;
 
-/* Weights (device, bf16 unless noted).  Routed: w_gate, w_up [E][I][D];
- * w_down [E][D][I].  MXFP8 copies (nullable for BF16): q_* E4M3 bytes of the
- * same shapes, sc_* E8M0 bytes, one per 32 elements along the last dim
- * ([E][I][D/32], [E][I][D/32], [E][D][I/32]).  Shared expert: ws_gate,
- * ws_up [I_shared][D]; ws_down [D][I_shared] (null when I_shared = 0). */
+/* MXFP8 tensors (paper note, "The production details").  A [rows][cols]
+ * tensor quantised along cols is E4M3 ("fn") codes [rows][cols] plus E8M0
+ * scales, one per 32 consecutive elements of a row, stored as 32-bit words
+ * [cols/128][ld] with ld = rows rounded up to a multiple of 4: word (g, r)
+ * holds the scales of row r for columns [128 g, 128 g + 128), byte b (the
+ * least significant first) for columns [128 g + 32 b, 128 g + 32 b + 32).
+ * Element value = code * 2^(scale - 127).  cols must be a multiple of 128.
+ *
+ * Weights (device, bf16 unless noted).  Routed: w_gate, w_up [E][I][D];
+ * w_down [E][D][I].  MXFP8 copies (used when shape.dtype = MOK_MXFP8, may be
+ * NULL otherwise): q_gate, q_up, q_down codes of the same shapes (as
+ * [E*I][D], [E*I][D], [E*D][I] tensors quantised along the last dim) and
+ * sc_* their scale words (mok_quantize_mxfp8 writes both).  Shared expert,
+ * always BF16: ws_gate, ws_up [I_shared][D]; ws_down [D][I_shared] (NULL
+ * when I_shared = 0). */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
   const void *q_gate, *q_up, *q_down;
@@ -143,16 +153,20 @@ mok_status mok_plan_static(const int32_t *topk_idx, int32_t T, int32_t E, int32_
 
 /* Gather (blog, "Scheduling": tokens land expert-contiguous, zero local
  * copies).  xg[p] = x[table[p].src_index / K] for p < R; x bf16 [T][D],
- * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives E4M3 codes [R][D] and
- * xg_scale E8M0 bytes [R][D/32] (quantisation fused into the dispatch);
- * xg_scale is ignored for BF16. */
+ * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives the E4M3 codes [R][D]
+ * of the gathered rows and xg_scale their scale words ([D/128][ld],
+ * ld = R rounded up to 4; quantisation fused into the dispatch); xg_scale
+ * is ignored for BF16. */
 mok_status mok_dispatch(const mok_shape *shape, const void *x, const int32_t *table,
                         void *xg, uint8_t *xg_scale, void *stream);
 
 /* Grouped expert FFN over expert-contiguous rows: expert e owns rows
  * [offsets[e], offsets[e+1]) of xg.  a = bf16(SiLU(xg W_gate^T) * (xg W_up^T))
  * [R][I] (written to a_out when non-null, else to the workspace), then
- * yg = bf16(a W_down^T) [R][D].  fp32 accumulation on the tensor cores. */
+ * yg = bf16(a W_down^T) [R][D].  fp32 accumulation on the tensor cores.
+ * MOK_MXFP8: xg / xg_scale are MXFP8 (from mok_dispatch), the weights are
+ * q_* / sc_*, a is quantised to MXFP8 along I before the down projection
+ * and kept in the workspace (a_out must be NULL); yg stays bf16. */
 mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const void *xg,
                           const uint8_t *xg_scale, const int32_t *offsets, void *a_out,
                           void *yg, void *ws, size_t ws_bytes, void *stream);
@@ -160,10 +174,12 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
 /* The two halves of mok_expert_ffn, for callers that schedule them apart.
  * mok_expert_upgate: a = bf16(SiLU(xg W_gate^T) * (xg W_up^T)) [R][I].
  * mok_expert_down: yg = bf16(a W_down^T) [R][D].  Same rules as
- * mok_expert_ffn; xg_scale / a_scale are reserved for MXFP8 (NULL). */
+ * mok_expert_ffn.  For MOK_MXFP8, a is written as codes [R][I] plus scale
+ * words a_scale ([I/128][ld], ld = R rounded up to 4) and read back that way
+ * by mok_expert_down; xg_scale / a_scale are ignored for BF16. */
 mok_status mok_expert_upgate(const mok_shape *shape, const mok_weights *w, const void *xg,
                              const uint8_t *xg_scale, const int32_t *offsets, void *a,
-                             void *stream);
+                             uint8_t *a_scale, void *stream);
 mok_status mok_expert_down(const mok_shape *shape, const mok_weights *w, const void *a,
                            const uint8_t *a_scale, const int32_t *offsets, void *yg,
                            void *stream);
@@ -182,7 +198,10 @@ mok_status mok_combine(const mok_shape *shape, const void *yg, const void *ys, c
 
 /* Whole forward: route -> plan -> dispatch -> shared FFN -> grouped FFN ->
  * combine.  x bf16 [T][D]; s fp32 [T][E]; out bf16 [T][D].  `saved`
- * (nullable) receives the routing and plan for mok_moe_bwd. */
+ * (nullable) receives the routing and plan for mok_moe_bwd.  With
+ * shape.dtype = MOK_MXFP8 the routed experts run in MXFP8 (dispatch
+ * quantises x, the up/gate epilogue quantises a) and the shared expert in
+ * BF16. */
 mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void *x,
                        const float *s, void *out, mok_plan_buf *saved, void *ws,
                        size_t ws_bytes, void *stream);
@@ -201,10 +220,11 @@ mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void 
                        void *dws_up, void *dws_down, float *ds, float *dg, void *ws,
                        size_t ws_bytes, void *stream);
 
-/* MXFP8 quantiser: src bf16 [rows][cols] (cols % 32 == 0) -> q E4M3 bytes
- * [rows][cols] and scale E8M0 bytes [rows][cols/32]; per 1x32 block the
- * scale is 2^e with e the smallest integer such that amax <= 448 * 2^e
- * (all-zero block: byte 0), codes round to nearest even. */
+/* MXFP8 quantiser: src bf16 [rows][cols] (cols % 128 == 0) -> q E4M3 codes
+ * [rows][cols] and scale words ([cols/128][ld], ld = rows rounded up to 4,
+ * see the MXFP8 layout above; scale needs cols/128 * ld * 4 bytes).  Per
+ * 1x32 block the scale is 2^e with e the smallest integer such that
+ * amax <= 448 * 2^e (all-zero block: byte 0); codes round to nearest even. */
 mok_status mok_quantize_mxfp8(const void *src, int64_t rows, int64_t cols, void *q,
                               uint8_t *scale, void *stream);
 

@@ -53,7 +53,7 @@ __all__ = [
     "HostWeights", "moe_forward_tokens",
     "route_backward_rows", "moe_backward", "router_grad", "router_grad_slack",
     "e4m3_code_values", "e4m3_encode", "mx_scale_exponent", "mxfp8_quantize",
-    "mxfp8_dequantize", "moe_forward_mxfp8",
+    "mxfp8_dequantize", "expert_ffn_rows_mxfp8", "moe_forward_mxfp8",
 ]
 
 
@@ -592,6 +592,23 @@ def mxfp8_dequantize(codes, scales) -> np.ndarray:
     vals = e4m3_code_values()[codes].reshape(codes.shape[:-1] + (n // 32, 32))
     e = np.asarray(scales, dtype=np.int32) - 127
     return (vals * np.ldexp(1.0, e)[..., None]).reshape(codes.shape)
+
+
+def expert_ffn_rows_mxfp8(xrows, Wg, Wu, Wd):
+    """One expert's FFN with MXFP8 operands for a batch of rows ([note]
+    "The production details"): x quantised per row along D, W_gate / W_up
+    along D, W_down along I, a = bf16(SiLU(h) u) quantised along I; every
+    GEMM contracts the exactly dequantised values in fp32.  Inputs are bf16
+    bits (or float values).  Returns dict(a_pre, a, aq, asc, y)."""
+    deq = lambda v: mxfp8_dequantize(*mxfp8_quantize(FP32.w(v))).astype(np.float32)
+    X, Wgd, Wud, Wdd = deq(xrows), deq(Wg), deq(Wu), deq(Wd)
+    h = X @ Wgd.T
+    u = X @ Wud.T
+    a_pre = silu(h) * u
+    a = round_bf16(a_pre)
+    aq, asc = mxfp8_quantize(a)
+    y = round_bf16(mxfp8_dequantize(aq, asc).astype(np.float32) @ Wdd.T)
+    return dict(a_pre=a_pre, a=a, aq=aq, asc=asc, y=y)
 
 
 def moe_forward_mxfp8(inp: Dict[str, np.ndarray], K: int, quant: Optional[Dict[str, tuple]] = None,

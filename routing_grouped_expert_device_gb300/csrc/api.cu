@@ -36,7 +36,8 @@ struct Carve {
 };
 
 struct FwdLayout {
-  size_t topk, g, counts, offsets, table, route_dst, hist, xg, xg_scale, a, yg, as, ys, total;
+  size_t topk, g, counts, offsets, table, route_dst, hist, xg, xg_scale, a, a_scale, yg, as, ys,
+      total;
 };
 
 FwdLayout fwd_layout(const mok_shape& s) {
@@ -51,8 +52,10 @@ FwdLayout fwd_layout(const mok_shape& s) {
   L.route_dst = c.take(R * 4);
   L.hist = c.take(plan_scratch_bytes(static_cast<int64_t>(R), s.E));
   L.xg = c.take(R * D * 2);
-  L.xg_scale = c.take(s.dtype == MOK_MXFP8 ? R * D / 32 : 0);
+  const bool mx = s.dtype == MOK_MXFP8;
+  L.xg_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D) : 0);
   L.a = c.take(R * I * 2);
+  L.a_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), I) : 0);
   L.yg = c.take(R * D * 2);
   L.as = c.take(T * Is * 2);
   L.ys = c.take(Is ? T * D * 2 : 0);
@@ -84,6 +87,19 @@ BwdLayout bwd_layout(const mok_shape& s) {
   return L;
 }
 
+bool mx_weights_ok(const mok_weights* w) {
+  return w->q_gate && w->q_up && w->q_down && w->sc_gate && w->sc_up && w->sc_down &&
+         aligned16(w->q_gate) && aligned16(w->q_up) && aligned16(w->q_down) &&
+         aligned16(w->sc_gate) && aligned16(w->sc_up) && aligned16(w->sc_down);
+}
+
+// Workspace of mok_expert_ffn: a (bf16), or a codes + scale words (MXFP8).
+size_t ffn_ws_bytes(const mok_shape& s) {
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  if (s.dtype == MOK_MXFP8) return round_up(static_cast<size_t>(R) * s.I) + round_up(mx_scale_bytes(R, s.I));
+  return round_up(static_cast<size_t>(R) * s.I * 2);
+}
+
 template <class T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -100,7 +116,7 @@ extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   switch (op) {
     case MOK_OP_PLAN: return round_up(plan_scratch_bytes(R, s.E));
-    case MOK_OP_EXPERT_FFN: return round_up(static_cast<size_t>(R) * s.I * 2);
+    case MOK_OP_EXPERT_FFN: return ffn_ws_bytes(s);
     case MOK_OP_SHARED_FFN: return round_up(static_cast<size_t>(s.T) * (s.I_shared ? s.I_shared : 1) * 2);
     case MOK_OP_FWD: return fwd_layout(s).total;
     case MOK_OP_BWD: return bwd_layout(s).total;
@@ -126,12 +142,24 @@ extern "C" mok_status mok_dispatch(const mok_shape* shape, const void* x, const 
 extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* w, const void* xg,
                                      const uint8_t* xg_scale, const int32_t* offsets, void* a_out,
                                      void* yg, void* ws, size_t ws_bytes, void* stream) {
-  (void)xg_scale;
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
-  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   if (R == 0) return MOK_OK;
+  if (s.dtype == MOK_MXFP8) {
+    if (!xg || !xg_scale || !offsets || !yg || a_out || !mx_weights_ok(w) || !aligned16(xg) ||
+        !aligned16(xg_scale) || !aligned16(yg))
+      return MOK_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < ffn_ws_bytes(s) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+      return MOK_ERR_WORKSPACE;
+    void* aq = ws;
+    void* asc = static_cast<uint8_t*>(ws) + round_up(static_cast<size_t>(R) * s.I);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mok_status r = launch_upgate_mx(xg, xg_scale, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up,
+                                    offsets, s.E, s.D, s.I, aq, asc, st);
+    if (r != MOK_OK) return r;
+    return launch_down_mx(aq, asc, R, w->q_down, w->sc_down, offsets, s.E, s.D, s.I, yg, st);
+  }
   if (!xg || !offsets || !yg || !w->w_gate || !w->w_up || !w->w_down) return MOK_ERR_INVALID_ARG;
   if (!aligned16(xg) || !aligned16(yg) || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
       !aligned16(w->w_down) || (a_out && !aligned16(a_out)))
@@ -149,13 +177,19 @@ extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* 
 
 extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weights* w,
                                         const void* xg, const uint8_t* xg_scale,
-                                        const int32_t* offsets, void* a, void* stream) {
-  (void)xg_scale;
+                                        const int32_t* offsets, void* a, uint8_t* a_scale,
+                                        void* stream) {
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
-  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   if (R == 0) return MOK_OK;
+  if (s.dtype == MOK_MXFP8) {
+    if (!xg || !xg_scale || !offsets || !a || !a_scale || !mx_weights_ok(w) || !aligned16(xg) ||
+        !aligned16(xg_scale) || !aligned16(a) || !aligned16(a_scale))
+      return MOK_ERR_INVALID_ARG;
+    return launch_upgate_mx(xg, xg_scale, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, offsets,
+                            s.E, s.D, s.I, a, a_scale, static_cast<cudaStream_t>(stream));
+  }
   if (!xg || !offsets || !a || !w->w_gate || !w->w_up || !aligned16(xg) || !aligned16(a) ||
       !aligned16(w->w_gate) || !aligned16(w->w_up))
     return MOK_ERR_INVALID_ARG;
@@ -166,12 +200,17 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
 extern "C" mok_status mok_expert_down(const mok_shape* shape, const mok_weights* w, const void* a,
                                       const uint8_t* a_scale, const int32_t* offsets, void* yg,
                                       void* stream) {
-  (void)a_scale;
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
-  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   if (R == 0) return MOK_OK;
+  if (s.dtype == MOK_MXFP8) {
+    if (!a || !a_scale || !offsets || !yg || !mx_weights_ok(w) || !aligned16(a) ||
+        !aligned16(a_scale) || !aligned16(yg))
+      return MOK_ERR_INVALID_ARG;
+    return launch_down_mx(a, a_scale, R, w->q_down, w->sc_down, offsets, s.E, s.D, s.I, yg,
+                          static_cast<cudaStream_t>(stream));
+  }
   if (!a || !offsets || !yg || !w->w_down || !aligned16(a) || !aligned16(yg) ||
       !aligned16(w->w_down))
     return MOK_ERR_INVALID_ARG;
@@ -211,11 +250,10 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
                                   size_t ws_bytes, void* stream) {
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
-  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
   if (s.T == 0) return MOK_OK;
-  if (!x || !s_in || !out || !aligned16(x) || !aligned16(out) || !w->w_gate || !w->w_up ||
-      !w->w_down)
-    return MOK_ERR_INVALID_ARG;
+  const bool mx = s.dtype == MOK_MXFP8;
+  if (!x || !s_in || !out || !aligned16(x) || !aligned16(out)) return MOK_ERR_INVALID_ARG;
+  if (mx ? !mx_weights_ok(w) : (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
   if (s.I_shared && (!w->ws_gate || !w->ws_up || !w->ws_down)) return MOK_ERR_INVALID_ARG;
   const FwdLayout L = fwd_layout(s);
   if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOK_ERR_WORKSPACE;
@@ -243,8 +281,12 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
   void* a = at<void>(ws, L.a);
   void* yg = at<void>(ws, L.yg);
   void* ys = nullptr;
-  if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
+  if (mx) {
+    if ((r = launch_dispatch_mxfp8(x, pb.table, R, s.K, s.D, xg, at<uint8_t>(ws, L.xg_scale), st)) != MOK_OK)
+      return r;
+  } else if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK) {
     return r;
+  }
   if (s.I_shared) {
     ys = at<void>(ws, L.ys);
     void* as = at<void>(ws, L.as);
@@ -254,15 +296,25 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     if ((r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st)) != MOK_OK)
       return r;
   }
-  if ((r = launch_upgate(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st)) != MOK_OK)
-    return r;
-  if ((r = launch_down(a, R, w->w_down, pb.offsets, s.E, R, s.D, s.I, yg, st)) != MOK_OK) return r;
+  if (mx) {
+    void* asc = at<void>(ws, L.a_scale);
+    if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
+                              w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st)) != MOK_OK)
+      return r;
+    if ((r = launch_down_mx(a, asc, R, w->q_down, w->sc_down, pb.offsets, s.E, s.D, s.I, yg, st)) !=
+        MOK_OK)
+      return r;
+  } else {
+    if ((r = launch_upgate(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st)) != MOK_OK)
+      return r;
+    if ((r = launch_down(a, R, w->w_down, pb.offsets, s.E, R, s.D, s.I, yg, st)) != MOK_OK) return r;
+  }
   return launch_combine(yg, ys, pb.g, pb.route_dst, s.T, s.K, s.D, out, st);
 }
 
 extern "C" mok_status mok_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
                                          uint8_t* scale, void* stream) {
-  if (rows < 0 || cols <= 0 || cols % 32) return MOK_ERR_INVALID_ARG;
+  if (rows < 0 || cols <= 0 || cols % 128) return MOK_ERR_INVALID_ARG;
   if (rows == 0) return MOK_OK;
   if (!src || !q || !scale || !aligned16(src) || !aligned16(q)) return MOK_ERR_INVALID_ARG;
   return launch_quantize_mxfp8(src, rows, cols, q, scale, static_cast<cudaStream_t>(stream));

@@ -88,29 +88,36 @@ __device__ __forceinline__ void quant_block(const uint4 (&v)[4], uint4 (&q)[2], 
   sc = static_cast<uint8_t>(e + 127);
 }
 
-// One thread per 1x32 block.  row_map == nullptr: identity rows (plain
-// quantiser); else source row = table[p].src / K (dispatch with fused
-// quantisation).
+// One thread per (128-column group, row): 4 blocks of 32, their codes and
+// one scale word.  Threads of a warp take consecutive rows of one group, so
+// the scale words ([cols/128][ld], see kernels.h) are written contiguously.
+// table == nullptr: identity rows (plain quantiser); else the source row of
+// row p is table[p].src / K (dispatch with fused quantisation).
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ src,
                                                          const int32_t* __restrict__ table, int K,
-                                                         int64_t rows, int64_t cols,
+                                                         int64_t rows, int64_t cols, int64_t ld,
                                                          uint4* __restrict__ q,
-                                                         uint8_t* __restrict__ scale) {
-  const int64_t nb = cols / 32;
-  const int64_t total = rows * nb;
+                                                         uint32_t* __restrict__ scale) {
+  const int64_t total = rows * (cols / 128);
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = i / nb, blk = i - row * nb;
+    const int64_t grp = i / rows, row = i - grp * rows;
     const int64_t srow = table ? static_cast<int64_t>(__ldg(table + row * 3) / K) : row;
-    const uint4* in = src + (srow * cols + blk * 32) / 8;
-    uint4 v[4] = {ld_nc_v4(in), ld_nc_v4(in + 1), ld_nc_v4(in + 2), ld_nc_v4(in + 3)};
-    uint4 o[2];
-    uint8_t sc;
-    quant_block(v, o, sc);
-    uint4* out = q + (row * cols + blk * 32) / 16;
-    out[0] = o[0];
-    out[1] = o[1];
-    scale[i] = sc;
+    const uint4* in = src + (srow * cols + grp * 128) / 8;
+    uint4* out = q + (row * cols + grp * 128) / 16;
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint4 v[4] = {ld_nc_v4(in + 4 * b), ld_nc_v4(in + 4 * b + 1), ld_nc_v4(in + 4 * b + 2),
+                    ld_nc_v4(in + 4 * b + 3)};
+      uint4 o[2];
+      uint8_t sc;
+      quant_block(v, o, sc);
+      out[2 * b] = o[0];
+      out[2 * b + 1] = o[1];
+      word |= static_cast<uint32_t>(sc) << (8 * b);
+    }
+    scale[grp * ld + row] = word;
   }
 }
 
@@ -221,8 +228,9 @@ mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, 
 mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, int64_t R, int K, int D,
                                  void* xg_q, uint8_t* xg_scale, cudaStream_t st) {
   if (R == 0) return MOK_OK;
-  quant_rows_kernel<<<grid_for(R * (D / 32), 256), 256, 0, st>>>(
-      static_cast<const uint4*>(x), table, K, R, D, static_cast<uint4*>(xg_q), xg_scale);
+  quant_rows_kernel<<<grid_for(R * (D / 128), 256), 256, 0, st>>>(
+      static_cast<const uint4*>(x), table, K, R, D, mx_scale_ld(R), static_cast<uint4*>(xg_q),
+      reinterpret_cast<uint32_t*>(xg_scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -230,8 +238,9 @@ mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, int64_t R,
 mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
                                  uint8_t* scale, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
-  quant_rows_kernel<<<grid_for(rows * (cols / 32), 256), 256, 0, st>>>(
-      static_cast<const uint4*>(src), nullptr, 1, rows, cols, static_cast<uint4*>(q), scale);
+  quant_rows_kernel<<<grid_for(rows * (cols / 128), 256), 256, 0, st>>>(
+      static_cast<const uint4*>(src), nullptr, 1, rows, cols, mx_scale_ld(rows),
+      static_cast<uint4*>(q), reinterpret_cast<uint32_t*>(scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

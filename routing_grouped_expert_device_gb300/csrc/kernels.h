@@ -61,6 +61,21 @@ mok_status launch_router_grad(const float* dgp, int nI, const int32_t* route_dst
                               const int32_t* topk, const float* g, const float* s, int T, int E,
                               int K, float* ds, float* dg, cudaStream_t st);
 
+// MXFP8 scale storage of a [rows][K] tensor: int32 words [K/128][ld],
+// ld = rows rounded up to a multiple of 4; word (g, r) holds the E8M0 scales
+// of row r for K columns [128 g, 128 g + 128), byte b = 32-column block b.
+inline int64_t mx_scale_ld(int64_t rows) { return (rows + 3) & ~int64_t(3); }
+inline size_t mx_scale_bytes(int64_t rows, int64_t K) {
+  return static_cast<size_t>(K / 128) * static_cast<size_t>(mx_scale_ld(rows)) * 4;
+}
+// MXFP8 grouped GEMMs: a codes [rows][I] + scales, y bf16 [rows][D]
+mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
+                            const void* sg, const void* qu, const void* su, const int32_t* offsets,
+                            int G, int D, int I, void* aq, void* asc, cudaStream_t st);
+mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
+                          const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
+                          cudaStream_t st);
+
 bool shape_ok(const mok_shape* s);
 
 }  // namespace mok

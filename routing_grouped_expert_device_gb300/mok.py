@@ -58,7 +58,7 @@ _SIGS = {
     "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
-    "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P]),
+    "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P]),
     "mok_expert_down": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P]),
     "mok_shared_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _SZ, _P]),
     "mok_combine": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
@@ -172,9 +172,10 @@ def expert_ffn(shape: Shape, weights: Weights, xg, offsets, yg, a_out=None, ws=N
                                         _stream(stream)), "mok_expert_ffn")
 
 
-def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None, stream=None):
+def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None, a_scale=None, stream=None):
     _check(_lib_handle().mok_expert_upgate(ctypes.byref(shape), ctypes.byref(weights), _ptr(xg), _ptr(xg_scale),
-                                           _ptr(offsets), _ptr(a), _stream(stream)), "mok_expert_upgate")
+                                           _ptr(offsets), _ptr(a), _ptr(a_scale), _stream(stream)),
+           "mok_expert_upgate")
 
 
 def expert_down(shape: Shape, weights: Weights, a, offsets, yg, a_scale=None, stream=None):
@@ -211,6 +212,16 @@ def quantize_mxfp8(src, q, scale, stream=None):
     rows, cols = src.shape
     _check(_lib_handle().mok_quantize_mxfp8(_ptr(src), rows, cols, _ptr(q), _ptr(scale), _stream(stream)),
            "mok_quantize_mxfp8")
+
+
+def mx_scale_ld(rows: int) -> int:
+    """Row pitch (in 32-bit words) of MXFP8 scale storage: rows rounded up to 4."""
+    return (rows + 3) // 4 * 4
+
+
+def mx_scale_words(rows: int, cols: int) -> int:
+    """32-bit scale words of a [rows][cols] MXFP8 tensor ([cols/128][ld])."""
+    return cols // 128 * mx_scale_ld(rows)
 
 
 def get_error(stream=None) -> int:

@@ -193,3 +193,15 @@ def test_mxfp8_forward_close_to_bf16_forward():
     d = O.mxfp8_dequantize(rq["aq"], rq["asc"])
     assert np.all(np.abs(d - rq["a"]) <= 2.0 ** -4 * np.abs(rq["a"]) + 2.0 ** -10 * 2.0 ** (
         np.repeat(rq["asc"].astype(np.int64) - 127, 32, axis=1)))
+
+
+def test_mxfp8_rows_function_matches_layer_function():
+    cfg = W.CONFIGS["tiny"]
+    inp = _np_inputs(cfg)
+    rq = O.moe_forward_mxfp8(inp, cfg.K)
+    e = 3
+    p0, p1 = rq["offsets"][e], rq["offsets"][e + 1]
+    rows = inp["x"][rq["table"][p0:p1, 0] // cfg.K]
+    r = O.expert_ffn_rows_mxfp8(rows, inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+    assert np.array_equal(r["y"], rq["y"][p0:p1])
+    assert np.array_equal(r["aq"], rq["aq"][p0:p1])

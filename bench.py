@@ -51,7 +51,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=30)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="dsv3_bf16_fwd")
-    p.add_argument("--cpu-sample-tokens", type=int, default=4)
+    p.add_argument("--cpu-sample-tokens", type=int, default=48)
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -215,42 +215,74 @@ def run_ours(args, world, rank, local):
     from routing_grouped_expert_device_gb300 import mok as M
     M._lib_handle()
     cfg = W.CONFIGS[args.config]
-    if cfg.backward or cfg.dtype != "bf16":
-        raise SystemExit(f"config {cfg.name}: bench covers the BF16 forward workloads")
+    mx = cfg.dtype == "mxfp8"
     dev = torch.device("cuda", torch.cuda.current_device())
     d = W.make_inputs(cfg, dev, seed=rank)
     T, D, I, E, K, Is, R = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, cfg.R
     shape = M.shape_of(cfg)
+    i32, f32, bf, u8 = torch.int32, torch.float32, torch.bfloat16, torch.uint8
+    if mx:
+        # weights are model parameters: quantised once, outside the timed region
+        for name, key in (("gate", "w_gate"), ("up", "w_up"), ("down", "w_down")):
+            wt = d[key].reshape(-1, d[key].shape[-1])
+            q = torch.empty(wt.shape, dtype=u8, device=dev)
+            sc = torch.empty(M.mx_scale_words(*wt.shape), dtype=i32, device=dev)
+            M.quantize_mxfp8(wt, q, sc)
+            d["q_" + name], d["sc_" + name] = q, sc
+        torch.cuda.synchronize()
     w = M.make_weights(d)
-    i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
     topk = torch.empty(T, K, dtype=i32, device=dev)
     g = torch.empty(T, K, dtype=f32, device=dev)
     counts = torch.empty(E, dtype=i32, device=dev)
     offsets = torch.empty(E + 1, dtype=i32, device=dev)
     table = torch.empty(R, 3, dtype=i32, device=dev)
     route_dst = torch.empty(R, dtype=i32, device=dev)
-    pws = torch.empty(M.workspace_bytes(shape, M.OP_PLAN), dtype=torch.uint8, device=dev)
-    xg = torch.empty(R, D, dtype=bf, device=dev)
-    a = torch.empty(R, I, dtype=bf, device=dev)
+    pws = torch.empty(M.workspace_bytes(shape, M.OP_PLAN), dtype=u8, device=dev)
+    xg = torch.empty(R, D, dtype=u8 if mx else bf, device=dev)
+    xs = torch.empty(M.mx_scale_words(R, D), dtype=i32, device=dev) if mx else None
+    a = torch.empty(R, I, dtype=u8 if mx else bf, device=dev)
+    asc = torch.empty(M.mx_scale_words(R, I), dtype=i32, device=dev) if mx else None
     yg = torch.empty(R, D, dtype=bf, device=dev)
     ys = torch.empty(T, D, dtype=bf, device=dev) if Is else None
-    sws = torch.empty(M.workspace_bytes(shape, M.OP_SHARED_FFN), dtype=torch.uint8, device=dev)
+    sws = torch.empty(M.workspace_bytes(shape, M.OP_SHARED_FFN), dtype=u8, device=dev)
     out = torch.empty(T, D, dtype=bf, device=dev)
     stream = torch.cuda.current_stream()
     launches_per_step = 1 + 3 + 1 + (2 if Is else 0) + 1 + 1 + 1
 
+    if cfg.backward:
+        bws = torch.empty(max(M.workspace_bytes(shape, M.OP_FWD), M.workspace_bytes(shape, M.OP_BWD)),
+                          dtype=u8, device=dev)
+        saved = dict(topk_idx=topk, g=g, counts=counts, offsets=offsets, table=table, route_dst=route_dst)
+        pb = M.make_plan_buf(saved)
+        gr = dict(dx=torch.empty(T, D, dtype=bf, device=dev), dw_gate=torch.empty(E, I, D, dtype=bf, device=dev),
+                  dw_up=torch.empty(E, I, D, dtype=bf, device=dev), dw_down=torch.empty(E, D, I, dtype=bf, device=dev),
+                  dws_gate=torch.empty(Is, D, dtype=bf, device=dev) if Is else None,
+                  dws_up=torch.empty(Is, D, dtype=bf, device=dev) if Is else None,
+                  dws_down=torch.empty(D, Is, dtype=bf, device=dev) if Is else None,
+                  ds=torch.empty(T, E, dtype=f32, device=dev), dg=torch.empty(T, K, dtype=f32, device=dev))
+        launches_per_step = (1 + 3 + 1 + (2 if Is else 0) + 2 + 1) + (2 + 2 + 1 + 3 + 1 + (5 if Is else 0))
+
     def step(ev0=None, ev1=None):
+        if cfg.backward:
+            M.moe_fwd(shape, w, d["x"], d["s"], out, bws, pb)
+            if ev0 is not None:
+                ev0.record(stream)
+            M.moe_bwd(shape, w, d["x"], d["s"], pb, d["dy"], gr["dx"], gr["dw_gate"], gr["dw_up"],
+                      gr["dw_down"], gr["dws_gate"], gr["dws_up"], gr["dws_down"], gr["ds"], gr["dg"], bws)
+            if ev1 is not None:
+                ev1.record(stream)
+            return
         M.route(d["s"], K, topk, g)
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
-        M.dispatch(shape, d["x"], table, xg)
+        M.dispatch(shape, d["x"], table, xg, xs)
         if Is:
             M.shared_ffn(shape, w, d["x"], ys, sws)
         if ev0 is not None:
             ev0.record(stream)
-        M.expert_upgate(shape, w, xg, offsets, a)
+        M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc)
         if ev1 is not None:
             ev1.record(stream)
-        M.expert_down(shape, w, a, offsets, yg)
+        M.expert_down(shape, w, a, offsets, yg, a_scale=asc)
         M.combine(shape, yg, ys, g, route_dst, out)
 
     for _ in range(args.warmup):
@@ -275,39 +307,67 @@ def run_ours(args, world, rank, local):
     barrier(world)
     M.check_device_status()
     total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world)
-    upgate_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    part_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     ms_step = total_ms / K_steps
     value = world * T * K_steps / (total_ms / 1e3)
-    flops = cfg.fwd_flops()
+    flops = cfg.fwd_flops() + (cfg.bwd_flops() if cfg.backward else 0.0)
     tflops = flops / (ms_step / 1e3) / 1e12
     peaks = measured_peaks()
+    # fp8 dense rate is twice bf16 on this part (nominal 4.5 vs 2.25 PFLOP/s)
+    tensor_peak = peaks["bf16"] * (2.0 if mx else 1.0)
+    wbytes = 1 if mx else 2  # bytes per weight / activation element on the routed path
 
-    # roofline of the dominant kernel: grouped up/gate + SwiGLU (HBM-bound:
-    # each expert's W_gate/W_up tile is read once per 128..256 routed rows)
-    w_bytes = nonempty * 2 * I * D * 2
-    alg_bytes = w_bytes + R * D * 2 + R * I * 2
-    achieved = alg_bytes / (upgate_ms / 1e3) / 1e9
+    if cfg.backward:
+        # the whole backward call (8 + 5 launches): ideal bytes = every weight
+        # read once + every weight gradient written once + x, dY, dX
+        alg_bytes = 2 * (nonempty * 3 * I * D + 3 * Is * D) * 2 + 3 * T * D * 2
+        kernel = "backward (mok_moe_bwd: gathers, dgrad+replay, dx, combine, wgrad, router grad)"
+        part_tflops = cfg.bwd_flops() / (part_ms / 1e3) / 1e12
+    else:
+        # grouped up/gate + SwiGLU: each expert's W_gate/W_up tile is read once
+        # per 128..256 routed rows (HBM-bound below ~290 FLOP/B for bf16)
+        scale_b = (1 / 32) if mx else 0.0
+        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + R * D * wbytes * (1 + scale_b)
+                        + R * I * wbytes * (1 + scale_b))
+        kernel = f"grouped up/gate + SwiGLU GEMM (tcgen05{', MXFP8 block-scaled' if mx else ''})"
+        part_tflops = 4.0 * R * D * I / (part_ms / 1e3) / 1e12
+    achieved = alg_bytes / (part_ms / 1e3) / 1e9
     traffic = recorded_traffic(cfg.name)
-    roofline = {"kernel": "grouped up/gate + SwiGLU GEMM (tcgen05)", "bound": "hbm",
+    roofline = {"kernel": kernel, "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "algorithmic_bytes": alg_bytes, "avg_launch_ms": round(upgate_ms, 4),
-                "peak_source": peaks["source"],
-                "tflops": round(6 * R * D * I * 2 / 3 / (upgate_ms / 1e3) / 1e12, 1)}
+                "algorithmic_bytes": alg_bytes, "avg_launch_ms": round(part_ms, 4),
+                "peak_source": peaks["source"], "tflops": round(part_tflops, 1)}
 
-    # end to end through mok_moe_fwd with host buffers (pinned), copies timed
+    # end to end through the public entry points with pinned host buffers:
+    # the step's inputs are copied in and its result read back every step
     x_h = d["x"].cpu().pin_memory()
     s_h = d["s"].cpu().pin_memory()
     out_h = torch.empty(T, D, dtype=bf, pin_memory=True)
-    ws = torch.empty(M.workspace_bytes(shape, M.OP_FWD), dtype=torch.uint8, device=dev)
+    ws = bws if cfg.backward else torch.empty(M.workspace_bytes(shape, M.OP_FWD), dtype=u8, device=dev)
     x_d = torch.empty_like(d["x"])
     s_d = torch.empty_like(d["s"])
+    h2d = T * D * 2 + T * E * 4
+    d2h = T * D * 2
+    if cfg.backward:
+        dy_h = d["dy"].cpu().pin_memory()
+        dy_d = torch.empty_like(d["dy"])
+        dx_h = torch.empty(T, D, dtype=bf, pin_memory=True)
+        h2d += T * D * 2
+        d2h += T * D * 2
     e2e_steps = max(3, min(K_steps, 100))
 
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
         s_d.copy_(s_h, non_blocking=True)
-        M.moe_fwd(shape, w, x_d, s_d, out, ws)
+        if cfg.backward:
+            dy_d.copy_(dy_h, non_blocking=True)
+            M.moe_fwd(shape, w, x_d, s_d, out, ws, pb)
+            M.moe_bwd(shape, w, x_d, s_d, pb, dy_d, gr["dx"], gr["dw_gate"], gr["dw_up"], gr["dw_down"],
+                      gr["dws_gate"], gr["dws_up"], gr["dws_down"], gr["ds"], gr["dg"], ws)
+            dx_h.copy_(gr["dx"], non_blocking=True)
+        else:
+            M.moe_fwd(shape, w, x_d, s_d, out, ws)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -323,11 +383,10 @@ def run_ours(args, world, rank, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     M.check_device_status()
     e2e = {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": T * D * 2 + T * E * 4, "d2h_bytes_per_step": T * D * 2,
-           "ms_per_step": round(e2e_ms, 4)}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not cfg.backward and not mx:
         tps, dt = oracle_tokens_per_s(cfg, d, args.cpu_sample_tokens)
         cpu = {"value": round(tps, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{args.cpu_sample_tokens} tokens of {cfg.name} (route, {K} routed + shared "
@@ -337,14 +396,17 @@ def run_ours(args, world, rank, local):
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3+e8m0 (routed), bf16 (shared)" if mx else "bf16",
             "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), logits~N(0,1) softmax; bf16)",
             "config": {"workload": cfg.name, "T": T, "D": D, "I": I, "E": E, "K": K, "I_shared": Is,
                        "global_batch": world * T, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: every step streams all expert weights "
                              f"({(nonempty * 3 * I * D + 3 * Is * D) * 2 / 1e9:.1f} GB)"},
-            "tflops": round(tflops, 1), "tensor_frac": round(tflops / peaks["bf16"], 4),
-            "tensor_peak": peaks["bf16"], "tensor_peak_source": peaks["source"] + " burst bf16",
+            "tflops": round(tflops, 1), "tensor_frac": round(tflops / tensor_peak, 4),
+            "tensor_peak": tensor_peak,
+            "tensor_peak_source": peaks["source"] + (" burst bf16 x 2 (fp8)" if mx else " burst bf16"),
+            "pass": "fwd+bwd" if cfg.backward else "fwd",
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_step * K_steps, "clocks": clk,
         }

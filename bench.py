@@ -3,10 +3,11 @@
 
 One step = one forward pass of the whole layer over one batch of synthetic
 tokens: route -> plan -> dispatch -> shared expert -> grouped up/gate +
-SwiGLU -> grouped down -> combine, every kernel launched through the C ABI of
-libmok.so on the current stream (the same kernels, in the same order, as one
-mok_moe_fwd call).  The default workload is the DSV3-shaped BF16 forward
-(T 7168, D 7168, I 2048, 256 experts top-8 + one shared expert, I 2048).
+SwiGLU -> grouped down -> combine, every kernel launched through the C ABI
+of libmok.so on the current stream (the same kernels, in the same order, as
+one mok_moe_fwd call).  The default workload is the DSV3-shaped BF16
+forward (T 7168, D 7168, I 2048, 256 experts top-8 + one shared expert,
+I 2048).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config NAME]
@@ -327,7 +328,8 @@ def run_ours(args, world, rank, local):
         # grouped up/gate + SwiGLU: each expert's W_gate/W_up tile is read once
         # per 128..256 routed rows (HBM-bound below ~290 FLOP/B for bf16)
         scale_b = (1 / 32) if mx else 0.0
-        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + R * D * wbytes * (1 + scale_b)
+        a_rows = R
+        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + a_rows * D * wbytes * (1 + scale_b)
                         + R * I * wbytes * (1 + scale_b))
         kernel = f"grouped up/gate + SwiGLU GEMM (tcgen05{', MXFP8 block-scaled' if mx else ''})"
         part_tflops = 4.0 * R * D * I / (part_ms / 1e3) / 1e12

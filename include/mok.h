@@ -180,6 +180,20 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
 mok_status mok_expert_upgate(const mok_shape *shape, const mok_weights *w, const void *xg,
                              const uint8_t *xg_scale, const int32_t *offsets, void *a,
                              uint8_t *a_scale, void *stream);
+/* mok_expert_upgate with the dispatch fused in (BF16): the grouped operand's
+ * row p is x[table[p].src_index / K], fetched by the GEMM's TMA producer
+ * straight from x bf16 [T][D] into shared memory (blog, "Scheduling":
+ * tokens land where the expert GEMM reads them, zero local copies), so no
+ * gathered copy of x is written (16-byte asynchronous copies, eight lanes per
+ * 128-byte row piece).  table: mok_plan's [R][3].  a bf16 [R][I].
+ * Results are bit-identical to mok_dispatch followed by mok_expert_upgate.
+ * It saves the R x D gathered copy (0.8 GB for the DSV3 shapes) at a cost in
+ * speed: one producer warp feeding 128 scattered rows per K block keeps far
+ * fewer bytes in flight than a tiled TMA load, so mok_moe_fwd uses the
+ * explicit dispatch. */
+mok_status mok_expert_upgate_gather(const mok_shape *shape, const mok_weights *w, const void *x,
+                                    const int32_t *table, const int32_t *offsets, void *a,
+                                    void *stream);
 mok_status mok_expert_down(const mok_shape *shape, const mok_weights *w, const void *a,
                            const uint8_t *a_scale, const int32_t *offsets, void *yg,
                            void *stream);

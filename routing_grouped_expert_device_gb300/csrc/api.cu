@@ -51,7 +51,7 @@ FwdLayout fwd_layout(const mok_shape& s) {
   L.table = c.take(R * 12);
   L.route_dst = c.take(R * 4);
   L.hist = c.take(plan_scratch_bytes(static_cast<int64_t>(R), s.E));
-  L.xg = c.take(R * D * 2);
+  L.xg = c.take(R * D * (s.dtype == MOK_MXFP8 ? 1 : 2));
   const bool mx = s.dtype == MOK_MXFP8;
   L.xg_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D) : 0);
   L.a = c.take(R * I * 2);
@@ -195,6 +195,21 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
     return MOK_ERR_INVALID_ARG;
   return launch_upgate(xg, R, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a,
                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mok_status mok_expert_upgate_gather(const mok_shape* shape, const mok_weights* w,
+                                               const void* x, const int32_t* table,
+                                               const int32_t* offsets, void* a, void* stream) {
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  if (R == 0) return MOK_OK;
+  if (!x || !table || !offsets || !a || !w->w_gate || !w->w_up || !aligned16(x) || !aligned16(a) ||
+      !aligned16(w->w_gate) || !aligned16(w->w_up))
+    return MOK_ERR_INVALID_ARG;
+  return launch_upgate(x, s.T, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a,
+                       static_cast<cudaStream_t>(stream), table, s.K);
 }
 
 extern "C" mok_status mok_expert_down(const mok_shape* shape, const mok_weights* w, const void* a,

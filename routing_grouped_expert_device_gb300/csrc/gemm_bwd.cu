@@ -32,6 +32,7 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t a) { return sdesc_sw128(a, M
 struct DgradCfg {
   static constexpr int STAGES = 2;
   static constexpr int STAGE_BYTES = 4 * KTILE + 2 * MNCHUNK;  // 80 KB
+  static constexpr int EPI_SMEM_BYTES = 0;
   static constexpr int NUM_ACC = 1;
   static constexpr int ACC_COLS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -50,8 +51,12 @@ struct DgradCfg {
     float* dgp;              // [rows][I/128] or null
   };
 
+  __device__ static uint32_t full_arrivals(const Params&) { return 1; }
+  __device__ static uint32_t tx_bytes(const Params&) { return STAGE_BYTES; }
+
   __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
-                              uint64_t* bar) {
+                              uint64_t* bar, int lane) {
+    if (lane != 0) return;
     const int k0 = kb * BK;
     const int r = c.row0 + c.mt * BM;
     const int wrow = c.g * P.I + c.nt * 128;
@@ -79,7 +84,7 @@ struct DgradCfg {
   }
 
   __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
-                                  int lane, bool) {
+                                  int lane, bool, uint8_t*) {
     const int r = ew * 32 + lane;
     const bool valid = c.mt * BM + r < c.rows;
     const int64_t row = c.row0 + c.mt * BM + r;
@@ -131,6 +136,7 @@ struct DgradCfg {
 struct DxCfg {
   static constexpr int STAGES = 4;
   static constexpr int STAGE_BYTES = KTILE + 4 * MNCHUNK;  // 48 KB
+  static constexpr int EPI_SMEM_BYTES = 0;
   static constexpr int NUM_ACC = 2;
   static constexpr int ACC_COLS = 256;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -146,8 +152,12 @@ struct DxCfg {
     int32_t out_ld;
   };
 
+  __device__ static uint32_t full_arrivals(const Params&) { return 1; }
+  __device__ static uint32_t tx_bytes(const Params&) { return STAGE_BYTES; }
+
   __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
-                              uint64_t* bar) {
+                              uint64_t* bar, int lane) {
+    if (lane != 0) return;
     const bool up = kb >= P.half_kb;
     const int k0 = (up ? kb - P.half_kb : kb) * BK;
     tma_load_2d(st, up ? &P.tmDu : &P.tmDh, k0, c.row0 + c.mt * BM, bar);
@@ -167,7 +177,7 @@ struct DxCfg {
   }
 
   __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
-                                  int lane, bool) {
+                                  int lane, bool, uint8_t*) {
     const int r = ew * 32 + lane;
     const bool valid = c.mt * BM + r < c.rows;
     __nv_bfloat16* orow =
@@ -196,8 +206,11 @@ struct DxCfg {
 template <int BN>
 struct WgradCfg {
   static constexpr int NB = BN / 64;  // 64-wide MN chunks of B
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = 3;  // K loops are short (rows per expert / 64)
   static constexpr int STAGE_BYTES = (2 + NB) * MNCHUNK;
+  // per epilogue warp: two staging blocks of 32 rows x 64 columns of bf16,
+  // 128-byte swizzled, each the source of one TMA store
+  static constexpr int EPI_SMEM_BYTES = 4 * 2 * 32 * 128;
   static constexpr int NUM_ACC = 2;
   static constexpr int ACC_COLS = BN;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -208,12 +221,17 @@ struct WgradCfg {
     int* status;
     CUtensorMap tmA;  // [rows][M], MN-major boxes 64 x 64
     CUtensorMap tmB;  // [rows][N], MN-major boxes 64 x 64
+    CUtensorMap tmOut;  // dW as [G*M][N], boxes 32 rows x 64 columns, 128-byte swizzle
     int32_t M, N;
     __nv_bfloat16* out;  // [G][M][N]
   };
 
+  __device__ static uint32_t full_arrivals(const Params&) { return 1; }
+  __device__ static uint32_t tx_bytes(const Params&) { return STAGE_BYTES; }
+
   __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
-                              uint64_t* bar) {
+                              uint64_t* bar, int lane) {
+    if (lane != 0) return;
     const int rk = c.row0 + kb * BK;
 #pragma unroll
     for (int j = 0; j < 2; ++j) tma_load_2d(st + j * MNCHUNK, &P.tmA, c.mt * 128 + 64 * j, rk, bar);
@@ -246,28 +264,48 @@ struct WgradCfg {
       mma_bf16(d, mndesc(s + k * 2048), mndesc(s + 2 * MNCHUNK + k * 2048), IDESC, (kb | k) != 0);
   }
 
+  // Each warp converts its 32 rows x 64 columns to bf16, writes them to its
+  // staging block in the 128-byte swizzle the store's tensor map expects
+  // (16-byte chunk c of row r at chunk c ^ (r % 8)) and issues one TMA store,
+  // so every store instruction moves whole rows instead of 16 bytes of 32
+  // different rows.  All wgrad tiles are full, so no row needs masking.
   __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
-                                  int lane, bool has_acc) {
-    const int r = ew * 32 + lane;
-    __nv_bfloat16* orow = P.out + static_cast<size_t>(c.g) * P.M * P.N +
-                          static_cast<size_t>(c.mt * 128 + r) * P.N + c.nt * BN;
+                                  int lane, bool has_acc, uint8_t* epi) {
+    const int y = c.g * P.M + c.mt * 128 + ew * 32;
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 32; ++ch) {
-      uint32_t pk[16];
+    for (int cp = 0; cp < BN / 64; ++cp) {
+      uint32_t pk[32];
       if (has_acc) {
         uint32_t v[32];
-        tmem_ld32(taddr + ch * 32, v);
-        tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        for (int h = 0; h < 2; ++h) {
+          tmem_ld32(taddr + cp * 64 + h * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = 0u;
+        for (int j = 0; j < 32; ++j) pk[j] = 0u;
       }
+      // the store that last used this staging block (two stores back) has
+      // finished reading it
+      if (lane == 0) bulk_wait_read1();
+      __syncwarp();
+      uint8_t* blk = epi + (cp & 1) * 4096;
+      uint8_t* row = blk + lane * 128;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4* dst = reinterpret_cast<uint4*>(row + ((ch ^ (lane & 7)) * 16));
+        *dst = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&P.tmOut, blk, c.nt * BN + cp * 64, y);
+        bulk_commit();
+      }
     }
   }
 };
@@ -370,7 +408,10 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int64_t map_rows = rows > 0 ? rows : 1;
-  if (!mnmap(&P.tmA, pm, map_rows, M) || !mnmap(&P.tmB, qn, map_rows, N)) return MOK_ERR_CUDA;
+  if (!mnmap(&P.tmA, pm, map_rows, M) || !mnmap(&P.tmB, qn, map_rows, N) ||
+      !make_tmap_2d(&P.tmOut, dw, kBF16, static_cast<uint64_t>(s.G) * M, N,
+                    static_cast<uint64_t>(N) * 2, 32, 64, true))
+    return MOK_ERR_CUDA;
   P.M = M;
   P.N = N;
   P.out = static_cast<__nv_bfloat16*>(dw);

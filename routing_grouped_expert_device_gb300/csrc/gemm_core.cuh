@@ -102,24 +102,28 @@ __device__ __forceinline__ TileCoord decode_tile(const SchedArgs& s, const int* 
   return c;
 }
 
+// Shared memory: [STAGES x STAGE_BYTES][1 KB barriers and flags]
+// [EPI_SMEM_BYTES epilogue staging, 1 KB aligned][tile table].
 template <class Cfg>
 constexpr size_t gemm_smem_bytes(int G) {
   return 1024 /*alignment slack*/ + static_cast<size_t>(Cfg::STAGES) * Cfg::STAGE_BYTES +
-         256 /*barriers and flags*/ + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+         1024 /*barriers and flags*/ + Cfg::EPI_SMEM_BYTES + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
 // Cfg interface:
 //   STAGES, STAGE_BYTES, NUM_ACC (1|2), ACC_COLS (TMEM columns per buffer),
+//   full_arrivals(P) / tx_bytes(P): arrivals and TMA bytes that complete a stage,
 //   TMEM_COLS (power of two >= NUM_ACC*ACC_COLS)
 //   struct Params { SchedArgs sched; int* status; ... }
 //   static __device__ void load(const Params&, const TileCoord&, int kb, uint8_t* stage,
-//                               uint64_t* full_bar);              // lane 0 of warp 0
+//                               uint64_t* full_bar, int lane);    // all lanes of warp 0
 //   static __device__ void fixup(const Params&, const TileCoord&, int kb, uint8_t* stage,
 //                                int lane);                       // whole warp 1
 //   static __device__ void mma(const Params&, const TileCoord&, int kb, uint8_t* stage,
 //                              uint32_t d_tmem);                  // lane 0 of warp 1
+//   EPI_SMEM_BYTES: shared staging for the epilogue (a quarter per epilogue warp)
 //   static __device__ void epilogue(const Params&, const TileCoord&, uint32_t taddr, int ew,
-//                                   int lane, bool has_acc);      // warps 4..7
+//                                   int lane, bool has_acc, uint8_t* epi);  // warps 4..7
 template <class Cfg>
 __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant__ typename Cfg::Params P) {
   extern __shared__ uint8_t smem_raw[];
@@ -133,7 +137,8 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
-  int* tstart = reinterpret_cast<int*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES + 256);
+  uint8_t* epi_smem = smem + Cfg::STAGES * Cfg::STAGE_BYTES + 1024;
+  int* tstart = reinterpret_cast<int*>(epi_smem + Cfg::EPI_SMEM_BYTES);
   int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::STAGES; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], Cfg::full_arrivals(P));
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -165,37 +170,38 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t issued_parity[Cfg::STAGES];
-      bool issued[Cfg::STAGES];
-      for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = false;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
-        for (int kb = 0; kb < c.kblocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
-          Cfg::load(P, c, kb, smem + stage * Cfg::STAGE_BYTES, &full[stage]);
-          issued[stage] = true;
-          issued_parity[stage] = phase;
-          if (++stage == Cfg::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+    // Lane 0 waits for a free stage and arms its barrier; then every lane
+    // may issue copies into it (Cfg::load decides which lanes do).
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_parity[Cfg::STAGES];
+    bool issued[Cfg::STAGES];
+    for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = false;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      for (int kb = 0; kb < c.kblocks; ++kb) {
+        bool got = false;
+        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER);
+        ok = __shfl_sync(0xffffffffu, got, 0);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], Cfg::tx_bytes(P));
+        __syncwarp();
+        Cfg::load(P, c, kb, smem + stage * Cfg::STAGE_BYTES, &full[stage], lane);
+        issued[stage] = true;
+        issued_parity[stage] = phase;
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1;
         }
       }
-      if (!ok) {
-        // Let every load this thread issued land before the CTA exits.
-        for (int i = 0; i < Cfg::STAGES; ++i) {
-          if (!issued[i]) continue;
-          const uint64_t t0 = globaltimer();
-          while (!mbar_try_wait(&full[i], issued_parity[i]) &&
-                 globaltimer() - t0 < kWaitBudgetNs) {
-          }
+    }
+    if (!ok && lane == 0) {
+      // Let every load issued into a stage land before the CTA exits.
+      for (int i = 0; i < Cfg::STAGES; ++i) {
+        if (!issued[i]) continue;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&full[i], issued_parity[i]) &&
+               globaltimer() - t0 < kWaitBudgetNs) {
         }
       }
     }
@@ -256,10 +262,12 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
         break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * Cfg::ACC_COLS + (static_cast<uint32_t>(ew * 32) << 16);
-      Cfg::epilogue(P, c, taddr, ew, lane, c.kblocks > 0);
+      Cfg::epilogue(P, c, taddr, ew, lane, c.kblocks > 0, epi_smem + ew * (Cfg::EPI_SMEM_BYTES / 4));
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    // bulk stores issued from staging must finish before shared memory goes
+    if (Cfg::EPI_SMEM_BYTES > 0 && lane == 0) bulk_wait0();
   }
 
   tc_fence_before();

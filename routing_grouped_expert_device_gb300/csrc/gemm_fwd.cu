@@ -23,6 +23,7 @@ struct FwdCfg {
   static constexpr int A_BYTES = BM * BK * 2;    // 16 KB
   static constexpr int B_HALF = 128 * BK * 2;    // 16 KB
   static constexpr int STAGE_BYTES = A_BYTES + 2 * B_HALF;
+  static constexpr int EPI_SMEM_BYTES = 0;
   static constexpr int NUM_ACC = 2;
   static constexpr int ACC_COLS = 256;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -31,7 +32,7 @@ struct FwdCfg {
   struct Params {
     SchedArgs sched;
     int* status;
-    CUtensorMap tmA;   // activations [rows][K]
+    CUtensorMap tmA;   // activations [rows][K]; with gtable: x [T][D], boxes one row high
     CUtensorMap tmB0;  // up/gate: W_gate [E*I][D]; down: W_down [E*D][I]
     CUtensorMap tmB1;  // up/gate: W_up;           down: W_down again
     int32_t b_group_rows;  // weight rows per expert (I or D)
@@ -39,18 +40,59 @@ struct FwdCfg {
     int32_t b1_off;        // row offset of the second B half (0 or 128)
     __nv_bfloat16* out;
     int32_t out_ld;
+    const int32_t* gtable;  // non-null: A row p is x[gtable[3 p] / gK] (fused dispatch)
+    int32_t gK;
+    const void* gx;          // x [T][D] bf16
+    int64_t gld;             // x row pitch in bytes
   };
 
+  // Fused dispatch: A arrives by cp.async (one arrival per producer lane),
+  // only B by TMA.
+  __device__ static uint32_t full_arrivals(const Params& P) { return P.gtable ? 33u : 1u; }
+  __device__ static uint32_t tx_bytes(const Params& P) {
+    return P.gtable ? static_cast<uint32_t>(2 * B_HALF) : static_cast<uint32_t>(STAGE_BYTES);
+  }
+
   __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
-                              uint64_t* bar) {
+                              uint64_t* bar, int lane) {
     const int k0 = kb * BK;
-    tma_load_2d(st, &P.tmA, k0, c.row0 + c.mt * BM, bar);
+    if (P.gtable) {
+      // Fused dispatch (Mixture-of-Kittens blog, "Scheduling": tokens land
+      // expert-contiguous with zero local copies): the producer warp copies
+      // the tile's 128 token rows (64 columns each) straight from x into the
+      // stage, already in the 128-byte swizzle the MMA reads.  Eight lanes
+      // cover one 128-byte row, so each instruction moves 4 whole rows.
+      // Rows past the expert's end read token 0; their results are dropped.
+      const int p0 = c.row0 + c.mt * BM;
+      const int end = c.row0 + c.rows;
+      int32_t tok[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int p = p0 + lane + 32 * j;
+        tok[j] = p < end ? __ldg(P.gtable + 3 * p) / P.gK : 0;
+      }
+      const int chunk = lane & 7;
+      const uint8_t* xb = reinterpret_cast<const uint8_t*>(P.gx) + static_cast<int64_t>(k0) * 2 + chunk * 16;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int row = 4 * i + (lane >> 3);
+        const int t = __shfl_sync(0xffffffffu, tok[i >> 3], row & 31);
+        cp_async16(st + row * 128 + ((chunk ^ (row & 7)) << 4), xb + static_cast<int64_t>(t) * P.gld);
+      }
+      cp_async_arrive(bar);
+    }
+    if (lane != 0) return;
+    if (!P.gtable) tma_load_2d(st, &P.tmA, k0, c.row0 + c.mt * BM, bar);
     const int brow = c.g * P.b_group_rows + c.nt * P.b_tile_rows;
     tma_load_2d(st + A_BYTES, &P.tmB0, k0, brow, bar);
     tma_load_2d(st + A_BYTES + B_HALF, &P.tmB1, k0, brow + P.b1_off, bar);
   }
 
-  __device__ static void fixup(const Params&, const TileCoord&, int, uint8_t*, int) {}
+  // Rows copied by cp.async (generic proxy) are read by the tensor core
+  // (async proxy).
+  __device__ static void fixup(const Params& P, const TileCoord&, int, uint8_t*, int) {
+    if (P.gtable) fence_proxy_async_smem();
+  }
 
   __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
     const uint32_t a = smem_u32(st);
@@ -64,7 +106,7 @@ struct FwdCfg {
   }
 
   __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
-                                  int lane, bool) {
+                                  int lane, bool, uint8_t*) {
     const int r = ew * 32 + lane;
     const bool valid = c.mt * BM + r < c.rows;
     __nv_bfloat16* orow = P.out + static_cast<size_t>(c.row0 + c.mt * BM + r) * P.out_ld;
@@ -144,9 +186,13 @@ SchedArgs fwd_sched(const int32_t* offsets, int G, int64_t m_total, int n_tiles,
 
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st) {
-  if (a_rows == 0) return MOK_OK;
+                         cudaStream_t st, const int32_t* gather_table, int gather_k) {
+  if (a_rows == 0 || m_total == 0) return MOK_OK;
   UpGate::Params P;
+  P.gtable = gather_table;
+  P.gK = gather_k;
+  P.gx = A;
+  P.gld = static_cast<int64_t>(D) * 2;
   P.sched = fwd_sched(offsets, G, m_total, I / 128, D / BK);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
@@ -180,6 +226,10 @@ mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const 
                     static_cast<uint64_t>(I) * 2, 128, BK, true))
     return MOK_ERR_CUDA;
   P.tmB1 = P.tmB0;
+  P.gtable = nullptr;
+  P.gK = 1;
+  P.gx = nullptr;
+  P.gld = 0;
   P.b_group_rows = D;
   P.b_tile_rows = 256;
   P.b1_off = 128;

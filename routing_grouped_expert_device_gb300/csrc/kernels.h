@@ -37,9 +37,12 @@ mok_status launch_combine(const void* rows, const void* base, const float* w,
 // Forward grouped GEMMs.  offsets == nullptr: one group of m_total rows.
 //  up/gate: a[rows][I] = bf16(SiLU(A W_gate^T) * (A W_up^T)), A [rows][D]
 //  down   : y[rows][D] = bf16(a W_down^T)
+// gather_table non-null: A is x [a_rows = T][D] and row p of the grouped
+// operand is x[gather_table[3 p] / gather_k] (the dispatch fused into the TMA
+// loads); m_total is then R.
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st);
+                         cudaStream_t st, const int32_t* gather_table = nullptr, int gather_k = 1);
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
 

@@ -59,6 +59,8 @@ _SIGS = {
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
     "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P]),
+    "mok_expert_upgate_gather": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P,
+                                                _P]),
     "mok_expert_down": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P]),
     "mok_shared_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _SZ, _P]),
     "mok_combine": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
@@ -176,6 +178,12 @@ def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None,
     _check(_lib_handle().mok_expert_upgate(ctypes.byref(shape), ctypes.byref(weights), _ptr(xg), _ptr(xg_scale),
                                            _ptr(offsets), _ptr(a), _ptr(a_scale), _stream(stream)),
            "mok_expert_upgate")
+
+
+def expert_upgate_gather(shape: Shape, weights: Weights, x, table, offsets, a, stream=None):
+    _check(_lib_handle().mok_expert_upgate_gather(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(table),
+                                                  _ptr(offsets), _ptr(a), _stream(stream)),
+           "mok_expert_upgate_gather")
 
 
 def expert_down(shape: Shape, weights: Weights, a, offsets, yg, a_scale=None, stream=None):

@@ -155,7 +155,6 @@ struct FwdCfg {
 };
 
 using UpGate = FwdCfg<true>;
-using Down = FwdCfg<false>;
 
 template <class Cfg>
 mok_status run(const typename Cfg::Params& P, int G, cudaStream_t st) {
@@ -188,6 +187,7 @@ mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, cons
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
                          cudaStream_t st, const int32_t* gather_table, int gather_k) {
   if (a_rows == 0 || m_total == 0) return MOK_OK;
+  if (!gather_table) return launch_upgate_pair(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st);
   UpGate::Params P;
   P.gtable = gather_table;
   P.gK = gather_k;
@@ -214,28 +214,7 @@ mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, cons
 
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st) {
-  if (a_rows == 0) return MOK_OK;
-  Down::Params P;
-  P.sched = fwd_sched(offsets, G, m_total, D / 256, I / BK);
-  P.status = status_ptr();
-  if (!P.status) return MOK_ERR_CUDA;
-  const int groups = offsets ? G : 1;
-  const auto bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_tmap_2d(&P.tmA, a, bf16, a_rows, I, static_cast<uint64_t>(I) * 2, BM, BK, true) ||
-      !make_tmap_2d(&P.tmB0, w_down, bf16, static_cast<uint64_t>(groups) * D, I,
-                    static_cast<uint64_t>(I) * 2, 128, BK, true))
-    return MOK_ERR_CUDA;
-  P.tmB1 = P.tmB0;
-  P.gtable = nullptr;
-  P.gK = 1;
-  P.gx = nullptr;
-  P.gld = 0;
-  P.b_group_rows = D;
-  P.b_tile_rows = 256;
-  P.b1_off = 128;
-  P.out = static_cast<__nv_bfloat16*>(y_out);
-  P.out_ld = D;
-  return run<Down>(P, P.sched.G, st);
+  return launch_down_pair(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st);
 }
 
 }  // namespace mok

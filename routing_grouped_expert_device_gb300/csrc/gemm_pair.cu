@@ -1,0 +1,368 @@
+// Forward grouped expert GEMMs on CTA pairs (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs on two SMs computes one 256-row x 256-column tile:
+// CTA rank r loads rows [128 r, 128 r + 128) of the tile's A operand and
+// half of the B operand (up/gate: rank 0 the 128 W_gate rows, rank 1 the 128
+// W_up rows; down: output columns [128 r, 128 r + 128)), and the leader
+// (rank 0) issues M256 N256 MMAs that read both CTAs' shared memory and
+// write each CTA's 128 rows of the accumulator into that CTA's TMEM.  Each
+// expert's weight tile therefore crosses L2 once per 256 routed rows, and an
+// SM fills 32 KB of shared memory per 64-wide K block instead of 48 KB.
+//
+// Barriers: both CTAs' TMA loads complete on the leader's full[stage]
+// (armed by the leader for both halves); MMA completion is multicast to
+// both CTAs' empty[stage] and tfull[acc]; both CTAs' epilogues arrive on the
+// leader's tempty[acc].  Every wait is bounded as in gemm_core.cuh.
+#include "gemm_core.cuh"
+#include "kernels.h"
+
+namespace mok {
+namespace {
+
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;  // this CTA's 128 rows
+constexpr int B_BYTES = 128 * BK * 2;  // this CTA's half of B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t IDESC = idesc_bf16(256, 256, false, false);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t* holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(holder)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void mma2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` (same offset) in every CTA of `mask` once this thread's
+// earlier tcgen05 operations have completed.
+__device__ __forceinline__ void commit2(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+// TMA 2D load into this CTA's shared memory, completing on an mbarrier that
+// may live in the peer CTA (leader_bar is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, int32_t x, int32_t y,
+                                                 uint32_t leader_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(leader_bar)
+      : "memory");
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+struct PairParams {
+  SchedArgs sched;  // bm = 256: one tile = 256 rows of one group
+  int* status;
+  CUtensorMap tmA;   // activations [rows][K], boxes 128 x 64
+  CUtensorMap tmB0;  // B half of rank 0, boxes 128 x 64
+  CUtensorMap tmB1;  // B half of rank 1
+  int32_t b_group_rows, b_tile_rows, b1_off;
+  __nv_bfloat16* out;
+  int32_t out_ld;
+};
+
+template <bool kSwiglu>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    gemm_pair_persistent(const __grid_constant__ PairParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
+  int* tstart = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 1024);
+  int* rstart = tstart + (P.sched.G + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 256);  // both CTAs' 128 epilogue threads
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) tmem_alloc2(tmem_holder, 512);
+  if (warp == 3) {
+    const int total = build_tile_table(P.sched, tstart, rstart, lane);
+    if (lane == 0) *total_holder = total;
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *total_holder;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued[i] = false;
+      bool ok = true;
+      const CUtensorMap* tmB = rank ? &P.tmB1 : &P.tmB0;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        const int arow = c.row0 + c.mt * 256 + static_cast<int>(rank) * 128;
+        const int brow = c.g * P.b_group_rows + c.nt * P.b_tile_rows + (rank ? P.b1_off : 0);
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+          const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
+          uint8_t* st = smem + stage * STAGE_BYTES;
+          tma_load_2d_pair(st, &P.tmA, kb * BK, arow, lbar);
+          tma_load_2d_pair(st + A_BYTES, tmB, kb * BK, brow, lbar);
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok && leader) {
+        for (int i = 0; i < STAGES; ++i) {
+          if (!issued[i]) continue;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&full[i], issued_parity[i]) && globaltimer() - t0 < kWaitBudgetNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader only) ----------------
+    if (leader) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true, any = false;
+      int it = 0;
+      for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
+        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        const uint32_t acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, P.status, SITE_MMA));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * 256;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t b = a + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma2(d, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024), (kb | k) != 0);
+            commit2(&empty[stage], 0x3);
+            any = true;
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) commit2(&tfull[acc], 0x3);
+        __syncwarp();
+      }
+      any = __shfl_sync(0xffffffffu, any, 0);
+      if (any) {
+        if (lane == 0) commit2(drain, 0x1);
+        __syncwarp();
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitBudgetNs) {
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue (both CTAs, own 128 rows) ----------------
+    const int ew = warp - 4;
+    int it = 0;
+    for (int tile = cid; tile < total; tile += ncl, ++it) {
+      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      const uint32_t acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, P.status, SITE_EPILOGUE)))
+        break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(ew * 32) << 16);
+      const int r = static_cast<int>(rank) * 128 + ew * 32 + lane;  // row within the 256-row tile
+      const bool valid = c.mt * 256 + r < c.rows;
+      __nv_bfloat16* orow = P.out + static_cast<size_t>(c.row0 + c.mt * 256 + r) * P.out_ld;
+      if (kSwiglu) {
+        orow += c.nt * 128;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t h[32], u[32];
+          tmem_ld32(taddr + ch * 32, h);
+          tmem_ld32(taddr + 128 + ch * 32, u);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(silu_f(__uint_as_float(h[2 * j])) * __uint_as_float(u[2 * j]),
+                                silu_f(__uint_as_float(h[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      } else {
+        orow += c.nt * 256;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(taddr + ch * 32, v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          if (valid) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      if (leader) mbar_arrive(&tempty[acc]);
+      else remote_arrive(map_to_rank(smem_u32(&tempty[acc]), 0));
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync();  // the leader's MMAs (which read the peer's shared memory) and all remote arrivals are done
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc2(tmem_base, 512);
+}
+
+size_t pair_smem_bytes(int G) {
+  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+}
+
+template <bool kSwiglu>
+mok_status run_pair(const PairParams& P, cudaStream_t st) {
+  const size_t smem = pair_smem_bytes(P.sched.G);
+  if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(gemm_pair_persistent<kSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  const int grid = (num_sms() / 2) * 2;
+  gemm_pair_persistent<kSwiglu><<<grid, 256, smem, st>>>(P);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+SchedArgs pair_sched(const int32_t* offsets, int G, int64_t m_total, int n_tiles, int k_blocks) {
+  SchedArgs s;
+  s.offsets = offsets;
+  s.G = offsets ? G : 1;
+  s.m_total = static_cast<int32_t>(m_total);
+  s.n_tiles = n_tiles;
+  s.m_tiles_fixed = 0;
+  s.k_blocks_fixed = k_blocks;
+  s.bm = 256;
+  s.bk_rows = BK;
+  return s;
+}
+
+constexpr auto kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+}  // namespace
+
+mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
+                              const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
+                              cudaStream_t st) {
+  if (a_rows == 0 || m_total == 0) return MOK_OK;
+  PairParams P;
+  P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const int groups = offsets ? G : 1;
+  if (!make_tmap_2d(&P.tmA, A, kBF16, a_rows, D, static_cast<uint64_t>(D) * 2, 128, BK, true) ||
+      !make_tmap_2d(&P.tmB0, w_gate, kBF16, static_cast<uint64_t>(groups) * I, D, static_cast<uint64_t>(D) * 2,
+                    128, BK, true) ||
+      !make_tmap_2d(&P.tmB1, w_up, kBF16, static_cast<uint64_t>(groups) * I, D, static_cast<uint64_t>(D) * 2,
+                    128, BK, true))
+    return MOK_ERR_CUDA;
+  P.b_group_rows = I;
+  P.b_tile_rows = 128;
+  P.b1_off = 0;
+  P.out = static_cast<__nv_bfloat16*>(a_out);
+  P.out_ld = I;
+  return run_pair<true>(P, st);
+}
+
+mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
+                            int64_t m_total, int D, int I, void* y_out, cudaStream_t st) {
+  if (a_rows == 0 || m_total == 0) return MOK_OK;
+  PairParams P;
+  P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const int groups = offsets ? G : 1;
+  if (!make_tmap_2d(&P.tmA, a, kBF16, a_rows, I, static_cast<uint64_t>(I) * 2, 128, BK, true) ||
+      !make_tmap_2d(&P.tmB0, w_down, kBF16, static_cast<uint64_t>(groups) * D, I, static_cast<uint64_t>(I) * 2,
+                    128, BK, true))
+    return MOK_ERR_CUDA;
+  P.tmB1 = P.tmB0;
+  P.b_group_rows = D;
+  P.b_tile_rows = 256;
+  P.b1_off = 128;
+  P.out = static_cast<__nv_bfloat16*>(y_out);
+  P.out_ld = D;
+  return run_pair<false>(P, st);
+}
+
+}  // namespace mok

@@ -2,8 +2,9 @@
 """Throughput of the single-GPU MoE layer (tokens/s, TFLOP/s, % of peak).
 
 One step = one forward pass of the whole layer over one batch of synthetic
-tokens: route -> plan -> dispatch -> shared expert -> grouped up/gate +
-SwiGLU -> grouped down -> combine, every kernel launched through the C ABI
+tokens: route -> plan -> dispatch -> grouped up/gate + SwiGLU -> grouped
+down -> combine (the shared expert's tiles run inside the two grouped
+launches), every kernel launched through the C ABI
 of libmok.so on the current stream (the same kernels, in the same order, as
 one mok_moe_fwd call).  The default workload is the DSV3-shaped BF16
 forward (T 7168, D 7168, I 2048, 256 experts top-8 + one shared expert,
@@ -245,10 +246,10 @@ def run_ours(args, world, rank, local):
     asc = torch.empty(M.mx_scale_words(R, I), dtype=i32, device=dev) if mx else None
     yg = torch.empty(R, D, dtype=bf, device=dev)
     ys = torch.empty(T, D, dtype=bf, device=dev) if Is else None
-    sws = torch.empty(M.workspace_bytes(shape, M.OP_SHARED_FFN), dtype=u8, device=dev)
+    a_s = torch.empty(T, Is, dtype=bf, device=dev) if Is else None
     out = torch.empty(T, D, dtype=bf, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 1 + 3 + 1 + (2 if Is else 0) + 1 + 1 + 1
+    launches_per_step = 1 + 3 + 1 + 1 + 1 + 1 + (2 if (Is and mx) else 0)
 
     if cfg.backward:
         bws = torch.empty(max(M.workspace_bytes(shape, M.OP_FWD), M.workspace_bytes(shape, M.OP_BWD)),
@@ -261,7 +262,7 @@ def run_ours(args, world, rank, local):
                   dws_up=torch.empty(Is, D, dtype=bf, device=dev) if Is else None,
                   dws_down=torch.empty(D, Is, dtype=bf, device=dev) if Is else None,
                   ds=torch.empty(T, E, dtype=f32, device=dev), dg=torch.empty(T, K, dtype=f32, device=dev))
-        launches_per_step = (1 + 3 + 1 + (2 if Is else 0) + 2 + 1) + (2 + 2 + 1 + 3 + 1 + (5 if Is else 0))
+        launches_per_step = (1 + 3 + 1 + 2 + 1) + (2 + 2 + 1 + 3 + 1 + (5 if Is else 0))
 
     def step(ev0=None, ev1=None):
         if cfg.backward:
@@ -276,14 +277,14 @@ def run_ours(args, world, rank, local):
         M.route(d["s"], K, topk, g)
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
         M.dispatch(shape, d["x"], table, xg, xs)
-        if Is:
-            M.shared_ffn(shape, w, d["x"], ys, sws)
         if ev0 is not None:
             ev0.record(stream)
-        M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc)
+        # the shared expert's tiles run inside the routed launches
+        M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc, x_shared=d["x"] if Is else None,
+                        a_shared=a_s)
         if ev1 is not None:
             ev1.record(stream)
-        M.expert_down(shape, w, a, offsets, yg, a_scale=asc)
+        M.expert_down(shape, w, a, offsets, yg, a_scale=asc, a_shared=a_s, ys=ys)
         M.combine(shape, yg, ys, g, route_dst, out)
 
     for _ in range(args.warmup):
@@ -328,11 +329,15 @@ def run_ours(args, world, rank, local):
         # grouped up/gate + SwiGLU: each expert's W_gate/W_up tile is read once
         # per 128..256 routed rows (HBM-bound below ~290 FLOP/B for bf16)
         scale_b = (1 / 32) if mx else 0.0
-        a_rows = R
-        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + a_rows * D * wbytes * (1 + scale_b)
+        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + R * D * wbytes * (1 + scale_b)
                         + R * I * wbytes * (1 + scale_b))
-        kernel = f"grouped up/gate + SwiGLU GEMM (tcgen05{', MXFP8 block-scaled' if mx else ''})"
-        part_tflops = 4.0 * R * D * I / (part_ms / 1e3) / 1e12
+        part_flops = 4.0 * R * D * I
+        if Is and not mx:  # the shared expert's up/gate runs in the same launch
+            alg_bytes += 2 * Is * D * 2 + T * D * 2 + T * Is * 2
+            part_flops += 4.0 * T * D * Is
+        kernel = (f"grouped up/gate + SwiGLU GEMM (tcgen05 {'MXFP8 block-scaled' if mx else 'cta_group::2'}"
+                  f"{', shared expert tiles in the same launch' if Is and not mx else ''})")
+        part_tflops = part_flops / (part_ms / 1e3) / 1e12
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
     traffic = recorded_traffic(cfg.name)
     roofline = {"kernel": kernel, "bound": "hbm",

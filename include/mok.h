@@ -176,10 +176,16 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
  * mok_expert_down: yg = bf16(a W_down^T) [R][D].  Same rules as
  * mok_expert_ffn.  For MOK_MXFP8, a is written as codes [R][I] plus scale
  * words a_scale ([I/128][ld], ld = R rounded up to 4) and read back that way
- * by mok_expert_down; xg_scale / a_scale are ignored for BF16. */
+ * by mok_expert_down; xg_scale / a_scale are ignored for BF16.
+ * Shared expert in the same launch (paper note, "The production details":
+ * the shared expert fills compute while routed rows stream): when
+ * shape.I_shared > 0 and x_shared / a_shared (resp. a_shared / ys) are
+ * non-NULL, the shared expert's up/gate (x_shared bf16 [T][D] -> a_shared
+ * bf16 [T][I_shared]) or down (a_shared -> ys bf16 [T][D]) tiles are spread
+ * through the routed launch (BF16; after the routed launch for MXFP8). */
 mok_status mok_expert_upgate(const mok_shape *shape, const mok_weights *w, const void *xg,
                              const uint8_t *xg_scale, const int32_t *offsets, void *a,
-                             uint8_t *a_scale, void *stream);
+                             uint8_t *a_scale, const void *x_shared, void *a_shared, void *stream);
 /* mok_expert_upgate with the dispatch fused in (BF16): the grouped operand's
  * row p is x[table[p].src_index / K], fetched by the GEMM's TMA producer
  * straight from x bf16 [T][D] into shared memory (blog, "Scheduling":
@@ -196,7 +202,7 @@ mok_status mok_expert_upgate_gather(const mok_shape *shape, const mok_weights *w
                                     void *stream);
 mok_status mok_expert_down(const mok_shape *shape, const mok_weights *w, const void *a,
                            const uint8_t *a_scale, const int32_t *offsets, void *yg,
-                           void *stream);
+                           const void *a_shared, void *ys, void *stream);
 
 /* Shared expert (paper note, "The production details": kept in BF16).
  * ys = bf16(W_sd bf16(SiLU(W_sg x) * (W_su x))) [T][D]. */

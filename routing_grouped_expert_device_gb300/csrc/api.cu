@@ -178,23 +178,31 @@ extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* 
 extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weights* w,
                                         const void* xg, const uint8_t* xg_scale,
                                         const int32_t* offsets, void* a, uint8_t* a_scale,
-                                        void* stream) {
+                                        const void* x_shared, void* a_shared, void* stream) {
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   if (R == 0) return MOK_OK;
+  const bool with_shared = s.I_shared > 0 && x_shared && a_shared;
+  if (with_shared && (!w->ws_gate || !w->ws_up || !aligned16(x_shared) || !aligned16(a_shared)))
+    return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s.dtype == MOK_MXFP8) {
     if (!xg || !xg_scale || !offsets || !a || !a_scale || !mx_weights_ok(w) || !aligned16(xg) ||
         !aligned16(xg_scale) || !aligned16(a) || !aligned16(a_scale))
       return MOK_ERR_INVALID_ARG;
-    return launch_upgate_mx(xg, xg_scale, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, offsets,
-                            s.E, s.D, s.I, a, a_scale, static_cast<cudaStream_t>(stream));
+    mok_status r = launch_upgate_mx(xg, xg_scale, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, offsets,
+                                    s.E, s.D, s.I, a, a_scale, st);
+    if (r != MOK_OK || !with_shared) return r;
+    return launch_upgate(x_shared, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared,
+                         a_shared, st);
   }
   if (!xg || !offsets || !a || !w->w_gate || !w->w_up || !aligned16(xg) || !aligned16(a) ||
       !aligned16(w->w_gate) || !aligned16(w->w_up))
     return MOK_ERR_INVALID_ARG;
-  return launch_upgate(xg, R, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a,
-                       static_cast<cudaStream_t>(stream));
+  SharedOperands sh{x_shared, s.T, w->ws_gate, w->ws_up, s.I_shared, a_shared};
+  return launch_upgate_pair(xg, R, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a, st,
+                            with_shared ? &sh : nullptr);
 }
 
 extern "C" mok_status mok_expert_upgate_gather(const mok_shape* shape, const mok_weights* w,
@@ -214,23 +222,27 @@ extern "C" mok_status mok_expert_upgate_gather(const mok_shape* shape, const mok
 
 extern "C" mok_status mok_expert_down(const mok_shape* shape, const mok_weights* w, const void* a,
                                       const uint8_t* a_scale, const int32_t* offsets, void* yg,
-                                      void* stream) {
+                                      const void* a_shared, void* ys, void* stream) {
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   if (R == 0) return MOK_OK;
+  const bool with_shared = s.I_shared > 0 && a_shared && ys;
+  if (with_shared && (!w->ws_down || !aligned16(a_shared) || !aligned16(ys))) return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s.dtype == MOK_MXFP8) {
     if (!a || !a_scale || !offsets || !yg || !mx_weights_ok(w) || !aligned16(a) ||
         !aligned16(a_scale) || !aligned16(yg))
       return MOK_ERR_INVALID_ARG;
-    return launch_down_mx(a, a_scale, R, w->q_down, w->sc_down, offsets, s.E, s.D, s.I, yg,
-                          static_cast<cudaStream_t>(stream));
+    mok_status r = launch_down_mx(a, a_scale, R, w->q_down, w->sc_down, offsets, s.E, s.D, s.I, yg, st);
+    if (r != MOK_OK || !with_shared) return r;
+    return launch_down(a_shared, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st);
   }
   if (!a || !offsets || !yg || !w->w_down || !aligned16(a) || !aligned16(yg) ||
       !aligned16(w->w_down))
     return MOK_ERR_INVALID_ARG;
-  return launch_down(a, R, w->w_down, offsets, s.E, R, s.D, s.I, yg,
-                     static_cast<cudaStream_t>(stream));
+  SharedOperands sh{a_shared, s.T, w->ws_down, nullptr, s.I_shared, ys};
+  return launch_down_pair(a, R, w->w_down, offsets, s.E, R, s.D, s.I, yg, st, with_shared ? &sh : nullptr);
 }
 
 extern "C" mok_status mok_shared_ffn(const mok_shape* shape, const mok_weights* w, const void* x,
@@ -302,14 +314,10 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
   } else if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK) {
     return r;
   }
+  void* as = nullptr;
   if (s.I_shared) {
     ys = at<void>(ws, L.ys);
-    void* as = at<void>(ws, L.as);
-    if ((r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as,
-                           st)) != MOK_OK)
-      return r;
-    if ((r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st)) != MOK_OK)
-      return r;
+    as = at<void>(ws, L.as);
   }
   if (mx) {
     void* asc = at<void>(ws, L.a_scale);
@@ -319,10 +327,22 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     if ((r = launch_down_mx(a, asc, R, w->q_down, w->sc_down, pb.offsets, s.E, s.D, s.I, yg, st)) !=
         MOK_OK)
       return r;
+    if (s.I_shared) {  // the shared expert stays BF16
+      if ((r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, st)) != MOK_OK)
+        return r;
+      if ((r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st)) != MOK_OK)
+        return r;
+    }
   } else {
-    if ((r = launch_upgate(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st)) != MOK_OK)
+    // the shared expert's tiles run inside the routed launches
+    SharedOperands sh_up{x, s.T, w->ws_gate, w->ws_up, s.I_shared, as};
+    SharedOperands sh_dn{as, s.T, w->ws_down, nullptr, s.I_shared, ys};
+    if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st,
+                                s.I_shared ? &sh_up : nullptr)) != MOK_OK)
       return r;
-    if ((r = launch_down(a, R, w->w_down, pb.offsets, s.E, R, s.D, s.I, yg, st)) != MOK_OK) return r;
+    if ((r = launch_down_pair(a, R, w->w_down, pb.offsets, s.E, R, s.D, s.I, yg, st,
+                              s.I_shared ? &sh_dn : nullptr)) != MOK_OK)
+      return r;
   }
   return launch_combine(yg, ys, pb.g, pb.route_dst, s.T, s.K, s.D, out, st);
 }

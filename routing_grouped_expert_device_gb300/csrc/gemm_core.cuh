@@ -33,9 +33,16 @@ struct SchedArgs {
   int32_t k_blocks_fixed;  // > 0: K blocks per tile; 0: ceil(M_g / bk_rows) (K runs over rows)
   int32_t bm;
   int32_t bk_rows;
+  // Optional extra group (the shared expert) with its own operands: rows
+  // [0, extra_rows), extra_n_tiles N tiles, extra_k_blocks K blocks.  Its
+  // tiles are spread evenly through the tile order (extra_rows = 0: none).
+  int32_t extra_rows = 0;
+  int32_t extra_n_tiles = 0;
+  int32_t extra_k_blocks = 0;
 };
 
 struct TileCoord {
+  int extra;  // 1: a tile of the extra group
   int g, mt, nt;
   int row0;     // first row of the group
   int rows;     // rows of the group
@@ -47,6 +54,10 @@ __device__ __forceinline__ int sched_m_tiles(const SchedArgs& s, int rows) {
 }
 __device__ __forceinline__ int sched_k_blocks(const SchedArgs& s, int rows) {
   return s.k_blocks_fixed > 0 ? s.k_blocks_fixed : (rows + s.bk_rows - 1) / s.bk_rows;
+}
+
+__device__ __forceinline__ int extra_tiles(const SchedArgs& s) {
+  return s.extra_rows > 0 ? ((s.extra_rows + s.bm - 1) / s.bm) * s.extra_n_tiles : 0;
 }
 
 // Warp-wide: rstart[g] = first row of group g, tstart[g] = first tile of
@@ -79,11 +90,39 @@ __device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart,
   }
   int total = __shfl_sync(0xffffffffu, incl, 31);
   if (lane == 0) tstart[G] = total;
-  return total;
+  return total + extra_tiles(s);
 }
 
+__device__ __forceinline__ TileCoord decode_group_tile(const SchedArgs& s, const int* tstart,
+                                                       const int* rstart, int tile);
+
+// Tile t of the whole launch: with an extra group of S tiles among Rt grouped
+// ones, positions k*p + p - 1 (k < S, p = (Rt + S) / S) hold the extra
+// tiles, the rest the grouped tiles in order.
 __device__ __forceinline__ TileCoord decode_tile(const SchedArgs& s, const int* tstart,
                                                  const int* rstart, int tile) {
+  const int S = extra_tiles(s);
+  if (S == 0) return decode_group_tile(s, tstart, rstart, tile);
+  const int Rt = tstart[s.G];
+  const int p = (Rt + S) / S;
+  const int q = tile / p;
+  if (tile % p == p - 1 && q < S) {
+    const int mtiles = (s.extra_rows + s.bm - 1) / s.bm;
+    TileCoord c;
+    c.extra = 1;
+    c.g = 0;
+    c.nt = q / mtiles;
+    c.mt = q - c.nt * mtiles;
+    c.row0 = 0;
+    c.rows = s.extra_rows;
+    c.kblocks = s.extra_k_blocks;
+    return c;
+  }
+  return decode_group_tile(s, tstart, rstart, tile - (q < S ? q : S));
+}
+
+__device__ __forceinline__ TileCoord decode_group_tile(const SchedArgs& s, const int* tstart,
+                                                       const int* rstart, int tile) {
   int lo = 0, hi = s.G - 1;
   while (lo < hi) {  // last group whose first tile is <= tile (skips empty groups)
     int mid = (lo + hi + 1) >> 1;
@@ -91,6 +130,7 @@ __device__ __forceinline__ TileCoord decode_tile(const SchedArgs& s, const int* 
     else hi = mid - 1;
   }
   TileCoord c;
+  c.extra = 0;
   c.g = lo;
   c.row0 = rstart[lo];
   c.rows = rstart[lo + 1] - c.row0;

@@ -88,6 +88,11 @@ struct PairParams {
   int32_t b_group_rows, b_tile_rows, b1_off;
   __nv_bfloat16* out;
   int32_t out_ld;
+  // The extra group of the schedule (the shared expert): its own A, B and
+  // output (B rows nt * b_tile_rows + (rank ? b1_off : 0), as above).
+  CUtensorMap tmAs, tmBs0, tmBs1;
+  __nv_bfloat16* out_s;
+  int32_t out_ld_s;
 };
 
 template <bool kSwiglu>
@@ -146,11 +151,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       bool issued[STAGES];
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
-      const CUtensorMap* tmB = rank ? &P.tmB1 : &P.tmB0;
       for (int tile = cid; tile < total && ok; tile += ncl) {
         const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
         const int arow = c.row0 + c.mt * 256 + static_cast<int>(rank) * 128;
         const int brow = c.g * P.b_group_rows + c.nt * P.b_tile_rows + (rank ? P.b1_off : 0);
+        const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
+        const CUtensorMap* tmB = c.extra ? (rank ? &P.tmBs1 : &P.tmBs0) : (rank ? &P.tmB1 : &P.tmB0);
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
             ok = false;
@@ -159,7 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
           uint8_t* st = smem + stage * STAGE_BYTES;
-          tma_load_2d_pair(st, &P.tmA, kb * BK, arow, lbar);
+          tma_load_2d_pair(st, tmA, kb * BK, arow, lbar);
           tma_load_2d_pair(st + A_BYTES, tmB, kb * BK, brow, lbar);
           issued[stage] = true;
           issued_parity[stage] = phase;
@@ -238,7 +244,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(ew * 32) << 16);
       const int r = static_cast<int>(rank) * 128 + ew * 32 + lane;  // row within the 256-row tile
       const bool valid = c.mt * 256 + r < c.rows;
-      __nv_bfloat16* orow = P.out + static_cast<size_t>(c.row0 + c.mt * 256 + r) * P.out_ld;
+      __nv_bfloat16* orow = c.extra ? P.out_s + static_cast<size_t>(c.mt * 256 + r) * P.out_ld_s
+                                    : P.out + static_cast<size_t>(c.row0 + c.mt * 256 + r) * P.out_ld;
       if (kSwiglu) {
         orow += c.nt * 128;
 #pragma unroll 1
@@ -323,14 +330,15 @@ constexpr auto kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                              cudaStream_t st) {
-  if (a_rows == 0 || m_total == 0) return MOK_OK;
+                              cudaStream_t st, const SharedOperands* sh) {
+  if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
   PairParams P;
   P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int groups = offsets ? G : 1;
-  if (!make_tmap_2d(&P.tmA, A, kBF16, a_rows, D, static_cast<uint64_t>(D) * 2, 128, BK, true) ||
+  const uint64_t arows = a_rows > 0 ? a_rows : 1;
+  if (!make_tmap_2d(&P.tmA, A, kBF16, arows, D, static_cast<uint64_t>(D) * 2, 128, BK, true) ||
       !make_tmap_2d(&P.tmB0, w_gate, kBF16, static_cast<uint64_t>(groups) * I, D, static_cast<uint64_t>(D) * 2,
                     128, BK, true) ||
       !make_tmap_2d(&P.tmB1, w_up, kBF16, static_cast<uint64_t>(groups) * I, D, static_cast<uint64_t>(D) * 2,
@@ -341,18 +349,37 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
   P.b1_off = 0;
   P.out = static_cast<__nv_bfloat16*>(a_out);
   P.out_ld = I;
+  P.tmAs = P.tmA;
+  P.tmBs0 = P.tmB0;
+  P.tmBs1 = P.tmB1;
+  P.out_s = nullptr;
+  P.out_ld_s = 0;
+  if (sh && sh->rows > 0) {
+    const int Is = sh->inner;
+    if (!make_tmap_2d(&P.tmAs, sh->A, kBF16, sh->rows, D, static_cast<uint64_t>(D) * 2, 128, BK, true) ||
+        !make_tmap_2d(&P.tmBs0, sh->w0, kBF16, Is, D, static_cast<uint64_t>(D) * 2, 128, BK, true) ||
+        !make_tmap_2d(&P.tmBs1, sh->w1, kBF16, Is, D, static_cast<uint64_t>(D) * 2, 128, BK, true))
+      return MOK_ERR_CUDA;
+    P.sched.extra_rows = static_cast<int32_t>(sh->rows);
+    P.sched.extra_n_tiles = Is / 128;
+    P.sched.extra_k_blocks = D / BK;
+    P.out_s = static_cast<__nv_bfloat16*>(sh->out);
+    P.out_ld_s = Is;
+  }
   return run_pair<true>(P, st);
 }
 
 mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
-                            int64_t m_total, int D, int I, void* y_out, cudaStream_t st) {
-  if (a_rows == 0 || m_total == 0) return MOK_OK;
+                            int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
+                            const SharedOperands* sh) {
+  if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
   PairParams P;
   P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int groups = offsets ? G : 1;
-  if (!make_tmap_2d(&P.tmA, a, kBF16, a_rows, I, static_cast<uint64_t>(I) * 2, 128, BK, true) ||
+  const uint64_t arows = a_rows > 0 ? a_rows : 1;
+  if (!make_tmap_2d(&P.tmA, a, kBF16, arows, I, static_cast<uint64_t>(I) * 2, 128, BK, true) ||
       !make_tmap_2d(&P.tmB0, w_down, kBF16, static_cast<uint64_t>(groups) * D, I, static_cast<uint64_t>(I) * 2,
                     128, BK, true))
     return MOK_ERR_CUDA;
@@ -362,6 +389,23 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
   P.b1_off = 128;
   P.out = static_cast<__nv_bfloat16*>(y_out);
   P.out_ld = D;
+  P.tmAs = P.tmA;
+  P.tmBs0 = P.tmB0;
+  P.tmBs1 = P.tmB0;
+  P.out_s = nullptr;
+  P.out_ld_s = 0;
+  if (sh && sh->rows > 0) {
+    const int Is = sh->inner;
+    if (!make_tmap_2d(&P.tmAs, sh->A, kBF16, sh->rows, Is, static_cast<uint64_t>(Is) * 2, 128, BK, true) ||
+        !make_tmap_2d(&P.tmBs0, sh->w0, kBF16, D, Is, static_cast<uint64_t>(Is) * 2, 128, BK, true))
+      return MOK_ERR_CUDA;
+    P.tmBs1 = P.tmBs0;
+    P.sched.extra_rows = static_cast<int32_t>(sh->rows);
+    P.sched.extra_n_tiles = D / 256;
+    P.sched.extra_k_blocks = Is / BK;
+    P.out_s = static_cast<__nv_bfloat16*>(sh->out);
+    P.out_ld_s = D;
+  }
   return run_pair<false>(P, st);
 }
 

@@ -45,13 +45,25 @@ mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, cons
                          cudaStream_t st, const int32_t* gather_table = nullptr, int gather_k = 1);
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
+// The shared expert as an extra group of a routed launch: A [rows][K],
+// weights w0 (, w1) with `inner` = I_shared, output [rows][N].
+struct SharedOperands {
+  const void* A;
+  int64_t rows;
+  const void* w0;
+  const void* w1;
+  int inner;
+  void* out;
+};
 // The same two GEMMs on CTA pairs (cta_group::2, 256-row tiles); the
-// launch_upgate / launch_down above use these whenever A is dense.
+// launch_upgate / launch_down above use these whenever A is dense.  With
+// sh, the shared expert's tiles run in the same launch, spread through it.
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                              cudaStream_t st);
+                              cudaStream_t st, const SharedOperands* sh = nullptr);
 mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
-                            int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
+                            int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
+                            const SharedOperands* sh = nullptr);
 
 // Backward.  dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
 // non-null, dgp [rows][I/128] partial <t, a>; g_route null = weight 1.

@@ -58,10 +58,11 @@ _SIGS = {
     "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
-    "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P]),
+    "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _P,
+                                         _P]),
     "mok_expert_upgate_gather": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P,
                                                 _P]),
-    "mok_expert_down": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P]),
+    "mok_expert_down": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _P]),
     "mok_shared_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _SZ, _P]),
     "mok_combine": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
     "mok_moe_fwd": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P,
@@ -174,10 +175,13 @@ def expert_ffn(shape: Shape, weights: Weights, xg, offsets, yg, a_out=None, ws=N
                                         _stream(stream)), "mok_expert_ffn")
 
 
-def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None, a_scale=None, stream=None):
+def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None, a_scale=None,
+                  x_shared=None, a_shared=None, stream=None):
+    """Grouped up/gate + SwiGLU; with x_shared / a_shared the shared expert's
+    up/gate runs in the same launch."""
     _check(_lib_handle().mok_expert_upgate(ctypes.byref(shape), ctypes.byref(weights), _ptr(xg), _ptr(xg_scale),
-                                           _ptr(offsets), _ptr(a), _ptr(a_scale), _stream(stream)),
-           "mok_expert_upgate")
+                                           _ptr(offsets), _ptr(a), _ptr(a_scale), _ptr(x_shared), _ptr(a_shared),
+                                           _stream(stream)), "mok_expert_upgate")
 
 
 def expert_upgate_gather(shape: Shape, weights: Weights, x, table, offsets, a, stream=None):
@@ -186,9 +190,12 @@ def expert_upgate_gather(shape: Shape, weights: Weights, x, table, offsets, a, s
            "mok_expert_upgate_gather")
 
 
-def expert_down(shape: Shape, weights: Weights, a, offsets, yg, a_scale=None, stream=None):
+def expert_down(shape: Shape, weights: Weights, a, offsets, yg, a_scale=None, a_shared=None, ys=None, stream=None):
+    """Grouped down projection; with a_shared / ys the shared expert's down
+    projection runs in the same launch."""
     _check(_lib_handle().mok_expert_down(ctypes.byref(shape), ctypes.byref(weights), _ptr(a), _ptr(a_scale),
-                                         _ptr(offsets), _ptr(yg), _stream(stream)), "mok_expert_down")
+                                         _ptr(offsets), _ptr(yg), _ptr(a_shared), _ptr(ys), _stream(stream)),
+           "mok_expert_down")
 
 
 def shared_ffn(shape: Shape, weights: Weights, x, ys, ws, stream=None):

@@ -268,6 +268,19 @@ def test_split_expert_entry_points_match_expert_ffn(m):
     m.expert_down(shape, m.make_weights(d), a2, off, y2)
     assert torch.equal(a1.view(torch.int16), a2.view(torch.int16))
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    # the shared expert inside the same launches gives the bytes of mok_shared_ffn
+    a3, y3 = torch.empty_like(a1), torch.empty_like(y1)
+    as_ = torch.empty(cfg.T, cfg.I_shared, dtype=torch.bfloat16, device=DEV)
+    ys1 = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+    m.expert_upgate(shape, m.make_weights(d), xg, off, a3, x_shared=d["x"], a_shared=as_)
+    m.expert_down(shape, m.make_weights(d), a3, off, y3, a_shared=as_, ys=ys1)
+    ys2 = torch.empty_like(ys1)
+    sws = torch.empty(m.workspace_bytes(shape, m.OP_SHARED_FFN), dtype=torch.uint8, device=DEV)
+    m.shared_ffn(shape, m.make_weights(d), d["x"], ys2, sws)
+    m.check_device_status()
+    assert torch.equal(a1.view(torch.int16), a3.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+    assert torch.equal(ys1.view(torch.int16), ys2.view(torch.int16))
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "skew_small"])

@@ -241,9 +241,9 @@ def run_ours(args, world, rank, local):
     route_dst = torch.empty(R, dtype=i32, device=dev)
     pws = torch.empty(M.workspace_bytes(shape, M.OP_PLAN), dtype=u8, device=dev)
     xg = torch.empty(R, D, dtype=u8 if mx else bf, device=dev)
-    xs = torch.empty(M.mx_scale_words(R, D), dtype=i32, device=dev) if mx else None
+    xs = torch.empty(M.mx_scale_words(R, D, E), dtype=i32, device=dev) if mx else None
     a = torch.empty(R, I, dtype=u8 if mx else bf, device=dev)
-    asc = torch.empty(M.mx_scale_words(R, I), dtype=i32, device=dev) if mx else None
+    asc = torch.empty(M.mx_scale_words(R, I, E), dtype=i32, device=dev) if mx else None
     yg = torch.empty(R, D, dtype=bf, device=dev)
     ys = torch.empty(T, D, dtype=bf, device=dev) if Is else None
     a_s = torch.empty(T, Is, dtype=bf, device=dev) if Is else None
@@ -276,7 +276,7 @@ def run_ours(args, world, rank, local):
             return
         M.route(d["s"], K, topk, g)
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
-        M.dispatch(shape, d["x"], table, xg, xs)
+        M.dispatch(shape, d["x"], table, xg, xs, offsets=offsets)
         if ev0 is not None:
             ev0.record(stream)
         # the shared expert's tiles run inside the routed launches

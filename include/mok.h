@@ -79,11 +79,23 @@ typedef struct {
 
 /* MXFP8 tensors (paper note, "The production details").  A [rows][cols]
  * tensor quantised along cols is E4M3 ("fn") codes [rows][cols] plus E8M0
- * scales, one per 32 consecutive elements of a row, stored as 32-bit words
- * [cols/128][ld] with ld = rows rounded up to a multiple of 4: word (g, r)
- * holds the scales of row r for columns [128 g, 128 g + 128), byte b (the
- * least significant first) for columns [128 g + 32 b, 128 g + 32 b + 32).
- * Element value = code * 2^(scale - 127).  cols must be a multiple of 128.
+ * scales, one per 32 consecutive elements of a row.  Element value =
+ * code * 2^(scale - 127).  cols must be a multiple of 128.  The scales are
+ * 32-bit words [cols/128][ld], ld a multiple of 128: the word of row
+ * position p for columns [128 g, 128 g + 128) holds, byte b (the least
+ * significant first), the scale of columns [128 g + 32 b, 128 g + 32 b + 32),
+ * and sits at index g * ld + (p & ~127) + 4 * (p % 32) + (p % 128) / 32
+ * (within each block of 128 positions, position 32 c + l at word 4 l + c: the
+ * order the tensor cores read scale blocks in).  Row r has position
+ *   plain layout   : p = r, ld = rows rounded up to 128
+ *                    (mok_quantize_mxfp8, the weights' sc_*);
+ *   grouped layout : rows grouped by expert as mok_plan's offsets (expert e
+ *                    owns rows [offsets[e], offsets[e+1])), every expert
+ *                    starting a new block: p = 128 (offsets[e] / 128 + e) +
+ *                    r - offsets[e], ld = 128 (ceil(rows / 128) + E)
+ *                    (the routed activations xg_scale, a_scale).
+ * Positions that hold no row are never read for a valid output.
+ * mok_mxfp8_scale_bytes gives the size of either layout.
  *
  * Weights (device, bf16 unless noted).  Routed: w_gate, w_up [E][I][D];
  * w_down [E][D][I].  MXFP8 copies (used when shape.dtype = MOK_MXFP8, may be
@@ -154,11 +166,11 @@ mok_status mok_plan_static(const int32_t *topk_idx, int32_t T, int32_t E, int32_
 /* Gather (blog, "Scheduling": tokens land expert-contiguous, zero local
  * copies).  xg[p] = x[table[p].src_index / K] for p < R; x bf16 [T][D],
  * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives the E4M3 codes [R][D]
- * of the gathered rows and xg_scale their scale words ([D/128][ld],
- * ld = R rounded up to 4; quantisation fused into the dispatch); xg_scale
- * is ignored for BF16. */
+ * of the gathered rows and xg_scale their scale words in the grouped layout
+ * (quantisation fused into the dispatch), for which offsets (mok_plan's)
+ * is required; xg_scale and offsets are ignored for BF16. */
 mok_status mok_dispatch(const mok_shape *shape, const void *x, const int32_t *table,
-                        void *xg, uint8_t *xg_scale, void *stream);
+                        const int32_t *offsets, void *xg, uint8_t *xg_scale, void *stream);
 
 /* Grouped expert FFN over expert-contiguous rows: expert e owns rows
  * [offsets[e], offsets[e+1]) of xg.  a = bf16(SiLU(xg W_gate^T) * (xg W_up^T))
@@ -175,8 +187,8 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
  * mok_expert_upgate: a = bf16(SiLU(xg W_gate^T) * (xg W_up^T)) [R][I].
  * mok_expert_down: yg = bf16(a W_down^T) [R][D].  Same rules as
  * mok_expert_ffn.  For MOK_MXFP8, a is written as codes [R][I] plus scale
- * words a_scale ([I/128][ld], ld = R rounded up to 4) and read back that way
- * by mok_expert_down; xg_scale / a_scale are ignored for BF16.
+ * words a_scale (grouped layout) and read back that way by
+ * mok_expert_down; xg_scale / a_scale are ignored for BF16.
  * Shared expert in the same launch (paper note, "The production details":
  * the shared expert fills compute while routed rows stream): when
  * shape.I_shared > 0 and x_shared / a_shared (resp. a_shared / ys) are
@@ -240,11 +252,17 @@ mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void 
                        void *dws_up, void *dws_down, float *ds, float *dg, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* Bytes of MXFP8 scale storage for a [rows][cols] tensor: plain layout
+ * when groups = 0, grouped layout over `groups` experts otherwise (see the
+ * MXFP8 layout above).  0 for invalid sizes (cols not a positive multiple
+ * of 128, negative rows or groups).  Host-only. */
+size_t mok_mxfp8_scale_bytes(int64_t rows, int64_t cols, int32_t groups);
+
 /* MXFP8 quantiser: src bf16 [rows][cols] (cols % 128 == 0) -> q E4M3 codes
- * [rows][cols] and scale words ([cols/128][ld], ld = rows rounded up to 4,
- * see the MXFP8 layout above; scale needs cols/128 * ld * 4 bytes).  Per
- * 1x32 block the scale is 2^e with e the smallest integer such that
- * amax <= 448 * 2^e (all-zero block: byte 0); codes round to nearest even. */
+ * [rows][cols] and scale words in the plain layout (see the MXFP8 layout
+ * above; mok_mxfp8_scale_bytes(rows, cols, 0) bytes).  Per 1x32 block the
+ * scale is 2^e with e the smallest integer such that amax <= 448 * 2^e
+ * (all-zero block: byte 0); codes round to nearest even. */
 mok_status mok_quantize_mxfp8(const void *src, int64_t rows, int64_t cols, void *q,
                               uint8_t *scale, void *stream);
 

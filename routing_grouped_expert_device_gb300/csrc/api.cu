@@ -53,9 +53,9 @@ FwdLayout fwd_layout(const mok_shape& s) {
   L.hist = c.take(plan_scratch_bytes(static_cast<int64_t>(R), s.E));
   L.xg = c.take(R * D * (s.dtype == MOK_MXFP8 ? 1 : 2));
   const bool mx = s.dtype == MOK_MXFP8;
-  L.xg_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D) : 0);
+  L.xg_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
   L.a = c.take(R * I * 2);
-  L.a_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), I) : 0);
+  L.a_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), I, s.E) : 0);
   L.yg = c.take(R * D * 2);
   L.as = c.take(T * Is * 2);
   L.ys = c.take(Is ? T * D * 2 : 0);
@@ -96,7 +96,7 @@ bool mx_weights_ok(const mok_weights* w) {
 // Workspace of mok_expert_ffn: a (bf16), or a codes + scale words (MXFP8).
 size_t ffn_ws_bytes(const mok_shape& s) {
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
-  if (s.dtype == MOK_MXFP8) return round_up(static_cast<size_t>(R) * s.I) + round_up(mx_scale_bytes(R, s.I));
+  if (s.dtype == MOK_MXFP8) return round_up(static_cast<size_t>(R) * s.I) + round_up(mx_scale_bytes(R, s.I, s.E));
   return round_up(static_cast<size_t>(R) * s.I * 2);
 }
 
@@ -125,7 +125,7 @@ extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
 }
 
 extern "C" mok_status mok_dispatch(const mok_shape* shape, const void* x, const int32_t* table,
-                                   void* xg, uint8_t* xg_scale, void* stream) {
+                                   const int32_t* offsets, void* xg, uint8_t* xg_scale, void* stream) {
   if (!shape_ok(shape)) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
@@ -133,8 +133,8 @@ extern "C" mok_status mok_dispatch(const mok_shape* shape, const void* x, const 
   if (!x || !table || !xg || !aligned16(x) || !aligned16(xg)) return MOK_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s.dtype == MOK_MXFP8) {
-    if (!xg_scale) return MOK_ERR_INVALID_ARG;
-    return launch_dispatch_mxfp8(x, table, R, s.K, s.D, xg, xg_scale, st);
+    if (!xg_scale || !offsets) return MOK_ERR_INVALID_ARG;
+    return launch_dispatch_mxfp8(x, table, offsets, R, s.K, s.D, s.E, xg, xg_scale, st);
   }
   return launch_dispatch_bf16(x, table, R, s.K, s.D, xg, nullptr, nullptr, st);
 }
@@ -309,7 +309,8 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
   void* yg = at<void>(ws, L.yg);
   void* ys = nullptr;
   if (mx) {
-    if ((r = launch_dispatch_mxfp8(x, pb.table, R, s.K, s.D, xg, at<uint8_t>(ws, L.xg_scale), st)) != MOK_OK)
+    if ((r = launch_dispatch_mxfp8(x, pb.table, pb.offsets, R, s.K, s.D, s.E, xg, at<uint8_t>(ws, L.xg_scale),
+                                   st)) != MOK_OK)
       return r;
   } else if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK) {
     return r;
@@ -345,6 +346,11 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
       return r;
   }
   return launch_combine(yg, ys, pb.g, pb.route_dst, s.T, s.K, s.D, out, st);
+}
+
+extern "C" size_t mok_mxfp8_scale_bytes(int64_t rows, int64_t cols, int32_t groups) {
+  if (rows < 0 || cols <= 0 || cols % 128 || groups < 0) return 0;
+  return mx_scale_bytes(rows, cols, groups);
 }
 
 extern "C" mok_status mok_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,

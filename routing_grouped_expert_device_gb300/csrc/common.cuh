@@ -286,7 +286,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-__device__ __forceinline__ float silu_f(float h) { return h / (1.0f + __expf(-h)); }
+// sigma(h) = 1 / (1 + e^-h) through the fast exponential and reciprocal
+// (a few ulp; 0 once e^-h passes 2^126, i.e. h < -87, where sigma < 2^-125).
+// An IEEE division here costs far more than the rest of the epilogues.
+__device__ __forceinline__ float sigmoid_f(float h) { return __fdividef(1.0f, 1.0f + __expf(-h)); }
+// SiLU(h) = h sigma(h); the forward and the backward replay both form
+// a = bf16(silu_f(h) * u) from it.
+__device__ __forceinline__ float silu_f(float h) { return h * sigmoid_f(h); }
 
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

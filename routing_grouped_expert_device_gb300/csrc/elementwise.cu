@@ -90,11 +90,14 @@ __device__ __forceinline__ void quant_block(const uint4 (&v)[4], uint4 (&q)[2], 
 
 // One thread per (128-column group, row): 4 blocks of 32, their codes and
 // one scale word.  Threads of a warp take consecutive rows of one group, so
-// the scale words ([cols/128][ld], see kernels.h) are written contiguously.
-// table == nullptr: identity rows (plain quantiser); else the source row of
-// row p is table[p].src / K (dispatch with fused quantisation).
+// a warp's scale words land in one 512-byte block of the scale storage
+// (layout in kernels.h).  table == nullptr: identity rows, plain layout
+// (the quantiser); else row p is x[table[p].src / K] and its scale goes to
+// the grouped layout of expert table[p].e (the dispatch with fused
+// quantisation).
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ src,
-                                                         const int32_t* __restrict__ table, int K,
+                                                         const int32_t* __restrict__ table,
+                                                         const int32_t* __restrict__ offsets, int K,
                                                          int64_t rows, int64_t cols, int64_t ld,
                                                          uint4* __restrict__ q,
                                                          uint32_t* __restrict__ scale) {
@@ -102,7 +105,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t grp = i / rows, row = i - grp * rows;
-    const int64_t srow = table ? static_cast<int64_t>(__ldg(table + row * 3) / K) : row;
+    int64_t srow = row, srow_pos = row;
+    if (table) {
+      srow = __ldg(table + row * 3) / K;
+      const int e = __ldg(table + row * 3 + 1);
+      const int64_t off = __ldg(offsets + e);
+      srow_pos = mx_group_row0(off, e) + (row - off);
+    }
     const uint4* in = src + (srow * cols + grp * 128) / 8;
     uint4* out = q + (row * cols + grp * 128) / 16;
     uint32_t word = 0;
@@ -117,7 +126,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
       out[2 * b + 1] = o[1];
       word |= static_cast<uint32_t>(sc) << (8 * b);
     }
-    scale[grp * ld + row] = word;
+    scale[grp * ld + mx_scale_pos(srow_pos)] = word;
   }
 }
 
@@ -225,11 +234,11 @@ mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, 
   return MOK_OK;
 }
 
-mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, int64_t R, int K, int D,
-                                 void* xg_q, uint8_t* xg_scale, cudaStream_t st) {
+mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int32_t* offsets, int64_t R,
+                                 int K, int D, int E, void* xg_q, uint8_t* xg_scale, cudaStream_t st) {
   if (R == 0) return MOK_OK;
   quant_rows_kernel<<<grid_for(R * (D / 128), 256), 256, 0, st>>>(
-      static_cast<const uint4*>(x), table, K, R, D, mx_scale_ld(R), static_cast<uint4*>(xg_q),
+      static_cast<const uint4*>(x), table, offsets, K, R, D, mx_scale_ld(R, E), static_cast<uint4*>(xg_q),
       reinterpret_cast<uint32_t*>(xg_scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
@@ -239,7 +248,7 @@ mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, vo
                                  uint8_t* scale, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
   quant_rows_kernel<<<grid_for(rows * (cols / 128), 256), 256, 0, st>>>(
-      static_cast<const uint4*>(src), nullptr, 1, rows, cols, mx_scale_ld(rows),
+      static_cast<const uint4*>(src), nullptr, nullptr, 1, rows, cols, mx_scale_ld(rows),
       static_cast<uint4*>(q), reinterpret_cast<uint32_t*>(scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;

@@ -107,8 +107,8 @@ struct DgradCfg {
           const float h = __uint_as_float(hv[2 * j + q]);
           const float u = __uint_as_float(uv[2 * j + q]);
           const float t = __uint_as_float(tv[2 * j + q]);
-          const float sig = 1.0f / (1.0f + __expf(-h));
-          const float a = __bfloat162float(__float2bfloat16_rn(silu_f(h) * u));
+          const float sig = sigmoid_f(h);
+          const float a = __bfloat162float(__float2bfloat16_rn((h * sig) * u));  // = bf16(silu_f(h) * u)
           dot = __fmaf_rn(t, a, dot);
           const float da = g * t;
           dhv[q] = da * u * sig * (1.0f + h * (1.0f - sig));

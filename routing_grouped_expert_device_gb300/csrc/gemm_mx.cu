@@ -1,74 +1,70 @@
-// MXFP8 grouped expert GEMMs (Mixture-of-Kittens paper note, "The
-// production details": MXFP8 with quantisation fused into the dispatch, the
-// grouped GEMMs and the gated activation).
+// MXFP8 grouped expert GEMMs on CTA pairs (Mixture-of-Kittens paper note,
+// "The production details": MXFP8 with quantisation fused into the
+// dispatch, the grouped GEMMs and the gated activation).
 //
-// Operands are E4M3 codes with one E8M0 scale per 1x32 block along K.  Scale
-// storage of a [rows][K] tensor: int32 words sc[K/128][ld] (ld = rows rounded
-// up to 4); word (g, r) holds the 4 block scales of row r for K columns
-// [128 g, 128 g + 128), byte b for block 4 g + b.
+// Operands are E4M3 codes with one E8M0 scale per 1x32 block along K, scale
+// words in 128-row blocks (layout in kernels.h): the A operand (routed rows)
+// in the grouped layout, in which every expert starts a new block, and the
+// weights in the plain layout.
 //
-// Per stage (128 K columns = 4 MMAs of K 32) the TMA producer loads the A and
-// B code tiles (128-byte swizzle) and the tile's scale words.  The epilogue
-// warps, idle during the main loop (one TMEM accumulator), copy the scale
-// words into a TMEM ring with tcgen05.st, in the layout the block-scaled MMA
-// reads for M = 128 and one scale per 32 K:
-//   A row m : TMEM lane m,                     column sfa + m/32, byte = MMA k
-//   B row n : lanes 32 q + n%32, every quarter q, column sfb + n/32, byte = MMA k
-// then arrive on sf_ready[stage]; the MMA thread issues the 4 block-scaled
-// MMAs of the stage.
+// A cluster of two CTAs computes a 256-row x 256-column tile as the BF16
+// pair kernel does: CTA rank r loads its 128 rows of A and one half of B
+// (up/gate: rank 0 the 128 W_gate rows, rank 1 the 128 W_up rows; down:
+// output columns [128 r, 128 r + 128)), and the leader issues
+// cta_group::2 block-scaled MMAs (M 256, N 256, K 32, four per 128-column
+// stage).  Per stage each CTA also loads three scale blocks of 512 B: its
+// own 128 rows of A, and B's two halves (every CTA needs the scales of all
+// 256 B rows).  All loads of both CTAs complete on the leader's
+// full[stage]; the MMA thread then copies the three blocks into a TMEM ring
+// with tcgen05.cp (each CTA from its own shared memory) and issues the four
+// MMAs, which read
+//   A row m : lane m (own 128 rows), column sfa + m / 32
+//   B row n : lane 32 q + n % 32 for every quarter q, column sfb + n / 32
+// with the byte of the 32-bit scale word chosen by the MMA's scale id.
+// The copy and the MMAs that follow it from the same thread execute in
+// order; the ring slot of a stage is refilled only after the MMAs that read
+// it have committed (the stage's empty barrier), as for its shared memory.
 //
-// up/gate : tile 128 rows x (128 gate | 128 up); the epilogue forms
-//           a = bf16(SiLU(h) u) and quantises it to E4M3 per 32 columns (one
-//           TMEM load of 32 columns is one block).
-// down    : tile 128 rows x 256 columns; y = bf16(acc).
+// up/gate : the epilogue forms a = bf16(SiLU(h) u) and quantises it to E4M3
+//           per 32 columns (one TMEM load of 32 columns is one block),
+//           writing a's scale words in the grouped layout.
+// down    : y = bf16(acc).
 #include <cuda_fp8.h>
 
 #include "gemm_core.cuh"
 #include "kernels.h"
+#include "pair.cuh"
 
 namespace mok {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BKB = 128;                      // K columns (bytes) per stage
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BKB;             // 16 KB
-constexpr int B_HALF = 128 * BKB;             // 16 KB
-constexpr int SA_OFF = A_BYTES + 2 * B_HALF;  // raw A scale words (132 used)
-constexpr int SB_OFF = SA_OFF + 1024;         // raw B scale words (256)
-constexpr int STAGE_BYTES = SB_OFF + 1024;    // 50 KB
-constexpr int SA_WORDS = 132;                 // 128 rows + up to 3 words of misalignment
-constexpr uint32_t TX_BYTES = A_BYTES + 2 * B_HALF + SA_WORDS * 4 + 256 * 4;
+constexpr int BKB = 128;  // K columns (bytes) per stage
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows
+constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B
+constexpr int CODE_BYTES = A_BYTES + B_BYTES;
+constexpr int SF_BLOCK = 512;           // one 128-row block of scale words
+constexpr int SF_BYTES = 3 * SF_BLOCK;  // A's block, B's two halves
+constexpr uint32_t TX_BYTES = 2 * (CODE_BYTES + SF_BYTES);
 constexpr uint32_t ACC_COLS = 256;
-constexpr uint32_t SF_COLS = 12;  // per stage: 4 (A) + 8 (B)
+constexpr uint32_t SF_COLS = 12;  // per stage: A 4, B 8
 
-// Block-scaled instruction descriptor, kind::mxf8f6f4: B scale id (bits 4-5),
-// A and B format E4M3 = 0 (7-9, 10-12), both K-major, N >> 3 (17-22), scale
-// format UE8M0 (23), M >> 4 (24-28), A scale id (29-30).
-__device__ __forceinline__ uint32_t idesc_mx(int N, uint32_t sf_id) {
-  return (sf_id << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) |
-         (sf_id << 29);
+// Block-scaled instruction descriptor, kind::mxf8f6f4: B scale id (bits
+// 4-5), A and B format E4M3 = 0 (7-9, 10-12), both K-major, N >> 3 (17-22),
+// scale format UE8M0 (23), M >> 4 (24-28), A scale id (29-30).
+__device__ __forceinline__ uint32_t idesc_mx(uint32_t sf_id) {
+  return (sf_id << 4) | ((256u >> 3) << 17) | (1u << 23) | ((256u >> 4) << 24) | (sf_id << 29);
 }
 
-__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+__device__ __forceinline__ void mma_mx2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
 }
-
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Smallest e with amax <= 448 * 2^e (same rule as the quantiser in
 // elementwise.cu): amax = 1.f * 2^E and 448 = 1.75 * 2^8.
@@ -81,93 +77,99 @@ __device__ __forceinline__ int mx_exp(float amax) {
 }
 
 struct MxParams {
-  SchedArgs sched;
+  SchedArgs sched;  // bm = 256
   int* status;
   CUtensorMap tmA;    // codes [rows][K] u8, box 128 x 128
-  CUtensorMap tmSA;   // scale words [K/128][ld] i32, box 132 x 1
+  CUtensorMap tmSA;   // A scale words, grouped layout [K/128][lda], box 128 x 1
   CUtensorMap tmB0;   // codes [G*NB][K], box 128 x 128
   CUtensorMap tmB1;
-  CUtensorMap tmSB0;  // scale words of B0 [K/128][G*NB] i32, box 128 x 1
+  CUtensorMap tmSB0;  // scale words of B0, plain layout [K/128][G*NB], box 128 x 1
   CUtensorMap tmSB1;  // scale words of B1
   int32_t b_group_rows, b_tile_rows, b1_off;
-  uint8_t* aq;        // up/gate: a codes [rows][I]
-  uint32_t* asc;      // up/gate: a scale words [I/128][a_ld]
-  int32_t a_ld;
-  __nv_bfloat16* y;   // down: y [rows][D]
+  uint8_t* aq;    // up/gate: a codes [rows][I]
+  uint32_t* asc;  // up/gate: a scale words, grouped layout [I/128][a_ld]
+  int64_t a_ld;
+  __nv_bfloat16* y;  // down: y [rows][D]
   int32_t out_ld;
 };
 
 template <bool kSwiglu>
-__global__ void __launch_bounds__(256, 1) gemm_mx_persistent(const __grid_constant__ MxParams P) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sf_smem = smem + STAGES * CODE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sf_smem + STAGES * SF_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* sfready = empty + STAGES;
-  uint64_t* tfull = sfready + STAGES;
+  uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
-  int* tstart = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);
+  int* tstart = reinterpret_cast<int*>(sf_smem + STAGES * SF_BYTES + 1024);
   int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&sfready[i], 128);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 128);
+    mbar_init(tempty, 256);  // both CTAs' 128 epilogue threads
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2) tmem_alloc(tmem_holder, 512);
+  if (warp == 2) tmem_alloc2(tmem_holder, 512);
   if (warp == 3) {
     const int total = build_tile_table(P.sched, tstart, rstart, lane);
     if (lane == 0) *total_holder = total;
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int total = *total_holder;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer (both CTAs) ----------------
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t issued_parity[STAGES];
       bool issued[STAGES];
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const CUtensorMap* tmB = rank ? &P.tmB1 : &P.tmB0;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
         const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
-        const int r0 = c.row0 + c.mt * BM;
-        const int brow = c.g * P.b_group_rows + c.nt * P.b_tile_rows;
+        const int local0 = c.mt * 256 + static_cast<int>(rank) * 128;  // this CTA's first row in the group
+        const int arow = c.row0 + local0;
+        const int sfrow = static_cast<int>(mx_group_row0(c.row0, c.g)) + local0;  // a multiple of 128
+        const int brow0 = c.g * P.b_group_rows + c.nt * P.b_tile_rows;
+        const int brow = brow0 + (rank ? P.b1_off : 0);
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], TX_BYTES);
-          tma_load_2d(st, &P.tmA, kb * BKB, r0, &full[stage]);
-          tma_load_2d(st + A_BYTES, &P.tmB0, kb * BKB, brow, &full[stage]);
-          tma_load_2d(st + A_BYTES + B_HALF, &P.tmB1, kb * BKB, brow + P.b1_off, &full[stage]);
-          // A's scale words start at row r0, which need not sit on a 16-byte
-          // boundary: fetch from r0 rounded down to 4 words, index from the
-          // remainder.
-          tma_load_2d(st + SA_OFF, &P.tmSA, r0 & ~3, kb, &full[stage]);
-          tma_load_2d(st + SB_OFF, &P.tmSB0, brow, kb, &full[stage]);
-          tma_load_2d(st + SB_OFF + 512, &P.tmSB1, brow + P.b1_off, kb, &full[stage]);
+          if (leader) mbar_arrive_expect_tx(&full[stage], TX_BYTES);
+          const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
+          uint8_t* st = smem + stage * CODE_BYTES;
+          uint8_t* sf = sf_smem + stage * SF_BYTES;
+          tma_load_2d_pair(st, &P.tmA, kb * BKB, arow, lbar);
+          tma_load_2d_pair(st + A_BYTES, tmB, kb * BKB, brow, lbar);
+          tma_load_2d_pair(sf, &P.tmSA, sfrow, kb, lbar);
+          tma_load_2d_pair(sf + SF_BLOCK, &P.tmSB0, brow0, kb, lbar);
+          tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSB1, brow0 + P.b1_off, kb, lbar);
           issued[stage] = true;
           issued_parity[stage] = phase;
           if (++stage == STAGES) {
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(256, 1) gemm_mx_persistent(const __grid_consta
           }
         }
       }
-      if (!ok) {
+      if (!ok && leader) {
         for (int i = 0; i < STAGES; ++i) {
           if (!issued[i]) continue;
           const uint64_t t0 = globaltimer();
@@ -186,88 +188,66 @@ __global__ void __launch_bounds__(256, 1) gemm_mx_persistent(const __grid_consta
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    uint32_t stage = 0, phase = 0;
-    bool ok = true, any = false;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
-      ok = __all_sync(0xffffffffu, mbar_wait(tempty, (it & 1) ^ 1, abort_flag, P.status, SITE_MMA));
-      if (!ok) break;
-      tc_fence_after();
-      for (int kb = 0; kb < c.kblocks; ++kb) {
-        const bool got = mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA) &&
-                         mbar_wait(&sfready[stage], phase, abort_flag, P.status, SITE_MMA);
-        ok = __all_sync(0xffffffffu, got);
+    // ---------------- scale copies + MMA issuer (leader only) ----------------
+    if (leader) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true, any = false;
+      int it = 0;
+      for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
+        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        ok = __all_sync(0xffffffffu, mbar_wait(tempty, (it & 1) ^ 1, abort_flag, P.status, SITE_MMA));
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b = a + A_BYTES;
-          const uint32_t sfa = tmem_base + ACC_COLS + stage * SF_COLS;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sft = tmem_base + ACC_COLS + stage * SF_COLS;
+            const uint32_t sfs = smem_u32(sf_smem + stage * SF_BYTES);
+            tmem_cp_block2(sft, sfs);                     // A: columns sft .. sft + 3
+            tmem_cp_block2(sft + 4, sfs + SF_BLOCK);      // B rows 0..127: sft + 4 .. sft + 7
+            tmem_cp_block2(sft + 8, sfs + 2 * SF_BLOCK);  // B rows 128..255: sft + 8 .. sft + 11
+            const uint32_t a = smem_u32(smem + stage * CODE_BYTES);
+            const uint32_t b = a + A_BYTES;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_mx(tmem_base, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024),
-                   idesc_mx(256, k), sfa, sfa + 4, (kb | k) != 0);
-          mma_commit(&empty[stage]);
-          any = true;
+            for (int k = 0; k < 4; ++k)
+              mma_mx2(tmem_base, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024),
+                      idesc_mx(k), sft, sft + 4, (kb | k) != 0);
+            commit2(&empty[stage], 0x3);
+            any = true;
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
+        if (!ok) break;
+        if (lane == 0) commit2(tfull, 0x3);
         __syncwarp();
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(tfull);
-      __syncwarp();
-    }
-    any = __shfl_sync(0xffffffffu, any, 0);
-    if (any) {
-      if (lane == 0) mma_commit(drain);
-      __syncwarp();
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitBudgetNs) {
+      any = __shfl_sync(0xffffffffu, any, 0);
+      if (any) {
+        if (lane == 0) commit2(drain, 0x1);
+        __syncwarp();
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitBudgetNs) {
+        }
       }
     }
   } else if (warp >= 4) {
-    // ---------------- scales into TMEM, then the epilogue ----------------
+    // ---------------- epilogue (both CTAs, own 128 rows) ----------------
     const int q = warp - 4;  // TMEM lane quarter of this warp
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t stage = 0, phase = 0;
     int it = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+    for (int tile = cid; tile < total; tile += ncl, ++it) {
       const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
-      const int r0 = c.row0 + c.mt * BM;
-      for (int kb = 0; kb < c.kblocks; ++kb) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_EPILOGUE));
-        if (!ok) break;
-        const uint8_t* st = smem + stage * STAGE_BYTES;
-        const uint32_t* sa = reinterpret_cast<const uint32_t*>(st + SA_OFF) + (r0 & 3);
-        const uint32_t* sb = reinterpret_cast<const uint32_t*>(st + SB_OFF);
-        const uint32_t sf = tmem_base + lane_off + ACC_COLS + stage * SF_COLS;
-        tmem_st1(sf + q, sa[q * 32 + lane]);
-        uint32_t v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = sb[j * 32 + lane];
-        tmem_st8(sf + 4, v);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&sfready[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-      if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(tfull, it & 1, abort_flag, P.status, SITE_EPILOGUE));
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull, it & 1, abort_flag, P.status, SITE_EPILOGUE))) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + lane_off;
-      const int r = q * 32 + lane;
-      const bool valid = c.mt * BM + r < c.rows;
-      const int64_t row = r0 + r;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const int local = c.mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;  // row within the group
+      const bool valid = local < c.rows;
+      const int64_t row = c.row0 + local;
       if (kSwiglu) {
         uint32_t words = 0;
 #pragma unroll 1
@@ -302,7 +282,7 @@ __global__ void __launch_bounds__(256, 1) gemm_mx_persistent(const __grid_consta
             st_global_v4(dst + 16, pk[4], pk[5], pk[6], pk[7]);
           }
         }
-        if (valid) P.asc[static_cast<int64_t>(c.nt) * P.a_ld + row] = words;
+        if (valid) P.asc[c.nt * P.a_ld + mx_scale_pos(mx_group_row0(c.row0, c.g) + local)] = words;
       } else {
         __nv_bfloat16* orow = P.y + row * P.out_ld + c.nt * 256;
 #pragma unroll 1
@@ -321,28 +301,30 @@ __global__ void __launch_bounds__(256, 1) gemm_mx_persistent(const __grid_consta
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty);
+      if (leader) mbar_arrive(tempty);
+      else remote_arrive(map_to_rank(smem_u32(tempty), 0));
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the leader's MMAs (which read the peer's shared memory) and all remote arrivals are done
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem_base, 512);
+  if (warp == 2) tmem_dealloc2(tmem_base, 512);
 }
 
 size_t mx_smem_bytes(int G) {
-  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 256 + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+  return 1024 + static_cast<size_t>(STAGES) * (CODE_BYTES + SF_BYTES) + 1024 +
+         static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
 template <bool kSwiglu>
 mok_status run_mx(const MxParams& P, cudaStream_t st) {
   const size_t smem = mx_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(gemm_mx_persistent<kSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_mx_pair_persistent<kSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MOK_ERR_CUDA;
-  gemm_mx_persistent<kSwiglu><<<num_sms(), 256, smem, st>>>(P);
+  gemm_mx_pair_persistent<kSwiglu><<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -353,22 +335,21 @@ constexpr auto kI32 = CU_TENSOR_MAP_DATA_TYPE_INT32;
 bool code_map(CUtensorMap* m, const void* p, int64_t rows, int K) {
   return make_tmap_2d(m, p, kU8, rows, K, static_cast<uint64_t>(K), 128, BKB, true);
 }
-// scale words [K/128][ld] (ld = rows rounded up to 4 words, so that the row
-// pitch is a multiple of 16 bytes) as a 2D tensor of K/128 rows of `rows` words
-bool scale_map(CUtensorMap* m, const void* p, int64_t rows, int K, uint32_t box) {
-  return make_tmap_2d(m, p, kI32, K / 128, rows, static_cast<uint64_t>(mx_scale_ld(rows)) * 4, 1, box,
-                      false);
+// scale words [K/128][ld] as a 2D tensor of K/128 rows of ld words (ld is a
+// multiple of 128), boxes of one 128-row block
+bool scale_map(CUtensorMap* m, const void* p, int64_t ld, int K) {
+  return make_tmap_2d(m, p, kI32, K / 128, ld, static_cast<uint64_t>(ld) * 4, 1, 128, false);
 }
 
 SchedArgs mx_sched(const int32_t* offsets, int G, int64_t m_total, int n_tiles, int k_blocks) {
   SchedArgs s;
   s.offsets = offsets;
-  s.G = offsets ? G : 1;
+  s.G = G;
   s.m_total = static_cast<int32_t>(m_total);
   s.n_tiles = n_tiles;
   s.m_tiles_fixed = 0;
   s.k_blocks_fixed = k_blocks;
-  s.bm = BM;
+  s.bm = 256;
   s.bk_rows = BKB;
   return s;
 }
@@ -379,21 +360,22 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
                             const void* sg, const void* qu, const void* su, const int32_t* offsets,
                             int G, int D, int I, void* aq, void* asc, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
+  if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
   P.sched = mx_sched(offsets, G, rows, I / 128, D / BKB);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
-  const int64_t wrows = static_cast<int64_t>(offsets ? G : 1) * I;
-  if (!code_map(&P.tmA, xq, rows, D) || !scale_map(&P.tmSA, xsc, rows, D, SA_WORDS) ||
+  const int64_t wrows = static_cast<int64_t>(G) * I;
+  if (!code_map(&P.tmA, xq, rows, D) || !scale_map(&P.tmSA, xsc, mx_scale_ld(rows, G), D) ||
       !code_map(&P.tmB0, qg, wrows, D) || !code_map(&P.tmB1, qu, wrows, D) ||
-      !scale_map(&P.tmSB0, sg, wrows, D, 128) || !scale_map(&P.tmSB1, su, wrows, D, 128))
+      !scale_map(&P.tmSB0, sg, mx_scale_ld(wrows), D) || !scale_map(&P.tmSB1, su, mx_scale_ld(wrows), D))
     return MOK_ERR_CUDA;
   P.b_group_rows = I;
   P.b_tile_rows = 128;
   P.b1_off = 0;
   P.aq = static_cast<uint8_t*>(aq);
   P.asc = static_cast<uint32_t*>(asc);
-  P.a_ld = static_cast<int32_t>(mx_scale_ld(rows));
+  P.a_ld = mx_scale_ld(rows, G);
   P.y = nullptr;
   P.out_ld = I;
   return run_mx<true>(P, st);
@@ -403,13 +385,14 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
                           const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
                           cudaStream_t st) {
   if (rows == 0) return MOK_OK;
+  if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
   P.sched = mx_sched(offsets, G, rows, D / 256, I / BKB);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
-  const int64_t wrows = static_cast<int64_t>(offsets ? G : 1) * D;
-  if (!code_map(&P.tmA, aq, rows, I) || !scale_map(&P.tmSA, asc, rows, I, SA_WORDS) ||
-      !code_map(&P.tmB0, qd, wrows, I) || !scale_map(&P.tmSB0, sd, wrows, I, 128))
+  const int64_t wrows = static_cast<int64_t>(G) * D;
+  if (!code_map(&P.tmA, aq, rows, I) || !scale_map(&P.tmSA, asc, mx_scale_ld(rows, G), I) ||
+      !code_map(&P.tmB0, qd, wrows, I) || !scale_map(&P.tmSB0, sd, mx_scale_ld(wrows), I))
     return MOK_ERR_CUDA;
   P.tmB1 = P.tmB0;
   P.tmSB1 = P.tmSB0;

@@ -24,8 +24,8 @@ mok_status launch_plan(const int32_t* topk, int64_t R, int E, int32_t* counts, i
 // g_route[p] = g[table[p].src].
 mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, int K, int D,
                                 void* xg, const float* g, float* g_route, cudaStream_t st);
-mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, int64_t R, int K, int D,
-                                 void* xg_q, uint8_t* xg_scale, cudaStream_t st);
+mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int32_t* offsets, int64_t R,
+                                 int K, int D, int E, void* xg_q, uint8_t* xg_scale, cudaStream_t st);
 mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
                                  uint8_t* scale, cudaStream_t st);
 // out[t] = bf16(base[t] + sum_k w[t,k] * rows[route_dst[t*K+k]]); base and w
@@ -83,12 +83,27 @@ mok_status launch_router_grad(const float* dgp, int nI, const int32_t* route_dst
                               const int32_t* topk, const float* g, const float* s, int T, int E,
                               int K, float* ds, float* dg, cudaStream_t st);
 
-// MXFP8 scale storage of a [rows][K] tensor: int32 words [K/128][ld],
-// ld = rows rounded up to a multiple of 4; word (g, r) holds the E8M0 scales
-// of row r for K columns [128 g, 128 g + 128), byte b = 32-column block b.
-inline int64_t mx_scale_ld(int64_t rows) { return (rows + 3) & ~int64_t(3); }
-inline size_t mx_scale_bytes(int64_t rows, int64_t K) {
-  return static_cast<size_t>(K / 128) * static_cast<size_t>(mx_scale_ld(rows)) * 4;
+// MXFP8 scale storage of a [rows][K] tensor: int32 words [K/128][ld] with
+// ld a multiple of 128; word (g, r) holds the E8M0 scales of row r for K
+// columns [128 g, 128 g + 128), byte b = 32-column block b.  Within each
+// aligned block of 128 rows, row 32 c + l sits at word 4 l + c: the order in
+// which tcgen05.cp (32x128b, warpx4) puts a block where the block-scaled MMA
+// reads it (lane 32 q + l, column c).
+//  plain   : row r at position r, ld = rows rounded up to 128;
+//  grouped : expert-contiguous rows (expert e owns [offsets[e], offsets[e+1]))
+//            with each expert starting a new block: row offsets[e] + i at
+//            position 128 (offsets[e] / 128 + e) + i, ld = 128 (ceil(rows/128) + E).
+__host__ __device__ inline int64_t mx_scale_pos(int64_t r) {
+  return (r & ~int64_t(127)) | ((r & 31) << 2) | ((r >> 5) & 3);
+}
+__host__ __device__ inline int64_t mx_group_row0(int64_t offset, int e) {
+  return 128 * (offset / 128 + e);
+}
+inline int64_t mx_scale_ld(int64_t rows, int groups = 0) {
+  return groups > 0 ? 128 * ((rows + 127) / 128 + groups) : (rows + 127) / 128 * 128;
+}
+inline size_t mx_scale_bytes(int64_t rows, int64_t K, int groups = 0) {
+  return static_cast<size_t>(K / 128) * static_cast<size_t>(mx_scale_ld(rows, groups)) * 4;
 }
 // MXFP8 grouped GEMMs: a codes [rows][I] + scales, y bf16 [rows][D]
 mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,

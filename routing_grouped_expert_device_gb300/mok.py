@@ -55,7 +55,7 @@ _SIGS = {
     "mok_route": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "mok_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "mok_plan_static": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
-    "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P]),
+    "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
     "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _P,
@@ -71,6 +71,7 @@ _SIGS = {
                                    ctypes.POINTER(PlanBuf), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _SZ, _P]),
     "mok_quantize_mxfp8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "mok_mxfp8_scale_bytes": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int32]),
     "mok_get_error": (ctypes.c_int, [_P]),
     "mok_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -163,9 +164,10 @@ def plan_static(topk_idx, E, counts, offsets, table, route_dst, stream=None):
                                          _ptr(route_dst), _stream(stream)), "mok_plan_static")
 
 
-def dispatch(shape: Shape, x, table, xg, xg_scale=None, stream=None):
-    _check(_lib_handle().mok_dispatch(ctypes.byref(shape), _ptr(x), _ptr(table), _ptr(xg), _ptr(xg_scale),
-                                      _stream(stream)), "mok_dispatch")
+def dispatch(shape: Shape, x, table, xg, xg_scale=None, offsets=None, stream=None):
+    """Gather; for MXFP8 also quantise, which needs the plan's offsets."""
+    _check(_lib_handle().mok_dispatch(ctypes.byref(shape), _ptr(x), _ptr(table), _ptr(offsets), _ptr(xg),
+                                      _ptr(xg_scale), _stream(stream)), "mok_dispatch")
 
 
 def expert_ffn(shape: Shape, weights: Weights, xg, offsets, yg, a_out=None, ws=None, xg_scale=None, stream=None):
@@ -229,14 +231,13 @@ def quantize_mxfp8(src, q, scale, stream=None):
            "mok_quantize_mxfp8")
 
 
-def mx_scale_ld(rows: int) -> int:
-    """Row pitch (in 32-bit words) of MXFP8 scale storage: rows rounded up to 4."""
-    return (rows + 3) // 4 * 4
-
-
-def mx_scale_words(rows: int, cols: int) -> int:
-    """32-bit scale words of a [rows][cols] MXFP8 tensor ([cols/128][ld])."""
-    return cols // 128 * mx_scale_ld(rows)
+def mx_scale_words(rows: int, cols: int, groups: int = 0) -> int:
+    """32-bit scale words of a [rows][cols] MXFP8 tensor: plain layout
+    (groups = 0) or grouped over `groups` experts (mok_mxfp8_scale_bytes)."""
+    n = int(_lib_handle().mok_mxfp8_scale_bytes(rows, cols, groups))
+    if n == 0 and rows > 0:
+        raise MokError(MOK_ERR_INVALID_ARG, f"mok_mxfp8_scale_bytes({rows}, {cols}, {groups})")
+    return n // 4
 
 
 def get_error(stream=None) -> int:

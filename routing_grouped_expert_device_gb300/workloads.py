@@ -74,6 +74,9 @@ CONFIGS: Dict[str, MoEConfig] = {
     # 1/8 of the DSV3 layer (32 experts, same rows per expert): a profiling
     # case for the same kernels that still exceeds L2
     "dsv3_slice_bf16_fwd": MoEConfig("dsv3_slice_bf16_fwd", T=896, D=7168, I=2048, E=32, K=8, I_shared=2048),
+    # the same slice with MXFP8 expert GEMMs
+    "dsv3_slice_mxfp8_fwd": MoEConfig("dsv3_slice_mxfp8_fwd", T=896, D=7168, I=2048, E=32, K=8, I_shared=2048,
+                                      dtype="mxfp8"),
     # 1/8 of the fwd+bwd layer (32 experts, 128 rows per expert): a
     # profiling case for the backward kernels that still exceeds L2
     "dsv3_slice_bf16_fwdbwd": MoEConfig("dsv3_slice_bf16_fwdbwd", T=512, D=7168, I=2048, E=32, K=8,

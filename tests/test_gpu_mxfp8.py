@@ -31,10 +31,21 @@ def m():
     return mok()
 
 
-def words_to_bytes(words: torch.Tensor, rows: int, cols: int) -> np.ndarray:
+def scale_positions(rows: int, offsets=None) -> np.ndarray:
+    """Word index (within one 128-column group) of each row's scale word:
+    plain layout, or grouped by expert when offsets are given (mok.h)."""
+    r = np.arange(rows, dtype=np.int64)
+    if offsets is not None:
+        off = np.asarray(offsets, dtype=np.int64)
+        e = np.searchsorted(off, r, side="right") - 1
+        r = 128 * (off[e] // 128 + e) + r - off[e]
+    return (r & ~127) | ((r & 31) << 2) | ((r >> 5) & 3)
+
+
+def words_to_bytes(words: torch.Tensor, rows: int, cols: int, offsets=None) -> np.ndarray:
     """Scale words [cols/128][ld] -> E8M0 bytes [rows][cols/32] (the oracle's order)."""
-    ld = (rows + 3) // 4 * 4
-    w = words.cpu().numpy().view(np.uint32).reshape(cols // 128, ld)[:, :rows]
+    w = words.cpu().numpy().view(np.uint32)
+    w = w.reshape(cols // 128, w.size // (cols // 128))[:, scale_positions(rows, offsets)]
     return np.ascontiguousarray(w).view(np.uint8).reshape(cols // 128, rows, 4).transpose(1, 0, 2).reshape(
         rows, cols // 32)
 
@@ -74,20 +85,21 @@ def test_dispatch_mxfp8_bitexact(m, name):
     inp = W.make_inputs(cfg, "cpu")
     h = host(inp)
     idx, _, _ = O.route(h["s"], cfg.K)
-    _, _, table, _ = O.plan(idx, cfg.E)
+    _, offsets, table, _ = O.plan(idx, cfg.E)
     xq = torch.empty(cfg.R, cfg.D, dtype=torch.uint8, device=DEV)
-    xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D), dtype=torch.int32, device=DEV)
-    m.dispatch(m.shape_of(cfg), inp["x"].to(DEV), torch.from_numpy(table).to(DEV), xq, xs)
+    xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D, cfg.E), dtype=torch.int32, device=DEV)
+    m.dispatch(m.shape_of(cfg), inp["x"].to(DEV), torch.from_numpy(table).to(DEV), xq, xs,
+               offsets=torch.from_numpy(offsets).to(DEV))
     qr, sr = O.mxfp8_quantize(O.gather(O.bf16_to_f32(h["x"]), table, cfg.K))
     assert np.array_equal(xq.cpu().numpy(), qr)
-    assert np.array_equal(words_to_bytes(xs, cfg.R, cfg.D), sr)
+    assert np.array_equal(words_to_bytes(xs, cfg.R, cfg.D, offsets), sr)
 
 
-def _check_a_codes(aq_gpu, asc_gpu, ref_rows, rows_idx, R, I):
+def _check_a_codes(aq_gpu, asc_gpu, ref_rows, rows_idx, R, I, offsets):
     """a codes and scales equal the oracle's except in blocks holding an
     ambiguous bf16 rounding of a."""
     aq = aq_gpu.cpu().numpy()[rows_idx]
-    sb = words_to_bytes(asc_gpu, R, I)[rows_idx]
+    sb = words_to_bytes(asc_gpu, R, I, offsets)[rows_idx]
     amb = (O.bf16_flip_ulp(ref_rows["a_pre"]) > 0).reshape(len(rows_idx), I // 32, 32).any(-1)
     ok_blocks = ~amb
     assert np.array_equal(sb[ok_blocks], ref_rows["asc"][ok_blocks])
@@ -106,14 +118,14 @@ def test_expert_ffn_mxfp8_elementwise(m, name):
     idx, _, _ = O.route(h["s"], cfg.K)
     _, offsets, table, _ = O.plan(idx, cfg.E)
     shape = m.shape_of(cfg)
+    off = torch.from_numpy(offsets).to(DEV)
     xq = torch.empty(cfg.R, cfg.D, dtype=torch.uint8, device=DEV)
-    xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D), dtype=torch.int32, device=DEV)
-    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xq, xs)
+    xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D, cfg.E), dtype=torch.int32, device=DEV)
+    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xq, xs, offsets=off)
     aq = torch.empty(cfg.R, cfg.I, dtype=torch.uint8, device=DEV)
-    asc = torch.empty(m.mx_scale_words(cfg.R, cfg.I), dtype=torch.int32, device=DEV)
+    asc = torch.empty(m.mx_scale_words(cfg.R, cfg.I, cfg.E), dtype=torch.int32, device=DEV)
     yg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
     w = m.make_weights(d)
-    off = torch.from_numpy(offsets).to(DEV)
     m.expert_upgate(shape, w, xq, off, aq, xg_scale=xs, a_scale=asc)
     m.expert_down(shape, w, aq, off, yg, a_scale=asc)
     m.check_device_status()
@@ -124,7 +136,7 @@ def test_expert_ffn_mxfp8_elementwise(m, name):
         rows = h["x"][table[p0:p1, 0] // cfg.K]
         ref = O.expert_ffn_rows_mxfp8(rows, h["w_gate"][e], h["w_up"][e], h["w_down"][e])
         assert_close(yg[p0:p1].float().cpu().numpy(), ref["y"], MXFP8_TOL, f"y expert {e}")
-        _check_a_codes(aq, asc, ref, np.arange(p0, p1), cfg.R, cfg.I)
+        _check_a_codes(aq, asc, ref, np.arange(p0, p1), cfg.R, cfg.I, offsets)
     # mok_expert_ffn (both halves, a kept in the workspace) gives the same bytes
     ws = torch.empty(m.workspace_bytes(shape, m.OP_EXPERT_FFN), dtype=torch.uint8, device=DEV)
     y2 = torch.empty_like(yg)
@@ -169,8 +181,8 @@ def test_mxfp8_full_size_sampled_rows(m):
     m.check_device_status()
     assert np.array_equal(saved["table"].cpu().numpy(), table)
     xq = torch.empty(cfg.R, cfg.D, dtype=torch.uint8, device=DEV)
-    xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D), dtype=torch.int32, device=DEV)
-    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xq, xs)
+    xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D, cfg.E), dtype=torch.int32, device=DEV)
+    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xq, xs, offsets=torch.from_numpy(offsets).to(DEV))
     yg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
     fws = torch.empty(m.workspace_bytes(shape, m.OP_EXPERT_FFN), dtype=torch.uint8, device=DEV)
     m.expert_ffn(shape, m.make_weights(d), xq, torch.from_numpy(offsets).to(DEV), yg, ws=fws, xg_scale=xs)

@@ -45,3 +45,25 @@ def test_bad_arguments_rejected_on_host(m):
     assert lib.mok_moe_fwd(ctypes.byref(sh), ctypes.byref(m.Weights()), None, None, None, None, None, 0,
                            None) == m.MOK_ERR_INVALID_ARG
     assert lib.mok_quantize_mxfp8(None, 4, 33, None, None, None) == m.MOK_ERR_INVALID_ARG
+
+
+def test_mxfp8_scale_bytes(m):
+    lib = m._lib_handle()
+    # plain layout: rows rounded up to 128, one word per row and 128 columns
+    assert lib.mok_mxfp8_scale_bytes(301, 512, 0) == 4 * 384 * 4
+    assert lib.mok_mxfp8_scale_bytes(128, 128, 0) == 128 * 4
+    assert lib.mok_mxfp8_scale_bytes(0, 128, 0) == 0
+    # grouped layout: room for every expert to start a new 128-row block
+    R, D, E = 7168 * 8, 7168, 256
+    assert lib.mok_mxfp8_scale_bytes(R, D, E) == (D // 128) * 128 * (R // 128 + E) * 4
+    assert lib.mok_mxfp8_scale_bytes(301, 256, 5) == 2 * 128 * (3 + 5) * 4
+    for bad in ((10, 100, 0), (-1, 128, 0), (10, 128, -1), (10, 0, 0)):
+        assert lib.mok_mxfp8_scale_bytes(*bad) == 0
+    assert m.mx_scale_words(301, 512) == 4 * 384
+
+
+def test_mxfp8_dispatch_needs_offsets(m):
+    lib = m._lib_handle()
+    sh = m.make_shape(T=16, D=256, I=128, E=8, K=2, dtype=m.MOK_MXFP8)
+    fake = ctypes.c_void_p(256)  # never dereferenced: the call is rejected first
+    assert lib.mok_dispatch(ctypes.byref(sh), fake, fake, None, fake, fake, None) == m.MOK_ERR_INVALID_ARG

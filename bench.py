@@ -41,7 +41,7 @@ import torch  # noqa: E402
 from routing_grouped_expert_device_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MoE layer fwd/bwd tokens/s and TFLOP/s (% dense tensor peak), 1×GB300"
-KERNEL_SOURCES = ["common.cuh", "gemm_core.cuh", "gemm_fwd.cu"]
+KERNEL_SOURCES = ["common.cuh", "gemm_core.cuh", "pair.cuh", "gemm_pair.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "upgate_gemm_dsv3_bf16_fwd_traffic.txt")
 
 
@@ -249,7 +249,11 @@ def run_ours(args, world, rank, local):
     a_s = torch.empty(T, Is, dtype=bf, device=dev) if Is else None
     out = torch.empty(T, D, dtype=bf, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 1 + 3 + 1 + 1 + 1 + 1 + (2 if (Is and mx) else 0)
+    # route, plan (3), dispatch, up/gate, down, combine; the shared expert's
+    # up/gate (BF16) or whole FFN (MXFP8) on the side stream
+    launches_per_step = 1 + 3 + 1 + 1 + 1 + 1 + ((2 if mx else 1) if Is else 0)
+    side = torch.cuda.Stream() if Is else None
+    sws = torch.empty(M.workspace_bytes(shape, M.OP_SHARED_FFN), dtype=u8, device=dev) if (Is and mx) else None
 
     if cfg.backward:
         bws = torch.empty(max(M.workspace_bytes(shape, M.OP_FWD), M.workspace_bytes(shape, M.OP_BWD)),
@@ -274,17 +278,28 @@ def run_ours(args, world, rank, local):
             if ev1 is not None:
                 ev1.record(stream)
             return
+        # the same schedule as mok_moe_fwd: the shared expert depends on x
+        # alone and runs on a side stream next to route, plan, dispatch and
+        # the routed up/gate
+        if Is:
+            side.wait_stream(stream)
+            if mx:
+                M.shared_ffn(shape, w, d["x"], ys, sws, stream=side)
+            else:
+                M.expert_upgate(shape, w, None, None, None, x_shared=d["x"], a_shared=a_s, stream=side)
         M.route(d["s"], K, topk, g)
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
         M.dispatch(shape, d["x"], table, xg, xs, offsets=offsets)
         if ev0 is not None:
             ev0.record(stream)
-        # the shared expert's tiles run inside the routed launches
-        M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc, x_shared=d["x"] if Is else None,
-                        a_shared=a_s)
+        M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc)
         if ev1 is not None:
             ev1.record(stream)
-        M.expert_down(shape, w, a, offsets, yg, a_scale=asc, a_shared=a_s, ys=ys)
+        if Is:
+            stream.wait_stream(side)
+        # BF16: the shared expert's down tiles run inside the routed down launch
+        M.expert_down(shape, w, a, offsets, yg, a_scale=asc, a_shared=None if mx else a_s,
+                      ys=None if mx else ys)
         M.combine(shape, yg, ys, g, route_dst, out)
 
     for _ in range(args.warmup):
@@ -332,11 +347,8 @@ def run_ours(args, world, rank, local):
         alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + R * D * wbytes * (1 + scale_b)
                         + R * I * wbytes * (1 + scale_b))
         part_flops = 4.0 * R * D * I
-        if Is and not mx:  # the shared expert's up/gate runs in the same launch
-            alg_bytes += 2 * Is * D * 2 + T * D * 2 + T * Is * 2
-            part_flops += 4.0 * T * D * Is
-        kernel = (f"grouped up/gate + SwiGLU GEMM (tcgen05 {'MXFP8 block-scaled' if mx else 'cta_group::2'}"
-                  f"{', shared expert tiles in the same launch' if Is and not mx else ''})")
+        kernel = (f"grouped up/gate + SwiGLU GEMM (tcgen05 cta_group::2"
+                  f"{', MXFP8 block-scaled' if mx else ''}, routed experts)")
         part_tflops = part_flops / (part_ms / 1e3) / 1e12
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
     traffic = recorded_traffic(cfg.name)

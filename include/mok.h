@@ -194,7 +194,10 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
  * shape.I_shared > 0 and x_shared / a_shared (resp. a_shared / ys) are
  * non-NULL, the shared expert's up/gate (x_shared bf16 [T][D] -> a_shared
  * bf16 [T][I_shared]) or down (a_shared -> ys bf16 [T][D]) tiles are spread
- * through the routed launch (BF16; after the routed launch for MXFP8). */
+ * through the routed launch (BF16; after the routed launch for MXFP8).
+ * mok_expert_upgate with xg, offsets and a all NULL runs the shared
+ * expert's up/gate alone (x_shared -> a_shared), e.g. on a second stream
+ * while the routing, plan and dispatch run. */
 mok_status mok_expert_upgate(const mok_shape *shape, const mok_weights *w, const void *xg,
                              const uint8_t *xg_scale, const int32_t *offsets, void *a,
                              uint8_t *a_scale, const void *x_shared, void *a_shared, void *stream);
@@ -229,7 +232,11 @@ mok_status mok_combine(const mok_shape *shape, const void *yg, const void *ys, c
                        const int32_t *route_dst, void *out, void *stream);
 
 /* Whole forward: route -> plan -> dispatch -> shared FFN -> grouped FFN ->
- * combine.  x bf16 [T][D]; s fp32 [T][E]; out bf16 [T][D].  `saved`
+ * combine.  x bf16 [T][D]; s fp32 [T][E]; out bf16 [T][D].  Ordered on
+ * `stream` as one operation: the shared expert's up/gate (and, for MXFP8,
+ * its down projection) runs on an internal side stream (one per device and
+ * host thread, created on first use), forked from `stream` after the work
+ * already queued there and joined back before its output is read.  `saved`
  * (nullable) receives the routing and plan for mok_moe_bwd.  With
  * shape.dtype = MOK_MXFP8 the routed experts run in MXFP8 (dispatch
  * quantises x, the up/gate epilogue quantises a) and the shared expert in

@@ -105,6 +105,29 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
+// A non-blocking side stream and two events per device and host thread,
+// created on first use and kept for the life of the process: mok_moe_fwd
+// runs the shared expert on it, forked from and joined back into the
+// caller's stream.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_device[kMaxDevices];
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = per_device[dev];
+  if (!ss.s) {
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess)
+      return nullptr;
+  }
+  return &ss;
+}
+
 }  // namespace
 }  // namespace mok
 
@@ -187,6 +210,10 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
   if (with_shared && (!w->ws_gate || !w->ws_up || !aligned16(x_shared) || !aligned16(a_shared)))
     return MOK_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!xg && !offsets && !a) {  // the shared expert's up/gate alone
+    if (!with_shared) return MOK_ERR_INVALID_ARG;
+    return launch_upgate(x_shared, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, a_shared, st);
+  }
   if (s.dtype == MOK_MXFP8) {
     if (!xg || !xg_scale || !offsets || !a || !a_scale || !mx_weights_ok(w) || !aligned16(xg) ||
         !aligned16(xg_scale) || !aligned16(a) || !aligned16(a_scale))
@@ -300,47 +327,61 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mok_status r;
-  if ((r = launch_route(s_in, s.T, s.E, s.K, pb.topk_idx, pb.g, st)) != MOK_OK) return r;
-  if ((r = launch_plan(pb.topk_idx, R, s.E, pb.counts, pb.offsets, pb.table, pb.route_dst,
-                       at<int>(ws, L.hist), st)) != MOK_OK)
-    return r;
   void* xg = at<void>(ws, L.xg);
   void* a = at<void>(ws, L.a);
   void* yg = at<void>(ws, L.yg);
-  void* ys = nullptr;
+  void* ys = s.I_shared ? at<void>(ws, L.ys) : nullptr;
+  void* as = s.I_shared ? at<void>(ws, L.as) : nullptr;
+  // The shared expert depends on x alone (paper note, "The production
+  // details": it fills the first dispatch window).  Its up/gate (and for
+  // MXFP8 its down projection) runs on a side stream next to route, plan,
+  // dispatch and the routed up/gate; the stream joins back before the first
+  // launch that reads its output.
+  SideStream* side = nullptr;
+  bool joined = true;
+  // on an error after the fork, the caller's stream still waits for the side stream
+  auto fail = [&](mok_status e) {
+    if (!joined) cudaStreamWaitEvent(st, side->join, 0);
+    return e;
+  };
+  if (s.I_shared) {
+    if (!(side = side_stream())) return MOK_ERR_CUDA;
+    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+      return MOK_ERR_CUDA;
+    r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, side->s);
+    if (r == MOK_OK && mx) r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, side->s);
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess) return MOK_ERR_CUDA;
+    joined = false;
+    if (r != MOK_OK) return fail(r);
+  }
+  if ((r = launch_route(s_in, s.T, s.E, s.K, pb.topk_idx, pb.g, st)) != MOK_OK) return fail(r);
+  if ((r = launch_plan(pb.topk_idx, R, s.E, pb.counts, pb.offsets, pb.table, pb.route_dst,
+                       at<int>(ws, L.hist), st)) != MOK_OK)
+    return fail(r);
   if (mx) {
     if ((r = launch_dispatch_mxfp8(x, pb.table, pb.offsets, R, s.K, s.D, s.E, xg, at<uint8_t>(ws, L.xg_scale),
                                    st)) != MOK_OK)
-      return r;
-  } else if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK) {
-    return r;
-  }
-  void* as = nullptr;
-  if (s.I_shared) {
-    ys = at<void>(ws, L.ys);
-    as = at<void>(ws, L.as);
-  }
-  if (mx) {
+      return fail(r);
     void* asc = at<void>(ws, L.a_scale);
     if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
                               w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st)) != MOK_OK)
-      return r;
+      return fail(r);
     if ((r = launch_down_mx(a, asc, R, w->q_down, w->sc_down, pb.offsets, s.E, s.D, s.I, yg, st)) !=
         MOK_OK)
-      return r;
-    if (s.I_shared) {  // the shared expert stays BF16
-      if ((r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, st)) != MOK_OK)
-        return r;
-      if ((r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st)) != MOK_OK)
-        return r;
-    }
+      return fail(r);
   } else {
-    // the shared expert's tiles run inside the routed launches
-    SharedOperands sh_up{x, s.T, w->ws_gate, w->ws_up, s.I_shared, as};
+    if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK) return fail(r);
+    if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr)) !=
+        MOK_OK)
+      return fail(r);
+  }
+  if (!joined) {
+    joined = true;
+    if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return MOK_ERR_CUDA;
+  }
+  if (!mx) {
+    // the shared expert's down tiles run inside the routed down launch
     SharedOperands sh_dn{as, s.T, w->ws_down, nullptr, s.I_shared, ys};
-    if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st,
-                                s.I_shared ? &sh_up : nullptr)) != MOK_OK)
-      return r;
     if ((r = launch_down_pair(a, R, w->w_down, pb.offsets, s.E, R, s.D, s.I, yg, st,
                               s.I_shared ? &sh_dn : nullptr)) != MOK_OK)
       return r;

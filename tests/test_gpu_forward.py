@@ -277,10 +277,19 @@ def test_split_expert_entry_points_match_expert_ffn(m):
     ys2 = torch.empty_like(ys1)
     sws = torch.empty(m.workspace_bytes(shape, m.OP_SHARED_FFN), dtype=torch.uint8, device=DEV)
     m.shared_ffn(shape, m.make_weights(d), d["x"], ys2, sws)
+    # the shared expert's up/gate alone (routed operands NULL) on a second stream
+    as2 = torch.empty_like(as_)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    m.expert_upgate(shape, m.make_weights(d), None, None, None, x_shared=d["x"], a_shared=as2, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
     m.check_device_status()
     assert torch.equal(a1.view(torch.int16), a3.view(torch.int16))
     assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
     assert torch.equal(ys1.view(torch.int16), ys2.view(torch.int16))
+    assert torch.equal(as_.view(torch.int16), as2.view(torch.int16))
+    with pytest.raises(m.MokError):  # no routed operands and no shared expert: nothing to run
+        m.expert_upgate(shape, m.make_weights(d), None, None, None)
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "skew_small"])

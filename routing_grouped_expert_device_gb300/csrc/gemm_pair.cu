@@ -25,6 +25,7 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = 128 * BK * 2;  // this CTA's 128 rows
 constexpr int B_BYTES = 128 * BK * 2;  // this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_BLOCK = 32 * 128;  // one epilogue warp's staging block: 32 rows x 64 bf16
 constexpr uint32_t IDESC = idesc_bf16(256, 256, false, false);
 
 __device__ __forceinline__ void mma2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
@@ -44,11 +45,13 @@ struct PairParams {
   int32_t b_group_rows, b_tile_rows, b1_off;
   __nv_bfloat16* out;
   int32_t out_ld;
+  CUtensorMap tmOut;  // out as [rows][out_ld], boxes 32 rows x 64 columns, 128-byte swizzle
   // The extra group of the schedule (the shared expert): its own A, B and
   // output (B rows nt * b_tile_rows + (rank ? b1_off : 0), as above).
   CUtensorMap tmAs, tmBs0, tmBs1;
   __nv_bfloat16* out_s;
   int32_t out_ld_s;
+  CUtensorMap tmOut_s;
 };
 
 template <bool kSwiglu>
@@ -57,7 +60,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi_smem = smem + STAGES * STAGE_BYTES;  // 4 staging blocks, 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + 4 * EPI_BLOCK);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -65,7 +69,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
-  int* tstart = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 1024);
+  int* tstart = reinterpret_cast<int*>(epi_smem + 4 * EPI_BLOCK + 1024);
   int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -188,7 +192,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
+    // Each warp owns 32 rows of the tile.  Per 64 output columns it packs its
+    // rows to bf16, writes them to its staging block in the 128-byte swizzle
+    // of the output's tensor map (16-byte chunk c of row r at chunk c ^ (r % 8))
+    // and issues one TMA store, so whole rows leave in bulk instead of
+    // 16-byte pieces of 32 rows.  A 32-row slab that crosses the group's end
+    // is written row by row (lanes past the end write nothing): a TMA store
+    // would overwrite the next group's rows.
     const int ew = warp - 4;
+    uint8_t* blk = epi_smem + ew * EPI_BLOCK;
+    uint8_t* srow = blk + lane * 128;
     int it = 0;
     for (int tile = cid; tile < total; tile += ncl, ++it) {
       const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
@@ -198,50 +211,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(ew * 32) << 16);
-      const int r = static_cast<int>(rank) * 128 + ew * 32 + lane;  // row within the 256-row tile
-      const bool valid = c.mt * 256 + r < c.rows;
-      __nv_bfloat16* orow = c.extra ? P.out_s + static_cast<size_t>(c.mt * 256 + r) * P.out_ld_s
-                                    : P.out + static_cast<size_t>(c.row0 + c.mt * 256 + r) * P.out_ld;
-      if (kSwiglu) {
-        orow += c.nt * 128;
+      const int slab = c.mt * 256 + static_cast<int>(rank) * 128 + ew * 32;  // first row of this warp in the group
+      const int nvalid = min(max(c.rows - slab, 0), 32);
+      const int y = (c.extra ? 0 : c.row0) + slab;  // its row in the output tensor
+      const CUtensorMap* tmOut = c.extra ? &P.tmOut_s : &P.tmOut;
+      __nv_bfloat16* orow = c.extra ? P.out_s + static_cast<size_t>(y + lane) * P.out_ld_s
+                                    : P.out + static_cast<size_t>(y + lane) * P.out_ld;
+      constexpr int kBoxes = kSwiglu ? 2 : 4;  // 64-column boxes: a 128 columns, y 256
+      const int x0 = c.nt * (kSwiglu ? 128 : 256);
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t h[32], u[32];
-          tmem_ld32(taddr + ch * 32, h);
-          tmem_ld32(taddr + 128 + ch * 32, u);
-          tmem_ld_wait();
-          uint32_t pk[16];
+      for (int bx = 0; bx < kBoxes && nvalid > 0; ++bx) {
+        uint32_t pk[32];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(silu_f(__uint_as_float(h[2 * j])) * __uint_as_float(u[2 * j]),
-                                silu_f(__uint_as_float(h[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
-          if (valid) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ch = 2 * bx + hh;
+          if (kSwiglu) {
+            uint32_t h[32], u[32];
+            tmem_ld32(taddr + ch * 32, h);
+            tmem_ld32(taddr + 128 + ch * 32, u);
+            tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int j = 0; j < 16; ++j)
+              pk[hh * 16 + j] = pack_bf16x2(silu_f(__uint_as_float(h[2 * j])) * __uint_as_float(u[2 * j]),
+                                            silu_f(__uint_as_float(h[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
+          } else {
+            uint32_t v[32];
+            tmem_ld32(taddr + ch * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[hh * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
           }
         }
-      } else {
-        orow += c.nt * 256;
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(taddr + ch * 32, v);
-          tmem_ld_wait();
-          uint32_t pk[16];
+        if (nvalid == 32) {
+          if (lane == 0) bulk_wait_read0();  // the block's previous store has read it
+          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          if (valid) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_global_v4(orow + ch * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(srow + ((q ^ (lane & 7)) * 16)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmOut, blk, x0 + bx * 64, y);
+            bulk_commit();
           }
+        } else if (lane < nvalid) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_global_v4(orow + x0 + bx * 64 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
       tc_fence_before();
       if (leader) mbar_arrive(&tempty[acc]);
       else remote_arrive(map_to_rank(smem_u32(&tempty[acc]), 0));
     }
+    if (lane == 0) bulk_wait0();  // every store of this warp has landed before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -251,7 +277,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 }
 
 size_t pair_smem_bytes(int G) {
-  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 1024 + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 4 * EPI_BLOCK + 1024 +
+         static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
 template <bool kSwiglu>
@@ -281,6 +308,24 @@ SchedArgs pair_sched(const int32_t* offsets, int G, int64_t m_total, int n_tiles
 }
 
 constexpr auto kBF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+
+// Output [rows][ld] bf16 for the epilogue's TMA stores (32 x 64 boxes).
+bool out_map(CUtensorMap* m, const void* p, int64_t rows, int ld) {
+  return make_tmap_2d(m, p, kBF16, static_cast<uint64_t>(rows > 0 ? rows : 1), ld, static_cast<uint64_t>(ld) * 2, 32,
+                      64, true);
+}
+
+// Every launch needs valid output maps; with no routed rows (or no extra
+// group) the unused one repeats the other.
+bool set_out_maps(PairParams& P, int64_t m_total) {
+  const bool routed = m_total > 0 && P.out;
+  const bool extra = P.sched.extra_rows > 0 && P.out_s;
+  if (routed && !out_map(&P.tmOut, P.out, m_total, P.out_ld)) return false;
+  if (extra && !out_map(&P.tmOut_s, P.out_s, P.sched.extra_rows, P.out_ld_s)) return false;
+  if (!routed) P.tmOut = P.tmOut_s;
+  if (!extra) P.tmOut_s = P.tmOut;
+  return routed || extra;
+}
 
 }  // namespace
 
@@ -322,6 +367,7 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
     P.out_s = static_cast<__nv_bfloat16*>(sh->out);
     P.out_ld_s = Is;
   }
+  if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
   return run_pair<true>(P, st);
 }
 
@@ -362,6 +408,7 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
     P.out_s = static_cast<__nv_bfloat16*>(sh->out);
     P.out_ld_s = D;
   }
+  if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
   return run_pair<false>(P, st);
 }
 

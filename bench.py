@@ -333,7 +333,8 @@ def run_ours(args, world, rank, local):
     # A long timed region runs under the 1.4 kW power cap, so its peak is the
     # sustained cuBLAS figure (measured the same way); a short one that kept
     # the SM clock near its maximum is compared with the burst figure.
-    capped = bool(clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"])
+    ck = clk or {}
+    capped = bool(ck.get("sm_mhz") and ck.get("sm_max_mhz") and ck["sm_mhz"] < 0.95 * ck["sm_max_mhz"])
     bf16_peak = peaks["bf16_sustained"] if (capped and peaks.get("bf16_sustained")) else peaks["bf16"]
     # fp8 dense rate is twice bf16 on this part (nominal 4.5 vs 2.25 PFLOP/s)
     tensor_peak = bf16_peak * (2.0 if mx else 1.0)

@@ -55,6 +55,9 @@ def parse_args():
     p.add_argument("--config", default="dsv3_bf16_fwd")
     p.add_argument("--cpu-sample-tokens", type=int, default=48)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--chunk-rows", type=int, default=0,
+                   help="BF16 forward: gather through a ring of chunks of this many routed rows "
+                        "(512..32768; 0 = whole-batch dispatch)")
     return p.parse_args()
 
 
@@ -221,7 +224,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     d = W.make_inputs(cfg, dev, seed=rank)
     T, D, I, E, K, Is, R = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, cfg.R
-    shape = M.shape_of(cfg)
+    ring = args.chunk_rows > 0 and not mx and not cfg.backward
+    shape = M.shape_of(cfg, chunk_rows=args.chunk_rows if ring else 0)
     i32, f32, bf, u8 = torch.int32, torch.float32, torch.bfloat16, torch.uint8
     if mx:
         # weights are model parameters: quantised once, outside the timed region
@@ -240,7 +244,8 @@ def run_ours(args, world, rank, local):
     table = torch.empty(R, 3, dtype=i32, device=dev)
     route_dst = torch.empty(R, dtype=i32, device=dev)
     pws = torch.empty(M.workspace_bytes(shape, M.OP_PLAN), dtype=u8, device=dev)
-    xg = torch.empty(R, D, dtype=u8 if mx else bf, device=dev)
+    xg = None if ring else torch.empty(R, D, dtype=u8 if mx else bf, device=dev)
+    rws = torch.empty(M.workspace_bytes(shape, M.OP_RING), dtype=u8, device=dev) if ring else None
     xs = torch.empty(M.mx_scale_words(R, D, E), dtype=i32, device=dev) if mx else None
     a = torch.empty(R, I, dtype=u8 if mx else bf, device=dev)
     asc = torch.empty(M.mx_scale_words(R, I, E), dtype=i32, device=dev) if mx else None
@@ -251,7 +256,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
     # route, plan (3), dispatch, up/gate, down, combine; the shared expert's
     # up/gate (BF16) or whole FFN (MXFP8) on the side stream
-    launches_per_step = 1 + 3 + 1 + 1 + 1 + 1 + ((2 if mx else 1) if Is else 0)
+    launches_per_step = 1 + 3 + (0 if ring else 1) + 1 + 1 + 1 + ((2 if mx else 1) if Is else 0)
     side = torch.cuda.Stream() if Is else None
     sws = torch.empty(M.workspace_bytes(shape, M.OP_SHARED_FFN), dtype=u8, device=dev) if (Is and mx) else None
 
@@ -289,10 +294,14 @@ def run_ours(args, world, rank, local):
                 M.expert_upgate(shape, w, None, None, None, x_shared=d["x"], a_shared=a_s, stream=side)
         M.route(d["s"], K, topk, g)
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
-        M.dispatch(shape, d["x"], table, xg, xs, offsets=offsets)
+        if not ring:
+            M.dispatch(shape, d["x"], table, xg, xs, offsets=offsets)
         if ev0 is not None:
             ev0.record(stream)
-        M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc)
+        if ring:  # the dispatch runs inside the up/gate launch (producer warps, ring of chunks)
+            M.expert_upgate_ring(shape, w, d["x"], table, offsets, a, rws)
+        else:
+            M.expert_upgate(shape, w, xg, offsets, a, xg_scale=xs, a_scale=asc)
         if ev1 is not None:
             ev1.record(stream)
         if Is:
@@ -351,14 +360,16 @@ def run_ours(args, world, rank, local):
         # grouped up/gate + SwiGLU: each expert's W_gate/W_up tile is read once
         # per 128..256 routed rows (HBM-bound below ~290 FLOP/B for bf16)
         scale_b = (1 / 32) if mx else 0.0
-        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + R * D * wbytes * (1 + scale_b)
+        # (with the ring: x read once instead of xg; the ring itself stays on chip)
+        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + (T if ring else R) * D * wbytes * (1 + scale_b)
                         + R * I * wbytes * (1 + scale_b))
         part_flops = 4.0 * R * D * I
         kernel = (f"grouped up/gate + SwiGLU GEMM (tcgen05 cta_group::2"
-                  f"{', MXFP8 block-scaled' if mx else ''}, routed experts)")
+                  f"{', MXFP8 block-scaled' if mx else ''}, routed experts"
+                  f"{f', ring dispatch in the same launch, chunk {args.chunk_rows} rows' if ring else ''})")
         part_tflops = part_flops / (part_ms / 1e3) / 1e12
     achieved = alg_bytes / (part_ms / 1e3) / 1e9
-    traffic = recorded_traffic(cfg.name)
+    traffic = None if ring else recorded_traffic(cfg.name)
     roofline = {"kernel": kernel, "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
@@ -427,6 +438,7 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), logits~N(0,1) softmax; bf16)",
             "config": {"workload": cfg.name, "T": T, "D": D, "I": I, "E": E, "K": K, "I_shared": Is,
                        "global_batch": world * T, "parallelism": f"replicas x{world}",
+                       "chunk_rows": args.chunk_rows if ring else 0,
                        "l2": "inputs larger than L2: every step streams all expert weights "
                              f"({(nonempty * 3 * I * D + 3 * Is * D) * 2 / 1e9:.1f} GB)"},
             "tflops": round(tflops, 1), "tensor_frac": round(tflops / tensor_peak, 4),

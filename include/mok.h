@@ -62,14 +62,18 @@ typedef enum {
   MOK_OP_EXPERT_FFN = 1,
   MOK_OP_SHARED_FFN = 2,
   MOK_OP_FWD = 3,
-  MOK_OP_BWD = 4
+  MOK_OP_BWD = 4,
+  MOK_OP_RING = 5
 } mok_op;
 
 /* Layer shape.  I_shared = 0 means no shared expert.  dtype selects the
  * arithmetic of the routed experts (the shared expert is always BF16).
- * chunk_rows: routed rows per dispatch chunk (0 = whole batch; else
- * 512..32768, the overlap granularity b of the Mixture-of-Kittens paper
- * note, "Granularity as a tunable").  producer_sms: reserved, must be 0. */
+ * chunk_rows: routed rows per dispatch chunk b (the overlap granularity of
+ * the Mixture-of-Kittens paper note, "Granularity as a tunable"): 0 = the
+ * dispatch gathers the whole batch before the expert GEMMs; 512..32768 =
+ * the BF16 forward gathers through a ring of 4 chunks that producer warps
+ * fill while the up/gate GEMM consumes it (mok_expert_upgate_ring).
+ * producer_sms: reserved, must be 0. */
 typedef struct {
   int32_t T, D, I, E, K, I_shared;
   int32_t dtype;
@@ -201,20 +205,26 @@ mok_status mok_expert_ffn(const mok_shape *shape, const mok_weights *w, const vo
 mok_status mok_expert_upgate(const mok_shape *shape, const mok_weights *w, const void *xg,
                              const uint8_t *xg_scale, const int32_t *offsets, void *a,
                              uint8_t *a_scale, const void *x_shared, void *a_shared, void *stream);
-/* mok_expert_upgate with the dispatch fused in (BF16): the grouped operand's
- * row p is x[table[p].src_index / K], fetched by the GEMM's TMA producer
- * straight from x bf16 [T][D] into shared memory (blog, "Scheduling":
- * tokens land where the expert GEMM reads them, zero local copies), so no
- * gathered copy of x is written (16-byte asynchronous copies, eight lanes per
- * 128-byte row piece).  table: mok_plan's [R][3].  a bf16 [R][I].
- * Results are bit-identical to mok_dispatch followed by mok_expert_upgate.
- * It saves the R x D gathered copy (0.8 GB for the DSV3 shapes) at a cost in
- * speed: one producer warp feeding 128 scattered rows per K block keeps far
- * fewer bytes in flight than a tiled TMA load, so mok_moe_fwd uses the
- * explicit dispatch. */
-mok_status mok_expert_upgate_gather(const mok_shape *shape, const mok_weights *w, const void *x,
-                                    const int32_t *table, const int32_t *offsets, void *a,
-                                    void *stream);
+/* mok_expert_upgate with the dispatch fused in as a ring (BF16; blog,
+ * "Scheduling": rows land expert-contiguous with no second local copy;
+ * paper note, "Granularity as a tunable" and "A ring buffer instead of a
+ * host round-trip").  Routed row p (expert order) is x[table[p].src_index /
+ * K], x bf16 [T][D], table mok_plan's [R][3].  Inside the same launch,
+ * warps 2 and 3 of every CTA are producers: chunk by chunk (b =
+ * shape.chunk_rows routed rows, 0 = 2048) they copy their share of the
+ * chunk's rows into a ring of 4 chunks in `ws` with coalesced 16-byte vector
+ * loads and stores and count themselves in on a per-chunk device counter.
+ * Before loading a tile's rows the GEMM's TMA warp waits for their chunks;
+ * once a tile's loads have landed its MMA thread counts the rows as read, and
+ * a producer refills a slot only after every N tile has read the chunk it
+ * holds.  All waits are bounded (MOK_ERR_TIMEOUT on expiry) and the launch
+ * is cooperative, so producers and consumers are resident together.
+ * a bf16 [R][I], bit-identical to mok_dispatch followed by mok_expert_upgate.
+ * ws: mok_workspace_bytes(MOK_OP_RING) bytes (the ring, 4 b + 128 rows of
+ * D bf16, and 2 ceil(R / b) counters), 256-byte aligned. */
+mok_status mok_expert_upgate_ring(const mok_shape *shape, const mok_weights *w, const void *x,
+                                  const int32_t *table, const int32_t *offsets, void *a, void *ws,
+                                  size_t ws_bytes, void *stream);
 mok_status mok_expert_down(const mok_shape *shape, const mok_weights *w, const void *a,
                            const uint8_t *a_scale, const int32_t *offsets, void *yg,
                            const void *a_shared, void *ys, void *stream);
@@ -240,7 +250,8 @@ mok_status mok_combine(const mok_shape *shape, const void *yg, const void *ys, c
  * (nullable) receives the routing and plan for mok_moe_bwd.  With
  * shape.dtype = MOK_MXFP8 the routed experts run in MXFP8 (dispatch
  * quantises x, the up/gate epilogue quantises a) and the shared expert in
- * BF16. */
+ * BF16.  BF16 with shape.chunk_rows > 0 gathers through the ring of
+ * mok_expert_upgate_ring instead of a whole-batch dispatch. */
 mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void *x,
                        const float *s, void *out, mok_plan_buf *saved, void *ws,
                        size_t ws_bytes, void *stream);

@@ -37,8 +37,11 @@ struct Carve {
 
 struct FwdLayout {
   size_t topk, g, counts, offsets, table, route_dst, hist, xg, xg_scale, a, a_scale, yg, as, ys,
-      total;
+      ring_counters, total;
 };
+
+// The BF16 forward with chunk_rows > 0 gathers through a ring (no xg).
+bool uses_ring(const mok_shape& s) { return s.dtype == MOK_BF16 && s.chunk_rows > 0; }
 
 FwdLayout fwd_layout(const mok_shape& s) {
   const size_t T = s.T, D = s.D, I = s.I, E = s.E, K = s.K, Is = s.I_shared, R = T * K;
@@ -51,7 +54,11 @@ FwdLayout fwd_layout(const mok_shape& s) {
   L.table = c.take(R * 12);
   L.route_dst = c.take(R * 4);
   L.hist = c.take(plan_scratch_bytes(static_cast<int64_t>(R), s.E));
-  L.xg = c.take(R * D * (s.dtype == MOK_MXFP8 ? 1 : 2));
+  const bool ring = uses_ring(s);
+  const int64_t b = ring_chunk(s.chunk_rows);
+  // xg holds the ring when the forward gathers through one
+  L.xg = c.take(ring ? ring_bytes(static_cast<int64_t>(R), D, b) : R * D * (s.dtype == MOK_MXFP8 ? 1 : 2));
+  L.ring_counters = c.take(ring ? ring_counter_bytes(static_cast<int64_t>(R), b) : 0);
   const bool mx = s.dtype == MOK_MXFP8;
   L.xg_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
   L.a = c.take(R * I * 2);
@@ -143,6 +150,10 @@ extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
     case MOK_OP_SHARED_FFN: return round_up(static_cast<size_t>(s.T) * (s.I_shared ? s.I_shared : 1) * 2);
     case MOK_OP_FWD: return fwd_layout(s).total;
     case MOK_OP_BWD: return bwd_layout(s).total;
+    case MOK_OP_RING: {
+      const int64_t b = ring_chunk(s.chunk_rows);
+      return round_up(ring_bytes(R, s.D, b)) + round_up(ring_counter_bytes(R, b));
+    }
   }
   return 0;
 }
@@ -232,9 +243,9 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
                             with_shared ? &sh : nullptr);
 }
 
-extern "C" mok_status mok_expert_upgate_gather(const mok_shape* shape, const mok_weights* w,
-                                               const void* x, const int32_t* table,
-                                               const int32_t* offsets, void* a, void* stream) {
+extern "C" mok_status mok_expert_upgate_ring(const mok_shape* shape, const mok_weights* w, const void* x,
+                                             const int32_t* table, const int32_t* offsets, void* a, void* ws,
+                                             size_t ws_bytes, void* stream) {
   if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
@@ -243,8 +254,14 @@ extern "C" mok_status mok_expert_upgate_gather(const mok_shape* shape, const mok
   if (!x || !table || !offsets || !a || !w->w_gate || !w->w_up || !aligned16(x) || !aligned16(a) ||
       !aligned16(w->w_gate) || !aligned16(w->w_up))
     return MOK_ERR_INVALID_ARG;
-  return launch_upgate(x, s.T, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a,
-                       static_cast<cudaStream_t>(stream), table, s.K);
+  const int64_t b = ring_chunk(s.chunk_rows);
+  const size_t ring = round_up(ring_bytes(R, s.D, b));
+  if (!ws || ws_bytes < ring + round_up(ring_counter_bytes(R, b)) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOK_ERR_WORKSPACE;
+  return launch_upgate_ring(x, table, s.K, w->w_gate, w->w_up, offsets, s.E, R, s.D, s.I, a, ws,
+                            ring_rows_for(R, b), static_cast<int>(b),
+                            reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + ring),
+                            static_cast<cudaStream_t>(stream));
 }
 
 extern "C" mok_status mok_expert_down(const mok_shape* shape, const mok_weights* w, const void* a,
@@ -370,10 +387,20 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
         MOK_OK)
       return fail(r);
   } else {
-    if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK) return fail(r);
-    if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr)) !=
-        MOK_OK)
-      return fail(r);
+    if (uses_ring(s)) {
+      // the dispatch runs inside the up/gate launch, through the ring in xg
+      const int64_t b = ring_chunk(s.chunk_rows);
+      if ((r = launch_upgate_ring(x, pb.table, s.K, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, xg,
+                                  ring_rows_for(R, b), static_cast<int>(b), at<int32_t>(ws, L.ring_counters),
+                                  st)) != MOK_OK)
+        return fail(r);
+    } else {
+      if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
+        return fail(r);
+      if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr)) !=
+          MOK_OK)
+        return fail(r);
+    }
   }
   if (!joined) {
     joined = true;

@@ -21,6 +21,8 @@ enum : int {
   SITE_MMA = 2 << 8,
   SITE_EPILOGUE = 3 << 8,
   SITE_DRAIN = 4 << 8,
+  SITE_RING_SLOT = 5 << 8,   // a ring producer waiting for a slot to be consumed
+  SITE_RING_CHUNK = 6 << 8,  // a GEMM waiting for a ring chunk to be produced
 };
 
 __device__ __forceinline__ void report(int* status, int code) {

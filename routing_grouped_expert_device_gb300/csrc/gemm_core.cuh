@@ -39,6 +39,10 @@ struct SchedArgs {
   int32_t extra_rows = 0;
   int32_t extra_n_tiles = 0;
   int32_t extra_k_blocks = 0;
+  // Order of a group's tiles: N tile outer, M tile fastest (default: the M
+  // tiles that share a weight tile run together), or M tile outer (rows are
+  // consumed in order, as a ring dispatch needs).
+  int32_t m_outer = 0;
 };
 
 struct TileCoord {
@@ -136,8 +140,13 @@ __device__ __forceinline__ TileCoord decode_group_tile(const SchedArgs& s, const
   c.rows = rstart[lo + 1] - c.row0;
   const int mtiles = sched_m_tiles(s, c.rows);
   const int local = tile - tstart[lo];
-  c.nt = local / mtiles;
-  c.mt = local - c.nt * mtiles;
+  if (s.m_outer) {
+    c.mt = local / s.n_tiles;
+    c.nt = local - c.mt * s.n_tiles;
+  } else {
+    c.nt = local / mtiles;
+    c.mt = local - c.nt * mtiles;
+  }
   c.kblocks = sched_k_blocks(s, c.rows);
   return c;
 }

@@ -52,9 +52,124 @@ struct PairParams {
   __nv_bfloat16* out_s;
   int32_t out_ld_s;
   CUtensorMap tmOut_s;
+  // Ring dispatch (kRing): tmA maps the ring, [ring_rows + 128][D]; row r
+  // (expert order) sits at ring row r % ring_rows, and ring rows 0..127 are
+  // repeated after the end so that no 128-row box wraps.
+  const uint4* x;          // [T][D] bf16, as 16-byte vectors
+  const int32_t* table;    // the plan's [R][3]: row r comes from x[table[r].src / K]
+  int32_t K, D8;           // top-k; D / 8
+  uint4* ring;
+  int64_t ring_rows, R;
+  int32_t chunk_rows, nchunks, n_tiles;
+  int32_t* ready;          // [nchunks]: producer warps done with the chunk
+  int32_t* done;           // [nchunks]: (row, N tile) reads of the chunk completed
 };
 
-template <bool kSwiglu>
+// ---------------------------------------------------------------------------
+// Ring dispatch (Mixture-of-Kittens blog, "Scheduling"; paper note,
+// "Granularity as a tunable" and "A ring buffer instead of a host
+// round-trip"): producer warps gather routed rows of x into an
+// expert-ordered ring in chunks of b rows and signal each finished chunk
+// through a device counter; the GEMM's TMA warp waits for the chunks its
+// rows lie in, and the MMA thread reports the rows it has read so that the
+// slot can be refilled.  All CTAs of the launch are resident (cooperative
+// launch), and every wait is bounded.
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Spin until *p >= target; false (and MOK_ERR_TIMEOUT | site) past the budget
+// or once another role of the CTA has given up.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort, int* status,
+                                           int site) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (ld_acquire(p) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitBudgetNs) {
+      *abort = 1;
+      report(status, MOK_ERR_TIMEOUT | site);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+__device__ __forceinline__ int64_t ring_slots(const PairParams& P) { return P.ring_rows / P.chunk_rows; }
+__device__ __forceinline__ int chunk_row_count(const PairParams& P, int c) {
+  const int64_t r0 = static_cast<int64_t>(c) * P.chunk_rows;
+  const int64_t r1 = r0 + P.chunk_rows < P.R ? r0 + P.chunk_rows : P.R;
+  return static_cast<int>(r1 - r0);
+}
+
+// Producer warp `pw` of `np`: rows r = c b + pw, c b + pw + np, ... of every
+// chunk c in order.  Before writing chunk c it waits until chunk c - slots
+// (same ring slot) has been read by all its N tiles.
+__device__ void ring_produce(const PairParams& P, int pw, int np, int lane, volatile int* abort) {
+  const int64_t slots = ring_slots(P);
+  for (int c = 0; c < P.nchunks; ++c) {
+    if (c >= slots) {
+      bool ok = true;
+      if (lane == 0)
+        ok = wait_count(P.done + (c - slots), chunk_row_count(P, c - static_cast<int>(slots)) * P.n_tiles, abort,
+                        P.status, SITE_RING_SLOT);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    }
+    const int64_t r0 = static_cast<int64_t>(c) * P.chunk_rows;
+    const int64_t r1 = r0 + chunk_row_count(P, c);
+    for (int64_t r = r0 + pw; r < r1; r += np) {
+      const int src = __ldg(P.table + r * 3) / P.K;
+      const uint4* in = P.x + static_cast<int64_t>(src) * P.D8;
+      const int64_t q = r % P.ring_rows;
+      uint4* out = P.ring + q * P.D8;
+      uint4* mirror = q < 128 ? P.ring + (P.ring_rows + q) * P.D8 : nullptr;
+      int i = lane;
+      for (; i + 96 < P.D8; i += 128) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = __ldg(in + i + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          out[i + 32 * u] = v[u];
+          if (mirror) mirror[i + 32 * u] = v[u];
+        }
+      }
+      for (; i < P.D8; i += 32) {
+        const uint4 v = __ldg(in + i);
+        out[i] = v;
+        if (mirror) mirror[i] = v;
+      }
+    }
+    // the chunk's rows of this warp are written: make them visible to the
+    // consumers' TMA (async proxy) reads, then count this warp in
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0) red_release_add(P.ready + c, 1);
+  }
+}
+
+// Rows [max(r0, g0), min(r0 + 128, g1)) of a 128-row box that lie inside its
+// group [g0, g1): their chunks, and per chunk the count of those rows.
+template <class F>
+__device__ __forceinline__ void for_box_chunks(const PairParams& P, int64_t r0, int64_t g0, int64_t g1, F f) {
+  const int64_t v0 = r0 > g0 ? r0 : g0;
+  const int64_t v1 = r0 + 128 < g1 ? r0 + 128 : g1;
+  for (int64_t v = v0; v < v1;) {
+    const int c = static_cast<int>(v / P.chunk_rows);
+    const int64_t e = (static_cast<int64_t>(c) + 1) * P.chunk_rows < v1 ? (static_cast<int64_t>(c) + 1) * P.chunk_rows : v1;
+    f(c, static_cast<int>(e - v));
+    v = e;
+  }
+}
+
+template <bool kSwiglu, bool kRing = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_persistent(const __grid_constant__ PairParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -117,6 +232,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const int brow = c.g * P.b_group_rows + c.nt * P.b_tile_rows + (rank ? P.b1_off : 0);
         const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
         const CUtensorMap* tmB = c.extra ? (rank ? &P.tmBs1 : &P.tmBs0) : (rank ? &P.tmB1 : &P.tmB0);
+        int ay = arow;
+        if (kRing && !c.extra) {
+          // this CTA's rows of the tile must be in the ring
+          for_box_chunks(P, arow, c.row0, static_cast<int64_t>(c.row0) + c.rows, [&](int ch, int) {
+            if (ok) ok = wait_count(P.ready + ch, 2 * static_cast<int>(gridDim.x), abort_flag, P.status, SITE_RING_CHUNK);
+          });
+          if (!ok) break;
+          fence_proxy_async_global();
+          ay = static_cast<int>(arow % P.ring_rows);
+        }
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
             ok = false;
@@ -125,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
           uint8_t* st = smem + stage * STAGE_BYTES;
-          tma_load_2d_pair(st, tmA, kb * BK, arow, lbar);
+          tma_load_2d_pair(st, tmA, kb * BK, ay, lbar);
           tma_load_2d_pair(st + A_BYTES, tmB, kb * BK, brow, lbar);
           issued[stage] = true;
           issued_parity[stage] = phase;
@@ -162,6 +287,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA));
           if (!ok) break;
           tc_fence_after();
+          if (kRing && !c.extra && kb == c.kblocks - 1 && lane == 0) {
+            // every load of this tile (both CTAs) has landed: its ring rows
+            // are read for this N tile
+            for (int h = 0; h < 2; ++h)
+              for_box_chunks(P, static_cast<int64_t>(c.row0) + c.mt * 256 + h * 128, c.row0,
+                             static_cast<int64_t>(c.row0) + c.rows, [&](int ch, int n) { red_release_add(P.done + ch, n); });
+          }
           if (lane == 0) {
             const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
             const uint32_t b = a + A_BYTES;
@@ -190,6 +322,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         }
       }
     }
+  } else if (kRing && (warp == 2 || warp == 3)) {
+    // ---------------- ring producers (every CTA: warps 2 and 3) ----------------
+    ring_produce(P, static_cast<int>(blockIdx.x) * 2 + (warp - 2), 2 * static_cast<int>(gridDim.x), lane, abort_flag);
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
     // Each warp owns 32 rows of the tile.  Per 64 output columns it packs its
@@ -281,15 +416,31 @@ size_t pair_smem_bytes(int G) {
          static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
-template <bool kSwiglu>
+template <bool kSwiglu, bool kRing = false>
 mok_status run_pair(const PairParams& P, cudaStream_t st) {
   const size_t smem = pair_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(gemm_pair_persistent<kSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+  auto kern = gemm_pair_persistent<kSwiglu, kRing>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return MOK_ERR_CUDA;
   const int grid = (num_sms() / 2) * 2;
-  gemm_pair_persistent<kSwiglu><<<grid, 256, smem, st>>>(P);
+  if (!kRing) {
+    kern<<<grid, 256, smem, st>>>(P);
+    MOK_CHECK_LAUNCH();
+    return MOK_OK;
+  }
+  // ring producers and consumers wait on each other: all CTAs must be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, P) != cudaSuccess) return MOK_ERR_CUDA;
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -333,7 +484,7 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
                               cudaStream_t st, const SharedOperands* sh) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
-  PairParams P;
+  PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
@@ -375,7 +526,7 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
                             const SharedOperands* sh) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
-  PairParams P;
+  PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
@@ -410,6 +561,62 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
   }
   if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
   return run_pair<false>(P, st);
+}
+
+mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
+                         const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
+                         cudaStream_t st) {
+  if (a_rows == 0 || m_total == 0) return MOK_OK;
+  return launch_upgate_pair(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st);
+}
+
+mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
+                       int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st) {
+  return launch_down_pair(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st);
+}
+
+mok_status launch_upgate_ring(const void* x, const int32_t* table, int K, const void* w_gate, const void* w_up,
+                              const int32_t* offsets, int G, int64_t R, int D, int I, void* a_out, void* ring,
+                              int64_t ring_rows, int chunk_rows, int32_t* counters, cudaStream_t st) {
+  if (R == 0) return MOK_OK;
+  if (!offsets || chunk_rows < 128 || ring_rows < chunk_rows || ring_rows % chunk_rows) return MOK_ERR_INVALID_ARG;
+  const int64_t nchunks = (R + chunk_rows - 1) / chunk_rows;
+  if (nchunks > (int64_t{1} << 24)) return MOK_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(counters, 0, 2 * nchunks * sizeof(int32_t), st) != cudaSuccess) return MOK_ERR_CUDA;
+  PairParams P{};
+  P.sched = pair_sched(offsets, G, R, I / 128, D / BK);
+  P.sched.m_outer = 1;  // rows leave the ring in order: all N tiles of an M tile before the next M tile
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  if (!make_tmap_2d(&P.tmA, ring, kBF16, static_cast<uint64_t>(ring_rows) + 128, D, static_cast<uint64_t>(D) * 2,
+                    128, BK, true) ||
+      !make_tmap_2d(&P.tmB0, w_gate, kBF16, static_cast<uint64_t>(G) * I, D, static_cast<uint64_t>(D) * 2, 128, BK,
+                    true) ||
+      !make_tmap_2d(&P.tmB1, w_up, kBF16, static_cast<uint64_t>(G) * I, D, static_cast<uint64_t>(D) * 2, 128, BK,
+                    true))
+    return MOK_ERR_CUDA;
+  P.b_group_rows = I;
+  P.b_tile_rows = 128;
+  P.b1_off = 0;
+  P.out = static_cast<__nv_bfloat16*>(a_out);
+  P.out_ld = I;
+  P.tmAs = P.tmA;
+  P.tmBs0 = P.tmB0;
+  P.tmBs1 = P.tmB1;
+  P.x = static_cast<const uint4*>(x);
+  P.table = table;
+  P.K = K;
+  P.D8 = D / 8;
+  P.ring = static_cast<uint4*>(ring);
+  P.ring_rows = ring_rows;
+  P.R = R;
+  P.chunk_rows = chunk_rows;
+  P.nchunks = static_cast<int32_t>(nchunks);
+  P.n_tiles = I / 128;
+  P.ready = counters;
+  P.done = counters + nchunks;
+  if (!set_out_maps(P, R)) return MOK_ERR_CUDA;
+  return run_pair<true, true>(P, st);
 }
 
 }  // namespace mok

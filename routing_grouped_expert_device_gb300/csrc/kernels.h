@@ -34,15 +34,13 @@ mok_status launch_combine(const void* rows, const void* base, const float* w,
                           const int32_t* route_dst, int T, int K, int D, void* out,
                           cudaStream_t st);
 
-// Forward grouped GEMMs.  offsets == nullptr: one group of m_total rows.
+// Forward grouped GEMMs (CTA pairs, gemm_pair.cu).  offsets == nullptr: one
+// group of m_total rows.
 //  up/gate: a[rows][I] = bf16(SiLU(A W_gate^T) * (A W_up^T)), A [rows][D]
 //  down   : y[rows][D] = bf16(a W_down^T)
-// gather_table non-null: A is x [a_rows = T][D] and row p of the grouped
-// operand is x[gather_table[3 p] / gather_k] (the dispatch fused into the TMA
-// loads); m_total is then R.
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st, const int32_t* gather_table = nullptr, int gather_k = 1);
+                         cudaStream_t st);
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
 // The shared expert as an extra group of a routed launch: A [rows][K],
@@ -55,12 +53,30 @@ struct SharedOperands {
   int inner;
   void* out;
 };
-// The same two GEMMs on CTA pairs (cta_group::2, 256-row tiles); the
-// launch_upgate / launch_down above use these whenever A is dense.  With
-// sh, the shared expert's tiles run in the same launch, spread through it.
+// The same two GEMMs with the shared expert's tiles (sh) spread through the
+// routed launch (cta_group::2, 256-row tiles).
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
                               cudaStream_t st, const SharedOperands* sh = nullptr);
+// Ring dispatch fused into the routed up/gate (BF16): producer warps in the
+// same launch gather x rows into `ring` ([ring_rows + 128][D] bf16) in
+// chunks of chunk_rows routed rows; counters: 2 * ceil(R / chunk_rows) ints.
+mok_status launch_upgate_ring(const void* x, const int32_t* table, int K, const void* w_gate, const void* w_up,
+                              const int32_t* offsets, int G, int64_t R, int D, int I, void* a_out, void* ring,
+                              int64_t ring_rows, int chunk_rows, int32_t* counters, cudaStream_t st);
+// Ring geometry for R routed rows and chunk b (0: 2048): 4 slots of b rows,
+// or fewer when that already holds every row (then no slot is reused).
+constexpr int64_t kRingSlots = 4;
+inline int64_t ring_chunk(int chunk_rows) { return chunk_rows > 0 ? chunk_rows : 2048; }
+inline int64_t ring_rows_for(int64_t R, int64_t b) {
+  int64_t all = (R + b - 1) / b;
+  if (all < 1) all = 1;
+  return (all < kRingSlots ? all : kRingSlots) * b;
+}
+inline size_t ring_bytes(int64_t R, int64_t D, int64_t b) {
+  return static_cast<size_t>(ring_rows_for(R, b) + 128) * D * 2;
+}
+inline size_t ring_counter_bytes(int64_t R, int64_t b) { return static_cast<size_t>((R + b - 1) / b) * 8; }
 mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
                             const SharedOperands* sh = nullptr);

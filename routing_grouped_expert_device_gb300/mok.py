@@ -19,7 +19,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "mok.h")
 MOK_OK, MOK_ERR_INVALID_ARG, MOK_ERR_UNSUPPORTED, MOK_ERR_WORKSPACE, MOK_ERR_CUDA, \
     MOK_ERR_TIMEOUT, MOK_ERR_BAD_ROUTE = range(7)
 MOK_BF16, MOK_MXFP8 = 0, 1
-OP_PLAN, OP_EXPERT_FFN, OP_SHARED_FFN, OP_FWD, OP_BWD = range(5)
+OP_PLAN, OP_EXPERT_FFN, OP_SHARED_FFN, OP_FWD, OP_BWD, OP_RING = range(6)
 
 
 class MokError(RuntimeError):
@@ -60,8 +60,8 @@ _SIGS = {
                                       _P, _SZ, _P]),
     "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _P,
                                          _P]),
-    "mok_expert_upgate_gather": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P,
-                                                _P]),
+    "mok_expert_upgate_ring": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
+                                               ctypes.c_size_t, _P]),
     "mok_expert_down": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _P]),
     "mok_shared_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _SZ, _P]),
     "mok_combine": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
@@ -186,10 +186,11 @@ def expert_upgate(shape: Shape, weights: Weights, xg, offsets, a, xg_scale=None,
                                            _stream(stream)), "mok_expert_upgate")
 
 
-def expert_upgate_gather(shape: Shape, weights: Weights, x, table, offsets, a, stream=None):
-    _check(_lib_handle().mok_expert_upgate_gather(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(table),
-                                                  _ptr(offsets), _ptr(a), _stream(stream)),
-           "mok_expert_upgate_gather")
+def expert_upgate_ring(shape: Shape, weights: Weights, x, table, offsets, a, ws, stream=None):
+    """Up/gate with the dispatch fused in as a ring of shape.chunk_rows-row chunks."""
+    _check(_lib_handle().mok_expert_upgate_ring(ctypes.byref(shape), ctypes.byref(weights), _ptr(x), _ptr(table),
+                                                _ptr(offsets), _ptr(a), _ptr(ws), ws.numel() * ws.element_size(),
+                                                _stream(stream)), "mok_expert_upgate_ring")
 
 
 def expert_down(shape: Shape, weights: Weights, a, offsets, yg, a_scale=None, a_shared=None, ys=None, stream=None):

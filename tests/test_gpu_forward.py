@@ -292,23 +292,72 @@ def test_split_expert_entry_points_match_expert_ffn(m):
         m.expert_upgate(shape, m.make_weights(d), None, None, None)
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "skew_small"])
-def test_fused_gather_upgate_bitexact_vs_dispatch(m, name):
-    """The dispatch fused into the up/gate TMA loads gives the same bytes as
-    the explicit gather followed by the dense-A GEMM."""
-    cfg = SMALL[name]
+RING_REUSE = W.MoEConfig("ring_reuse", T=1024, D=256, I=128, E=16, K=4, I_shared=128)
+
+
+@pytest.mark.parametrize("name,chunk", [("tiny", 512), ("ragged", 512), ("skew_small", 512),
+                                        ("skew_small", 2048), ("ring_reuse", 512), ("ring_reuse", 32768)])
+def test_ring_upgate_bitexact_vs_dispatch(m, name, chunk):
+    """The dispatch fused into the up/gate as a ring of chunk-row slots (4
+    slots: R > 4 chunks reuses them) gives the bytes of the explicit gather
+    followed by the dense-A GEMM."""
+    cfg = RING_REUSE if name == "ring_reuse" else SMALL[name]
     inp = W.make_inputs(cfg, "cpu")
     ref = O.moe_forward(host(inp), cfg.K)
     d = {k: v.to(DEV) for k, v in inp.items()}
-    shape = m.shape_of(cfg)
+    shape = m.shape_of(cfg, chunk_rows=chunk)
     table = torch.from_numpy(ref["table"]).to(DEV)
     off = torch.from_numpy(ref["offsets"]).to(DEV)
     xg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
     m.dispatch(shape, d["x"], table, xg)
     a1 = torch.empty(cfg.R, cfg.I, dtype=torch.bfloat16, device=DEV)
-    a2 = torch.empty_like(a1)
     m.expert_upgate(shape, m.make_weights(d), xg, off, a1)
-    m.expert_upgate_gather(shape, m.make_weights(d), d["x"], table, off, a2)
-    m.check_device_status()
-    assert torch.equal(a1.view(torch.int16), a2.view(torch.int16))
+    ws = torch.empty(m.workspace_bytes(shape, m.OP_RING), dtype=torch.uint8, device=DEV)
+    for _ in range(2):  # the counters start from zero on every call
+        a2 = torch.full_like(a1, float("nan"))
+        m.expert_upgate_ring(shape, m.make_weights(d), d["x"], table, off, a2, ws)
+        m.check_device_status()
+        assert torch.equal(a1.view(torch.int16), a2.view(torch.int16))
     assert_close(a2.float().cpu().numpy(), ref["a"], BF16_TOL, "a")
+
+
+@pytest.mark.parametrize("name", ["ragged", "ring_reuse"])
+def test_moe_fwd_ring_matches_whole_batch_dispatch(m, name):
+    """mok_moe_fwd with a chunk size (ring dispatch) equals the whole-batch
+    dispatch bit for bit, and the oracle within tolerance."""
+    cfg = RING_REUSE if name == "ring_reuse" else SMALL[name]
+    inp = W.make_inputs(cfg, "cpu")
+    ref = O.moe_forward(host(inp), cfg.K)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    outs = []
+    for chunk in (0, 512, 512):
+        shape = m.shape_of(cfg, chunk_rows=chunk)
+        ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+        out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+        m.moe_fwd(shape, m.make_weights(d), d["x"], d["s"], out, ws)
+        m.check_device_status()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[1].view(torch.int16), outs[2].view(torch.int16))
+    assert_close(outs[1].float().cpu().numpy(), ref["out"], BF16_TOL, "out")
+
+
+@pytest.mark.parametrize("config,chunks", [("dsv3_bf16_fwd", (512, 2048, 32768)),
+                                           ("skewed_bf16_fwd", (512, 2048, 8192, 32768))])
+def test_moe_fwd_ring_full_size_bitexact(m, config, chunks):
+    """Full-size layers: every chunk size of the ring gives the whole-batch
+    dispatch's output bit for bit (including hot and empty experts)."""
+    cfg = W.CONFIGS[config]
+    d = W.make_inputs(cfg, DEV)
+    w = m.make_weights(d)
+    outs = []
+    for chunk in (0,) + chunks:
+        shape = m.shape_of(cfg, chunk_rows=chunk)
+        ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+        out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+        m.moe_fwd(shape, w, d["x"], d["s"], out, ws)
+        m.check_device_status()
+        outs.append(out)
+        del ws
+    for o in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), o.view(torch.int16))

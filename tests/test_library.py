@@ -32,6 +32,11 @@ def test_workspace_bytes_host_only(m):
     R = 7168 * 8
     assert fwd >= R * 7168 * 2 * 2 + R * 2048 * 2
     assert m.workspace_bytes(good, m.OP_PLAN) > 0
+    # the ring: 4 chunks of 2048 rows (+ 128 mirrored rows) and 2 counters per chunk
+    assert m.workspace_bytes(good, m.OP_RING) >= (4 * 2048 + 128) * 7168 * 2 + 2 * 28 * 4
+    ring = m.make_shape(T=7168, D=7168, I=2048, E=256, K=8, I_shared=2048, chunk_rows=512)
+    assert m.workspace_bytes(ring, m.OP_FWD) < fwd  # the ring replaces the R x D gathered copy
+    assert m.workspace_bytes(m.make_shape(T=16, D=256, I=128, E=8, K=2, chunk_rows=100), m.OP_RING) == 0
     assert m.workspace_bytes(m.make_shape(T=16, D=200, I=128, E=8, K=2), m.OP_FWD) == 0
     assert m.workspace_bytes(m.make_shape(T=16, D=256, I=128, E=8, K=9), m.OP_FWD) == 0
 

@@ -317,6 +317,9 @@ int* status_ptr();
 bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows,
                   uint64_t cols, uint64_t pitch_bytes, uint32_t box_rows, uint32_t box_cols,
                   bool swizzle128);
+bool make_tmap_2d_swz(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows,
+                      uint64_t cols, uint64_t pitch_bytes, uint32_t box_rows, uint32_t box_cols,
+                      CUtensorMapSwizzle swizzle);
 int num_sms();
 }  // namespace mok
 

@@ -30,26 +30,42 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t a) { return sdesc_sw128(a, M
 
 // ---------------------------------------------------------------------------
 struct DgradCfg {
-  static constexpr int STAGES = 2;
-  static constexpr int STAGE_BYTES = 4 * KTILE + 2 * MNCHUNK;  // 80 KB
+  // 32-wide K blocks (64-byte swizzle) keep five 40 KB stages in flight: the
+  // kernel streams three weight tensors and two activation tensors per tile,
+  // and with two 80 KB stages it waited on memory latency.
+  static constexpr int BKD = 32;
+  static constexpr int KT = 128 * BKD * 2;   // 8 KB: 128 rows x 32 bf16, K-major
+  static constexpr int WDCHUNK = BKD * 128;  // 4 KB: 32 K rows x 64 columns, MN-major
+  static constexpr int STAGES = 5;
+  static constexpr int STAGE_BYTES = 4 * KT + 2 * WDCHUNK;  // 40 KB: x, dY, W_gate, W_up, W_down
   static constexpr int EPI_SMEM_BYTES = 0;
   static constexpr int NUM_ACC = 1;
   static constexpr int ACC_COLS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t ID_KK = idesc_bf16(128, 128, false, false);
-  static constexpr uint32_t ID_KMN = idesc_bf16(128, 128, false, true);
+  static constexpr uint32_t ID_HU = idesc_bf16(128, 256, false, false);  // h | u in one N = 256 MMA
+  static constexpr uint32_t ID_T = idesc_bf16(128, 128, false, true);
 
   struct Params {
     SchedArgs sched;
     int* status;
-    CUtensorMap tmX, tmDy;   // [rows][D], K-major boxes 128 x 64
-    CUtensorMap tmWg, tmWu;  // [G*I][D], K-major boxes 128 x 64
-    CUtensorMap tmWd;        // [G*D][I], MN-major boxes 64 x 64
+    CUtensorMap tmX, tmDy;   // [rows][D], K-major boxes 128 x 32, 64-byte swizzle
+    CUtensorMap tmWg, tmWu;  // [G*I][D], K-major boxes 128 x 32, 64-byte swizzle
+    CUtensorMap tmWd;        // [G*D][I], MN-major boxes 32 x 64, 128-byte swizzle
     int32_t I, D;
     const float* g_route;    // [rows] or null (weight 1)
     __nv_bfloat16 *dh, *du, *ag;  // [rows][I]
     float* dgp;              // [rows][I/128] or null
   };
+
+  // K-major, 64-byte swizzle: 8-row groups of 64-byte rows 512 B apart.
+  __device__ static uint64_t kdesc64(uint32_t a) {
+    uint64_t d = static_cast<uint64_t>((a & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(512 >> 4) << 32;
+    d |= 1ull << 46;
+    d |= 4ull << 61;
+    return d;
+  }
 
   __device__ static uint32_t full_arrivals(const Params&) { return 1; }
   __device__ static uint32_t tx_bytes(const Params&) { return STAGE_BYTES; }
@@ -57,16 +73,16 @@ struct DgradCfg {
   __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
                               uint64_t* bar, int lane) {
     if (lane != 0) return;
-    const int k0 = kb * BK;
+    const int k0 = kb * BKD;
     const int r = c.row0 + c.mt * BM;
     const int wrow = c.g * P.I + c.nt * 128;
     tma_load_2d(st, &P.tmX, k0, r, bar);
-    tma_load_2d(st + KTILE, &P.tmDy, k0, r, bar);
-    tma_load_2d(st + 2 * KTILE, &P.tmWg, k0, wrow, bar);
-    tma_load_2d(st + 3 * KTILE, &P.tmWu, k0, wrow, bar);
+    tma_load_2d(st + KT, &P.tmDy, k0, r, bar);
+    tma_load_2d(st + 2 * KT, &P.tmWg, k0, wrow, bar);  // W_gate then W_up: one 256-row B operand
+    tma_load_2d(st + 3 * KT, &P.tmWu, k0, wrow, bar);
     const int drow = c.g * P.D + k0;
-    tma_load_2d(st + 4 * KTILE, &P.tmWd, c.nt * 128, drow, bar);
-    tma_load_2d(st + 4 * KTILE + MNCHUNK, &P.tmWd, c.nt * 128 + 64, drow, bar);
+    tma_load_2d(st + 4 * KT, &P.tmWd, c.nt * 128, drow, bar);
+    tma_load_2d(st + 4 * KT + WDCHUNK, &P.tmWd, c.nt * 128 + 64, drow, bar);
   }
 
   __device__ static void fixup(const Params&, const TileCoord&, int, uint8_t*, int) {}
@@ -74,12 +90,10 @@ struct DgradCfg {
   __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
     const uint32_t s = smem_u32(st);
 #pragma unroll
-    for (int k = 0; k < BK / 16; ++k) {
+    for (int k = 0; k < BKD / 16; ++k) {
       const uint32_t acc = (kb | k) != 0;
-      const uint64_t ax = kdesc(s + k * 32), ay = kdesc(s + KTILE + k * 32);
-      mma_bf16(d, ax, kdesc(s + 2 * KTILE + k * 32), ID_KK, acc);
-      mma_bf16(d + 128, ax, kdesc(s + 3 * KTILE + k * 32), ID_KK, acc);
-      mma_bf16(d + 256, ay, mndesc(s + 4 * KTILE + k * 2048), ID_KMN, acc);
+      mma_bf16(d, kdesc64(s + k * 32), kdesc64(s + 2 * KT + k * 32), ID_HU, acc);
+      mma_bf16(d + 256, kdesc64(s + KT + k * 32), sdesc_sw128(s + 4 * KT + k * 2048, WDCHUNK, 1024), ID_T, acc);
     }
   }
 
@@ -352,14 +366,19 @@ mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const
                             float* dgp, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
   DgradCfg::Params P;
-  P.sched = sched_rows(offsets, G, rows, I / 128, D / BK);
+  P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradCfg::BKD);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int groups = offsets ? G : 1;
-  if (!kmap(&P.tmX, xg, rows, D) || !kmap(&P.tmDy, dyg, rows, D) ||
-      !kmap(&P.tmWg, w_gate, static_cast<int64_t>(groups) * I, D) ||
-      !kmap(&P.tmWu, w_up, static_cast<int64_t>(groups) * I, D) ||
-      !mnmap(&P.tmWd, w_down, static_cast<int64_t>(groups) * D, I))
+  auto k64 = [](CUtensorMap* m, const void* p, int64_t r, int cols) {
+    return make_tmap_2d_swz(m, p, kBF16, r, cols, static_cast<uint64_t>(cols) * 2, 128, DgradCfg::BKD,
+                            CU_TENSOR_MAP_SWIZZLE_64B);
+  };
+  if (!k64(&P.tmX, xg, rows, D) || !k64(&P.tmDy, dyg, rows, D) ||
+      !k64(&P.tmWg, w_gate, static_cast<int64_t>(groups) * I, D) ||
+      !k64(&P.tmWu, w_up, static_cast<int64_t>(groups) * I, D) ||
+      !make_tmap_2d(&P.tmWd, w_down, kBF16, static_cast<int64_t>(groups) * D, I, static_cast<uint64_t>(I) * 2,
+                    DgradCfg::BKD, 64, true))
     return MOK_ERR_CUDA;
   P.I = I;
   P.D = D;

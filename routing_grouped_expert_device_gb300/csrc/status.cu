@@ -55,6 +55,13 @@ int num_sms() {
 bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows,
                   uint64_t cols, uint64_t pitch_bytes, uint32_t box_rows, uint32_t box_cols,
                   bool swizzle128) {
+  return make_tmap_2d_swz(m, base, dt, rows, cols, pitch_bytes, box_rows, box_cols,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+bool make_tmap_2d_swz(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t rows,
+                      uint64_t cols, uint64_t pitch_bytes, uint32_t box_rows, uint32_t box_cols,
+                      CUtensorMapSwizzle swizzle) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
@@ -72,8 +79,7 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

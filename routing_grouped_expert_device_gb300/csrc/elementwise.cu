@@ -57,76 +57,82 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
-// Quantise 32 bf16 values (4 x uint4) to E4M3 with one E8M0 scale.
-__device__ __forceinline__ void quant_block(const uint4 (&v)[4], uint4 (&q)[2], uint8_t& sc) {
-  float f[32];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[i * 8 + 2 * j] = bf16lo(w[j]);
-      f[i * 8 + 2 * j + 1] = bf16hi(w[j]);
-    }
-  }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-  const int e = mx_exponent(amax);
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
-  uint32_t packed[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-        make_float2(f[4 * i] * inv, f[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-        make_float2(f[4 * i + 2] * inv, f[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-    packed[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
-  q[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  q[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  sc = static_cast<uint8_t>(e + 127);
-}
-
-// One thread per (128-column group, row): 4 blocks of 32, their codes and
-// one scale word.  Threads of a warp take consecutive rows of one group, so
-// a warp's scale words land in one 512-byte block of the scale storage
-// (layout in kernels.h).  table == nullptr: identity rows, plain layout
-// (the quantiser); else row p is x[table[p].src / K] and its scale goes to
-// the grouped layout of expert table[p].e (the dispatch with fused
-// quantisation).
+// One warp per row: lane l holds 8 consecutive values (16 bytes), so a
+// 1x32 block is 4 lanes (its amax: two xor shuffles) and one pass of the warp
+// covers 256 columns, two 128-column scale groups; loads and code stores are
+// contiguous across the warp.  Each group's 4 scale bytes are gathered into
+// one 32-bit word (layout in kernels.h).  table == nullptr: identity rows,
+// plain layout (the quantiser); else row p is x[table[p].src / K] and its
+// scales go to the grouped layout of expert table[p].e (the dispatch with
+// fused quantisation).
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ src,
                                                          const int32_t* __restrict__ table,
                                                          const int32_t* __restrict__ offsets, int K,
                                                          int64_t rows, int64_t cols, int64_t ld,
-                                                         uint4* __restrict__ q,
+                                                         uint2* __restrict__ q,
                                                          uint32_t* __restrict__ scale) {
-  const int64_t total = rows * (cols / 128);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t grp = i / rows, row = i - grp * rows;
-    int64_t srow = row, srow_pos = row;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int c8 = static_cast<int>(cols / 8);  // 16-byte vectors per row
+  for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows;
+       row += nwarps) {
+    int64_t srow = row, pos_row = row;
     if (table) {
       srow = __ldg(table + row * 3) / K;
       const int e = __ldg(table + row * 3 + 1);
       const int64_t off = __ldg(offsets + e);
-      srow_pos = mx_group_row0(off, e) + (row - off);
+      pos_row = mx_group_row0(off, e) + (row - off);
     }
-    const uint4* in = src + (srow * cols + grp * 128) / 8;
-    uint4* out = q + (row * cols + grp * 128) / 16;
-    uint32_t word = 0;
+    const int64_t pos = mx_scale_pos(pos_row);
+    const uint4* in = src + srow * c8;
+    uint2* out = q + row * c8;
+#pragma unroll 1
+    for (int v0 = 0; v0 < c8; v0 += 128) {  // 4 passes of 256 columns in flight
+      uint4 v[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      uint4 v[4] = {ld_nc_v4(in + 4 * b), ld_nc_v4(in + 4 * b + 1), ld_nc_v4(in + 4 * b + 2),
-                    ld_nc_v4(in + 4 * b + 3)};
-      uint4 o[2];
-      uint8_t sc;
-      quant_block(v, o, sc);
-      out[2 * b] = o[0];
-      out[2 * b + 1] = o[1];
-      word |= static_cast<uint32_t>(sc) << (8 * b);
+      for (int u = 0; u < 4; ++u) {
+        const int vi = v0 + 32 * u + lane;
+        v[u] = vi < c8 ? ld_nc_v4(in + vi) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int vi = v0 + 32 * u + lane;
+        if (v0 + 32 * u >= c8) break;  // warp-uniform: cols is a multiple of 128 (16 vectors)
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          f[2 * j] = bf16lo(w[j]);
+          f[2 * j + 1] = bf16hi(w[j]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int e = mx_exponent(amax);
+        const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+        uint32_t packed[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+              make_float2(f[4 * j] * inv, f[4 * j + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+              make_float2(f[4 * j + 2] * inv, f[4 * j + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+          packed[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        if (vi < c8) out[vi] = make_uint2(packed[0], packed[1]);
+        // scale word of the 128-column group of lanes 16h .. 16h + 15: byte b
+        // from lane 16h + 4b
+        const uint32_t byte = static_cast<uint32_t>(e + 127);
+        const int base = lane & 16;
+        const uint32_t word = __shfl_sync(0xffffffffu, byte, base) |
+                              (__shfl_sync(0xffffffffu, byte, base + 4) << 8) |
+                              (__shfl_sync(0xffffffffu, byte, base + 8) << 16) |
+                              (__shfl_sync(0xffffffffu, byte, base + 12) << 24);
+        if ((lane & 15) == 0 && vi < c8) scale[static_cast<int64_t>(vi / 16) * ld + pos] = word;
+      }
     }
-    scale[grp * ld + mx_scale_pos(srow_pos)] = word;
   }
 }
 
@@ -237,9 +243,9 @@ mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, 
 mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int32_t* offsets, int64_t R,
                                  int K, int D, int E, void* xg_q, uint8_t* xg_scale, cudaStream_t st) {
   if (R == 0) return MOK_OK;
-  quant_rows_kernel<<<grid_for(R * (D / 128), 256), 256, 0, st>>>(
-      static_cast<const uint4*>(x), table, offsets, K, R, D, mx_scale_ld(R, E), static_cast<uint4*>(xg_q),
-      reinterpret_cast<uint32_t*>(xg_scale));
+  quant_rows_kernel<<<grid_for(R, 8), 256, 0, st>>>(static_cast<const uint4*>(x), table, offsets, K, R, D,
+                                                    mx_scale_ld(R, E), static_cast<uint2*>(xg_q),
+                                                    reinterpret_cast<uint32_t*>(xg_scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -247,9 +253,9 @@ mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int3
 mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
                                  uint8_t* scale, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
-  quant_rows_kernel<<<grid_for(rows * (cols / 128), 256), 256, 0, st>>>(
-      static_cast<const uint4*>(src), nullptr, nullptr, 1, rows, cols, mx_scale_ld(rows),
-      static_cast<uint4*>(q), reinterpret_cast<uint32_t*>(scale));
+  quant_rows_kernel<<<grid_for(rows, 8), 256, 0, st>>>(static_cast<const uint4*>(src), nullptr, nullptr, 1, rows,
+                                                       cols, mx_scale_ld(rows), static_cast<uint2*>(q),
+                                                       reinterpret_cast<uint32_t*>(scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

@@ -423,6 +423,9 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
   s.k_blocks_fixed = 0;
   s.bm = BM;
   s.bk_rows = BK;
+  // N tile fastest: CTAs working side by side write neighbouring column
+  // pieces of the same dW rows instead of 512-byte pieces of distant rows
+  s.m_outer = 1;
   P.sched = s;
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;

@@ -284,6 +284,14 @@ size_t mok_mxfp8_scale_bytes(int64_t rows, int64_t cols, int32_t groups);
 mok_status mok_quantize_mxfp8(const void *src, int64_t rows, int64_t cols, void *q,
                               uint8_t *scale, void *stream);
 
+/* Failure-detection check (no counterpart on the pages).  Enqueues on
+ * `stream` one pipeline wait on an mbarrier that nothing arrives on and one
+ * ring-counter wait on a counter that nothing increments: both give up after
+ * the 2 s budget of every device wait and record MOK_ERR_TIMEOUT, which the
+ * next mok_get_error returns; the GPU context stays usable.  About 4 s of
+ * one thread's time; no fault, trap or hang. */
+mok_status mok_check_wait_timeout(void *stream);
+
 /* Synchronises `stream`, returns the device status word of the current
  * device (MOK_OK, MOK_ERR_BAD_ROUTE or MOK_ERR_TIMEOUT) and clears it. */
 mok_status mok_get_error(void *stream);

@@ -23,6 +23,7 @@ enum : int {
   SITE_DRAIN = 4 << 8,
   SITE_RING_SLOT = 5 << 8,   // a ring producer waiting for a slot to be consumed
   SITE_RING_CHUNK = 6 << 8,  // a GEMM waiting for a ring chunk to be produced
+  SITE_CHECK = 7 << 8,       // mok_check_wait_timeout
 };
 
 __device__ __forceinline__ void report(int* status, int code) {
@@ -94,6 +95,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Device counters that one set of warps increments and another waits on
+// (the ring dispatch): acquire loads, release adds, and a bounded wait.
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Spin until *p >= target; false (and MOK_ERR_TIMEOUT | site) past the budget
+// or once another role of the CTA has given up.
+__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort, int* status,
+                                           int site) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (ld_acquire(p) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitBudgetNs) {
+      *abort = 1;
+      report(status, MOK_ERR_TIMEOUT | site);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor)
 // ---------------------------------------------------------------------------

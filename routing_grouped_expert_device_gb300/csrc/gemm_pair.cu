@@ -74,33 +74,8 @@ struct PairParams {
 // rows lie in, and the MMA thread reports the rows it has read so that the
 // slot can be refilled.  All CTAs of the launch are resident (cooperative
 // launch), and every wait is bounded.
-__device__ __forceinline__ int ld_acquire(const int32_t* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-// Spin until *p >= target; false (and MOK_ERR_TIMEOUT | site) past the budget
-// or once another role of the CTA has given up.
-__device__ __forceinline__ bool wait_count(const int32_t* p, int target, volatile int* abort, int* status,
-                                           int site) {
-  if (ld_acquire(p) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (ld_acquire(p) >= target) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitBudgetNs) {
-      *abort = 1;
-      report(status, MOK_ERR_TIMEOUT | site);
-      return false;
-    }
-    __nanosleep(64);
-  }
 }
 __device__ __forceinline__ int64_t ring_slots(const PairParams& P) { return P.ring_rows / P.chunk_rows; }
 __device__ __forceinline__ int chunk_row_count(const PairParams& P, int c) {

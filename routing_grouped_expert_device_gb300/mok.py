@@ -72,6 +72,7 @@ _SIGS = {
                                    _P, _SZ, _P]),
     "mok_quantize_mxfp8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "mok_mxfp8_scale_bytes": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int32]),
+    "mok_check_wait_timeout": (ctypes.c_int, [_P]),
     "mok_get_error": (ctypes.c_int, [_P]),
     "mok_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -239,6 +240,12 @@ def mx_scale_words(rows: int, cols: int, groups: int = 0) -> int:
     if n == 0 and rows > 0:
         raise MokError(MOK_ERR_INVALID_ARG, f"mok_mxfp8_scale_bytes({rows}, {cols}, {groups})")
     return n // 4
+
+
+def check_wait_timeout(stream=None):
+    """Enqueue the bounded-wait check (two waits that run out); read the
+    result with get_error()."""
+    _check(_lib_handle().mok_check_wait_timeout(_stream(stream)), "mok_check_wait_timeout")
 
 
 def get_error(stream=None) -> int:

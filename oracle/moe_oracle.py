@@ -48,7 +48,7 @@ import numpy as np
 __all__ = [
     "Numerics", "FP32", "FP64_SHADOW",
     "bf16_to_f32", "round_bf16", "f32_to_bf16_bits", "bf16_flip_ulp",
-    "silu", "route", "pull_schedule", "plan", "gather",
+    "silu", "softmax_rows", "router_scores", "route", "pull_schedule", "plan", "gather",
     "expert_ffn_rows", "expert_ffn", "shared_ffn", "combine", "moe_forward",
     "HostWeights", "moe_forward_tokens",
     "route_backward_rows", "moe_backward", "router_grad", "router_grad_slack",
@@ -127,8 +127,28 @@ def silu(h: np.ndarray) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
-# routing and the pull schedule
+# router scores, routing and the pull schedule
 # --------------------------------------------------------------------------
+def softmax_rows(logits: np.ndarray, num: Numerics = FP32) -> np.ndarray:
+    """Row softmax exp(l - max l) / sum exp(l - max l) in num's type."""
+    lv = np.asarray(logits, dtype=num.dtype)
+    e = np.exp(lv - lv.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def router_scores(x, w_router, num: Numerics = FP32):
+    """Router scores s = softmax(x W_r^T) over the E routed experts.
+
+    [blog] "Overlapping computation and communication in MoE": the gate g is
+    formed from router weights s over the routed experts; the pages show only
+    s, so the router is read as the usual projection of a DeepSeek-V3-style
+    layer, logits[t, e] = sum_d x[t, d] W_r[e, d] (x, W_r bf16; sums in num's
+    type), followed by a softmax over e.  Returns (logits, s), both [T][E].
+    """
+    logits = num.w(x) @ num.w(w_router).T
+    return logits, softmax_rows(logits, num)
+
+
 def route(s: np.ndarray, K: int, num: Numerics = FP32):
     """Top-K experts per token and their renormalised weights.
 

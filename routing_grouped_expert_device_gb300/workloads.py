@@ -15,7 +15,10 @@ inputs):
   * dY ~ N(0, 1), rounded to bf16.
 
 Draw order from one generator seeded with ``seed``: x, W_gate, W_up, W_down,
-shared W_gate, shared W_up, shared W_down, logits, dY.  Large tensors are drawn
+shared W_gate, shared W_up, shared W_down, logits, dY.  The router projection
+W_r [E][D] ~ N(0, 1/D) (``make_router_weights``) comes from a second
+generator seeded with ``seed + 7919``, so it leaves every tensor above as is;
+with x ~ N(0, 1) its logits x W_r^T are again about N(0, 1).  Large tensors are drawn
 in fixed-size slabs so that peak memory stays bounded; the slab size is part of
 the recipe, so the bytes are a pure function of (config, seed, device).
 """
@@ -133,6 +136,14 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, with_dy: Optional[b
     if with_dy:
         out["dy"] = _draw(gen, (T, D), 1.0, device)
     return out
+
+
+def make_router_weights(cfg: MoEConfig, device="cpu", seed: int = 0) -> torch.Tensor:
+    """Router projection W_r [E][D] bf16, N(0, 1/D)."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 7919)
+    return _draw(gen, (cfg.E, cfg.D), 1.0 / math.sqrt(cfg.D), device)
 
 
 def bf16_bits(t: torch.Tensor):

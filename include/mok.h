@@ -137,6 +137,16 @@ size_t mok_workspace_bytes(const mok_shape *shape, int op);
 mok_status mok_route(const float *s, int32_t T, int32_t E, int32_t K,
                      int32_t *topk_idx, float *g, void *stream);
 
+/* Router (blog, "Overlapping computation and communication in MoE": the
+ * gate is formed from router weights s over the routed experts).  s =
+ * softmax(x W_r^T) over the E experts, x bf16 [T][D], w_router bf16 [E][D],
+ * logits summed in fp32 on the tensor cores, the softmax (exp(l - max) /
+ * sum, fast exponential, one IEEE reciprocal per row) in the same launch;
+ * s fp32 [T][E] is written, then mok_route's top-K and g run on it
+ * (topk_idx, g as for mok_route).  E <= 256, else MOK_ERR_UNSUPPORTED. */
+mok_status mok_router(const mok_shape *shape, const void *x, const void *w_router, float *s,
+                      int32_t *topk_idx, float *g, void *stream);
+
 /* Device-side plan (blog, "Scheduling": the pull schedule with one source
  * rank).  From topk_idx int32 [T][K] writes counts int32 [E] (routes per
  * expert), offsets int32 [E+1] (exclusive scan, offsets[E] = R), table

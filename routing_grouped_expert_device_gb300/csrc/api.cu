@@ -243,6 +243,20 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
                             with_shared ? &sh : nullptr);
 }
 
+extern "C" mok_status mok_router(const mok_shape* shape, const void* x, const void* w_router, float* s_out,
+                                 int32_t* topk_idx, float* g, void* stream) {
+  if (!shape_ok(shape)) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.T == 0) return MOK_OK;
+  if (s.E > 256) return MOK_ERR_UNSUPPORTED;
+  if (!x || !w_router || !s_out || !topk_idx || !g || !aligned16(x) || !aligned16(w_router) || !aligned16(s_out))
+    return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mok_status r = launch_router_pair(x, s.T, w_router, s.E, s.D, s_out, st);
+  if (r != MOK_OK) return r;
+  return launch_route(s_out, s.T, s.E, s.K, topk_idx, g, st);
+}
+
 extern "C" mok_status mok_expert_upgate_ring(const mok_shape* shape, const mok_weights* w, const void* x,
                                              const int32_t* table, const int32_t* offsets, void* a, void* ws,
                                              size_t ws_bytes, void* stream) {

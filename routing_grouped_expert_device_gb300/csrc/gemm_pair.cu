@@ -63,6 +63,10 @@ struct PairParams {
   int32_t chunk_rows, nchunks, n_tiles;
   int32_t* ready;          // [nchunks]: producer warps done with the chunk
   int32_t* done;           // [nchunks]: (row, N tile) reads of the chunk completed
+  // Router scores (kSoftmax): one N tile of 256 logits per row, columns < E
+  // valid; s_out [rows][E] fp32.
+  float* s_out;
+  int32_t E;
 };
 
 // ---------------------------------------------------------------------------
@@ -144,7 +148,58 @@ __device__ __forceinline__ void for_box_chunks(const PairParams& P, int64_t r0, 
   }
 }
 
-template <bool kSwiglu, bool kRing = false>
+// Router scores epilogue: s = softmax over the row's E logits (fp32 in TMEM,
+// columns 0..255 of the accumulator).  Three passes over the row: the
+// maximum, the sum of exp(l - max), then exp(l - max) / sum, written as fp32.
+__device__ __forceinline__ void softmax_epilogue(const PairParams& P, uint32_t taddr, int64_t row, bool valid) {
+  const int E = P.E;
+  float m = -INFINITY;
+#pragma unroll 1
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(taddr + ch * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (ch * 32 + j < E) m = fmaxf(m, __uint_as_float(v[j]));
+  }
+  float sum = 0.0f;
+#pragma unroll 1
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(taddr + ch * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (ch * 32 + j < E) sum += __expf(__uint_as_float(v[j]) - m);
+  }
+  const float inv = 1.0f / sum;
+  float* orow = P.s_out + row * E;
+#pragma unroll 1
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t v[32];
+    tmem_ld32(taddr + ch * 32, v);
+    tmem_ld_wait();
+    if (valid) {
+      float o[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __expf(__uint_as_float(v[j]) - m) * inv;
+      if (ch * 32 + 32 <= E && (E & 3) == 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(orow + ch * 32 + 4 * q) =
+              make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (ch * 32 + j < E) orow[ch * 32 + j] = o[j];
+      }
+    }
+    __syncwarp();  // converged again before the next warp-wide TMEM load
+  }
+}
+
+template <bool kSwiglu, bool kRing = false, bool kSoftmax = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_persistent(const __grid_constant__ PairParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -323,6 +378,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(ew * 32) << 16);
       const int slab = c.mt * 256 + static_cast<int>(rank) * 128 + ew * 32;  // first row of this warp in the group
       const int nvalid = min(max(c.rows - slab, 0), 32);
+      if (kSoftmax) {
+        softmax_epilogue(P, taddr, static_cast<int64_t>(c.row0) + slab + lane, lane < nvalid);
+        tc_fence_before();
+        if (leader) mbar_arrive(&tempty[acc]);
+        else remote_arrive(map_to_rank(smem_u32(&tempty[acc]), 0));
+        continue;
+      }
       const int y = (c.extra ? 0 : c.row0) + slab;  // its row in the output tensor
       const CUtensorMap* tmOut = c.extra ? &P.tmOut_s : &P.tmOut;
       __nv_bfloat16* orow = c.extra ? P.out_s + static_cast<size_t>(y + lane) * P.out_ld_s
@@ -391,11 +453,11 @@ size_t pair_smem_bytes(int G) {
          static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
-template <bool kSwiglu, bool kRing = false>
+template <bool kSwiglu, bool kRing = false, bool kSoftmax = false>
 mok_status run_pair(const PairParams& P, cudaStream_t st) {
   const size_t smem = pair_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  auto kern = gemm_pair_persistent<kSwiglu, kRing>;
+  auto kern = gemm_pair_persistent<kSwiglu, kRing, kSoftmax>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return MOK_ERR_CUDA;
   const int grid = (num_sms() / 2) * 2;
@@ -548,6 +610,30 @@ mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, cons
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st) {
   return launch_down_pair(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st);
+}
+
+mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, int E, int D, float* s_out,
+                              cudaStream_t st) {
+  if (T == 0) return MOK_OK;
+  if (E < 1 || E > 256) return MOK_ERR_UNSUPPORTED;
+  PairParams P{};
+  P.sched = pair_sched(nullptr, 1, T, 1, D / BK);
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  if (!make_tmap_2d(&P.tmA, x, kBF16, static_cast<uint64_t>(T), D, static_cast<uint64_t>(D) * 2, 128, BK, true) ||
+      !make_tmap_2d(&P.tmB0, w_router, kBF16, static_cast<uint64_t>(E), D, static_cast<uint64_t>(D) * 2, 128, BK,
+                    true))
+    return MOK_ERR_CUDA;
+  P.tmB1 = P.tmB0;  // experts 128..255 (rows past E read as zeros, masked in the epilogue)
+  P.b_group_rows = 0;
+  P.b_tile_rows = 0;
+  P.b1_off = 128;
+  P.tmAs = P.tmA;
+  P.tmBs0 = P.tmB0;
+  P.tmBs1 = P.tmB0;
+  P.s_out = s_out;
+  P.E = E;
+  return run_pair<false, false, true>(P, st);
 }
 
 mok_status launch_upgate_ring(const void* x, const int32_t* table, int K, const void* w_gate, const void* w_up,

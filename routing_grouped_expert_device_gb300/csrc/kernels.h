@@ -58,6 +58,10 @@ struct SharedOperands {
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
                               cudaStream_t st, const SharedOperands* sh = nullptr);
+// Router scores s = softmax(x W_r^T) [T][E] fp32 (E <= 256): x [T][D], W_r
+// [E][D] bf16, on CTA pairs with the softmax in the epilogue.
+mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, int E, int D, float* s_out,
+                              cudaStream_t st);
 // Ring dispatch fused into the routed up/gate (BF16): producer warps in the
 // same launch gather x rows into `ring` ([ring_rows + 128][D] bf16) in
 // chunks of chunk_rows routed rows; counters: 2 * ceil(R / chunk_rows) ints.

@@ -73,6 +73,7 @@ _SIGS = {
     "mok_quantize_mxfp8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "mok_mxfp8_scale_bytes": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int32]),
     "mok_check_wait_timeout": (ctypes.c_int, [_P]),
+    "mok_router": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
     "mok_get_error": (ctypes.c_int, [_P]),
     "mok_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -240,6 +241,12 @@ def mx_scale_words(rows: int, cols: int, groups: int = 0) -> int:
     if n == 0 and rows > 0:
         raise MokError(MOK_ERR_INVALID_ARG, f"mok_mxfp8_scale_bytes({rows}, {cols}, {groups})")
     return n // 4
+
+
+def router(shape: Shape, x, w_router, s, topk_idx, g, stream=None):
+    """s = softmax(x W_r^T), then top-K and g on it."""
+    _check(_lib_handle().mok_router(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(s), _ptr(topk_idx), _ptr(g),
+                                    _stream(stream)), "mok_router")
 
 
 def check_wait_timeout(stream=None):

@@ -80,13 +80,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v: float, world: int) -> float:
+def max_over_ranks(v: float, world: int, device: str = "cuda") -> float:
+    """The slowest rank's time: the job ends when its last replica does."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput of N replicas: every rank's tokens over the
+    slowest rank's time (weak scaling: per-rank work is fixed)."""
+    return world * tokens_per_rank_step * steps / (max_ms / 1e3)
 
 
 def measured_peaks():
@@ -335,7 +342,7 @@ def run_ours(args, world, rank, local):
     total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world)
     part_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     ms_step = total_ms / K_steps
-    value = world * T * K_steps / (total_ms / 1e3)
+    value = job_tokens_per_s(world, T, K_steps, total_ms)
     flops = cfg.fwd_flops() + (cfg.bwd_flops() if cfg.backward else 0.0)
     tflops = flops / (ms_step / 1e3) / 1e12
     peaks = measured_peaks()

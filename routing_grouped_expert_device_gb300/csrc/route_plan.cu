@@ -127,10 +127,16 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(int* __restrict__ hist,
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int h = hist[static_cast<size_t>(c) * E + e];
-      hist[static_cast<size_t>(c) * E + e] = run;
-      run += h;
+    // eight independent loads in flight, then their running sum
+    for (int c0 = 0; c0 < nchunks; c0 += 8) {
+      int h[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) h[u] = c0 + u < nchunks ? hist[static_cast<size_t>(c0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (c0 + u < nchunks) hist[static_cast<size_t>(c0 + u) * E + e] = run;
+        run += h[u];
+      }
     }
   }
   // exclusive scan of run over e
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(1024) plan_scan_kernel(int* __restrict__ hist,
   if (e < E) {
     counts[e] = run;
     offsets[e] = excl;
-    for (int c = 0; c < nchunks; ++c) hist[static_cast<size_t>(c) * E + e] += excl;
+    for (int c = 0; c < nchunks; ++c) hist[static_cast<size_t>(c) * E + e] += excl;  // independent updates
   }
   if (e == 0) offsets[E] = static_cast<int32_t>(R);
 }

@@ -177,6 +177,20 @@ mok_status mok_plan_static(const int32_t *topk_idx, int32_t T, int32_t E, int32_
                            int32_t *counts, int32_t *offsets, int32_t *table,
                            int32_t *route_dst, void *stream);
 
+/* The pull schedule with several source ranks on one GPU (blog,
+ * "Scheduling": a destination's slots for local expert l are ordered by the
+ * per-source ordinal o, then the source rank r (paper note, "Pull dispatch,
+ * push combine"); the pages' garbled in-rank position read as
+ * p = sum_r' min(M[l][r'], o) + |{r' < r : M[l][r'] > o}|).  The T tokens
+ * form `ranks` contiguous virtual source ranks of T / ranks tokens (ranks
+ * must divide T); with ranks = 1 this is mok_plan.  Outputs as mok_plan;
+ * within each expert the rows follow the round-robin order.  ws:
+ * mok_plan_ranks_workspace_bytes(T, E, K, ranks) bytes (0 when invalid). */
+size_t mok_plan_ranks_workspace_bytes(int32_t T, int32_t E, int32_t K, int32_t ranks);
+mok_status mok_plan_ranks(const int32_t *topk_idx, int32_t T, int32_t E, int32_t K, int32_t ranks,
+                          int32_t *counts, int32_t *offsets, int32_t *table, int32_t *route_dst,
+                          void *ws, size_t ws_bytes, void *stream);
+
 /* Gather (blog, "Scheduling": tokens land expert-contiguous, zero local
  * copies).  xg[p] = x[table[p].src_index / K] for p < R; x bf16 [T][D],
  * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives the E4M3 codes [R][D]

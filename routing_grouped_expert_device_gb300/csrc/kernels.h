@@ -14,6 +14,11 @@ constexpr int kPlanChunk = 1024;
 
 int plan_chunks(int64_t R);
 size_t plan_scratch_bytes(int64_t R, int E);
+size_t plan_ranks_scratch_bytes(int64_t R, int E, int ranks);
+// the pull schedule with `ranks` virtual source ranks of T / ranks tokens
+mok_status launch_plan_ranks(const int32_t* topk, int64_t T, int K, int E, int ranks, int32_t* counts,
+                             int32_t* offsets, int32_t* table, int32_t* route_dst, int* scratch,
+                             cudaStream_t st);
 
 mok_status launch_route(const float* s, int T, int E, int K, int32_t* topk, float* g,
                         cudaStream_t st);

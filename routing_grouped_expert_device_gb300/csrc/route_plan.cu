@@ -215,6 +215,63 @@ __global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t*
   }
 }
 
+// ---------------------------------------------------------------------------
+// The pull schedule with several source ranks (blog, "Scheduling"; paper
+// note, "Pull dispatch, push combine": slots of a local expert ordered by
+// per-source ordinal, then source rank), on one GPU: the T tokens form
+// `ranks` contiguous virtual source ranks of T / ranks tokens.  Starting from
+// the one-rank plan, route (t, k) of expert e, rank r = t / (T / ranks) and
+// ordinal o among the routes of (e, r) gets slot
+// offsets[e] + sum_r' min(M[e][r'], o) + |{r' < r : M[e][r'] > o}|.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) plan_rank_count_kernel(const int32_t* __restrict__ topk, int64_t R, int K,
+                                                              int per_rank, int ranks, int* __restrict__ M) {
+  for (int64_t src = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; src < R;
+       src += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int e = __ldg(topk + src);
+    const int r = static_cast<int>((src / K) / per_rank);
+    atomicAdd(M + static_cast<int64_t>(e) * ranks + r, 1);  // integer counts: order-independent
+  }
+}
+
+// one thread per expert: exclusive prefix of M[e][.] over ranks
+__global__ void plan_rank_prefix_kernel(const int* __restrict__ M, int E, int ranks, int* __restrict__ pre) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  int run = 0;
+  for (int r = 0; r < ranks; ++r) {
+    pre[static_cast<int64_t>(e) * ranks + r] = run;
+    run += M[static_cast<int64_t>(e) * ranks + r];
+  }
+}
+
+__global__ void __launch_bounds__(256) plan_rank_place_kernel(const int32_t* __restrict__ topk, int64_t R, int K,
+                                                              int per_rank, int ranks, const int* __restrict__ M,
+                                                              const int* __restrict__ pre,
+                                                              const int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ table,
+                                                              int32_t* __restrict__ route_dst) {
+  for (int64_t src = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; src < R;
+       src += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int e = __ldg(topk + src);
+    const int r = static_cast<int>((src / K) / per_rank);
+    const int* Me = M + static_cast<int64_t>(e) * ranks;
+    // the one-rank slot is the route's ordinal within its expert
+    const int o = route_dst[src] - offsets[e] - pre[static_cast<int64_t>(e) * ranks + r];
+    int p = 0;
+    for (int q = 0; q < ranks; ++q) {
+      const int m = Me[q];
+      p += m < o ? m : o;
+      if (q < r && m > o) ++p;
+    }
+    const int dst = offsets[e] + p;
+    table[static_cast<int64_t>(dst) * 3 + 0] = static_cast<int32_t>(src);
+    table[static_cast<int64_t>(dst) * 3 + 1] = e;
+    table[static_cast<int64_t>(dst) * 3 + 2] = dst;
+    route_dst[src] = dst;
+  }
+}
+
 }  // namespace
 
 int plan_chunks(int64_t R) { return static_cast<int>((R + kPlanChunk - 1) / kPlanChunk); }
@@ -268,6 +325,30 @@ mok_status launch_plan(const int32_t* topk, int64_t R, int E, int32_t* counts, i
   return MOK_OK;
 }
 
+size_t plan_ranks_scratch_bytes(int64_t R, int E, int ranks) {
+  return plan_scratch_bytes(R, E) + 2 * static_cast<size_t>(E) * ranks * sizeof(int);
+}
+
+mok_status launch_plan_ranks(const int32_t* topk, int64_t T, int K, int E, int ranks, int32_t* counts,
+                             int32_t* offsets, int32_t* table, int32_t* route_dst, int* scratch,
+                             cudaStream_t st) {
+  const int64_t R = T * K;
+  mok_status r = launch_plan(topk, R, E, counts, offsets, table, route_dst, scratch, st);
+  if (r != MOK_OK || ranks == 1 || R == 0) return r;
+  int* M = scratch + plan_scratch_bytes(R, E) / sizeof(int);
+  int* pre = M + static_cast<int64_t>(E) * ranks;
+  const int per_rank = static_cast<int>(T / ranks);
+  if (cudaMemsetAsync(M, 0, static_cast<size_t>(E) * ranks * sizeof(int), st) != cudaSuccess) return MOK_ERR_CUDA;
+  const int blocks = static_cast<int>((R + 255) / 256 < num_sms() * 8 ? (R + 255) / 256 : num_sms() * 8);
+  plan_rank_count_kernel<<<blocks, 256, 0, st>>>(topk, R, K, per_rank, ranks, M);
+  MOK_CHECK_LAUNCH();
+  plan_rank_prefix_kernel<<<(E + 255) / 256, 256, 0, st>>>(M, E, ranks, pre);
+  MOK_CHECK_LAUNCH();
+  plan_rank_place_kernel<<<blocks, 256, 0, st>>>(topk, R, K, per_rank, ranks, M, pre, offsets, table, route_dst);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
 }  // namespace mok
 
 extern "C" mok_status mok_route(const float* s, int32_t T, int32_t E, int32_t K, int32_t* topk_idx,
@@ -289,4 +370,23 @@ extern "C" mok_status mok_plan(const int32_t* topk_idx, int32_t T, int32_t E, in
   if (ws_bytes < mok::plan_scratch_bytes(R, E)) return MOK_ERR_WORKSPACE;
   return mok::launch_plan(topk_idx, R, E, counts, offsets, table, route_dst, static_cast<int*>(ws),
                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t mok_plan_ranks_workspace_bytes(int32_t T, int32_t E, int32_t K, int32_t ranks) {
+  if (T < 0 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || ranks < 1 || (ranks > 1 && T % ranks)) return 0;
+  return mok::plan_ranks_scratch_bytes(static_cast<int64_t>(T) * K, E, ranks);
+}
+
+extern "C" mok_status mok_plan_ranks(const int32_t* topk_idx, int32_t T, int32_t E, int32_t K, int32_t ranks,
+                                     int32_t* counts, int32_t* offsets, int32_t* table, int32_t* route_dst,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || E < 1 || E > 1024 || K < 1 || K > 32 || K > E || ranks < 1 || ranks > 4096) return MOK_ERR_INVALID_ARG;
+  if (ranks > 1 && T % ranks) return MOK_ERR_INVALID_ARG;
+  const int64_t R = static_cast<int64_t>(T) * K;
+  if (R >= (int64_t(1) << 31)) return MOK_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !ws) return MOK_ERR_INVALID_ARG;
+  if (R > 0 && (!topk_idx || !table || !route_dst)) return MOK_ERR_INVALID_ARG;
+  if (ws_bytes < mok::plan_ranks_scratch_bytes(R, E, ranks)) return MOK_ERR_WORKSPACE;
+  return mok::launch_plan_ranks(topk_idx, T, K, E, ranks, counts, offsets, table, route_dst, static_cast<int*>(ws),
+                                static_cast<cudaStream_t>(stream));
 }

@@ -74,6 +74,9 @@ _SIGS = {
     "mok_mxfp8_scale_bytes": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int32]),
     "mok_check_wait_timeout": (ctypes.c_int, [_P]),
     "mok_router": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
+    "mok_plan_ranks_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 4),
+    "mok_plan_ranks": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "mok_get_error": (ctypes.c_int, [_P]),
     "mok_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -241,6 +244,18 @@ def mx_scale_words(rows: int, cols: int, groups: int = 0) -> int:
     if n == 0 and rows > 0:
         raise MokError(MOK_ERR_INVALID_ARG, f"mok_mxfp8_scale_bytes({rows}, {cols}, {groups})")
     return n // 4
+
+
+def plan_ranks(topk_idx, E: int, ranks: int, counts, offsets, table, route_dst, ws, stream=None):
+    """mok_plan with `ranks` virtual source ranks (round-robin order within each expert)."""
+    T, K = topk_idx.shape
+    _check(_lib_handle().mok_plan_ranks(_ptr(topk_idx), T, E, K, ranks, _ptr(counts), _ptr(offsets), _ptr(table),
+                                        _ptr(route_dst), _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)), "mok_plan_ranks")
+
+
+def plan_ranks_workspace_bytes(T: int, E: int, K: int, ranks: int) -> int:
+    return int(_lib_handle().mok_plan_ranks_workspace_bytes(T, E, K, ranks))
 
 
 def router(shape: Shape, x, w_router, s, topk_idx, g, stream=None):

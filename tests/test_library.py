@@ -72,3 +72,11 @@ def test_mxfp8_dispatch_needs_offsets(m):
     sh = m.make_shape(T=16, D=256, I=128, E=8, K=2, dtype=m.MOK_MXFP8)
     fake = ctypes.c_void_p(256)  # never dereferenced: the call is rejected first
     assert lib.mok_dispatch(ctypes.byref(sh), fake, fake, None, fake, fake, None) == m.MOK_ERR_INVALID_ARG
+
+
+def test_plan_ranks_host_checks(m):
+    lib = m._lib_handle()
+    assert m.plan_ranks_workspace_bytes(256, 8, 2, 4) > m.plan_ranks_workspace_bytes(256, 8, 2, 1)
+    assert m.plan_ranks_workspace_bytes(250, 8, 2, 4) == 0  # ranks must divide T
+    assert lib.mok_plan_ranks(None, 250, 8, 2, 4, None, None, None, None, None, 0, None) == m.MOK_ERR_INVALID_ARG
+    assert lib.mok_plan_ranks(None, 256, 8, 2, 0, None, None, None, None, None, 0, None) == m.MOK_ERR_INVALID_ARG

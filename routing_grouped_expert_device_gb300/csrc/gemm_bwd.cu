@@ -255,27 +255,33 @@ struct WgradCfg {
   }
 
   // Rows past the group's end in its last K block belong to the next group
-  // (or lie past the tensor and are zero-filled): zero them in A.
-  __device__ static void fixup(const Params&, const TileCoord& c, int kb, uint8_t* st, int lane) {
+  // (or lie past the tensor and are zero-filled).  The MMAs of that block
+  // stop at the first 16-row step at or past the end, and the rows between
+  // the end and that step are zeroed in A (both 64-column chunks; lane l
+  // clears 16-byte unit l % 8 of every fourth row).
+  __device__ static int k_rows(const TileCoord& c, int kb) {
     const int valid = c.rows - kb * BK;
-    if (valid >= BK) return;
-    const int nrows = BK - valid;
-    const int units = 2 * nrows * 8;  // 16-byte units: 2 chunks x rows x 128 B
-    for (int u = lane; u < units; u += 32) {
-      const int chunk = u / (nrows * 8);
-      const int rem = u - chunk * nrows * 8;
-      const int rrow = valid + rem / 8;
-      uint4* p = reinterpret_cast<uint4*>(st + chunk * MNCHUNK + rrow * 128 + (rem % 8) * 16);
-      *p = make_uint4(0, 0, 0, 0);
+    return valid < BK ? valid : BK;
+  }
+  __device__ static void fixup(const Params&, const TileCoord& c, int kb, uint8_t* st, int lane) {
+    const int valid = k_rows(c, kb);
+    const int end = (valid + 15) & ~15;
+    if (valid == end) return;
+    for (int r = valid + (lane >> 3); r < end; r += 4) {
+      uint8_t* p = st + r * 128 + (lane & 7) * 16;
+      *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(p + MNCHUNK) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
   }
 
-  __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
+  __device__ static void mma(const Params&, const TileCoord& c, int kb, uint8_t* st, uint32_t d) {
     const uint32_t s = smem_u32(st);
+    const int nk = (k_rows(c, kb) + 15) / 16;
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k)
-      mma_bf16(d, mndesc(s + k * 2048), mndesc(s + 2 * MNCHUNK + k * 2048), IDESC, (kb | k) != 0);
+      if (k < nk)
+        mma_bf16(d, mndesc(s + k * 2048), mndesc(s + 2 * MNCHUNK + k * 2048), IDESC, (kb | k) != 0);
   }
 
   // Each warp converts its 32 rows x 64 columns to bf16, writes them to its
@@ -290,14 +296,14 @@ struct WgradCfg {
     for (int cp = 0; cp < BN / 64; ++cp) {
       uint32_t pk[32];
       if (has_acc) {
-        uint32_t v[32];
+        uint32_t v0[32], v1[32];
+        tmem_ld32(taddr + cp * 64, v0);
+        tmem_ld32(taddr + cp * 64 + 32, v1);
+        tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tmem_ld32(taddr + cp * 64 + h * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            pk[h * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        for (int j = 0; j < 16; ++j) {
+          pk[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+          pk[16 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
         }
       } else {
 #pragma unroll

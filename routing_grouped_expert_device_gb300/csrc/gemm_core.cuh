@@ -97,59 +97,72 @@ __device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart,
   return total + extra_tiles(s);
 }
 
-__device__ __forceinline__ TileCoord decode_group_tile(const SchedArgs& s, const int* tstart,
-                                                       const int* rstart, int tile);
+// Tile -> coordinates for one role of a CTA.  Every role walks its tiles in
+// increasing order (first + i * stride), so the group of the next tile is
+// found by stepping forward from the group of the previous one, and the
+// per-group quantities (rows, M tiles, K blocks) are recomputed only when the
+// group changes; a tile then costs one integer division.
+//
+// Tile order with an extra group of S tiles among Rt grouped ones: positions
+// k*p + p - 1 (k < S, p = (Rt + S) / S) hold the extra tiles, the rest the
+// grouped tiles in order.
+struct TileWalker {
+  const SchedArgs& s;
+  const int* tstart;
+  const int* rstart;
+  int S, p, extra_mtiles;
+  int g;                                    // group of the last grouped tile
+  int cg, crow0, crows, cmtiles, ckblocks;  // cached quantities of group cg
 
-// Tile t of the whole launch: with an extra group of S tiles among Rt grouped
-// ones, positions k*p + p - 1 (k < S, p = (Rt + S) / S) hold the extra
-// tiles, the rest the grouped tiles in order.
-__device__ __forceinline__ TileCoord decode_tile(const SchedArgs& s, const int* tstart,
-                                                 const int* rstart, int tile) {
-  const int S = extra_tiles(s);
-  if (S == 0) return decode_group_tile(s, tstart, rstart, tile);
-  const int Rt = tstart[s.G];
-  const int p = (Rt + S) / S;
-  const int q = tile / p;
-  if (tile % p == p - 1 && q < S) {
-    const int mtiles = (s.extra_rows + s.bm - 1) / s.bm;
+  __device__ __forceinline__ TileWalker(const SchedArgs& s_, const int* tstart_, const int* rstart_)
+      : s(s_), tstart(tstart_), rstart(rstart_), g(0), cg(-1) {
+    S = extra_tiles(s);
+    p = S > 0 ? (tstart[s.G] + S) / S : 1;
+    extra_mtiles = S > 0 ? (s.extra_rows + s.bm - 1) / s.bm : 1;
+  }
+
+  __device__ __forceinline__ TileCoord at(int tile) {
     TileCoord c;
-    c.extra = 1;
-    c.g = 0;
-    c.nt = q / mtiles;
-    c.mt = q - c.nt * mtiles;
-    c.row0 = 0;
-    c.rows = s.extra_rows;
-    c.kblocks = s.extra_k_blocks;
+    int gt = tile;
+    if (S > 0) {
+      const int q = tile / p;
+      if (tile - q * p == p - 1 && q < S) {
+        c.extra = 1;
+        c.g = 0;
+        c.nt = q / extra_mtiles;
+        c.mt = q - c.nt * extra_mtiles;
+        c.row0 = 0;
+        c.rows = s.extra_rows;
+        c.kblocks = s.extra_k_blocks;
+        return c;
+      }
+      gt = tile - (q < S ? q : S);
+    }
+    // last group whose first tile is <= gt (steps over empty groups)
+    while (g + 1 < s.G && tstart[g + 1] <= gt) ++g;
+    if (g != cg) {
+      cg = g;
+      crow0 = rstart[g];
+      crows = rstart[g + 1] - crow0;
+      cmtiles = sched_m_tiles(s, crows);
+      ckblocks = sched_k_blocks(s, crows);
+    }
+    c.extra = 0;
+    c.g = g;
+    c.row0 = crow0;
+    c.rows = crows;
+    const int local = gt - tstart[g];
+    if (s.m_outer) {
+      c.mt = local / s.n_tiles;
+      c.nt = local - c.mt * s.n_tiles;
+    } else {
+      c.nt = local / cmtiles;
+      c.mt = local - c.nt * cmtiles;
+    }
+    c.kblocks = ckblocks;
     return c;
   }
-  return decode_group_tile(s, tstart, rstart, tile - (q < S ? q : S));
-}
-
-__device__ __forceinline__ TileCoord decode_group_tile(const SchedArgs& s, const int* tstart,
-                                                       const int* rstart, int tile) {
-  int lo = 0, hi = s.G - 1;
-  while (lo < hi) {  // last group whose first tile is <= tile (skips empty groups)
-    int mid = (lo + hi + 1) >> 1;
-    if (tstart[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  TileCoord c;
-  c.extra = 0;
-  c.g = lo;
-  c.row0 = rstart[lo];
-  c.rows = rstart[lo + 1] - c.row0;
-  const int mtiles = sched_m_tiles(s, c.rows);
-  const int local = tile - tstart[lo];
-  if (s.m_outer) {
-    c.mt = local / s.n_tiles;
-    c.nt = local - c.mt * s.n_tiles;
-  } else {
-    c.nt = local / mtiles;
-    c.mt = local - c.nt * mtiles;
-  }
-  c.kblocks = sched_k_blocks(s, c.rows);
-  return c;
-}
+};
 
 // Shared memory: [STAGES x STAGE_BYTES][1 KB barriers and flags]
 // [EPI_SMEM_BYTES epilogue staging, 1 KB aligned][tile table].
@@ -226,8 +239,9 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
     bool issued[Cfg::STAGES];
     for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = false;
     bool ok = true;
+    TileWalker walk(P.sched, tstart, rstart);
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      const TileCoord c = walk.at(tile);
       for (int kb = 0; kb < c.kblocks; ++kb) {
         bool got = false;
         if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER);
@@ -259,8 +273,9 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
     uint32_t stage = 0, phase = 0;
     bool ok = true, any = false;
     int it = 0;
+    TileWalker walk(P.sched, tstart, rstart);
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      const TileCoord c = walk.at(tile);
       const uint32_t acc = (Cfg::NUM_ACC == 2) ? (it & 1) : 0;
       const uint32_t acc_phase = (Cfg::NUM_ACC == 2) ? ((it >> 1) & 1) : (it & 1);
       // Waits are taken by every lane and made warp-uniform, so the warp
@@ -303,8 +318,9 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
     // ---------------- epilogue ----------------
     const int ew = warp - 4;
     int it = 0;
+    TileWalker walk(P.sched, tstart, rstart);
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      const TileCoord c = walk.at(tile);
       const uint32_t acc = (Cfg::NUM_ACC == 2) ? (it & 1) : 0;
       const uint32_t acc_phase = (Cfg::NUM_ACC == 2) ? ((it >> 1) & 1) : (it & 1);
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, P.status, SITE_EPILOGUE)))

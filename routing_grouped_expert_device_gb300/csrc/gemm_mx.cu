@@ -149,8 +149,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
       const CUtensorMap* tmB = rank ? &P.tmB1 : &P.tmB0;
+      TileWalker walk(P.sched, tstart, rstart);
       for (int tile = cid; tile < total && ok; tile += ncl) {
-        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        const TileCoord c = walk.at(tile);
         const int local0 = c.mt * 256 + static_cast<int>(rank) * 128;  // this CTA's first row in the group
         const int arow = c.row0 + local0;
         const int sfrow = static_cast<int>(mx_group_row0(c.row0, c.g)) + local0;  // a multiple of 128
@@ -193,8 +194,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true, any = false;
       int it = 0;
+      TileWalker walk(P.sched, tstart, rstart);
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
-        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        const TileCoord c = walk.at(tile);
         ok = __all_sync(0xffffffffu, mbar_wait(tempty, (it & 1) ^ 1, abort_flag, P.status, SITE_MMA));
         if (!ok) break;
         tc_fence_after();
@@ -240,8 +242,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
     const int q = warp - 4;  // TMEM lane quarter of this warp
     int it = 0;
+    TileWalker walk(P.sched, tstart, rstart);
     for (int tile = cid; tile < total; tile += ncl, ++it) {
-      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      const TileCoord c = walk.at(tile);
       if (!__all_sync(0xffffffffu, mbar_wait(tfull, it & 1, abort_flag, P.status, SITE_EPILOGUE))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);

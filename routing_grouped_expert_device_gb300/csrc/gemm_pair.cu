@@ -256,8 +256,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       bool issued[STAGES];
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
+      TileWalker walk(P.sched, tstart, rstart);
       for (int tile = cid; tile < total && ok; tile += ncl) {
-        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        const TileCoord c = walk.at(tile);
         const int arow = c.row0 + c.mt * 256 + static_cast<int>(rank) * 128;
         const int brow = c.g * P.b_group_rows + c.nt * P.b_tile_rows + (rank ? P.b1_off : 0);
         const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
@@ -305,8 +306,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true, any = false;
       int it = 0;
+      TileWalker walk(P.sched, tstart, rstart);
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
-        const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+        const TileCoord c = walk.at(tile);
         const uint32_t acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         ok = __all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, P.status, SITE_MMA));
@@ -368,8 +370,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     uint8_t* blk = epi_smem + ew * EPI_BLOCK;
     uint8_t* srow = blk + lane * 128;
     int it = 0;
+    TileWalker walk(P.sched, tstart, rstart);
     for (int tile = cid; tile < total; tile += ncl, ++it) {
-      const TileCoord c = decode_tile(P.sched, tstart, rstart, tile);
+      const TileCoord c = walk.at(tile);
       const uint32_t acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, P.status, SITE_EPILOGUE)))

@@ -11,7 +11,8 @@
 //  dx           : dx = bf16(dh W_gate + du W_up), K = 2I, weights MN-major.
 //  wgrad        : dW[e] = bf16(sum over the expert's rows of P^T Q) with both
 //                 operands MN-major and K running over rows; the last K block
-//                 of an expert is masked by zeroing the rows past its end.
+//                 of an expert stops at its end (16-row MMA steps, the few
+//                 rows past the end zeroed in A).
 #include "gemm_core.cuh"
 #include "kernels.h"
 

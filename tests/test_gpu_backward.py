@@ -24,6 +24,9 @@ SMALL = {
     "ragged": W.MoEConfig("ragged", T=300, D=512, I=256, E=5, K=3, I_shared=128),
     "skew_small": W.MoEConfig("skew_small", T=700, D=256, I=128, E=16, K=4, I_shared=0, skew=2.0),
     "one_expert": W.MoEConfig("one_expert", T=200, D=256, I=128, E=1, K=1, I_shared=0),
+    # D and I multiples of 256 (256-column weight-gradient tiles throughout),
+    # with empty experts and ragged expert ends
+    "skew_256": W.MoEConfig("skew_256", T=700, D=512, I=256, E=32, K=4, I_shared=256, skew=2.0),
 }
 
 
@@ -85,7 +88,7 @@ def test_backward_elementwise_and_deterministic(m, name):
         assert_close(_f(got["dws_down"]), ref["dWs_down"], BF16_TOL, "dWs_down", sl["dWs_down"])
     assert_close(_f(got["dg"]), ref["dg"], BF16_TOL, "dg", sl["dg"])
     assert_close(_f(got["ds"]), ref["ds"], BF16_TOL, "ds", sl["ds"])
-    if name == "skew_small":
+    if name in ("skew_small", "skew_256"):
         empty = np.flatnonzero(np.bincount(O.route(h["s"], cfg.K)[0].reshape(-1), minlength=cfg.E) == 0)
         assert len(empty) > 0 and torch.all(got["dw_down"][torch.from_numpy(empty).to(DEV)] == 0)
     again, _ = _fwd_bwd(m, cfg, d)

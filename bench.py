@@ -302,7 +302,7 @@ def run_ours(args, world, rank, local):
         M.route(d["s"], K, topk, g)
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
         if not ring:
-            M.dispatch(shape, d["x"], table, xg, xs, offsets=offsets)
+            M.dispatch(shape, d["x"], table, route_dst, xg, xs, offsets=offsets)
         if ev0 is not None:
             ev0.record(stream)
         if ring:  # the dispatch runs inside the up/gate launch (producer warps, ring of chunks)

@@ -191,14 +191,18 @@ mok_status mok_plan_ranks(const int32_t *topk_idx, int32_t T, int32_t E, int32_t
                           int32_t *counts, int32_t *offsets, int32_t *table, int32_t *route_dst,
                           void *ws, size_t ws_bytes, void *stream);
 
-/* Gather (blog, "Scheduling": tokens land expert-contiguous, zero local
- * copies).  xg[p] = x[table[p].src_index / K] for p < R; x bf16 [T][D],
- * xg bf16 [R][D].  With dtype MOK_MXFP8 xg receives the E4M3 codes [R][D]
- * of the gathered rows and xg_scale their scale words in the grouped layout
- * (quantisation fused into the dispatch), for which offsets (mok_plan's)
- * is required; xg_scale and offsets are ignored for BF16. */
+/* Dispatch (blog, "Scheduling": tokens land expert-contiguous, zero local
+ * copies).  xg[p] = x[table[p].src_index / K] for p < R, computed token by
+ * token: row t of x is read once and stored at its K positions
+ * route_dst[t*K + k] (mok_plan's inverse of the table); x bf16 [T][D], xg
+ * bf16 [R][D].  route_dst is required.  With dtype MOK_MXFP8 xg receives
+ * the E4M3 codes [R][D] of the dispatched rows and xg_scale their scale
+ * words in the grouped layout (quantisation fused into the dispatch, once
+ * per token), for which table and offsets (mok_plan's) are required; table,
+ * xg_scale and offsets are ignored for BF16. */
 mok_status mok_dispatch(const mok_shape *shape, const void *x, const int32_t *table,
-                        const int32_t *offsets, void *xg, uint8_t *xg_scale, void *stream);
+                        const int32_t *route_dst, const int32_t *offsets, void *xg, uint8_t *xg_scale,
+                        void *stream);
 
 /* Grouped expert FFN over expert-contiguous rows: expert e owns rows
  * [offsets[e], offsets[e+1]) of xg.  a = bf16(SiLU(xg W_gate^T) * (xg W_up^T))

@@ -159,18 +159,19 @@ extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
 }
 
 extern "C" mok_status mok_dispatch(const mok_shape* shape, const void* x, const int32_t* table,
-                                   const int32_t* offsets, void* xg, uint8_t* xg_scale, void* stream) {
+                                   const int32_t* route_dst, const int32_t* offsets, void* xg, uint8_t* xg_scale,
+                                   void* stream) {
   if (!shape_ok(shape)) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   if (R == 0) return MOK_OK;
-  if (!x || !table || !xg || !aligned16(x) || !aligned16(xg)) return MOK_ERR_INVALID_ARG;
+  if (!x || !route_dst || !xg || !aligned16(x) || !aligned16(xg)) return MOK_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s.dtype == MOK_MXFP8) {
-    if (!xg_scale || !offsets) return MOK_ERR_INVALID_ARG;
-    return launch_dispatch_mxfp8(x, table, offsets, R, s.K, s.D, s.E, xg, xg_scale, st);
+    if (!table || !xg_scale || !offsets) return MOK_ERR_INVALID_ARG;
+    return launch_dispatch_mxfp8(x, route_dst, table, offsets, s.T, s.K, s.D, s.E, xg, xg_scale, st);
   }
-  return launch_dispatch_bf16(x, table, R, s.K, s.D, xg, nullptr, nullptr, st);
+  return launch_dispatch_bf16(x, route_dst, s.T, s.K, s.D, xg, nullptr, nullptr, st);
 }
 
 extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* w, const void* xg,
@@ -390,8 +391,8 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
                        at<int>(ws, L.hist), st)) != MOK_OK)
     return fail(r);
   if (mx) {
-    if ((r = launch_dispatch_mxfp8(x, pb.table, pb.offsets, R, s.K, s.D, s.E, xg, at<uint8_t>(ws, L.xg_scale),
-                                   st)) != MOK_OK)
+    if ((r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xg,
+                                   at<uint8_t>(ws, L.xg_scale), st)) != MOK_OK)
       return fail(r);
     void* asc = at<void>(ws, L.a_scale);
     if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
@@ -409,7 +410,7 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
                                   st)) != MOK_OK)
         return fail(r);
     } else {
-      if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
+      if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
         return fail(r);
       if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr)) !=
           MOK_OK)
@@ -476,8 +477,8 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
   void* dxr = at<void>(ws, L.dxr);
   mok_status r;
   // gather x, dY and the route weights into expert order (the forward's plan)
-  if ((r = launch_dispatch_bf16(x, pb.table, R, s.K, s.D, xg, pb.g, g_route, st)) != MOK_OK) return r;
-  if ((r = launch_dispatch_bf16(dy, pb.table, R, s.K, s.D, dyg, nullptr, nullptr, st)) != MOK_OK)
+  if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, pb.g, g_route, st)) != MOK_OK) return r;
+  if ((r = launch_dispatch_bf16(dy, pb.route_dst, s.T, s.K, s.D, dyg, nullptr, nullptr, st)) != MOK_OK)
     return r;
   // replay h, u; t = dY W_down; dh, du, g*a, <t, a> partials
   if ((r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,

@@ -16,33 +16,44 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
   return v;
 }
 
-// Gather (Mixture-of-Kittens blog, "Scheduling": rows land expert-contiguous,
-// read once, written once).  One warp per destination row; 4 vectors in
-// flight per lane.
+// Dispatch (Mixture-of-Kittens blog, "Scheduling": rows land
+// expert-contiguous).  One warp per token: its row is read once, 4 vectors
+// per lane in flight, and stored at each of its K positions in expert order,
+// p = route_dst[t K + k] (lane k holds p, K <= 32).  Reading each row once
+// instead of once per route keeps x's K re-reads off DRAM while the K D-wide
+// copies stream out.  When g_route is non-null also g_route[p] = g[t K + k].
 __global__ void __launch_bounds__(256) dispatch_bf16_kernel(const uint4* __restrict__ x,
-                                                            const int32_t* __restrict__ table,
-                                                            int64_t R, int K, int D8,
+                                                            const int32_t* __restrict__ route_dst,
+                                                            int T, int K, int D8,
                                                             uint4* __restrict__ xg,
                                                             const float* __restrict__ g,
                                                             float* __restrict__ g_route) {
   const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; p < R;
-       p += nwarps) {
-    const int src = __ldg(table + p * 3);
-    const uint4* in = x + static_cast<int64_t>(src / K) * D8;
-    uint4* out = xg + p * D8;
-    int i = lane;
-    for (; i + 96 < D8; i += 128) {
-      const uint4 a = ld_nc_v4(in + i), b = ld_nc_v4(in + i + 32), c = ld_nc_v4(in + i + 64),
-                  d = ld_nc_v4(in + i + 96);
-      out[i] = a;
-      out[i + 32] = b;
-      out[i + 64] = c;
-      out[i + 96] = d;
+  const int nwarps = static_cast<int>((static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5);
+  for (int t = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5); t < T;
+       t += nwarps) {
+    const int64_t r0 = static_cast<int64_t>(t) * K;
+    const int dst = lane < K ? __ldg(route_dst + r0 + lane) : 0;
+    if (g_route && lane < K) g_route[dst] = g[r0 + lane];
+    const uint4* in = x + static_cast<int64_t>(t) * D8;
+#pragma unroll 1
+    for (int i0 = 0; i0 < D8; i0 += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + 32 * u + lane;
+        v[u] = i < D8 ? ld_nc_v4(in + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll 1
+      for (int k = 0; k < K; ++k) {
+        uint4* out = xg + static_cast<int64_t>(__shfl_sync(0xffffffffu, dst, k)) * D8;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + 32 * u + lane;
+          if (i < D8) out[i] = v[u];
+        }
+      }
     }
-    for (; i < D8; i += 32) out[i] = ld_nc_v4(in + i);
-    if (g_route && lane == 0) g_route[p] = g[src];
   }
 }
 
@@ -61,11 +72,14 @@ __device__ __forceinline__ int mx_exponent(float amax) {
 // 1x32 block is 4 lanes (its amax: two xor shuffles) and one pass of the warp
 // covers 256 columns, two 128-column scale groups; loads and code stores are
 // contiguous across the warp.  Each group's 4 scale bytes are gathered into
-// one 32-bit word (layout in kernels.h).  table == nullptr: identity rows,
-// plain layout (the quantiser); else row p is x[table[p].src / K] and its
-// scales go to the grouped layout of expert table[p].e (the dispatch with
-// fused quantisation).
+// one 32-bit word (layout in kernels.h).  route_dst == nullptr: row r is
+// stored at row r, plain layout (the quantiser).  Else (the dispatch with
+// fused quantisation) the rows are tokens: token t is quantised once and
+// stored at each of its K positions p = route_dst[t K + k] (lane k holds p
+// and its scale position, K <= 32), with the grouped scale layout of expert
+// table[p].e.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ src,
+                                                         const int32_t* __restrict__ route_dst,
                                                          const int32_t* __restrict__ table,
                                                          const int32_t* __restrict__ offsets, int K,
                                                          int64_t rows, int64_t cols, int64_t ld,
@@ -76,16 +90,18 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
   const int c8 = static_cast<int>(cols / 8);  // 16-byte vectors per row
   for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows;
        row += nwarps) {
-    int64_t srow = row, pos_row = row;
-    if (table) {
-      srow = __ldg(table + row * 3) / K;
-      const int e = __ldg(table + row * 3 + 1);
-      const int64_t off = __ldg(offsets + e);
-      pos_row = mx_group_row0(off, e) + (row - off);
+    int ndst = 1;
+    int64_t dst = row, dpos = mx_scale_pos(row);
+    if (route_dst) {
+      ndst = K;
+      if (lane < K) {
+        dst = __ldg(route_dst + row * K + lane);
+        const int e = __ldg(table + dst * 3 + 1);
+        const int64_t off = __ldg(offsets + e);
+        dpos = mx_scale_pos(mx_group_row0(off, e) + (dst - off));
+      }
     }
-    const int64_t pos = mx_scale_pos(pos_row);
-    const uint4* in = src + srow * c8;
-    uint2* out = q + row * c8;
+    const uint4* in = src + row * c8;
 #pragma unroll 1
     for (int v0 = 0; v0 < c8; v0 += 128) {  // 4 passes of 256 columns in flight
       uint4 v[4];
@@ -121,7 +137,6 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
               make_float2(f[4 * j + 2] * inv, f[4 * j + 3] * inv), __NV_SATFINITE, __NV_E4M3);
           packed[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
         }
-        if (vi < c8) out[vi] = make_uint2(packed[0], packed[1]);
         // scale word of the 128-column group of lanes 16h .. 16h + 15: byte b
         // from lane 16h + 4b
         const uint32_t byte = static_cast<uint32_t>(e + 127);
@@ -130,7 +145,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
                               (__shfl_sync(0xffffffffu, byte, base + 4) << 8) |
                               (__shfl_sync(0xffffffffu, byte, base + 8) << 16) |
                               (__shfl_sync(0xffffffffu, byte, base + 12) << 24);
-        if ((lane & 15) == 0 && vi < c8) scale[static_cast<int64_t>(vi / 16) * ld + pos] = word;
+#pragma unroll 1
+        for (int k = 0; k < ndst; ++k) {
+          const int64_t p = __shfl_sync(0xffffffffu, dst, k);
+          const int64_t pos = __shfl_sync(0xffffffffu, dpos, k);
+          if (vi < c8) q[p * c8 + vi] = make_uint2(packed[0], packed[1]);
+          if ((lane & 15) == 0 && vi < c8) scale[static_cast<int64_t>(vi / 16) * ld + pos] = word;
+        }
       }
     }
   }
@@ -231,20 +252,24 @@ int grid_for(int64_t work_items, int per_block) {
 
 }  // namespace
 
-mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, int K, int D,
-                                void* xg, const float* g, float* g_route, cudaStream_t st) {
-  if (R == 0) return MOK_OK;
-  dispatch_bf16_kernel<<<grid_for(R, 8), 256, 0, st>>>(static_cast<const uint4*>(x), table, R, K,
-                                                        D / 8, static_cast<uint4*>(xg), g, g_route);
+mok_status launch_dispatch_bf16(const void* x, const int32_t* route_dst, int T, int K, int D, void* xg,
+                                const float* g, float* g_route, cudaStream_t st) {
+  if (T == 0) return MOK_OK;
+  if (K > 32) return MOK_ERR_UNSUPPORTED;
+  dispatch_bf16_kernel<<<grid_for(T, 8), 256, 0, st>>>(static_cast<const uint4*>(x), route_dst, T, K, D / 8,
+                                                        static_cast<uint4*>(xg), g, g_route);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
 
-mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int32_t* offsets, int64_t R,
-                                 int K, int D, int E, void* xg_q, uint8_t* xg_scale, cudaStream_t st) {
-  if (R == 0) return MOK_OK;
-  quant_rows_kernel<<<grid_for(R, 8), 256, 0, st>>>(static_cast<const uint4*>(x), table, offsets, K, R, D,
-                                                    mx_scale_ld(R, E), static_cast<uint2*>(xg_q),
+mok_status launch_dispatch_mxfp8(const void* x, const int32_t* route_dst, const int32_t* table,
+                                 const int32_t* offsets, int T, int K, int D, int E, void* xg_q, uint8_t* xg_scale,
+                                 cudaStream_t st) {
+  if (T == 0) return MOK_OK;
+  if (K > 32) return MOK_ERR_UNSUPPORTED;
+  const int64_t R = static_cast<int64_t>(T) * K;
+  quant_rows_kernel<<<grid_for(T, 8), 256, 0, st>>>(static_cast<const uint4*>(x), route_dst, table, offsets, K, T,
+                                                    D, mx_scale_ld(R, E), static_cast<uint2*>(xg_q),
                                                     reinterpret_cast<uint32_t*>(xg_scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
@@ -253,8 +278,8 @@ mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int3
 mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
                                  uint8_t* scale, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
-  quant_rows_kernel<<<grid_for(rows, 8), 256, 0, st>>>(static_cast<const uint4*>(src), nullptr, nullptr, 1, rows,
-                                                       cols, mx_scale_ld(rows), static_cast<uint2*>(q),
+  quant_rows_kernel<<<grid_for(rows, 8), 256, 0, st>>>(static_cast<const uint4*>(src), nullptr, nullptr, nullptr, 1,
+                                                       rows, cols, mx_scale_ld(rows), static_cast<uint2*>(q),
                                                        reinterpret_cast<uint32_t*>(scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;

@@ -25,12 +25,15 @@ mok_status launch_route(const float* s, int T, int E, int K, int32_t* topk, floa
 mok_status launch_plan(const int32_t* topk, int64_t R, int E, int32_t* counts, int32_t* offsets,
                        int32_t* table, int32_t* route_dst, int* hist, cudaStream_t st);
 
-// xg[p] = x[table[p].src / K]; when g_route is non-null also
-// g_route[p] = g[table[p].src].
-mok_status launch_dispatch_bf16(const void* x, const int32_t* table, int64_t R, int K, int D,
-                                void* xg, const float* g, float* g_route, cudaStream_t st);
-mok_status launch_dispatch_mxfp8(const void* x, const int32_t* table, const int32_t* offsets, int64_t R,
-                                 int K, int D, int E, void* xg_q, uint8_t* xg_scale, cudaStream_t st);
+// xg[route_dst[t K + k]] = x[t] (each token row read once, stored K times;
+// K <= 32); when g_route is non-null also g_route[route_dst[r]] = g[r].
+mok_status launch_dispatch_bf16(const void* x, const int32_t* route_dst, int T, int K, int D, void* xg,
+                                const float* g, float* g_route, cudaStream_t st);
+// The same with MXFP8 quantisation: codes [R][D] and grouped scale words
+// (expert of position p: table[p].e).
+mok_status launch_dispatch_mxfp8(const void* x, const int32_t* route_dst, const int32_t* table,
+                                 const int32_t* offsets, int T, int K, int D, int E, void* xg_q, uint8_t* xg_scale,
+                                 cudaStream_t st);
 mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, void* q,
                                  uint8_t* scale, cudaStream_t st);
 // out[t] = bf16(base[t] + sum_k w[t,k] * rows[route_dst[t*K+k]]); base and w

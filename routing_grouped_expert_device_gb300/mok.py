@@ -55,7 +55,7 @@ _SIGS = {
     "mok_route": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "mok_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "mok_plan_static": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
-    "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
+    "mok_dispatch": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P, _P]),
     "mok_expert_ffn": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P,
                                       _P, _SZ, _P]),
     "mok_expert_upgate": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P, _P, _P, _P, _P,
@@ -169,10 +169,12 @@ def plan_static(topk_idx, E, counts, offsets, table, route_dst, stream=None):
                                          _ptr(route_dst), _stream(stream)), "mok_plan_static")
 
 
-def dispatch(shape: Shape, x, table, xg, xg_scale=None, offsets=None, stream=None):
-    """Gather; for MXFP8 also quantise, which needs the plan's offsets."""
-    _check(_lib_handle().mok_dispatch(ctypes.byref(shape), _ptr(x), _ptr(table), _ptr(offsets), _ptr(xg),
-                                      _ptr(xg_scale), _stream(stream)), "mok_dispatch")
+def dispatch(shape: Shape, x, table, route_dst, xg, xg_scale=None, offsets=None, stream=None):
+    """Rows of x to expert order (each token read once, stored at its
+    route_dst positions); for MXFP8 also quantise, which needs the plan's
+    table and offsets."""
+    _check(_lib_handle().mok_dispatch(ctypes.byref(shape), _ptr(x), _ptr(table), _ptr(route_dst), _ptr(offsets),
+                                      _ptr(xg), _ptr(xg_scale), _stream(stream)), "mok_dispatch")
 
 
 def expert_ffn(shape: Shape, weights: Weights, xg, offsets, yg, a_out=None, ws=None, xg_scale=None, stream=None):

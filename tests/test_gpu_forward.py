@@ -116,7 +116,7 @@ def test_dispatch_exact(m, name):
     table = torch.from_numpy(ref[4]).to(DEV)
     x = inp["x"].to(DEV)
     xg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
-    m.dispatch(m.shape_of(cfg), x, table, xg)
+    m.dispatch(m.shape_of(cfg), x, table, torch.from_numpy(ref[5]).to(DEV), xg)
     want = O.gather(h["x"], ref[4], cfg.K)
     assert np.array_equal(W.bf16_bits(xg), want)
 
@@ -212,7 +212,7 @@ def test_expert_ffn_full_size_sampled_rows(m):
     idx, g, counts, offsets, table, route_dst = _plan_ref(s_host, cfg.K, cfg.E)
     shape = m.shape_of(cfg)
     xg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
-    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xg)
+    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), torch.from_numpy(route_dst).to(DEV), xg)
     a = torch.empty(cfg.R, cfg.I, dtype=torch.bfloat16, device=DEV)
     yg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
     m.expert_ffn(shape, m.make_weights(d), xg, torch.from_numpy(offsets).to(DEV), yg, a_out=a)
@@ -309,7 +309,7 @@ def test_ring_upgate_bitexact_vs_dispatch(m, name, chunk):
     table = torch.from_numpy(ref["table"]).to(DEV)
     off = torch.from_numpy(ref["offsets"]).to(DEV)
     xg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
-    m.dispatch(shape, d["x"], table, xg)
+    m.dispatch(shape, d["x"], table, torch.from_numpy(ref["route_dst"]).to(DEV), xg)
     a1 = torch.empty(cfg.R, cfg.I, dtype=torch.bfloat16, device=DEV)
     m.expert_upgate(shape, m.make_weights(d), xg, off, a1)
     ws = torch.empty(m.workspace_bytes(shape, m.OP_RING), dtype=torch.uint8, device=DEV)

@@ -85,11 +85,11 @@ def test_dispatch_mxfp8_bitexact(m, name):
     inp = W.make_inputs(cfg, "cpu")
     h = host(inp)
     idx, _, _ = O.route(h["s"], cfg.K)
-    _, offsets, table, _ = O.plan(idx, cfg.E)
+    _, offsets, table, route_dst = O.plan(idx, cfg.E)
     xq = torch.empty(cfg.R, cfg.D, dtype=torch.uint8, device=DEV)
     xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D, cfg.E), dtype=torch.int32, device=DEV)
-    m.dispatch(m.shape_of(cfg), inp["x"].to(DEV), torch.from_numpy(table).to(DEV), xq, xs,
-               offsets=torch.from_numpy(offsets).to(DEV))
+    m.dispatch(m.shape_of(cfg), inp["x"].to(DEV), torch.from_numpy(table).to(DEV),
+               torch.from_numpy(route_dst).to(DEV), xq, xs, offsets=torch.from_numpy(offsets).to(DEV))
     qr, sr = O.mxfp8_quantize(O.gather(O.bf16_to_f32(h["x"]), table, cfg.K))
     assert np.array_equal(xq.cpu().numpy(), qr)
     assert np.array_equal(words_to_bytes(xs, cfg.R, cfg.D, offsets), sr)
@@ -116,12 +116,13 @@ def test_expert_ffn_mxfp8_elementwise(m, name):
     h = host(inp)
     d = mx_weights(m, {k: v.to(DEV) for k, v in inp.items()})
     idx, _, _ = O.route(h["s"], cfg.K)
-    _, offsets, table, _ = O.plan(idx, cfg.E)
+    _, offsets, table, route_dst = O.plan(idx, cfg.E)
     shape = m.shape_of(cfg)
     off = torch.from_numpy(offsets).to(DEV)
     xq = torch.empty(cfg.R, cfg.D, dtype=torch.uint8, device=DEV)
     xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D, cfg.E), dtype=torch.int32, device=DEV)
-    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xq, xs, offsets=off)
+    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), torch.from_numpy(route_dst).to(DEV), xq, xs,
+               offsets=off)
     aq = torch.empty(cfg.R, cfg.I, dtype=torch.uint8, device=DEV)
     asc = torch.empty(m.mx_scale_words(cfg.R, cfg.I, cfg.E), dtype=torch.int32, device=DEV)
     yg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
@@ -172,7 +173,7 @@ def test_mxfp8_full_size_sampled_rows(m):
     d = mx_weights(m, d)
     s_host = d["s"].cpu().numpy()
     idx, _, _ = O.route(s_host, cfg.K)
-    counts, offsets, table, _ = O.plan(idx, cfg.E)
+    counts, offsets, table, route_dst = O.plan(idx, cfg.E)
     shape = m.shape_of(cfg)
     out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
     ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
@@ -182,7 +183,8 @@ def test_mxfp8_full_size_sampled_rows(m):
     assert np.array_equal(saved["table"].cpu().numpy(), table)
     xq = torch.empty(cfg.R, cfg.D, dtype=torch.uint8, device=DEV)
     xs = torch.empty(m.mx_scale_words(cfg.R, cfg.D, cfg.E), dtype=torch.int32, device=DEV)
-    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), xq, xs, offsets=torch.from_numpy(offsets).to(DEV))
+    m.dispatch(shape, d["x"], torch.from_numpy(table).to(DEV), torch.from_numpy(route_dst).to(DEV), xq, xs,
+               offsets=torch.from_numpy(offsets).to(DEV))
     yg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
     fws = torch.empty(m.workspace_bytes(shape, m.OP_EXPERT_FFN), dtype=torch.uint8, device=DEV)
     m.expert_ffn(shape, m.make_weights(d), xq, torch.from_numpy(offsets).to(DEV), yg, ws=fws, xg_scale=xs)

@@ -69,7 +69,7 @@ def test_plan_ranks_one_rank_is_plan_and_layer_output_is_order_free(m):
         tab = torch.from_numpy(table).to(DEV)
         off = torch.from_numpy(offsets).to(DEV)
         xg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
-        m.dispatch(shape, d["x"], tab, xg)
+        m.dispatch(shape, d["x"], tab, torch.from_numpy(route_dst).to(DEV), xg)
         yg = torch.empty(cfg.R, cfg.D, dtype=torch.bfloat16, device=DEV)
         fws = torch.empty(m.workspace_bytes(shape, m.OP_EXPERT_FFN), dtype=torch.uint8, device=DEV)
         m.expert_ffn(shape, w, xg, off, yg, ws=fws)

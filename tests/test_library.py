@@ -67,11 +67,17 @@ def test_mxfp8_scale_bytes(m):
     assert m.mx_scale_words(301, 512) == 4 * 384
 
 
-def test_mxfp8_dispatch_needs_offsets(m):
+def test_dispatch_argument_checks(m):
     lib = m._lib_handle()
     sh = m.make_shape(T=16, D=256, I=128, E=8, K=2, dtype=m.MOK_MXFP8)
-    fake = ctypes.c_void_p(256)  # never dereferenced: the call is rejected first
-    assert lib.mok_dispatch(ctypes.byref(sh), fake, fake, None, fake, fake, None) == m.MOK_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(256)  # never dereferenced: each call is rejected first
+    # MXFP8 needs offsets, the table and the scale output
+    assert lib.mok_dispatch(ctypes.byref(sh), fake, fake, fake, None, fake, fake, None) == m.MOK_ERR_INVALID_ARG
+    assert lib.mok_dispatch(ctypes.byref(sh), fake, None, fake, fake, fake, fake, None) == m.MOK_ERR_INVALID_ARG
+    assert lib.mok_dispatch(ctypes.byref(sh), fake, fake, fake, fake, fake, None, None) == m.MOK_ERR_INVALID_ARG
+    # every dtype needs route_dst
+    sb = m.make_shape(T=16, D=256, I=128, E=8, K=2)
+    assert lib.mok_dispatch(ctypes.byref(sb), fake, fake, None, fake, fake, None, None) == m.MOK_ERR_INVALID_ARG
 
 
 def test_plan_ranks_host_checks(m):

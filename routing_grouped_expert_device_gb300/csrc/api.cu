@@ -84,7 +84,7 @@ BwdLayout bwd_layout(const mok_shape& s) {
   L.dh = c.take(R * I * 2);
   L.du = c.take(R * I * 2);
   L.ag = c.take(R * I * 2);
-  L.dgp = c.take(R * (I / 128) * 4);
+  L.dgp = c.take(R * (I / 32) * 4);
   L.dxr = c.take(R * D * 2);
   L.dhs = c.take(T * Is * 2);
   L.dus = c.take(T * Is * 2);
@@ -508,6 +508,6 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
   if ((r = launch_wgrad(dyg, ag, R, pb.offsets, s.E, s.D, s.I, dw_down, st)) != MOK_OK) return r;
   if ((r = launch_wgrad(dh, xg, R, pb.offsets, s.E, s.I, s.D, dw_gate, st)) != MOK_OK) return r;
   if ((r = launch_wgrad(du, xg, R, pb.offsets, s.E, s.I, s.D, dw_up, st)) != MOK_OK) return r;
-  return launch_router_grad(dgp, s.I / 128, pb.route_dst, pb.topk_idx, pb.g, s_in, s.T, s.E, s.K,
+  return launch_router_grad(dgp, s.I / 32, pb.route_dst, pb.topk_idx, pb.g, s_in, s.T, s.E, s.K,
                             ds, dg, st);
 }

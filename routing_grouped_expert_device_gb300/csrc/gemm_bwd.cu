@@ -1,9 +1,9 @@
 // Backward grouped GEMMs on tcgen05 / TMEM.
 //
-//  dgrad+replay : per (expert, 128 rows, 128 cols of I) one CTA accumulates
-//                 h = xg W_gate^T, u = xg W_up^T (the forward replay) and
-//                 t = dYg W_down (W_down read MN-major) in three TMEM
-//                 accumulators over K = D.  The epilogue forms, per row,
+//  dgrad+replay : per (expert, up to 160 rows, 128 cols of I) one CTA
+//                 accumulates h^T = W_gate xg^T, u^T = W_up xg^T (the
+//                 forward replay) and t^T = W_down^T dYg^T (W_down read
+//                 MN-major) in three TMEM accumulators over K = D.  The epilogue forms, per row,
 //                 a = bf16(SiLU(h) u), the router-gradient partial <t, a>
 //                 (paper note "The production details": the down-projection
 //                 output is never formed), da = g t,
@@ -31,31 +31,36 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t a) { return sdesc_sw128(a, M
 
 // ---------------------------------------------------------------------------
 struct DgradCfg {
-  // 32-wide K blocks (64-byte swizzle) keep five 40 KB stages in flight: the
-  // kernel streams three weight tensors and two activation tensors per tile,
-  // and with two 80 KB stages it waited on memory latency.
+  // Transposed products: the weights are the M operand (128 I columns of
+  // W_gate, W_up and W_down per tile) and the expert's rows the N operand
+  // (up to 160 rows, N = rows rounded up to 16), so a ragged row count costs
+  // at most 15 idle MMA columns, where 128-row tiles would run a second,
+  // mostly empty tile that streams the same weights again.  The accumulators
+  // are h^T, u^T, t^T: TMEM lane = I column, column = row.  32-wide K blocks
+  // (64-byte swizzle) keep five 44 KB stages in flight.
   static constexpr int BKD = 32;
-  static constexpr int KT = 128 * BKD * 2;   // 8 KB: 128 rows x 32 bf16, K-major
-  static constexpr int WDCHUNK = BKD * 128;  // 4 KB: 32 K rows x 64 columns, MN-major
+  static constexpr int ROWS = 160;                // rows per tile: three accumulators of 160 columns
+  static constexpr int WT = 128 * BKD * 2;        // 8 KB: 128 weight rows x 32 bf16, K-major
+  static constexpr int WDCHUNK = BKD * 128;       // 4 KB: 32 K rows x 64 I columns, MN-major
+  static constexpr int RT = ROWS * BKD * 2;       // 10 KB: 160 rows x 32 bf16, K-major
+  static constexpr int OFF_WU = WT, OFF_WD = 2 * WT, OFF_X = 2 * WT + 2 * WDCHUNK, OFF_DY = OFF_X + RT;
   static constexpr int STAGES = 5;
-  static constexpr int STAGE_BYTES = 4 * KT + 2 * WDCHUNK;  // 40 KB: x, dY, W_gate, W_up, W_down
+  static constexpr int STAGE_BYTES = OFF_DY + RT;  // 44 KB: W_gate, W_up, W_down, x, dY
   static constexpr int EPI_SMEM_BYTES = 0;
   static constexpr int NUM_ACC = 1;
-  static constexpr int ACC_COLS = 384;
+  static constexpr int ACC_COLS = 3 * ROWS;  // h^T | u^T | t^T
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t ID_HU = idesc_bf16(128, 256, false, false);  // h | u in one N = 256 MMA
-  static constexpr uint32_t ID_T = idesc_bf16(128, 128, false, true);
 
   struct Params {
-    SchedArgs sched;
+    SchedArgs sched;         // bm = ROWS
     int* status;
-    CUtensorMap tmX, tmDy;   // [rows][D], K-major boxes 128 x 32, 64-byte swizzle
+    CUtensorMap tmX, tmDy;   // [rows][D], K-major boxes 160 x 32, 64-byte swizzle
     CUtensorMap tmWg, tmWu;  // [G*I][D], K-major boxes 128 x 32, 64-byte swizzle
     CUtensorMap tmWd;        // [G*D][I], MN-major boxes 32 x 64, 128-byte swizzle
     int32_t I, D;
     const float* g_route;    // [rows] or null (weight 1)
     __nv_bfloat16 *dh, *du, *ag;  // [rows][I]
-    float* dgp;              // [rows][I/128] or null
+    float* dgp;              // [rows][I/32] or null
   };
 
   // K-major, 64-byte swizzle: 8-row groups of 64-byte rows 512 B apart.
@@ -75,75 +80,93 @@ struct DgradCfg {
                               uint64_t* bar, int lane) {
     if (lane != 0) return;
     const int k0 = kb * BKD;
-    const int r = c.row0 + c.mt * BM;
     const int wrow = c.g * P.I + c.nt * 128;
-    tma_load_2d(st, &P.tmX, k0, r, bar);
-    tma_load_2d(st + KT, &P.tmDy, k0, r, bar);
-    tma_load_2d(st + 2 * KT, &P.tmWg, k0, wrow, bar);  // W_gate then W_up: one 256-row B operand
-    tma_load_2d(st + 3 * KT, &P.tmWu, k0, wrow, bar);
+    tma_load_2d(st, &P.tmWg, k0, wrow, bar);
+    tma_load_2d(st + OFF_WU, &P.tmWu, k0, wrow, bar);
     const int drow = c.g * P.D + k0;
-    tma_load_2d(st + 4 * KT, &P.tmWd, c.nt * 128, drow, bar);
-    tma_load_2d(st + 4 * KT + WDCHUNK, &P.tmWd, c.nt * 128 + 64, drow, bar);
+    tma_load_2d(st + OFF_WD, &P.tmWd, c.nt * 128, drow, bar);
+    tma_load_2d(st + OFF_WD + WDCHUNK, &P.tmWd, c.nt * 128 + 64, drow, bar);
+    const int r = c.row0 + c.mt * ROWS;
+    tma_load_2d(st + OFF_X, &P.tmX, k0, r, bar);
+    tma_load_2d(st + OFF_DY, &P.tmDy, k0, r, bar);
   }
 
   __device__ static void fixup(const Params&, const TileCoord&, int, uint8_t*, int) {}
 
-  __device__ static void mma(const Params&, const TileCoord&, int kb, uint8_t* st, uint32_t d) {
+  // Rows past the tile's end within the N rounding belong to the next group
+  // (or are TMA zero fill): their accumulator columns are never read.
+  __device__ static int tile_rows(const TileCoord& c) {
+    const int n = c.rows - c.mt * ROWS;
+    return n < ROWS ? n : ROWS;
+  }
+
+  __device__ static void mma(const Params&, const TileCoord& c, int kb, uint8_t* st, uint32_t d) {
     const uint32_t s = smem_u32(st);
+    const int n = (tile_rows(c) + 15) & ~15;
+    const uint32_t id_hu = idesc_bf16(128, n, false, false);
+    const uint32_t id_t = idesc_bf16(128, n, true, false);
 #pragma unroll
     for (int k = 0; k < BKD / 16; ++k) {
       const uint32_t acc = (kb | k) != 0;
-      mma_bf16(d, kdesc64(s + k * 32), kdesc64(s + 2 * KT + k * 32), ID_HU, acc);
-      mma_bf16(d + 256, kdesc64(s + KT + k * 32), sdesc_sw128(s + 4 * KT + k * 2048, WDCHUNK, 1024), ID_T, acc);
+      const uint64_t bx = kdesc64(s + OFF_X + k * 32);
+      mma_bf16(d, kdesc64(s + k * 32), bx, id_hu, acc);
+      mma_bf16(d + ROWS, kdesc64(s + OFF_WU + k * 32), bx, id_hu, acc);
+      mma_bf16(d + 2 * ROWS, sdesc_sw128(s + OFF_WD + k * 2048, WDCHUNK, 1024), kdesc64(s + OFF_DY + k * 32),
+               id_t, acc);
     }
   }
 
+  // Lane l of warp w owns I column nt*128 + 32w + l; per chunk of 32 rows it
+  // loads h, u, t of those rows, forms a = bf16(SiLU(h) u), da = g t,
+  // dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)), a_g = bf16(g a) (each
+  // row's 32 columns of the warp are one 64-byte store), and the warp's
+  // partial <t, a> of each row over its 32 columns (a butterfly that leaves
+  // row 32 c + l's sum in lane l), stored at dgp[row][nt*4 + w].
   __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
                                   int lane, bool, uint8_t*) {
-    const int r = ew * 32 + lane;
-    const bool valid = c.mt * BM + r < c.rows;
-    const int64_t row = c.row0 + c.mt * BM + r;
-    const float g = (valid && P.g_route) ? P.g_route[row] : 1.0f;
-    const size_t o = static_cast<size_t>(row) * P.I + c.nt * 128;
-    float dot = 0.0f;
+    const int nrows = tile_rows(c);
+    const int64_t row0 = c.row0 + c.mt * ROWS;
+    const int icol = c.nt * 128 + ew * 32 + lane;
+    const int nI32 = P.I / 32;
 #pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
+    for (int cc = 0; cc * 32 < nrows; ++cc) {
       uint32_t hv[32], uv[32], tv[32];
-      tmem_ld32(taddr + ch * 32, hv);
-      tmem_ld32(taddr + 128 + ch * 32, uv);
-      tmem_ld32(taddr + 256 + ch * 32, tv);
+      tmem_ld32(taddr + cc * 32, hv);
+      tmem_ld32(taddr + ROWS + cc * 32, uv);
+      tmem_ld32(taddr + 2 * ROWS + cc * 32, tv);
       tmem_ld_wait();
-      uint32_t pdh[16], pdu[16], pag[16];
+      const int jr = cc * 32 + lane;
+      const float gl = (P.g_route && jr < nrows) ? P.g_route[row0 + jr] : 1.0f;
+      float dots[32];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float dhv[2], duv[2], agv[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float h = __uint_as_float(hv[2 * j + q]);
-          const float u = __uint_as_float(uv[2 * j + q]);
-          const float t = __uint_as_float(tv[2 * j + q]);
-          const float sig = sigmoid_f(h);
-          const float a = __bfloat162float(__float2bfloat16_rn((h * sig) * u));  // = bf16(silu_f(h) * u)
-          dot = __fmaf_rn(t, a, dot);
-          const float da = g * t;
-          dhv[q] = da * u * sig * (1.0f + h * (1.0f - sig));
-          duv[q] = da * h * sig;
-          agv[q] = g * a;
-        }
-        pdh[j] = pack_bf16x2(dhv[0], dhv[1]);
-        pdu[j] = pack_bf16x2(duv[0], duv[1]);
-        pag[j] = pack_bf16x2(agv[0], agv[1]);
-      }
-      if (valid) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          st_global_v4(P.dh + o + ch * 32 + q * 8, pdh[4 * q], pdh[4 * q + 1], pdh[4 * q + 2], pdh[4 * q + 3]);
-          st_global_v4(P.du + o + ch * 32 + q * 8, pdu[4 * q], pdu[4 * q + 1], pdu[4 * q + 2], pdu[4 * q + 3]);
-          st_global_v4(P.ag + o + ch * 32 + q * 8, pag[4 * q], pag[4 * q + 1], pag[4 * q + 2], pag[4 * q + 3]);
+      for (int j = 0; j < 32; ++j) {
+        const float g = __shfl_sync(0xffffffffu, gl, j);
+        const float h = __uint_as_float(hv[j]);
+        const float u = __uint_as_float(uv[j]);
+        const float t = __uint_as_float(tv[j]);
+        const float sig = sigmoid_f(h);
+        const float a = __bfloat162float(__float2bfloat16_rn((h * sig) * u));  // = bf16(silu_f(h) * u)
+        dots[j] = t * a;
+        const float da = g * t;
+        if (cc * 32 + j < nrows) {
+          const size_t o = static_cast<size_t>(row0 + cc * 32 + j) * P.I + icol;
+          P.dh[o] = __float2bfloat16_rn(da * u * sig * (1.0f + h * (1.0f - sig)));
+          P.du[o] = __float2bfloat16_rn(da * h * sig);
+          P.ag[o] = __float2bfloat16_rn(g * a);
         }
       }
+#pragma unroll
+      for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int j = 0; j < s; ++j) {
+          const float send = upper ? dots[j] : dots[j + s];
+          const float keep = upper ? dots[j + s] : dots[j];
+          dots[j] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+      }
+      if (P.dgp && jr < nrows) P.dgp[(row0 + jr) * nI32 + c.nt * 4 + ew] = dots[0];
     }
-    if (valid && P.dgp) P.dgp[row * (P.I / 128) + c.nt] = dot;
   }
 };
 
@@ -374,16 +397,17 @@ mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const
   if (rows == 0) return MOK_OK;
   DgradCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradCfg::BKD);
+  P.sched.bm = DgradCfg::ROWS;
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int groups = offsets ? G : 1;
-  auto k64 = [](CUtensorMap* m, const void* p, int64_t r, int cols) {
-    return make_tmap_2d_swz(m, p, kBF16, r, cols, static_cast<uint64_t>(cols) * 2, 128, DgradCfg::BKD,
+  auto k64 = [](CUtensorMap* m, const void* p, int64_t r, int cols, int box_rows) {
+    return make_tmap_2d_swz(m, p, kBF16, r, cols, static_cast<uint64_t>(cols) * 2, box_rows, DgradCfg::BKD,
                             CU_TENSOR_MAP_SWIZZLE_64B);
   };
-  if (!k64(&P.tmX, xg, rows, D) || !k64(&P.tmDy, dyg, rows, D) ||
-      !k64(&P.tmWg, w_gate, static_cast<int64_t>(groups) * I, D) ||
-      !k64(&P.tmWu, w_up, static_cast<int64_t>(groups) * I, D) ||
+  if (!k64(&P.tmX, xg, rows, D, DgradCfg::ROWS) || !k64(&P.tmDy, dyg, rows, D, DgradCfg::ROWS) ||
+      !k64(&P.tmWg, w_gate, static_cast<int64_t>(groups) * I, D, 128) ||
+      !k64(&P.tmWu, w_up, static_cast<int64_t>(groups) * I, D, 128) ||
       !make_tmap_2d(&P.tmWd, w_down, kBF16, static_cast<int64_t>(groups) * D, I, static_cast<uint64_t>(I) * 2,
                     DgradCfg::BKD, 64, true))
     return MOK_ERR_CUDA;

@@ -94,7 +94,8 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
                             const SharedOperands* sh = nullptr);
 
 // Backward.  dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
-// non-null, dgp [rows][I/128] partial <t, a>; g_route null = weight 1.
+// non-null, dgp [rows][I/32] partials of <t, a> (32 I columns each);
+// g_route null = weight 1.
 mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
                             const void* w_up, const void* w_down, const int32_t* offsets, int G,
                             int D, int I, const float* g_route, void* dh, void* du, void* ag,

@@ -244,11 +244,13 @@ struct DxCfg {
 template <int BN>
 struct WgradCfg {
   static constexpr int NB = BN / 64;  // 64-wide MN chunks of B
-  static constexpr int STAGES = 3;  // K loops are short (rows per expert / 64)
+  // Four stages (two tiles of a ~128-row expert) ahead of the MMAs: with
+  // three the MMA warp waited on loads.
+  static constexpr int STAGES = 4;
   static constexpr int STAGE_BYTES = (2 + NB) * MNCHUNK;
-  // per epilogue warp: two staging blocks of 32 rows x 64 columns of bf16,
-  // 128-byte swizzled, each the source of one TMA store
-  static constexpr int EPI_SMEM_BYTES = 4 * 2 * 32 * 128;
+  // per epilogue warp: one staging block of 32 rows x 64 columns of bf16,
+  // 128-byte swizzled, the source of one TMA store
+  static constexpr int EPI_SMEM_BYTES = 4 * 32 * 128;
   static constexpr int NUM_ACC = 2;
   static constexpr int ACC_COLS = BN;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -333,11 +335,10 @@ struct WgradCfg {
 #pragma unroll
         for (int j = 0; j < 32; ++j) pk[j] = 0u;
       }
-      // the store that last used this staging block (two stores back) has
-      // finished reading it
-      if (lane == 0) bulk_wait_read1();
+      // the previous store has finished reading the staging block
+      if (lane == 0) bulk_wait_read0();
       __syncwarp();
-      uint8_t* blk = epi + (cp & 1) * 4096;
+      uint8_t* blk = epi;
       uint8_t* row = blk + lane * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {

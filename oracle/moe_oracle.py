@@ -54,6 +54,7 @@ __all__ = [
     "route_backward_rows", "moe_backward", "router_grad", "router_grad_slack",
     "e4m3_code_values", "e4m3_encode", "mx_scale_exponent", "mxfp8_quantize",
     "mxfp8_dequantize", "expert_ffn_rows_mxfp8", "moe_forward_mxfp8",
+    "mxfp8_roundtrip", "route_backward_rows_mxfp8", "moe_backward_mxfp8",
 ]
 
 
@@ -447,7 +448,8 @@ def router_grad(dg, g, den, topk_idx, E, num: Numerics = FP32):
 
 def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
                  fwd: Optional[Dict[str, np.ndarray]] = None,
-                 with_slack: bool = False) -> Dict[str, np.ndarray]:
+                 with_slack: bool = False,
+                 routed_rows: Optional[Callable] = None) -> Dict[str, np.ndarray]:
     """Gradients of L = <dY, MoE(x, s)> w.r.t. x, every weight and s.
 
     Routing is recomputed (or taken from ``fwd``); gradients do not flow
@@ -461,7 +463,11 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
     gradient element the sum over rows of |other operand| times the
     bf16_flip_ulp of the rounded factor (dh, du or a_g): how far another
     correct evaluation, which may round those ambiguous factors the other
-    way, can land from this one."""
+    way, can land from this one.
+
+    routed_rows: the per-expert backward of the routed experts (default
+    route_backward_rows; moe_backward_mxfp8 passes the MXFP8 one), called
+    as routed_rows(x_rows, dy_rows, g_rows, W_gate[e], W_up[e], W_down[e])."""
     if fwd is None:
         s = inp["s"]
         topk_idx, g, den = route(s, K, num)
@@ -493,8 +499,11 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
         if p0 == p1:
             continue
         rows = src_tok[p0:p1]
-        b = route_backward_rows(x[rows], dY[rows], g_route[p0:p1],
-                                inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], num)
+        if routed_rows is None:
+            b = route_backward_rows(x[rows], dY[rows], g_route[p0:p1],
+                                    inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], num)
+        else:
+            b = routed_rows(x[rows], dY[rows], g_route[p0:p1], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
         dx_r[p0:p1] = b["dx"]
         dg_route[p0:p1] = b["dg"]
         dW_down[e] = num.rnd(dY[rows].T @ b["a_g"])
@@ -684,3 +693,62 @@ def moe_forward_mxfp8(inp: Dict[str, np.ndarray], K: int, quant: Optional[Dict[s
     out = combine(y, ys, g, route_dst, num)
     return dict(topk_idx=topk_idx, g=g, counts=counts, offsets=offsets, table=table, route_dst=route_dst,
                 xq=xq, xs=xs, a=a, aq=aq, asc=asc, y=y, ys=ys, out=out)
+
+
+def mxfp8_roundtrip(v) -> np.ndarray:
+    """Quantise along the last axis and dequantise exactly, as float32: the
+    values a block-scaled GEMM contracts."""
+    return mxfp8_dequantize(*mxfp8_quantize(np.asarray(v, dtype=np.float64))).astype(np.float32)
+
+
+def route_backward_rows_mxfp8(xrows, dyrows, g, Wg, Wu, Wd, deq: Optional[Callable] = None):
+    """Backward of g * E_i(x) for rows of one expert with MXFP8 routed GEMMs
+    ([note] "The production details": MXFP8 with quantisation fused into the
+    dispatch, the grouped GEMMs and the gated activation; the router gradient
+    as the inner product of the gated activation with the down-projection
+    input gradient).  Each GEMM contracts operands quantised along its own
+    reduction dim, exactly dequantised, in fp32:
+      replay  h = X W_gate^T, u = X W_up^T : x, W_gate, W_up along D (the
+              forward's quantisation); h and u are kept as bf16;
+      t = dY W_down                        : dY along D, W_down^T along D;
+              t is kept as bf16;
+      dx = [dh | du] [W_gate ; W_up]       : [dh | du] along 2I,
+              [W_gate^T | W_up^T] along 2I; dx = bf16.
+    The activation gradient is the BF16 backward's, on the bf16 h, u, t:
+      a = bf16(SiLU(h) u), dg = <t, a>, da = g t,
+      dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)), a_g = bf16(g a).
+    ``deq`` is the quantise-dequantise step along the last axis (default
+    mxfp8_roundtrip); the identity turns the quantisation off.  Inputs are
+    bf16 bits or float values.  Returns dict(h, u, a, t, dg, dh, du, a_g, dx)."""
+    deq = mxfp8_roundtrip if deq is None else deq
+    X = deq(FP32.w(xrows))
+    dY = deq(FP32.w(dyrows))
+    gcol = np.asarray(g, dtype=np.float32).reshape(-1, 1)
+    Wg_, Wu_, Wd_ = FP32.w(Wg), FP32.w(Wu), FP32.w(Wd)
+    h = round_bf16(X @ deq(Wg_).T)
+    u = round_bf16(X @ deq(Wu_).T)
+    t = round_bf16(dY @ deq(np.ascontiguousarray(Wd_.T)).T)
+    a = round_bf16(silu(h) * u)
+    dg = np.sum(t * a, axis=1, dtype=np.float32)
+    da = gcol * t
+    one = np.float32(1)
+    with np.errstate(over="ignore"):
+        sig = one / (one + np.exp(-h))
+    dh = round_bf16(da * u * sig * (one + h * (one - sig)))
+    du = round_bf16(da * h * sig)
+    a_g = round_bf16(gcol * a)
+    dhu = deq(np.concatenate([dh, du], axis=1))
+    wgu_t = deq(np.concatenate([Wg_.T, Wu_.T], axis=1))  # [D][2I]
+    dx = round_bf16(dhu @ wgu_t.T)
+    return dict(h=h, u=u, a=a, t=t, dg=dg, dh=dh, du=du, a_g=a_g, dx=dx)
+
+
+def moe_backward_mxfp8(inp: Dict[str, np.ndarray], dy, K: int,
+                       fwd: Optional[Dict[str, np.ndarray]] = None,
+                       deq: Optional[Callable] = None) -> Dict[str, np.ndarray]:
+    """The backward with the routed experts' GEMMs in MXFP8
+    (route_backward_rows_mxfp8); the weight gradients are BF16 products of
+    the bf16 x, dY and the MXFP8 path's bf16 dh, du, a_g, as in moe_backward;
+    the shared expert is BF16 ([note] "The production details")."""
+    return moe_backward(inp, dy, K, FP32, fwd=fwd,
+                        routed_rows=lambda *a: route_backward_rows_mxfp8(*a, deq=deq))

@@ -242,6 +242,14 @@ def run_ours(args, world, rank, local):
             sc = torch.empty(M.mx_scale_words(*wt.shape), dtype=i32, device=dev)
             M.quantize_mxfp8(wt, q, sc)
             d["q_" + name], d["sc_" + name] = q, sc
+        if cfg.backward:
+            # the backward's copies: W_down^T along D, [W_gate^T | W_up^T] along 2I
+            d["qt_down"] = torch.empty(E * I, D, dtype=u8, device=dev)
+            d["sct_down"] = torch.empty(M.mx_scale_words(E * I, D), dtype=i32, device=dev)
+            d["qt_gu"] = torch.empty(E * D, 2 * I, dtype=u8, device=dev)
+            d["sct_gu"] = torch.empty(M.mx_scale_words(E * D, 2 * I), dtype=i32, device=dev)
+            M.quantize_mxfp8_bwd_weights(shape, M.make_weights(d), d["qt_down"], d["sct_down"], d["qt_gu"],
+                                         d["sct_gu"])
         torch.cuda.synchronize()
     w = M.make_weights(d)
     topk = torch.empty(T, K, dtype=i32, device=dev)
@@ -278,7 +286,13 @@ def run_ours(args, world, rank, local):
                   dws_up=torch.empty(Is, D, dtype=bf, device=dev) if Is else None,
                   dws_down=torch.empty(D, Is, dtype=bf, device=dev) if Is else None,
                   ds=torch.empty(T, E, dtype=f32, device=dev), dg=torch.empty(T, K, dtype=f32, device=dev))
-        launches_per_step = (1 + 3 + 1 + 2 + 1) + (2 + 2 + 1 + 3 + 1 + (5 if Is else 0))
+        # forward: route, plan (3), dispatch, up/gate, down, combine, the
+        # shared expert's up/gate (BF16) or FFN (MXFP8); backward: gathers
+        # (2), dgrad + dx (BF16) or 2 quantising dispatches, replay, t,
+        # activation gradient, dX (MXFP8), reverse combine, 3 wgrad, router
+        # grad, and the shared expert's dgrad, dx and 3 wgrad
+        launches_per_step = ((1 + 3 + 1 + 2 + 1 + ((2 if mx else 1) if Is else 0))
+                             + (2 + (6 if mx else 2) + 1 + 3 + 1 + (5 if Is else 0)))
 
     def step(ev0=None, ev1=None):
         if cfg.backward:
@@ -358,9 +372,11 @@ def run_ours(args, world, rank, local):
     wbytes = 1 if mx else 2  # bytes per weight / activation element on the routed path
 
     if cfg.backward:
-        # the whole backward call (8 + 5 launches): ideal bytes = every weight
-        # read once + every weight gradient written once + x, dY, dX
-        alg_bytes = 2 * (nonempty * 3 * I * D + 3 * Is * D) * 2 + 3 * T * D * 2
+        # the whole backward call: ideal bytes = every weight read once (the
+        # routed ones as fp8 codes + scales for MXFP8) + every weight
+        # gradient written once (bf16) + x, dY, dX
+        wread = nonempty * 3 * I * D * (wbytes + (1 / 32 if mx else 0.0)) + 3 * Is * D * 2
+        alg_bytes = int(wread + (nonempty * 3 * I * D + 3 * Is * D) * 2 + 3 * T * D * 2)
         kernel = "backward (mok_moe_bwd: gathers, dgrad+replay, dx, combine, wgrad, router grad)"
         part_tflops = cfg.bwd_flops() / (part_ms / 1e3) / 1e12
     else:

@@ -107,12 +107,21 @@ typedef struct {
  * [E*I][D], [E*I][D], [E*D][I] tensors quantised along the last dim) and
  * sc_* their scale words (mok_quantize_mxfp8 writes both).  Shared expert,
  * always BF16: ws_gate, ws_up [I_shared][D]; ws_down [D][I_shared] (NULL
- * when I_shared = 0). */
+ * when I_shared = 0).  MXFP8 backward (mok_moe_bwd with dtype MOK_MXFP8;
+ * may be NULL otherwise), written by mok_quantize_mxfp8_bwd_weights:
+ * qt_down the codes of W_down^T [E][I][D] (as [E*I][D] quantised along D)
+ * and sct_down its scale words (plain layout); qt_gu the codes of
+ * [W_gate^T | W_up^T] [E][D][2I] (as [E*D][2I] quantised along 2I) and
+ * sct_gu its scale words. */
 typedef struct {
   const void *w_gate, *w_up, *w_down;
   const void *q_gate, *q_up, *q_down;
   const uint8_t *sc_gate, *sc_up, *sc_down;
   const void *ws_gate, *ws_up, *ws_down;
+  const void *qt_down;
+  const uint8_t *sct_down;
+  const void *qt_gu;
+  const uint8_t *sct_gu;
 } mok_weights;
 
 /* Routing and plan state saved by the forward for the backward.
@@ -284,14 +293,21 @@ mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void 
                        const float *s, void *out, mok_plan_buf *saved, void *ws,
                        size_t ws_bytes, void *stream);
 
-/* Backward of L = <dy, MoE(x, s)> (BF16).  saved: the forward's routing and
+/* Backward of L = <dy, MoE(x, s)>.  saved: the forward's routing and
  * plan.  dy bf16 [T][D].  Writes dx bf16 [T][D]; dw_gate, dw_up bf16
  * [E][I][D]; dw_down bf16 [E][D][I]; dws_* the shared expert's (ignored
  * when I_shared = 0); ds fp32 [T][E] (zero outside the top-k);
  * dg fp32 [T][K] (nullable) = <t, a> per route with t = W_down^T dy (paper
  * note, "The production details": the router-gradient inner product; the
  * down-projection output is not formed).  h and u are recomputed.  Weight
- * gradients of experts with no routes are written as zeros. */
+ * gradients of experts with no routes are written as zeros.
+ * With shape.dtype = MOK_MXFP8 the routed experts' replay (h, u), t and dX
+ * products run in MXFP8, each operand quantised along that product's
+ * reduction dim (x, dY per row along D; w's q_gate, q_up, qt_down; the
+ * activation gradient quantises [dh | du] along 2I for qt_gu); h, u and t
+ * are kept as bf16 between the products and the activation gradient.  The
+ * weight gradients are BF16 products (of bf16 x, dY, dh, du, g a) and the
+ * shared expert is BF16. */
 mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void *x,
                        const float *s, const mok_plan_buf *saved, const void *dy, void *dx,
                        void *dw_gate, void *dw_up, void *dw_down, void *dws_gate,
@@ -303,6 +319,15 @@ mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void 
  * MXFP8 layout above).  0 for invalid sizes (cols not a positive multiple
  * of 128, negative rows or groups).  Host-only. */
 size_t mok_mxfp8_scale_bytes(int64_t rows, int64_t cols, int32_t groups);
+
+/* The MXFP8 weight copies of the backward, from the bf16 w_gate, w_up,
+ * w_down of `w`: qt_down = codes of W_down^T [E][I][D] quantised along D
+ * (E*I*D bytes) with sct_down (mok_mxfp8_scale_bytes(E*I, D, 0) bytes);
+ * qt_gu = codes of [W_gate^T | W_up^T] [E][D][2I] quantised along 2I
+ * (E*D*2I bytes) with sct_gu (mok_mxfp8_scale_bytes(E*D, 2I, 0) bytes).
+ * Same rounding as mok_quantize_mxfp8.  D and I multiples of 128. */
+mok_status mok_quantize_mxfp8_bwd_weights(const mok_shape *shape, const mok_weights *w, void *qt_down,
+                                          uint8_t *sct_down, void *qt_gu, uint8_t *sct_gu, void *stream);
 
 /* MXFP8 quantiser: src bf16 [rows][cols] (cols % 128 == 0) -> q E4M3 codes
  * [rows][cols] and scale words in the plain layout (see the MXFP8 layout

@@ -71,7 +71,11 @@ FwdLayout fwd_layout(const mok_shape& s) {
 }
 
 struct BwdLayout {
-  size_t xg, dyg, g_route, dh, du, ag, dgp, dxr, dhs, dus, ags, dxs, total;
+  size_t xg, dyg, g_route, dh, du, ag, dgp, dxr, dhs, dus, ags, dxs;
+  // MXFP8: x, dY codes and grouped scales; replay h, u and t (bf16); the
+  // codes and grouped scales of [dh | du]
+  size_t xq, xq_sc, dyq, dyq_sc, hh, uu, tt, dhu_q, dhu_sc;
+  size_t total;
 };
 
 BwdLayout bwd_layout(const mok_shape& s) {
@@ -90,8 +94,23 @@ BwdLayout bwd_layout(const mok_shape& s) {
   L.dus = c.take(T * Is * 2);
   L.ags = c.take(T * Is * 2);
   L.dxs = c.take(Is ? T * D * 2 : 0);
+  const bool mx = s.dtype == MOK_MXFP8;
+  L.xq = c.take(mx ? R * D : 0);
+  L.xq_sc = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
+  L.dyq = c.take(mx ? R * D : 0);
+  L.dyq_sc = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
+  L.hh = c.take(mx ? R * I * 2 : 0);
+  L.uu = c.take(mx ? R * I * 2 : 0);
+  L.tt = c.take(mx ? R * I * 2 : 0);
+  L.dhu_q = c.take(mx ? R * 2 * I : 0);
+  L.dhu_sc = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), 2 * I, s.E) : 0);
   L.total = c.off;
   return L;
+}
+
+bool mx_bwd_weights_ok(const mok_weights* w) {
+  return w->qt_down && w->sct_down && w->qt_gu && w->sct_gu && aligned16(w->qt_down) && aligned16(w->sct_down) &&
+         aligned16(w->qt_gu) && aligned16(w->sct_gu);
 }
 
 bool mx_weights_ok(const mok_weights* w) {
@@ -444,6 +463,24 @@ extern "C" mok_status mok_quantize_mxfp8(const void* src, int64_t rows, int64_t 
   return launch_quantize_mxfp8(src, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" mok_status mok_quantize_mxfp8_bwd_weights(const mok_shape* shape, const mok_weights* w, void* qt_down,
+                                                     uint8_t* sct_down, void* qt_gu, uint8_t* sct_gu, void* stream) {
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (s.D % 128 || s.I % 128) return MOK_ERR_INVALID_ARG;
+  if (!w->w_gate || !w->w_up || !w->w_down || !qt_down || !sct_down || !qt_gu || !sct_gu ||
+      !aligned16(w->w_gate) || !aligned16(w->w_up) || !aligned16(w->w_down) || !aligned16(qt_down) ||
+      !aligned16(sct_down) || !aligned16(qt_gu) || !aligned16(sct_gu))
+    return MOK_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mok_status r;
+  // W_down [E][D][I]: output rows (e, i), D values each
+  if ((r = launch_quantize_cols_mxfp8(w->w_down, s.E, s.D, s.I, qt_down, sct_down, s.D, 0, st)) != MOK_OK) return r;
+  // W_gate, W_up [E][I][D]: output rows (e, d), I values each, side by side
+  if ((r = launch_quantize_cols_mxfp8(w->w_gate, s.E, s.I, s.D, qt_gu, sct_gu, 2 * s.I, 0, st)) != MOK_OK) return r;
+  return launch_quantize_cols_mxfp8(w->w_up, s.E, s.I, s.D, qt_gu, sct_gu, 2 * s.I, s.I, st);
+}
+
 extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, const void* x,
                                   const float* s_in, const mok_plan_buf* saved, const void* dy,
                                   void* dx, void* dw_gate, void* dw_up, void* dw_down,
@@ -451,7 +488,9 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
                                   float* dg, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(shape) || !w || !saved) return MOK_ERR_INVALID_ARG;
   const mok_shape& s = *shape;
-  if (s.dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+  const bool mx = s.dtype == MOK_MXFP8;
+  if (mx && (!mx_weights_ok(w) || !mx_bwd_weights_ok(w))) return MOK_ERR_INVALID_ARG;
+  if (mx && (s.I % 256 || s.D % 256)) return MOK_ERR_UNSUPPORTED;  // 256-column tiles of t and dX
   if (s.T == 0) return MOK_OK;
   const mok_plan_buf& pb = *saved;
   if (!x || !s_in || !dy || !dx || !dw_gate || !dw_up || !dw_down || !ds || !pb.topk_idx ||
@@ -480,12 +519,44 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
   if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, pb.g, g_route, st)) != MOK_OK) return r;
   if ((r = launch_dispatch_bf16(dy, pb.route_dst, s.T, s.K, s.D, dyg, nullptr, nullptr, st)) != MOK_OK)
     return r;
-  // replay h, u; t = dY W_down; dh, du, g*a, <t, a> partials
-  if ((r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,
-                            g_route, dh, du, ag, dgp, st)) != MOK_OK)
-    return r;
-  if ((r = launch_bwd_dx(dh, du, R, w->w_gate, w->w_up, pb.offsets, s.E, s.D, s.I, dxr, st)) != MOK_OK)
-    return r;
+  if (mx) {
+    // MXFP8: quantising dispatches of x and dY; replay h, u; t = dY W_down
+    // (W_down^T quantised along D); the activation gradient with [dh | du]
+    // quantised along 2I; dX routes = [dh | du] [W_gate ; W_up]
+    void* xq = at<void>(ws, L.xq);
+    uint8_t* xq_sc = at<uint8_t>(ws, L.xq_sc);
+    void* dyq = at<void>(ws, L.dyq);
+    uint8_t* dyq_sc = at<uint8_t>(ws, L.dyq_sc);
+    void* hh = at<void>(ws, L.hh);
+    void* uu = at<void>(ws, L.uu);
+    void* tt = at<void>(ws, L.tt);
+    void* dhu_q = at<void>(ws, L.dhu_q);
+    uint8_t* dhu_sc = at<uint8_t>(ws, L.dhu_sc);
+    if ((r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xq, xq_sc, st)) !=
+        MOK_OK)
+      return r;
+    if ((r = launch_dispatch_mxfp8(dy, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, dyq, dyq_sc, st)) !=
+        MOK_OK)
+      return r;
+    if ((r = launch_replay_mx(xq, xq_sc, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, pb.offsets, s.E, s.D, s.I,
+                              hh, uu, st)) != MOK_OK)
+      return r;
+    if ((r = launch_down_mx(dyq, dyq_sc, R, w->qt_down, w->sct_down, pb.offsets, s.E, s.I, s.D, tt, st)) != MOK_OK)
+      return r;
+    if ((r = launch_act_grad_mx(hh, uu, tt, g_route, pb.table, pb.offsets, R, s.I, s.E, dh, du, ag, dhu_q, dhu_sc,
+                                dgp, st)) != MOK_OK)
+      return r;
+    if ((r = launch_down_mx(dhu_q, dhu_sc, R, w->qt_gu, w->sct_gu, pb.offsets, s.E, s.D, 2 * s.I, dxr, st)) !=
+        MOK_OK)
+      return r;
+  } else {
+    // replay h, u; t = dY W_down; dh, du, g*a, <t, a> partials
+    if ((r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,
+                              g_route, dh, du, ag, dgp, st)) != MOK_OK)
+      return r;
+    if ((r = launch_bwd_dx(dh, du, R, w->w_gate, w->w_up, pb.offsets, s.E, s.D, s.I, dxr, st)) != MOK_OK)
+      return r;
+  }
   void* dxs = nullptr;
   if (s.I_shared) {
     void* dhs = at<void>(ws, L.dhs);
@@ -508,6 +579,6 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
   if ((r = launch_wgrad(dyg, ag, R, pb.offsets, s.E, s.D, s.I, dw_down, st)) != MOK_OK) return r;
   if ((r = launch_wgrad(dh, xg, R, pb.offsets, s.E, s.I, s.D, dw_gate, st)) != MOK_OK) return r;
   if ((r = launch_wgrad(du, xg, R, pb.offsets, s.E, s.I, s.D, dw_up, st)) != MOK_OK) return r;
-  return launch_router_grad(dgp, s.I / 32, pb.route_dst, pb.topk_idx, pb.g, s_in, s.T, s.E, s.K,
+  return launch_router_grad(dgp, mx ? 1 : s.I / 32, pb.route_dst, pb.topk_idx, pb.g, s_in, s.T, s.E, s.K,
                             ds, dg, st);
 }

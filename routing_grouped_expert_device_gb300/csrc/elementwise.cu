@@ -68,6 +68,38 @@ __device__ __forceinline__ int mx_exponent(float amax) {
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 
+// E4M3 codes of 8 values held by one lane when 4 consecutive lanes hold one
+// 32-value block: the block's amax by two xor shuffles (warp-wide call),
+// scale 2^e with e = mx_exponent(amax), codes packed little-endian.
+__device__ __forceinline__ uint2 mx_codes8(const float (&f)[8], int& e) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  e = mx_exponent(amax);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+  uint32_t packed[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * j] * inv, f[4 * j + 1] * inv),
+                                                             __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(f[4 * j + 2] * inv, f[4 * j + 3] * inv),
+                                                             __NV_SATFINITE, __NV_E4M3);
+    packed[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return make_uint2(packed[0], packed[1]);
+}
+
+// The scale word of the 128 columns held by lanes 16h .. 16h + 15 (8 values
+// each): byte b from lane 16h + 4b (warp-wide call).
+__device__ __forceinline__ uint32_t mx_word16(int e, int lane) {
+  const uint32_t byte = static_cast<uint32_t>(e + 127);
+  const int base = lane & 16;
+  return __shfl_sync(0xffffffffu, byte, base) | (__shfl_sync(0xffffffffu, byte, base + 4) << 8) |
+         (__shfl_sync(0xffffffffu, byte, base + 8) << 16) | (__shfl_sync(0xffffffffu, byte, base + 12) << 24);
+}
+
 // One warp per row: lane l holds 8 consecutive values (16 bytes), so a
 // 1x32 block is 4 lanes (its amax: two xor shuffles) and one pass of the warp
 // covers 256 columns, two 128-column scale groups; loads and code stores are
@@ -121,39 +153,148 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
           f[2 * j] = bf16lo(w[j]);
           f[2 * j + 1] = bf16hi(w[j]);
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int e = mx_exponent(amax);
-        const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
-        uint32_t packed[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-              make_float2(f[4 * j] * inv, f[4 * j + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-              make_float2(f[4 * j + 2] * inv, f[4 * j + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-          packed[j] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-        }
-        // scale word of the 128-column group of lanes 16h .. 16h + 15: byte b
-        // from lane 16h + 4b
-        const uint32_t byte = static_cast<uint32_t>(e + 127);
-        const int base = lane & 16;
-        const uint32_t word = __shfl_sync(0xffffffffu, byte, base) |
-                              (__shfl_sync(0xffffffffu, byte, base + 4) << 8) |
-                              (__shfl_sync(0xffffffffu, byte, base + 8) << 16) |
-                              (__shfl_sync(0xffffffffu, byte, base + 12) << 24);
+        int e;
+        const uint2 codes = mx_codes8(f, e);
+        const uint32_t word = mx_word16(e, lane);
 #pragma unroll 1
         for (int k = 0; k < ndst; ++k) {
           const int64_t p = __shfl_sync(0xffffffffu, dst, k);
           const int64_t pos = __shfl_sync(0xffffffffu, dpos, k);
-          if (vi < c8) q[p * c8 + vi] = make_uint2(packed[0], packed[1]);
+          if (vi < c8) q[p * c8 + vi] = codes;
           if ((lane & 15) == 0 && vi < c8) scale[static_cast<int64_t>(vi / 16) * ld + pos] = word;
         }
       }
     }
+  }
+}
+
+// Activation gradient of the MXFP8 backward (paper note, "The production
+// details": MXFP8 with quantisation fused into the gated activation; the
+// router-gradient inner product).  One warp per routed row p, 8 columns per
+// lane: from the bf16 replay h, u and t = dY W_down it forms
+// a = bf16(SiLU(h) u), da = g t, dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)),
+// a_g = bf16(g a) (bf16 [R][I], for the weight gradients), the E4M3 codes of
+// [dh | du] [R][2I] with their scale words in the grouped layout of expert
+// table[p].e (for dX), and dgp[p] = <t, a> (per-lane sums in column order,
+// then a fixed butterfly over the lanes).  g_route null: weight 1.
+__global__ void __launch_bounds__(256) act_grad_mx_kernel(
+    const uint4* __restrict__ h, const uint4* __restrict__ u, const uint4* __restrict__ t,
+    const float* __restrict__ g_route, const int32_t* __restrict__ table, const int32_t* __restrict__ offsets,
+    int64_t R, int I, int64_t ld, uint4* __restrict__ dh, uint4* __restrict__ du, uint4* __restrict__ ag,
+    uint2* __restrict__ dhu_q, uint32_t* __restrict__ dhu_sc, float* __restrict__ dgp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int I8 = I / 8;
+  for (int64_t p = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; p < R; p += nwarps) {
+    const int e = __ldg(table + p * 3 + 1);
+    const int64_t off = __ldg(offsets + e);
+    const int64_t pos = mx_scale_pos(mx_group_row0(off, e) + (p - off));
+    const float g = g_route ? g_route[p] : 1.0f;
+    float dot = 0.0f;
+#pragma unroll 1
+    for (int v0 = 0; v0 < I8; v0 += 32) {
+      const int vi = v0 + lane;
+      const bool in = vi < I8;  // warp-uniform per 16 lanes: I is a multiple of 128
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      const uint4 hv = in ? h[p * I8 + vi] : z, uv = in ? u[p * I8 + vi] : z, tv = in ? t[p * I8 + vi] : z;
+      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w},
+                     tw[4] = {tv.x, tv.y, tv.z, tv.w};
+      float dhf[8], duf[8];
+      uint32_t pdh[4], pdu[4], pag[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float agv[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float hf = q ? bf16hi(hw[j]) : bf16lo(hw[j]);
+          const float uf = q ? bf16hi(uw[j]) : bf16lo(uw[j]);
+          const float tf = q ? bf16hi(tw[j]) : bf16lo(tw[j]);
+          const float sig = sigmoid_f(hf);
+          const float a = __bfloat162float(__float2bfloat16_rn((hf * sig) * uf));  // = bf16(silu_f(h) * u)
+          dot = __fmaf_rn(tf, a, dot);
+          const float da = g * tf;
+          dhf[2 * j + q] = __bfloat162float(__float2bfloat16_rn(da * uf * sig * (1.0f + hf * (1.0f - sig))));
+          duf[2 * j + q] = __bfloat162float(__float2bfloat16_rn(da * hf * sig));
+          agv[q] = g * a;
+        }
+        pdh[j] = pack_bf16x2(dhf[2 * j], dhf[2 * j + 1]);
+        pdu[j] = pack_bf16x2(duf[2 * j], duf[2 * j + 1]);
+        pag[j] = pack_bf16x2(agv[0], agv[1]);
+      }
+      if (in) {
+        dh[p * I8 + vi] = make_uint4(pdh[0], pdh[1], pdh[2], pdh[3]);
+        du[p * I8 + vi] = make_uint4(pdu[0], pdu[1], pdu[2], pdu[3]);
+        ag[p * I8 + vi] = make_uint4(pag[0], pag[1], pag[2], pag[3]);
+      }
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        int ex;
+        const uint2 codes = mx_codes8(part ? duf : dhf, ex);
+        const uint32_t word = mx_word16(ex, lane);
+        const int col8 = part * I8 + vi;  // 8-column unit within [dh | du]
+        if (in) dhu_q[p * (2 * I8) + col8] = codes;
+        if (in && (lane & 15) == 0) dhu_sc[static_cast<int64_t>(col8 / 16) * ld + pos] = word;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if (lane == 0) dgp[p] = dot;
+  }
+}
+
+// MXFP8 codes of transposed weights: output row (g, n) holds the M values
+// src[g][m][n] (src bf16 [G][M][N]), quantised along m in 1x32 blocks:
+// codes at q[(g N + n) * out_cols + col0 + m], scale words in the plain
+// layout of G*N rows and out_cols columns.  A CTA moves a 128 (m) x 64 (n)
+// tile through shared memory; each warp then quantises 8 output rows, lane
+// l holding m = 4l .. 4l + 3 (a 32-block is 8 lanes, one scale word per row).
+__global__ void __launch_bounds__(256) quant_cols_kernel(const uint4* __restrict__ src, int M, int N,
+                                                         uint32_t* __restrict__ q, uint32_t* __restrict__ scale,
+                                                         int out_cols, int col0, int64_t ld) {
+  __shared__ uint16_t tile[128][66];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t gn0 = static_cast<int64_t>(blockIdx.x) * 64;  // first output row (g N + n0)
+  const int64_t g = gn0 / N;
+  const int n0 = static_cast<int>(gn0 - g * N);
+  const int m0 = blockIdx.y * 128;
+  const int N8 = N / 8;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = threadIdx.x / 8 + 32 * i, seg = threadIdx.x % 8;
+    const uint4 v = src[(g * M + m0 + row) * N8 + n0 / 8 + seg];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      tile[row][seg * 8 + 2 * j] = static_cast<uint16_t>(w[j] & 0xFFFFu);
+      tile[row][seg * 8 + 2 * j + 1] = static_cast<uint16_t>(w[j] >> 16);
+    }
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int r = 0; r < 8; ++r) {
+    const int n = warp * 8 + r;
+    float f[4];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[i] = __uint_as_float(static_cast<uint32_t>(tile[4 * lane + i][n]) << 16);
+      amax = fmaxf(amax, fabsf(f[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const int e = mx_exponent(amax);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+    const __nv_fp8x2_storage_t lo =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[0] * inv, f[1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi =
+        __nv_cvt_float2_to_fp8x2(make_float2(f[2] * inv, f[3] * inv), __NV_SATFINITE, __NV_E4M3);
+    const int64_t orow = gn0 + n;
+    q[(orow * out_cols + col0 + m0) / 4 + lane] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    const uint32_t byte = static_cast<uint32_t>(e + 127);
+    const uint32_t word = __shfl_sync(0xffffffffu, byte, 0) | (__shfl_sync(0xffffffffu, byte, 8) << 8) |
+                          (__shfl_sync(0xffffffffu, byte, 16) << 16) | (__shfl_sync(0xffffffffu, byte, 24) << 24);
+    if (lane == 0) scale[static_cast<int64_t>((col0 + m0) / 128) * ld + mx_scale_pos(orow)] = word;
   }
 }
 
@@ -281,6 +422,31 @@ mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, vo
   quant_rows_kernel<<<grid_for(rows, 8), 256, 0, st>>>(static_cast<const uint4*>(src), nullptr, nullptr, nullptr, 1,
                                                        rows, cols, mx_scale_ld(rows), static_cast<uint2*>(q),
                                                        reinterpret_cast<uint32_t*>(scale));
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_act_grad_mx(const void* h, const void* u, const void* t, const float* g_route,
+                              const int32_t* table, const int32_t* offsets, int64_t R, int I, int E, void* dh,
+                              void* du, void* ag, void* dhu_q, uint8_t* dhu_sc, float* dgp, cudaStream_t st) {
+  if (R == 0) return MOK_OK;
+  if (I % 128) return MOK_ERR_UNSUPPORTED;
+  act_grad_mx_kernel<<<grid_for(R, 8), 256, 0, st>>>(
+      static_cast<const uint4*>(h), static_cast<const uint4*>(u), static_cast<const uint4*>(t), g_route, table,
+      offsets, R, I, mx_scale_ld(R, E), static_cast<uint4*>(dh), static_cast<uint4*>(du), static_cast<uint4*>(ag),
+      static_cast<uint2*>(dhu_q), reinterpret_cast<uint32_t*>(dhu_sc), dgp);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_quantize_cols_mxfp8(const void* src, int G, int M, int N, void* q, uint8_t* scale, int out_cols,
+                                      int col0, cudaStream_t st) {
+  if (G == 0) return MOK_OK;
+  if (M % 128 || N % 64 || col0 % 128 || out_cols % 128 || col0 + M > out_cols) return MOK_ERR_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(G) * N / 64), static_cast<unsigned>(M / 128));
+  quant_cols_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), M, N, static_cast<uint32_t*>(q),
+                                          reinterpret_cast<uint32_t*>(scale), out_cols, col0,
+                                          mx_scale_ld(static_cast<int64_t>(G) * N));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

@@ -28,6 +28,7 @@
 // up/gate : the epilogue forms a = bf16(SiLU(h) u) and quantises it to E4M3
 //           per 32 columns (one TMEM load of 32 columns is one block),
 //           writing a's scale words in the grouped layout.
+// replay  : the up/gate products of the backward, h and u written as bf16.
 // down    : y = bf16(acc).
 #include <cuda_fp8.h>
 
@@ -90,10 +91,12 @@ struct MxParams {
   uint32_t* asc;  // up/gate: a scale words, grouped layout [I/128][a_ld]
   int64_t a_ld;
   __nv_bfloat16* y;  // down: y [rows][D]
+  __nv_bfloat16* h_out;  // replay: h, u [rows][I]
+  __nv_bfloat16* u_out;
   int32_t out_ld;
 };
 
-template <bool kSwiglu>
+template <bool kSwiglu, bool kReplay = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -251,7 +254,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const int local = c.mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;  // row within the group
       const bool valid = local < c.rows;
       const int64_t row = c.row0 + local;
-      if (kSwiglu) {
+      if (kReplay) {
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t hv[32], uv[32];
+          tmem_ld32(taddr + ch * 32, hv);
+          tmem_ld32(taddr + 128 + ch * 32, uv);
+          tmem_ld_wait();
+          uint32_t ph[16], pu[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            ph[j] = pack_bf16x2(__uint_as_float(hv[2 * j]), __uint_as_float(hv[2 * j + 1]));
+            pu[j] = pack_bf16x2(__uint_as_float(uv[2 * j]), __uint_as_float(uv[2 * j + 1]));
+          }
+          if (valid) {
+            __nv_bfloat16* hd = P.h_out + row * P.out_ld + c.nt * 128 + ch * 32;
+            __nv_bfloat16* ud = P.u_out + row * P.out_ld + c.nt * 128 + ch * 32;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              st_global_v4(hd + qq * 8, ph[4 * qq], ph[4 * qq + 1], ph[4 * qq + 2], ph[4 * qq + 3]);
+              st_global_v4(ud + qq * 8, pu[4 * qq], pu[4 * qq + 1], pu[4 * qq + 2], pu[4 * qq + 3]);
+            }
+          }
+        }
+      } else if (kSwiglu) {
         uint32_t words = 0;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -320,14 +346,15 @@ size_t mx_smem_bytes(int G) {
          static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
-template <bool kSwiglu>
+template <bool kSwiglu, bool kReplay = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st) {
   const size_t smem = mx_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(gemm_mx_pair_persistent<kSwiglu>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
     return MOK_ERR_CUDA;
-  gemm_mx_pair_persistent<kSwiglu><<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
+  kern<<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -357,14 +384,10 @@ SchedArgs mx_sched(const int32_t* offsets, int G, int64_t m_total, int n_tiles, 
   return s;
 }
 
-}  // namespace
-
-mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
-                            const void* sg, const void* qu, const void* su, const int32_t* offsets,
-                            int G, int D, int I, void* aq, void* asc, cudaStream_t st) {
-  if (rows == 0) return MOK_OK;
-  if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
-  MxParams P;
+// Parameters of the up/gate pair GEMM (also the backward's replay).
+mok_status upgate_mx_params(MxParams& P, const void* xq, const void* xsc, int64_t rows, const void* qg,
+                            const void* sg, const void* qu, const void* su, const int32_t* offsets, int G, int D,
+                            int I) {
   P.sched = mx_sched(offsets, G, rows, I / 128, D / BKB);
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
@@ -376,12 +399,41 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
   P.b_group_rows = I;
   P.b_tile_rows = 128;
   P.b1_off = 0;
-  P.aq = static_cast<uint8_t*>(aq);
-  P.asc = static_cast<uint32_t*>(asc);
+  P.aq = nullptr;
+  P.asc = nullptr;
   P.a_ld = mx_scale_ld(rows, G);
   P.y = nullptr;
+  P.h_out = nullptr;
+  P.u_out = nullptr;
   P.out_ld = I;
+  return MOK_OK;
+}
+}  // namespace
+
+mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
+                            const void* sg, const void* qu, const void* su, const int32_t* offsets,
+                            int G, int D, int I, void* aq, void* asc, cudaStream_t st) {
+  if (rows == 0) return MOK_OK;
+  if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
+  MxParams P;
+  mok_status r = upgate_mx_params(P, xq, xsc, rows, qg, sg, qu, su, offsets, G, D, I);
+  if (r != MOK_OK) return r;
+  P.aq = static_cast<uint8_t*>(aq);
+  P.asc = static_cast<uint32_t*>(asc);
   return run_mx<true>(P, st);
+}
+
+mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const void* qg, const void* sg,
+                            const void* qu, const void* su, const int32_t* offsets, int G, int D, int I, void* h,
+                            void* u, cudaStream_t st) {
+  if (rows == 0) return MOK_OK;
+  if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
+  MxParams P;
+  mok_status r = upgate_mx_params(P, xq, xsc, rows, qg, sg, qu, su, offsets, G, D, I);
+  if (r != MOK_OK) return r;
+  P.h_out = static_cast<__nv_bfloat16*>(h);
+  P.u_out = static_cast<__nv_bfloat16*>(u);
+  return run_mx<true, true>(P, st);
 }
 
 mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
@@ -406,6 +458,8 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   P.asc = nullptr;
   P.a_ld = 0;
   P.y = static_cast<__nv_bfloat16*>(y);
+  P.h_out = nullptr;
+  P.u_out = nullptr;
   P.out_ld = D;
   return run_mx<false>(P, st);
 }

@@ -107,6 +107,22 @@ mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const voi
 // dw [G][M][N] = bf16(sum over each group's rows of pm[p][m] qn[p][n])
 mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
                         int G, int M, int N, void* dw, cudaStream_t st);
+// MXFP8 backward.  Replay: h, u bf16 [rows][I] from the up/gate pair GEMM
+// (operands as launch_upgate_mx).  Activation gradient: from bf16 h, u, t
+// [R][I] and g_route (null = 1): dh, du, a_g bf16 [R][I], the codes of
+// [dh | du] [R][2I] with grouped scale words (ld = mx_scale_ld(R, E)) and
+// dgp [R] = <t, a>.
+mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const void* qg, const void* sg,
+                            const void* qu, const void* su, const int32_t* offsets, int G, int D, int I, void* h,
+                            void* u, cudaStream_t st);
+mok_status launch_act_grad_mx(const void* h, const void* u, const void* t, const float* g_route,
+                              const int32_t* table, const int32_t* offsets, int64_t R, int I, int E, void* dh,
+                              void* du, void* ag, void* dhu_q, uint8_t* dhu_sc, float* dgp, cudaStream_t st);
+// Codes of src^T per matrix: src bf16 [G][M][N]; output row g N + n holds
+// src[g][:, n] quantised along M at columns [col0, col0 + M) of out_cols,
+// plain scale layout of G*N rows (M, col0, out_cols multiples of 128, N of 64).
+mok_status launch_quantize_cols_mxfp8(const void* src, int G, int M, int N, void* q, uint8_t* scale, int out_cols,
+                                      int col0, cudaStream_t st);
 // ds [T][E], dg [T][K] (nullable) from the partials dgp [R][nI]
 mok_status launch_router_grad(const float* dgp, int nI, const int32_t* route_dst,
                               const int32_t* topk, const float* g, const float* s, int T, int E,

@@ -37,7 +37,8 @@ class Shape(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_gate", "w_up", "w_down", "q_gate", "q_up", "q_down",
-                 "sc_gate", "sc_up", "sc_down", "ws_gate", "ws_up", "ws_down")]
+                 "sc_gate", "sc_up", "sc_down", "ws_gate", "ws_up", "ws_down",
+                 "qt_down", "sct_down", "qt_gu", "sct_gu")]
 
 
 class PlanBuf(ctypes.Structure):
@@ -71,6 +72,8 @@ _SIGS = {
                                    ctypes.POINTER(PlanBuf), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _SZ, _P]),
     "mok_quantize_mxfp8": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "mok_quantize_mxfp8_bwd_weights": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P,
+                                                      _P, _P]),
     "mok_mxfp8_scale_bytes": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int32]),
     "mok_check_wait_timeout": (ctypes.c_int, [_P]),
     "mok_router": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
@@ -136,7 +139,8 @@ def shape_of(cfg, dtype=None, chunk_rows=0) -> Shape:
 def make_weights(t: Dict[str, object]) -> Weights:
     w = Weights()
     for name in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down",
-                 "q_gate", "q_up", "q_down", "sc_gate", "sc_up", "sc_down"):
+                 "q_gate", "q_up", "q_down", "sc_gate", "sc_up", "sc_down",
+                 "qt_down", "sct_down", "qt_gu", "sct_gu"):
         if t.get(name) is not None:
             setattr(w, name, _ptr(t[name]))
     return w
@@ -237,6 +241,14 @@ def quantize_mxfp8(src, q, scale, stream=None):
     rows, cols = src.shape
     _check(_lib_handle().mok_quantize_mxfp8(_ptr(src), rows, cols, _ptr(q), _ptr(scale), _stream(stream)),
            "mok_quantize_mxfp8")
+
+
+def quantize_mxfp8_bwd_weights(shape: Shape, weights: Weights, qt_down, sct_down, qt_gu, sct_gu, stream=None):
+    """The backward's MXFP8 weight copies (W_down^T along D; [W_gate^T | W_up^T]
+    along 2I) from the bf16 weights in `weights`."""
+    _check(_lib_handle().mok_quantize_mxfp8_bwd_weights(ctypes.byref(shape), ctypes.byref(weights), _ptr(qt_down),
+                                                        _ptr(sct_down), _ptr(qt_gu), _ptr(sct_gu),
+                                                        _stream(stream)), "mok_quantize_mxfp8_bwd_weights")
 
 
 def mx_scale_words(rows: int, cols: int, groups: int = 0) -> int:

@@ -86,6 +86,9 @@ CONFIGS: Dict[str, MoEConfig] = {
                                         I_shared=2048, backward=True),
     "dsv3_bf16_fwdbwd": MoEConfig("dsv3_bf16_fwdbwd", T=4096, D=7168, I=2048, E=256, K=8, I_shared=2048,
                                   backward=True),
+    # the same layer with the routed experts in MXFP8, forward and backward
+    "dsv3_mxfp8_fwdbwd": MoEConfig("dsv3_mxfp8_fwdbwd", T=4096, D=7168, I=2048, E=256, K=8, I_shared=2048,
+                                   backward=True, dtype="mxfp8"),
 }
 
 _SLAB = 1 << 26  # elements drawn per randn call

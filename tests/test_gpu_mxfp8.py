@@ -197,3 +197,89 @@ def test_mxfp8_full_size_sampled_rows(m):
                                       W.bf16_bits(d["w_down"][e]))
         assert_close(yg[torch.from_numpy(picks).to(DEV)].float().cpu().numpy(), ref["y"], MXFP8_TOL,
                      f"y expert {e}")
+
+
+# ---------------------------------------------------------------- backward
+BWD = {
+    "ragged": W.MoEConfig("ragged_bwd", T=300, D=512, I=256, E=5, K=3, I_shared=128, dtype="mxfp8"),
+    # empty experts, a hot expert and ragged expert ends
+    "skew": W.MoEConfig("skew_bwd", T=700, D=512, I=256, E=32, K=4, I_shared=256, skew=2.0, dtype="mxfp8"),
+}
+
+
+def bwd_weights(m, cfg, d):
+    """The forward's MXFP8 copies plus the backward's (W_down^T along D,
+    [W_gate^T | W_up^T] along 2I) from mok_quantize_mxfp8_bwd_weights."""
+    out = mx_weights(m, d)
+    E, I, D = cfg.E, cfg.I, cfg.D
+    out["qt_down"] = torch.empty(E * I, D, dtype=torch.uint8, device=DEV)
+    out["sct_down"] = torch.empty(m.mx_scale_words(E * I, D), dtype=torch.int32, device=DEV)
+    out["qt_gu"] = torch.empty(E * D, 2 * I, dtype=torch.uint8, device=DEV)
+    out["sct_gu"] = torch.empty(m.mx_scale_words(E * D, 2 * I), dtype=torch.int32, device=DEV)
+    m.quantize_mxfp8_bwd_weights(m.shape_of(cfg), m.make_weights(out), out["qt_down"], out["sct_down"],
+                                 out["qt_gu"], out["sct_gu"])
+    return out
+
+
+def test_bwd_weight_copies_bitexact(m):
+    cfg = BWD["ragged"]
+    inp = W.make_inputs(cfg, "cpu")
+    h = host(inp)
+    d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
+    E, I, D = cfg.E, cfg.I, cfg.D
+    wd_t = O.bf16_to_f32(h["w_down"]).transpose(0, 2, 1).reshape(E * I, D)
+    q, sc = O.mxfp8_quantize(wd_t)
+    assert np.array_equal(d["qt_down"].cpu().numpy(), q)
+    assert np.array_equal(words_to_bytes(d["sct_down"], E * I, D), sc)
+    wgu_t = np.concatenate([O.bf16_to_f32(h["w_gate"]).transpose(0, 2, 1),
+                            O.bf16_to_f32(h["w_up"]).transpose(0, 2, 1)], axis=2).reshape(E * D, 2 * I)
+    q, sc = O.mxfp8_quantize(wgu_t)
+    assert np.array_equal(d["qt_gu"].cpu().numpy(), q)
+    assert np.array_equal(words_to_bytes(d["sct_gu"], E * D, 2 * I), sc)
+
+
+def _mx_fwd_bwd(m, cfg, d):
+    shape = m.shape_of(cfg)
+    w = m.make_weights(d)
+    ws = torch.empty(max(m.workspace_bytes(shape, m.OP_FWD), m.workspace_bytes(shape, m.OP_BWD)),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+    saved = alloc_plan(cfg, DEV)
+    pb = m.make_plan_buf(saved)
+    m.moe_fwd(shape, w, d["x"], d["s"], out, ws, pb)
+    bf = torch.bfloat16
+    T, D, I, E, K, Is = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared
+    g = dict(dx=torch.empty(T, D, dtype=bf, device=DEV), dw_gate=torch.empty(E, I, D, dtype=bf, device=DEV),
+             dw_up=torch.empty(E, I, D, dtype=bf, device=DEV), dw_down=torch.empty(E, D, I, dtype=bf, device=DEV),
+             dws_gate=torch.empty(Is, D, dtype=bf, device=DEV), dws_up=torch.empty(Is, D, dtype=bf, device=DEV),
+             dws_down=torch.empty(D, Is, dtype=bf, device=DEV), ds=torch.empty(T, E, device=DEV),
+             dg=torch.empty(T, K, device=DEV))
+    for v in g.values():
+        v.fill_(float("nan"))
+    m.moe_bwd(shape, w, d["x"], d["s"], pb, d["dy"], g["dx"], g["dw_gate"], g["dw_up"], g["dw_down"],
+              g["dws_gate"], g["dws_up"], g["dws_down"], g["ds"], g["dg"], ws)
+    m.check_device_status()
+    return g
+
+
+@pytest.mark.parametrize("name", list(BWD))
+def test_backward_mxfp8_elementwise_and_deterministic(m, name):
+    cfg = BWD[name]
+    inp = W.make_inputs(cfg, "cpu", with_dy=True)
+    h = host(inp)
+    d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
+    got = _mx_fwd_bwd(m, cfg, d)
+    ref = O.moe_backward_mxfp8(h, h["dy"], cfg.K)
+    f = lambda t: t.float().cpu().numpy()
+    for k, r in (("dx", "dX"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down"),
+                 ("dws_gate", "dWs_gate"), ("dws_up", "dWs_up"), ("dws_down", "dWs_down"),
+                 ("dg", "dg"), ("ds", "ds")):
+        assert_close(f(got[k]), ref[r], MXFP8_TOL, k)
+    if name == "skew":
+        empty = np.flatnonzero(np.bincount(O.route(h["s"], cfg.K)[0].reshape(-1), minlength=cfg.E) == 0)
+        assert len(empty) > 0 and torch.all(got["dw_gate"][torch.from_numpy(empty).to(DEV)] == 0)
+    again = _mx_fwd_bwd(m, cfg, d)
+    for k, v in got.items():
+        bits = (lambda t: t.view(torch.int16)) if v.dtype == torch.bfloat16 else (lambda t: t.view(torch.int32))
+        assert torch.equal(bits(v), bits(again[k])), k
+

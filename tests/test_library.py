@@ -86,3 +86,25 @@ def test_plan_ranks_host_checks(m):
     assert m.plan_ranks_workspace_bytes(250, 8, 2, 4) == 0  # ranks must divide T
     assert lib.mok_plan_ranks(None, 250, 8, 2, 4, None, None, None, None, None, 0, None) == m.MOK_ERR_INVALID_ARG
     assert lib.mok_plan_ranks(None, 256, 8, 2, 0, None, None, None, None, None, 0, None) == m.MOK_ERR_INVALID_ARG
+
+
+def test_mxfp8_backward_argument_checks(m):
+    lib = m._lib_handle()
+    fake = ctypes.c_void_p(256)  # never dereferenced: each call is rejected first
+    names = ("w_gate", "w_up", "w_down", "q_gate", "q_up", "q_down", "sc_gate", "sc_up", "sc_down",
+             "qt_down", "sct_down", "qt_gu", "sct_gu")
+    w = m.Weights(**{n: 256 for n in names})
+    pb = m.PlanBuf(*([256] * 6))
+    args = lambda sh, ww: (ctypes.byref(sh), ctypes.byref(ww), fake, fake, ctypes.byref(pb), fake, fake, fake,
+                           fake, fake, fake, fake, fake, fake, fake, fake, 0, None)
+    # the t and dX products run on 256-column tiles: I = 128 is unsupported
+    sh = m.make_shape(T=16, D=256, I=128, E=8, K=2, dtype=m.MOK_MXFP8)
+    assert lib.mok_moe_bwd(*args(sh, w)) == m.MOK_ERR_UNSUPPORTED
+    # the backward's weight copies are required
+    sh = m.make_shape(T=16, D=256, I=256, E=8, K=2, dtype=m.MOK_MXFP8)
+    w2 = m.Weights(**{n: 256 for n in names[:9]})
+    assert lib.mok_moe_bwd(*args(sh, w2)) == m.MOK_ERR_INVALID_ARG
+    # the weight-copy quantiser wants D and I multiples of 128
+    bad = m.make_shape(T=16, D=192, I=256, E=8, K=2)
+    assert lib.mok_quantize_mxfp8_bwd_weights(ctypes.byref(bad), ctypes.byref(w), fake, fake, fake, fake,
+                                              None) == m.MOK_ERR_INVALID_ARG

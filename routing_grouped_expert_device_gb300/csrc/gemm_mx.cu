@@ -40,7 +40,13 @@ namespace mok {
 namespace {
 
 constexpr int BKB = 128;  // K columns (bytes) per stage
-constexpr int STAGES = 6;
+// The quantising up/gate keeps six stages in flight.  The modes with bf16
+// outputs (down, replay) keep four and use 64 KB per CTA to drain the
+// accumulator into shared memory, so that it is free for the next tile's
+// MMAs while TMA stores write the tile out.
+constexpr int kMaxStages = 6;
+constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 warps x 4 boxes of 32 rows x 64 bf16
+__host__ __device__ constexpr int mx_stages(bool bf16_out) { return bf16_out ? 4 : kMaxStages; }
 constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows
 constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B
 constexpr int CODE_BYTES = A_BYTES + B_BYTES;
@@ -94,16 +100,22 @@ struct MxParams {
   __nv_bfloat16* h_out;  // replay: h, u [rows][I]
   __nv_bfloat16* u_out;
   int32_t out_ld;
+  // bf16 outputs as [rows][out_ld], boxes 32 rows x 64 columns, 128-byte
+  // swizzle: y (down), or h and u (replay)
+  CUtensorMap tmO0, tmO1;
 };
 
 template <bool kSwiglu, bool kReplay = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
+  constexpr bool kBf16Out = !kSwiglu || kReplay;
+  constexpr int STAGES = mx_stages(kBf16Out);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sf_smem = smem + STAGES * CODE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sf_smem + STAGES * SF_BYTES);
+  uint8_t* staging = sf_smem + STAGES * SF_BYTES;  // 1024-byte aligned; STAGING_BYTES when kBf16Out
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + (kBf16Out ? STAGING_BYTES : 0));
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
@@ -111,7 +123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
-  int* tstart = reinterpret_cast<int*>(sf_smem + STAGES * SF_BYTES + 1024);
+  int* tstart = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 1024);
   int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -254,30 +266,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const int local = c.mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;  // row within the group
       const bool valid = local < c.rows;
       const int64_t row = c.row0 + local;
-      if (kReplay) {
+      if (kBf16Out) {
+        // 256 bf16 columns per row: y (down), or h then u (replay).  A full
+        // 32-row slab is drained into this warp's four 4 KB boxes (128-byte
+        // swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), the
+        // accumulator is released, and four TMA stores write the boxes.  A
+        // slab that crosses the group's end is written row by row (a TMA
+        // store would overwrite the next group's rows).
+        const int nvalid = min(max(c.rows - (local - lane), 0), 32);
+        uint8_t* boxes = staging + q * (4 * 4096);
+        if (nvalid == 32) {
+          if (lane == 0) bulk_wait_read0();  // the previous tile's stores have read the boxes
+          __syncwarp();
+        }
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t hv[32], uv[32];
-          tmem_ld32(taddr + ch * 32, hv);
-          tmem_ld32(taddr + 128 + ch * 32, uv);
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(taddr + ch * 32, v);
           tmem_ld_wait();
-          uint32_t ph[16], pu[16];
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            ph[j] = pack_bf16x2(__uint_as_float(hv[2 * j]), __uint_as_float(hv[2 * j + 1]));
-            pu[j] = pack_bf16x2(__uint_as_float(uv[2 * j]), __uint_as_float(uv[2 * j + 1]));
-          }
-          if (valid) {
-            __nv_bfloat16* hd = P.h_out + row * P.out_ld + c.nt * 128 + ch * 32;
-            __nv_bfloat16* ud = P.u_out + row * P.out_ld + c.nt * 128 + ch * 32;
+          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          if (nvalid == 32) {
+            uint8_t* rowp = boxes + (ch >> 1) * 4096 + lane * 128;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
-              st_global_v4(hd + qq * 8, ph[4 * qq], ph[4 * qq + 1], ph[4 * qq + 2], ph[4 * qq + 3]);
-              st_global_v4(ud + qq * 8, pu[4 * qq], pu[4 * qq + 1], pu[4 * qq + 2], pu[4 * qq + 3]);
+              const int chunk = (ch & 1) * 4 + qq;
+              *reinterpret_cast<uint4*>(rowp + ((chunk ^ (lane & 7)) * 16)) =
+                  make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
             }
+          } else if (valid) {
+            __nv_bfloat16* dst = kReplay ? (ch < 4 ? P.h_out : P.u_out) + row * P.out_ld + c.nt * 128 + (ch & 3) * 32
+                                         : P.y + row * P.out_ld + c.nt * 256 + ch * 32;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+              st_global_v4(dst + qq * 8, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
           }
         }
-      } else if (kSwiglu) {
+        if (nvalid == 32) {
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tc_fence_before();
+        if (leader) mbar_arrive(tempty);
+        else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+        if (nvalid == 32 && lane == 0) {
+          const int y0 = static_cast<int>(row - lane);  // the slab's first row
+#pragma unroll
+          for (int bx = 0; bx < 4; ++bx) {
+            if (kReplay) tma_store_2d(bx < 2 ? &P.tmO0 : &P.tmO1, boxes + bx * 4096, c.nt * 128 + (bx & 1) * 64, y0);
+            else tma_store_2d(&P.tmO0, boxes + bx * 4096, c.nt * 256 + bx * 64, y0);
+          }
+          bulk_commit();
+        }
+        continue;
+      }
+      if (kSwiglu) {
         uint32_t words = 0;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
@@ -312,27 +356,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           }
         }
         if (valid) P.asc[c.nt * P.a_ld + mx_scale_pos(mx_group_row0(c.row0, c.g) + local)] = words;
-      } else {
-        __nv_bfloat16* orow = P.y + row * P.out_ld + c.nt * 256;
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t v[32];
-          tmem_ld32(taddr + ch * 32, v);
-          tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          if (valid) {
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-              st_global_v4(orow + ch * 32 + qq * 8, pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
-          }
-        }
       }
       tc_fence_before();
       if (leader) mbar_arrive(tempty);
       else remote_arrive(map_to_rank(smem_u32(tempty), 0));
     }
+    if (kBf16Out && lane == 0) bulk_wait0();  // this warp's stores have landed before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -341,14 +371,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   if (warp == 2) tmem_dealloc2(tmem_base, 512);
 }
 
-size_t mx_smem_bytes(int G) {
-  return 1024 + static_cast<size_t>(STAGES) * (CODE_BYTES + SF_BYTES) + 1024 +
-         static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+size_t mx_smem_bytes(int G, bool bf16_out) {
+  return 1024 + static_cast<size_t>(mx_stages(bf16_out)) * (CODE_BYTES + SF_BYTES) +
+         (bf16_out ? STAGING_BYTES : 0) + 1024 + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
 }
 
 template <bool kSwiglu, bool kReplay = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st) {
-  const size_t smem = mx_smem_bytes(P.sched.G);
+  const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -361,6 +391,12 @@ mok_status run_mx(const MxParams& P, cudaStream_t st) {
 
 constexpr auto kU8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 constexpr auto kI32 = CU_TENSOR_MAP_DATA_TYPE_INT32;
+
+// bf16 [rows][cols] output, boxes of 32 rows x 64 columns, 128-byte swizzle
+bool out_map(CUtensorMap* m, const void* p, int64_t rows, int cols) {
+  return make_tmap_2d(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows > 0 ? rows : 1, cols,
+                      static_cast<uint64_t>(cols) * 2, 32, 64, true);
+}
 
 bool code_map(CUtensorMap* m, const void* p, int64_t rows, int K) {
   return make_tmap_2d(m, p, kU8, rows, K, static_cast<uint64_t>(K), 128, BKB, true);
@@ -433,6 +469,7 @@ mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const
   if (r != MOK_OK) return r;
   P.h_out = static_cast<__nv_bfloat16*>(h);
   P.u_out = static_cast<__nv_bfloat16*>(u);
+  if (!out_map(&P.tmO0, h, rows, I) || !out_map(&P.tmO1, u, rows, I)) return MOK_ERR_CUDA;
   return run_mx<true, true>(P, st);
 }
 
@@ -461,6 +498,8 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   P.h_out = nullptr;
   P.u_out = nullptr;
   P.out_ld = D;
+  if (!out_map(&P.tmO0, y, rows, D)) return MOK_ERR_CUDA;
+  P.tmO1 = P.tmO0;
   return run_mx<false>(P, st);
 }
 

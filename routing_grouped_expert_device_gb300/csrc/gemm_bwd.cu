@@ -244,10 +244,12 @@ struct DxCfg {
 template <int BN>
 struct WgradCfg {
   static constexpr int NB = BN / 64;  // 64-wide MN chunks of B
+  static constexpr int BKW = 64;        // rows (K) per stage
+  static constexpr int CH = BKW * 128;  // one 64-wide MN chunk of a stage: BKW rows of 128 B
   // Four stages (two tiles of a ~128-row expert) ahead of the MMAs: with
   // three the MMA warp waited on loads.
   static constexpr int STAGES = 4;
-  static constexpr int STAGE_BYTES = (2 + NB) * MNCHUNK;
+  static constexpr int STAGE_BYTES = (2 + NB) * CH;
   // per epilogue warp: one staging block of 32 rows x 64 columns of bf16,
   // 128-byte swizzled, the source of one TMA store
   static constexpr int EPI_SMEM_BYTES = 4 * 32 * 128;
@@ -272,12 +274,12 @@ struct WgradCfg {
   __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
                               uint64_t* bar, int lane) {
     if (lane != 0) return;
-    const int rk = c.row0 + kb * BK;
+    const int rk = c.row0 + kb * BKW;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) tma_load_2d(st + j * MNCHUNK, &P.tmA, c.mt * 128 + 64 * j, rk, bar);
+    for (int j = 0; j < 2; ++j) tma_load_2d(st + j * CH, &P.tmA, c.mt * 128 + 64 * j, rk, bar);
 #pragma unroll
     for (int j = 0; j < NB; ++j)
-      tma_load_2d(st + (2 + j) * MNCHUNK, &P.tmB, c.nt * BN + 64 * j, rk, bar);
+      tma_load_2d(st + (2 + j) * CH, &P.tmB, c.nt * BN + 64 * j, rk, bar);
   }
 
   // Rows past the group's end in its last K block belong to the next group
@@ -286,8 +288,8 @@ struct WgradCfg {
   // the end and that step are zeroed in A (both 64-column chunks; lane l
   // clears 16-byte unit l % 8 of every fourth row).
   __device__ static int k_rows(const TileCoord& c, int kb) {
-    const int valid = c.rows - kb * BK;
-    return valid < BK ? valid : BK;
+    const int valid = c.rows - kb * BKW;
+    return valid < BKW ? valid : BKW;
   }
   __device__ static void fixup(const Params&, const TileCoord& c, int kb, uint8_t* st, int lane) {
     const int valid = k_rows(c, kb);
@@ -296,18 +298,20 @@ struct WgradCfg {
     for (int r = valid + (lane >> 3); r < end; r += 4) {
       uint8_t* p = st + r * 128 + (lane & 7) * 16;
       *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(p + MNCHUNK) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(p + CH) = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
   }
+
+  // MN-major, 128-byte swizzle: LBO = one 64-wide MN chunk, SBO = 8 K rows
+  __device__ static uint64_t desc(uint32_t a) { return sdesc_sw128(a, CH, 1024); }
 
   __device__ static void mma(const Params&, const TileCoord& c, int kb, uint8_t* st, uint32_t d) {
     const uint32_t s = smem_u32(st);
     const int nk = (k_rows(c, kb) + 15) / 16;
 #pragma unroll
-    for (int k = 0; k < BK / 16; ++k)
-      if (k < nk)
-        mma_bf16(d, mndesc(s + k * 2048), mndesc(s + 2 * MNCHUNK + k * 2048), IDESC, (kb | k) != 0);
+    for (int k = 0; k < BKW / 16; ++k)
+      if (k < nk) mma_bf16(d, desc(s + k * 2048), desc(s + 2 * CH + k * 2048), IDESC, (kb | k) != 0);
   }
 
   // Each warp converts its 32 rows x 64 columns to bf16, writes them to its
@@ -454,7 +458,7 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
   s.m_tiles_fixed = M / 128;
   s.k_blocks_fixed = 0;
   s.bm = BM;
-  s.bk_rows = BK;
+  s.bk_rows = WgradCfg<BN>::BKW;
   // N tile fastest: CTAs working side by side write neighbouring column
   // pieces of the same dW rows instead of 512-byte pieces of distant rows
   s.m_outer = 1;
@@ -462,7 +466,10 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int64_t map_rows = rows > 0 ? rows : 1;
-  if (!mnmap(&P.tmA, pm, map_rows, M) || !mnmap(&P.tmB, qn, map_rows, N) ||
+  auto mn = [](CUtensorMap* m, const void* p, int64_t rows, int cols) {
+    return make_tmap_2d(m, p, kBF16, rows, cols, static_cast<uint64_t>(cols) * 2, WgradCfg<BN>::BKW, 64, true);
+  };
+  if (!mn(&P.tmA, pm, map_rows, M) || !mn(&P.tmB, qn, map_rows, N) ||
       !make_tmap_2d(&P.tmOut, dw, kBF16, static_cast<uint64_t>(s.G) * M, N,
                     static_cast<uint64_t>(N) * 2, 32, 64, true))
     return MOK_ERR_CUDA;

@@ -1,5 +1,8 @@
 """GPU parity of the MXFP8 path (E4M3 codes, E8M0 1x32 scales) against the oracle.
 
+Forward and backward, small shapes element by element and the DSV3 layers on
+sampled tokens and experts.
+
 Codes and scales of quantised inputs (the quantiser, the dispatch with fused
 quantisation) must match bit-exactly.  Floats from the MXFP8 GEMMs must be
 within 6e-2 * max(1, |oracle|) per element.  The codes of a (quantised in the
@@ -283,3 +286,56 @@ def test_backward_mxfp8_elementwise_and_deterministic(m, name):
         bits = (lambda t: t.view(torch.int16)) if v.dtype == torch.bfloat16 else (lambda t: t.view(torch.int32))
         assert torch.equal(bits(v), bits(again[k])), k
 
+
+
+def test_backward_mxfp8_full_size_sampled(m):
+    """The DSV3 fwd+bwd layer (T 4096, 256 experts) with MXFP8 routed experts:
+    one token's dX, dg and ds (its 8 routes), and whole weight gradients of
+    two experts (the fullest and a middle one), each from the oracle's MXFP8
+    backward of that expert's rows.  The oracle quantises each expert's
+    full weights (about 10 s per expert on one core), so the calls run on a
+    thread pool."""
+    from concurrent.futures import ThreadPoolExecutor
+    cfg = W.CONFIGS["dsv3_mxfp8_fwdbwd"]
+    d = bwd_weights(m, cfg, W.make_inputs(cfg, DEV))
+    got = _mx_fwd_bwd(m, cfg, d)
+    s_host = d["s"].cpu().numpy()
+    idx, g, den = O.route(s_host, cfg.K)
+    counts, offsets, table, _ = O.plan(idx, cfg.E)
+    f = lambda t: t.float().cpu().numpy()
+    Wsh = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
+    x_all = W.bf16_bits(d["x"])
+    dy_all = W.bf16_bits(d["dy"])
+
+    def ew(e):
+        return W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e])
+
+    t = int(np.random.default_rng(2).integers(cfg.T))
+    experts = [int(np.argmax(counts)), cfg.E // 2]
+    jobs = [(t, k, int(idx[t, k])) for k in range(cfg.K)]
+    with ThreadPoolExecutor(max_workers=len(jobs) + len(experts)) as pool:
+        tok = [pool.submit(O.route_backward_rows_mxfp8, x_all[t:t + 1], dy_all[t:t + 1], g[t:t + 1, k], *ew(e))
+               for _, k, e in jobs]
+        rows = {}
+        for e in experts:
+            p0, p1 = int(offsets[e]), int(offsets[e + 1])
+            toks_e = table[p0:p1, 0] // cfg.K
+            gr = g[toks_e, table[p0:p1, 0] % cfg.K]
+            rows[e] = (toks_e, pool.submit(O.route_backward_rows_mxfp8, x_all[toks_e], dy_all[toks_e], gr, *ew(e)))
+        acc = O.route_backward_rows(x_all[t:t + 1], dy_all[t:t + 1], np.ones(1, np.float32), *Wsh)["dx"][0].copy()
+        dg_t = np.zeros(cfg.K, np.float32)
+        for k, fut in enumerate(tok):
+            b = fut.result()
+            acc = acc + b["dx"][0]
+            dg_t[k] = b["dg"][0]
+        assert_close(f(got["dx"][t]), O.round_bf16(acc), MXFP8_TOL, f"dX[{t}]")
+        assert_close(f(got["dg"][t]), dg_t, MXFP8_TOL, f"dg[{t}]")
+        ds_ref = O.router_grad(dg_t[None], g[t:t + 1], den[t:t + 1], idx[t:t + 1], cfg.E)[0]
+        assert_close(f(got["ds"][t]), ds_ref, MXFP8_TOL, f"ds[{t}]")
+        for e, (toks_e, fut) in rows.items():
+            b = fut.result()
+            X = O.bf16_to_f32(x_all[toks_e])
+            dY = O.bf16_to_f32(dy_all[toks_e])
+            assert_close(f(got["dw_down"][e]), O.round_bf16(dY.T @ b["a_g"]), MXFP8_TOL, f"dW_down[{e}]")
+            assert_close(f(got["dw_gate"][e]), O.round_bf16(b["dh"].T @ X), MXFP8_TOL, f"dW_gate[{e}]")
+            assert_close(f(got["dw_up"][e]), O.round_bf16(b["du"].T @ X), MXFP8_TOL, f"dW_up[{e}]")

@@ -64,10 +64,10 @@ __device__ __forceinline__ int extra_tiles(const SchedArgs& s) {
   return s.extra_rows > 0 ? ((s.extra_rows + s.bm - 1) / s.bm) * s.extra_n_tiles : 0;
 }
 
-// Warp-wide: rstart[g] = first row of group g, tstart[g] = first tile of
-// group g (exclusive scan), both [G+1].  Returns the tile count.
-__device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart, int* rstart,
-                                                int lane) {
+// Warp-wide: tstart[g] = first tile of group g (exclusive scan), [G+1].
+// Returns the tile count.  (Rows of a group come from s.offsets when a
+// role reaches the group, so only the tile starts take shared memory.)
+__device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart, int lane) {
   const int G = s.G;
   const int per = (G + 31) / 32;
   const int g0 = lane * per;
@@ -75,8 +75,6 @@ __device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart,
   for (int g = g0; g < g0 + per && g < G; ++g) {
     int r0 = s.offsets ? s.offsets[g] : 0;
     int r1 = s.offsets ? s.offsets[g + 1] : s.m_total;
-    rstart[g] = r0;
-    if (g == G - 1) rstart[G] = r1;
     local += sched_m_tiles(s, r1 - r0) * s.n_tiles;
   }
   int incl = local;
@@ -109,13 +107,12 @@ __device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart,
 struct TileWalker {
   const SchedArgs& s;
   const int* tstart;
-  const int* rstart;
   int S, p, extra_mtiles;
   int g;                                    // group of the last grouped tile
   int cg, crow0, crows, cmtiles, ckblocks;  // cached quantities of group cg
 
-  __device__ __forceinline__ TileWalker(const SchedArgs& s_, const int* tstart_, const int* rstart_)
-      : s(s_), tstart(tstart_), rstart(rstart_), g(0), cg(-1) {
+  __device__ __forceinline__ TileWalker(const SchedArgs& s_, const int* tstart_)
+      : s(s_), tstart(tstart_), g(0), cg(-1) {
     S = extra_tiles(s);
     p = S > 0 ? (tstart[s.G] + S) / S : 1;
     extra_mtiles = S > 0 ? (s.extra_rows + s.bm - 1) / s.bm : 1;
@@ -142,8 +139,8 @@ struct TileWalker {
     while (g + 1 < s.G && tstart[g + 1] <= gt) ++g;
     if (g != cg) {
       cg = g;
-      crow0 = rstart[g];
-      crows = rstart[g + 1] - crow0;
+      crow0 = s.offsets ? __ldg(s.offsets + g) : 0;
+      crows = (s.offsets ? __ldg(s.offsets + g + 1) : s.m_total) - crow0;
       cmtiles = sched_m_tiles(s, crows);
       ckblocks = sched_k_blocks(s, crows);
     }
@@ -165,11 +162,11 @@ struct TileWalker {
 };
 
 // Shared memory: [STAGES x STAGE_BYTES][1 KB barriers and flags]
-// [EPI_SMEM_BYTES epilogue staging, 1 KB aligned][tile table].
+// [EPI_SMEM_BYTES epilogue staging, 1 KB aligned][tile starts, G + 1 ints].
 template <class Cfg>
 constexpr size_t gemm_smem_bytes(int G) {
   return 1024 /*alignment slack*/ + static_cast<size_t>(Cfg::STAGES) * Cfg::STAGE_BYTES +
-         1024 /*barriers and flags*/ + Cfg::EPI_SMEM_BYTES + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+         1024 /*barriers and flags*/ + Cfg::EPI_SMEM_BYTES + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 // Cfg interface:
@@ -201,7 +198,6 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
   uint8_t* epi_smem = smem + Cfg::STAGES * Cfg::STAGE_BYTES + 1024;
   int* tstart = reinterpret_cast<int*>(epi_smem + Cfg::EPI_SMEM_BYTES);
-  int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -221,7 +217,7 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
   }
   if (warp == 2) tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
   if (warp == 3) {
-    int total = build_tile_table(P.sched, tstart, rstart, lane);
+    int total = build_tile_table(P.sched, tstart, lane);
     if (lane == 0) *total_holder = total;
   }
   tc_fence_before();
@@ -239,7 +235,7 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
     bool issued[Cfg::STAGES];
     for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = false;
     bool ok = true;
-    TileWalker walk(P.sched, tstart, rstart);
+    TileWalker walk(P.sched, tstart);
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const TileCoord c = walk.at(tile);
       for (int kb = 0; kb < c.kblocks; ++kb) {
@@ -273,7 +269,7 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
     uint32_t stage = 0, phase = 0;
     bool ok = true, any = false;
     int it = 0;
-    TileWalker walk(P.sched, tstart, rstart);
+    TileWalker walk(P.sched, tstart);
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
       const TileCoord c = walk.at(tile);
       const uint32_t acc = (Cfg::NUM_ACC == 2) ? (it & 1) : 0;
@@ -318,7 +314,7 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
     // ---------------- epilogue ----------------
     const int ew = warp - 4;
     int it = 0;
-    TileWalker walk(P.sched, tstart, rstart);
+    TileWalker walk(P.sched, tstart);
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const TileCoord c = walk.at(tile);
       const uint32_t acc = (Cfg::NUM_ACC == 2) ? (it & 1) : 0;

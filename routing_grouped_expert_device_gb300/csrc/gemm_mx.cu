@@ -124,7 +124,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
   int* tstart = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 1024);
-  int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -144,7 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   }
   if (warp == 2) tmem_alloc2(tmem_holder, 512);
   if (warp == 3) {
-    const int total = build_tile_table(P.sched, tstart, rstart, lane);
+    const int total = build_tile_table(P.sched, tstart, lane);
     if (lane == 0) *total_holder = total;
   }
   tc_fence_before();
@@ -164,7 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
       const CUtensorMap* tmB = rank ? &P.tmB1 : &P.tmB0;
-      TileWalker walk(P.sched, tstart, rstart);
+      TileWalker walk(P.sched, tstart);
       for (int tile = cid; tile < total && ok; tile += ncl) {
         const TileCoord c = walk.at(tile);
         const int local0 = c.mt * 256 + static_cast<int>(rank) * 128;  // this CTA's first row in the group
@@ -209,7 +208,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true, any = false;
       int it = 0;
-      TileWalker walk(P.sched, tstart, rstart);
+      TileWalker walk(P.sched, tstart);
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         const TileCoord c = walk.at(tile);
         ok = __all_sync(0xffffffffu, mbar_wait(tempty, (it & 1) ^ 1, abort_flag, P.status, SITE_MMA));
@@ -257,7 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
     const int q = warp - 4;  // TMEM lane quarter of this warp
     int it = 0;
-    TileWalker walk(P.sched, tstart, rstart);
+    TileWalker walk(P.sched, tstart);
     for (int tile = cid; tile < total; tile += ncl, ++it) {
       const TileCoord c = walk.at(tile);
       if (!__all_sync(0xffffffffu, mbar_wait(tfull, it & 1, abort_flag, P.status, SITE_EPILOGUE))) break;
@@ -373,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 
 size_t mx_smem_bytes(int G, bool bf16_out) {
   return 1024 + static_cast<size_t>(mx_stages(bf16_out)) * (CODE_BYTES + SF_BYTES) +
-         (bf16_out ? STAGING_BYTES : 0) + 1024 + static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+         (bf16_out ? STAGING_BYTES : 0) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 template <bool kSwiglu, bool kReplay = false>

@@ -220,7 +220,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
   int* tstart = reinterpret_cast<int*>(epi_smem + 4 * EPI_BLOCK + 1024);
-  int* rstart = tstart + (P.sched.G + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -242,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   }
   if (warp == 2) tmem_alloc2(tmem_holder, 512);
   if (warp == 3) {
-    const int total = build_tile_table(P.sched, tstart, rstart, lane);
+    const int total = build_tile_table(P.sched, tstart, lane);
     if (lane == 0) *total_holder = total;
   }
   tc_fence_before();
@@ -261,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       bool issued[STAGES];
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
-      TileWalker walk(P.sched, tstart, rstart);
+      TileWalker walk(P.sched, tstart);
       for (int tile = cid; tile < total && ok; tile += ncl) {
         const TileCoord c = walk.at(tile);
         const int arow = c.row0 + c.mt * 256 + static_cast<int>(rank) * 128;
@@ -314,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true, any = false;
       int it = 0;
-      TileWalker walk(P.sched, tstart, rstart);
+      TileWalker walk(P.sched, tstart);
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         const TileCoord c = walk.at(tile);
         const uint32_t acc = it & 1;
@@ -380,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     uint8_t* blk = epi_smem + ew * EPI_BLOCK;
     uint8_t* srow = blk + lane * 128;
     int it = 0;
-    TileWalker walk(P.sched, tstart, rstart);
+    TileWalker walk(P.sched, tstart);
     for (int tile = cid; tile < total; tile += ncl, ++it) {
       const TileCoord c = walk.at(tile);
       const uint32_t acc = it & 1;
@@ -463,7 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 
 size_t pair_smem_bytes(int G) {
   return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 4 * EPI_BLOCK + 1024 +
-         static_cast<size_t>(2 * (G + 1)) * sizeof(int);
+         static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 template <bool kSwiglu, bool kRing = false, bool kSoftmax = false>

@@ -27,6 +27,11 @@ SMALL = {
     # D and I multiples of 256 (256-column weight-gradient tiles throughout),
     # with empty experts and ragged expert ends
     "skew_256": W.MoEConfig("skew_256", T=700, D=512, I=256, E=32, K=4, I_shared=256, skew=2.0),
+    # degenerate shapes: one token; every expert chosen by every token; the
+    # largest E and K the boundary accepts (most experts empty)
+    "one_token": W.MoEConfig("one_token", T=1, D=256, I=128, E=8, K=2, I_shared=128),
+    "k_equals_e": W.MoEConfig("k_equals_e", T=65, D=256, I=128, E=8, K=8, I_shared=128),
+    "max_e_k": W.MoEConfig("max_e_k", T=40, D=256, I=128, E=1024, K=32, I_shared=0),
 }
 
 

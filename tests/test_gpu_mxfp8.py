@@ -207,6 +207,7 @@ BWD = {
     "ragged": W.MoEConfig("ragged_bwd", T=300, D=512, I=256, E=5, K=3, I_shared=128, dtype="mxfp8"),
     # empty experts, a hot expert and ragged expert ends
     "skew": W.MoEConfig("skew_bwd", T=700, D=512, I=256, E=32, K=4, I_shared=256, skew=2.0, dtype="mxfp8"),
+    "one_token": W.MoEConfig("one_token_bwd", T=1, D=256, I=256, E=8, K=2, I_shared=256, dtype="mxfp8"),
 }
 
 

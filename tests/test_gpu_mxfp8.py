@@ -208,6 +208,8 @@ BWD = {
     # empty experts, a hot expert and ragged expert ends
     "skew": W.MoEConfig("skew_bwd", T=700, D=512, I=256, E=32, K=4, I_shared=256, skew=2.0, dtype="mxfp8"),
     "one_token": W.MoEConfig("one_token_bwd", T=1, D=256, I=256, E=8, K=2, I_shared=256, dtype="mxfp8"),
+    # the largest E and K the boundary accepts: most experts empty
+    "max_e_k": W.MoEConfig("max_e_k_bwd", T=40, D=256, I=256, E=1024, K=32, I_shared=0, dtype="mxfp8"),
 }
 
 
@@ -275,9 +277,11 @@ def test_backward_mxfp8_elementwise_and_deterministic(m, name):
     got = _mx_fwd_bwd(m, cfg, d)
     ref = O.moe_backward_mxfp8(h, h["dy"], cfg.K)
     f = lambda t: t.float().cpu().numpy()
-    for k, r in (("dx", "dX"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down"),
-                 ("dws_gate", "dWs_gate"), ("dws_up", "dWs_up"), ("dws_down", "dWs_down"),
-                 ("dg", "dg"), ("ds", "ds")):
+    pairs = [("dx", "dX"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down"),
+             ("dg", "dg"), ("ds", "ds")]
+    if cfg.I_shared:
+        pairs += [("dws_gate", "dWs_gate"), ("dws_up", "dWs_up"), ("dws_down", "dWs_down")]
+    for k, r in pairs:
         assert_close(f(got[k]), ref[r], MXFP8_TOL, k)
     if name == "skew":
         empty = np.flatnonzero(np.bincount(O.route(h["s"], cfg.K)[0].reshape(-1), minlength=cfg.E) == 0)

@@ -307,7 +307,9 @@ mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void 
  * activation gradient quantises [dh | du] along 2I for qt_gu); h, u and t
  * are kept as bf16 between the products and the activation gradient.  The
  * weight gradients are BF16 products (of bf16 x, dY, dh, du, g a) and the
- * shared expert is BF16. */
+ * shared expert is BF16.  MXFP8 needs I % 256 == 0 (the t and dX products
+ * run on 256-column tiles; MOK_ERR_UNSUPPORTED otherwise) and w's q_* and
+ * qt_* copies (MOK_ERR_INVALID_ARG without them). */
 mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void *x,
                        const float *s, const mok_plan_buf *saved, const void *dy, void *dx,
                        void *dw_gate, void *dw_up, void *dw_down, void *dws_gate,

@@ -45,7 +45,7 @@ constexpr int BKB = 128;  // K columns (bytes) per stage
 // accumulator into shared memory, so that it is free for the next tile's
 // MMAs while TMA stores write the tile out.
 constexpr int kMaxStages = 6;
-constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 warps x 4 boxes of 32 rows x 64 bf16
+constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 rows x 64 bf16
 __host__ __device__ constexpr int mx_stages(bool bf16_out) { return bf16_out ? 4 : kMaxStages; }
 constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows
 constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B
@@ -55,6 +55,11 @@ constexpr int SF_BYTES = 3 * SF_BLOCK;  // A's block, B's two halves
 constexpr uint32_t TX_BYTES = 2 * (CODE_BYTES + SF_BYTES);
 constexpr uint32_t ACC_COLS = 256;
 constexpr uint32_t SF_COLS = 12;  // per stage: A 4, B 8
+// Eight epilogue warps: warps 4 + 4h + q drain TMEM lane quarter q (the
+// hardware ties a warp to quarter warp % 4), columns of half h of the
+// accumulator, so each warp holds the accumulator for half as long.
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 128 + EPI_WARPS * 32;
 
 // Block-scaled instruction descriptor, kind::mxf8f6f4: B scale id (bits
 // 4-5), A and B format E4M3 = 0 (7-9, 10-12), both K-major, N >> 3 (17-22),
@@ -106,7 +111,7 @@ struct MxParams {
 };
 
 template <bool kSwiglu, bool kReplay = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
   constexpr bool kBf16Out = !kSwiglu || kReplay;
   constexpr int STAGES = mx_stages(kBf16Out);
@@ -136,7 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       mbar_init(&empty[i], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 256);  // both CTAs' 128 epilogue threads
+    mbar_init(tempty, 2 * EPI_WARPS * 32);  // both CTAs' epilogue threads
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -254,7 +259,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
-    const int q = warp - 4;  // TMEM lane quarter of this warp
+    const int q = warp & 3;             // TMEM lane quarter of this warp
+    const int half = (warp - 4) >> 2;  // column half of the accumulator
     int it = 0;
     TileWalker walk(P.sched, tstart);
     for (int tile = cid; tile < total; tile += ncl, ++it) {
@@ -266,20 +272,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const bool valid = local < c.rows;
       const int64_t row = c.row0 + local;
       if (kBf16Out) {
-        // 256 bf16 columns per row: y (down), or h then u (replay).  A full
-        // 32-row slab is drained into this warp's four 4 KB boxes (128-byte
-        // swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)), the
-        // accumulator is released, and four TMA stores write the boxes.  A
-        // slab that crosses the group's end is written row by row (a TMA
-        // store would overwrite the next group's rows).
+        // 256 bf16 columns per row: y (down), or h then u (replay); this
+        // warp drains 128 of them.  A full 32-row slab is drained into the
+        // warp's two 4 KB boxes (128-byte swizzle: 16-byte chunk c of row r
+        // at chunk c ^ (r % 8)), the accumulator is released, and two TMA
+        // stores write the boxes.  A slab that crosses the group's end is
+        // written row by row (a TMA store would overwrite the next group's
+        // rows).
         const int nvalid = min(max(c.rows - (local - lane), 0), 32);
-        uint8_t* boxes = staging + q * (4 * 4096);
+        uint8_t* boxes = staging + q * (4 * 4096);  // boxes 2 half, 2 half + 1 are this warp's
         if (nvalid == 32) {
           if (lane == 0) bulk_wait_read0();  // the previous tile's stores have read the boxes
           __syncwarp();
         }
 #pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 4 * half; ch < 4 * half + 4; ++ch) {
           uint32_t v[32];
           tmem_ld32(taddr + ch * 32, v);
           tmem_ld_wait();
@@ -312,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         if (nvalid == 32 && lane == 0) {
           const int y0 = static_cast<int>(row - lane);  // the slab's first row
 #pragma unroll
-          for (int bx = 0; bx < 4; ++bx) {
+          for (int bx = 2 * half; bx < 2 * half + 2; ++bx) {
             if (kReplay) tma_store_2d(bx < 2 ? &P.tmO0 : &P.tmO1, boxes + bx * 4096, c.nt * 128 + (bx & 1) * 64, y0);
             else tma_store_2d(&P.tmO0, boxes + bx * 4096, c.nt * 256 + bx * 64, y0);
           }
@@ -323,7 +330,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       if (kSwiglu) {
         uint32_t words = 0;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
           uint32_t hv[32], uv[32];
           tmem_ld32(taddr + ch * 32, hv);
           tmem_ld32(taddr + 128 + ch * 32, uv);
@@ -347,14 +354,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
                 make_float2(av[4 * i + 2] * inv, av[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
             pk[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
           }
-          words |= static_cast<uint32_t>(e + 127) << (8 * ch);
+          words |= static_cast<uint32_t>(e + 127) << (8 * (ch - 2 * half));
           if (valid) {
             uint8_t* dst = P.aq + row * P.out_ld + c.nt * 128 + ch * 32;
             st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
             st_global_v4(dst + 16, pk[4], pk[5], pk[6], pk[7]);
           }
         }
-        if (valid) P.asc[c.nt * P.a_ld + mx_scale_pos(mx_group_row0(c.row0, c.g) + local)] = words;
+        // this half's two bytes of the row's scale word (byte ch = block ch)
+        if (valid)
+          reinterpret_cast<uint16_t*>(P.asc + c.nt * P.a_ld + mx_scale_pos(mx_group_row0(c.row0, c.g) + local))[half] =
+              static_cast<uint16_t>(words);
       }
       tc_fence_before();
       if (leader) mbar_arrive(tempty);
@@ -383,7 +393,7 @@ mok_status run_mx(const MxParams& P, cudaStream_t st) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
-  kern<<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
+  kern<<<(num_sms() / 2) * 2, THREADS, smem, st>>>(P);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

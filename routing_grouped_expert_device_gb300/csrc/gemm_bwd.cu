@@ -250,9 +250,11 @@ struct WgradCfg {
   // three the MMA warp waited on loads.
   static constexpr int STAGES = 4;
   static constexpr int STAGE_BYTES = (2 + NB) * CH;
-  // per epilogue warp: one staging block of 32 rows x 64 columns of bf16,
-  // 128-byte swizzled, the source of one TMA store
-  static constexpr int EPI_SMEM_BYTES = 4 * 32 * 128;
+  // per epilogue warp: two staging blocks of 32 rows x 64 columns of bf16,
+  // 128-byte swizzled, each the source of one TMA store; chunk c of a tile
+  // is written to block c % 2 while the store of chunk c - 1 reads the other
+  static constexpr int EPI_SMEM_BYTES = 2 * 4 * 32 * 128;
+  static_assert((BN / 64) % 2 == 0, "an even chunk count keeps the alternation across tiles");
   static constexpr int NUM_ACC = 2;
   static constexpr int ACC_COLS = BN;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -339,10 +341,10 @@ struct WgradCfg {
 #pragma unroll
         for (int j = 0; j < 32; ++j) pk[j] = 0u;
       }
-      // the previous store has finished reading the staging block
-      if (lane == 0) bulk_wait_read0();
+      // the store that last read this block (two chunks back) has finished
+      if (lane == 0) bulk_wait_read1();
       __syncwarp();
-      uint8_t* blk = epi;
+      uint8_t* blk = epi + (cp & 1) * (32 * 128);
       uint8_t* row = blk + lane * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
@@ -481,7 +483,10 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
 
 mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
                         int G, int M, int N, void* dw, cudaStream_t st) {
-  if (N % 256 == 0) return wgrad_bn<256>(pm, qn, rows, offsets, G, M, N, dw, st);
+  // 256-wide tiles unless their shared memory (which grows with the
+  // number of groups) does not fit
+  if (N % 256 == 0 && gemm_smem_bytes<WgradCfg<256>>(offsets ? G : 1) <= 227 * 1024)
+    return wgrad_bn<256>(pm, qn, rows, offsets, G, M, N, dw, st);
   return wgrad_bn<128>(pm, qn, rows, offsets, G, M, N, dw, st);
 }
 

@@ -161,12 +161,12 @@ struct TileWalker {
   }
 };
 
-// Shared memory: [STAGES x STAGE_BYTES][1 KB barriers and flags]
-// [EPI_SMEM_BYTES epilogue staging, 1 KB aligned][tile starts, G + 1 ints].
+// Shared memory: [STAGES x STAGE_BYTES][EPI_SMEM_BYTES epilogue staging,
+// 1 KB aligned][256 B barriers and flags][tile starts, G + 1 ints].
 template <class Cfg>
 constexpr size_t gemm_smem_bytes(int G) {
-  return 1024 /*alignment slack*/ + static_cast<size_t>(Cfg::STAGES) * Cfg::STAGE_BYTES +
-         1024 /*barriers and flags*/ + Cfg::EPI_SMEM_BYTES + static_cast<size_t>(G + 1) * sizeof(int);
+  return 1024 /*alignment slack*/ + static_cast<size_t>(Cfg::STAGES) * Cfg::STAGE_BYTES + Cfg::EPI_SMEM_BYTES +
+         256 /*barriers and flags*/ + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 // Cfg interface:
@@ -188,7 +188,9 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  static_assert((2 * Cfg::STAGES + 5) * sizeof(uint64_t) + 3 * sizeof(uint32_t) <= 256, "barrier area");
+  uint8_t* epi_smem = smem + Cfg::STAGES * Cfg::STAGE_BYTES;  // 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + Cfg::EPI_SMEM_BYTES);
   uint64_t* empty = full + Cfg::STAGES;
   uint64_t* tfull = empty + Cfg::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -196,8 +198,7 @@ __global__ void __launch_bounds__(256, 1) gemm_persistent(const __grid_constant_
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
-  uint8_t* epi_smem = smem + Cfg::STAGES * Cfg::STAGE_BYTES + 1024;
-  int* tstart = reinterpret_cast<int*>(epi_smem + Cfg::EPI_SMEM_BYTES);
+  int* tstart = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;

@@ -53,7 +53,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=30)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="dsv3_bf16_fwd")
-    p.add_argument("--cpu-sample-tokens", type=int, default=48)
+    p.add_argument("--cpu-sample-tokens", type=int, default=160)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk-rows", type=int, default=0,
                    help="BF16 forward: gather through a ring of chunks of this many routed rows "

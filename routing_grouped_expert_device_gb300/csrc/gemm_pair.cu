@@ -843,6 +843,292 @@ mok_status launch_upgate_pair_t(const void* A, int64_t a_rows, const void* w_gat
   return MOK_OK;
 }
 
+// Routed down projection with the routed rows as the MMA's N dimension
+// (as the transposed up/gate above): CTA r holds rows d0 + 128 r .. + 127 of
+// W_down as A and half of the tile's N routed rows of a as B; its
+// accumulator lane d holds y[row][d0 + 128 r + d] for every routed row of
+// the tile.  Epilogue warps of lane quarters 0, 1 and 2, 3 fill the two
+// [32 rows][64 columns] boxes of each 32-row chunk, and one thread stores
+// both.  The shared expert's down tiles (the schedule's extra group, its
+// T rows in tiles of 256) run in the same launch.
+struct PairTDownParams {
+  SchedArgs sched;  // bm = 256 routed rows, n_tiles = D / 256
+  int* status;
+  CUtensorMap tmW, tmA, tmOut;     // W_down [G * D][I], a [rows][I] (boxes 128 x 64), y [rows][D]
+  CUtensorMap tmWs, tmAs, tmOut_s;  // the extra group: W_sd [D][I_s], a_s [T][I_s], ys [T][D]
+  __nv_bfloat16* out;
+  __nv_bfloat16* out_s;
+  int32_t D;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    gemm_pair_down_t(const __grid_constant__ PairTDownParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* ostage = smem + STAGES * STAGE_BYTES;  // two boxes, 1024-byte aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(ostage + 2 * T_OUT_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
+  int* tstart = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 1024);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 256);  // both CTAs' 128 epilogue threads
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) tmem_alloc2(tmem_holder, 512);
+  if (warp == 3) {
+    const int total = build_tile_table(P.sched, tstart, lane);
+    if (lane == 0) *total_holder = total;
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *total_holder;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int i = 0; i < STAGES; ++i) issued[i] = false;
+      bool ok = true;
+      TileWalker walk(P.sched, tstart);
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        const TileCoord c = walk.at(tile);
+        const int wrow = c.g * P.D + c.nt * 256 + static_cast<int>(rank) * 128;  // this CTA's W_down rows
+        const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
+        const CUtensorMap* tmW = c.extra ? &P.tmWs : &P.tmW;
+        const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
+          const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
+          uint8_t* st = smem + stage * STAGE_BYTES;
+#pragma unroll
+          for (int j = 0; j < BK / BOX_K; ++j) {
+            const int kx = kb * BK + j * BOX_K;
+            tma_load_2d_pair(st + j * BOX_BYTES, tmW, kx, wrow, lbar);
+            tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, tmA, kx, xrow, lbar);
+          }
+          issued[stage] = true;
+          issued_parity[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok && leader) {
+        for (int i = 0; i < STAGES; ++i) {
+          if (!issued[i]) continue;
+          const uint64_t t0 = globaltimer();
+          while (!mbar_try_wait(&full[i], issued_parity[i]) && globaltimer() - t0 < kWaitBudgetNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader only) ----------------
+    if (leader) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true, any = false;
+      int it = 0;
+      TileWalker walk(P.sched, tstart);
+      for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
+        const TileCoord c = walk.at(tile);
+        const uint32_t acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        const uint32_t idesc = idesc_bf16(256, t_ncols(c), false, false);
+        ok = __all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, P.status, SITE_MMA));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * 256;
+        for (int kb = 0; kb < c.kblocks; ++kb) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t b = a + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint32_t off = (k / (BOX_K / 16)) * BOX_BYTES + (k % (BOX_K / 16)) * 32;
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                  "l"(sdesc_sw128(a + off, 16, 1024)), "l"(sdesc_sw128(b + off, 16, 1024)), "r"(idesc),
+                  "r"(static_cast<uint32_t>((kb | k) != 0))
+                  : "memory");
+            }
+            commit2(&empty[stage], 0x3);
+            any = true;
+          }
+          __syncwarp();
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) commit2(&tfull[acc], 0x3);
+        __syncwarp();
+      }
+      any = __shfl_sync(0xffffffffu, any, 0);
+      if (any) {
+        if (lane == 0) commit2(drain, 0x1);
+        __syncwarp();
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitBudgetNs) {
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int ew = warp - 4;                     // TMEM lane quarter: columns 32 ew .. of the CTA's 128
+    uint8_t* box = ostage + (ew >> 1) * T_OUT_BYTES;  // quarters 0, 1: box 0; 2, 3: box 1
+    const bool issuer = ew == 2 && lane == 0;    // issues (and waits for) the TMA stores
+    int it = 0;
+    TileWalker walk(P.sched, tstart);
+    for (int tile = cid; tile < total; tile += ncl, ++it) {
+      const TileCoord c = walk.at(tile);
+      const uint32_t acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, P.status, SITE_EPILOGUE));
+      ok = named_bar_and(1, 128, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * 256 + (static_cast<uint32_t>(ew * 32) << 16);
+      const int n = t_ncols(c);
+      const int nrows = min(c.rows - c.mt * 256, 256);
+      const int row0 = c.row0 + c.mt * 256;  // the tile's first row of y (of ys for the extra group)
+      const int dcol = c.nt * 256 + static_cast<int>(rank) * 128;
+      const CUtensorMap* tmOut = c.extra ? &P.tmOut_s : &P.tmOut;
+      __nv_bfloat16* outp = c.extra ? P.out_s : P.out;
+#pragma unroll 1
+      for (int ch = 0; ch * 32 < n; ++ch) {
+        const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
+        uint32_t v[32];
+        tmem_ld32(taddr + ch * 32, v);
+        tmem_ld_wait();
+        if (issuer && nv == 32) bulk_wait_read0();  // the previous stores have read the boxes
+        named_bar(1, 128);
+        if (nv == 32) {
+          // row j, column 32 (ew & 1) + lane of the box (128-byte swizzle);
+          // lanes pair up so that each store writes two neighbouring columns
+          const bool odd = lane & 1;
+          const int c2 = 32 * (ew & 1) + (lane & ~1);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? v[j] : v[j + 1]), 1);
+            const int r = odd ? j + 1 : j;
+            const uint32_t w = odd ? pack_bf16x2(recv, __uint_as_float(v[j + 1]))
+                                   : pack_bf16x2(__uint_as_float(v[j]), recv);
+            st_shared_b32(box + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2, w);
+          }
+          fence_proxy_async_smem();
+        } else {
+          __nv_bfloat16* o = outp + static_cast<size_t>(row0 + ch * 32) * P.D + dcol + 32 * ew + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) o[static_cast<size_t>(j) * P.D] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+        named_bar(1, 128);  // both boxes written
+        if (issuer && nv == 32) {
+          tma_store_2d(tmOut, ostage, dcol, row0 + ch * 32);
+          tma_store_2d(tmOut, ostage + T_OUT_BYTES, dcol + 64, row0 + ch * 32);
+          bulk_commit();
+        }
+      }
+      tc_fence_before();
+      if (leader) mbar_arrive(&tempty[acc]);
+      else remote_arrive(map_to_rank(smem_u32(&tempty[acc]), 0));
+    }
+    if (issuer) bulk_wait0();  // the stores have landed before the CTA exits
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();  // the leader's MMAs (which read the peer's shared memory) and all remote arrivals are done
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc2(tmem_base, 512);
+}
+
+size_t pair_t_down_smem_bytes(int G) {
+  return 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 2 * T_OUT_BYTES + 1024 +
+         static_cast<size_t>(G + 1) * sizeof(int);
+}
+
+mok_status launch_down_pair_t(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
+                              int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
+                              const SharedOperands* sh) {
+  PairTDownParams P{};
+  P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const uint64_t arows = a_rows > 0 ? a_rows : 1;
+  if (!make_tmap_2d(&P.tmA, a, kBF16, arows, I, static_cast<uint64_t>(I) * 2, 128, BOX_K, true) ||
+      !make_tmap_2d(&P.tmW, w_down, kBF16, static_cast<uint64_t>(G) * D, I, static_cast<uint64_t>(I) * 2, 128,
+                    BOX_K, true))
+    return MOK_ERR_CUDA;
+  const bool routed = m_total > 0 && y_out;
+  if (routed && !out_map(&P.tmOut, y_out, m_total, D)) return MOK_ERR_CUDA;
+  P.out = static_cast<__nv_bfloat16*>(y_out);
+  P.D = D;
+  P.tmWs = P.tmW;
+  P.tmAs = P.tmA;
+  P.out_s = nullptr;
+  if (sh && sh->rows > 0) {
+    const int Is = sh->inner;
+    if (!make_tmap_2d(&P.tmAs, sh->A, kBF16, sh->rows, Is, static_cast<uint64_t>(Is) * 2, 128, BOX_K, true) ||
+        !make_tmap_2d(&P.tmWs, sh->w0, kBF16, D, Is, static_cast<uint64_t>(Is) * 2, 128, BOX_K, true) ||
+        !out_map(&P.tmOut_s, sh->out, sh->rows, D))
+      return MOK_ERR_CUDA;
+    P.sched.extra_rows = static_cast<int32_t>(sh->rows);
+    P.sched.extra_n_tiles = D / 256;
+    P.sched.extra_k_blocks = Is / BK;
+    P.out_s = static_cast<__nv_bfloat16*>(sh->out);
+    if (!routed) P.tmOut = P.tmOut_s;
+  } else {
+    if (!routed) return MOK_OK;
+    P.tmOut_s = P.tmOut;
+  }
+  const size_t smem = pair_t_down_smem_bytes(P.sched.G);
+  if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(gemm_pair_down_t, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                          static_cast<int>(smem)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  gemm_pair_down_t<<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
 }  // namespace
 
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
@@ -898,6 +1184,10 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
                             const SharedOperands* sh) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
+  // routed groups of fewer than 512 rows on average: the transposed kernel
+  // (no padding rows in the MMAs), as for the up/gate
+  if (offsets && m_total < static_cast<int64_t>(512) * G)
+    return launch_down_pair_t(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st, sh);
   PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);
   P.status = status_ptr();

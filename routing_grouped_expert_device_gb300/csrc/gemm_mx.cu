@@ -64,8 +64,8 @@ constexpr int THREADS = 128 + EPI_WARPS * 32;
 // Block-scaled instruction descriptor, kind::mxf8f6f4: B scale id (bits
 // 4-5), A and B format E4M3 = 0 (7-9, 10-12), both K-major, N >> 3 (17-22),
 // scale format UE8M0 (23), M >> 4 (24-28), A scale id (29-30).
-__device__ __forceinline__ uint32_t idesc_mx(uint32_t sf_id) {
-  return (sf_id << 4) | ((256u >> 3) << 17) | (1u << 23) | ((256u >> 4) << 24) | (sf_id << 29);
+__device__ __forceinline__ uint32_t idesc_mx(uint32_t sf_id, uint32_t n = 256) {
+  return (sf_id << 4) | ((n >> 3) << 17) | (1u << 23) | ((256u >> 4) << 24) | (sf_id << 29);
 }
 
 __device__ __forceinline__ void mma_mx2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -110,9 +110,16 @@ struct MxParams {
   CUtensorMap tmO0, tmO1;
 };
 
-template <bool kSwiglu, bool kReplay = false>
+// kT (down form only): the routed rows are the MMA's N dimension.  A is 128
+// weight rows per CTA (B0's rows, scale block of those rows), B is half of
+// the tile's N routed rows per CTA, and B's scales are the two grouped
+// 128-row blocks of the tile (every CTA copies both); N = the tile's rows
+// rounded up to 16, so the padding rows of a group's last tile cost no MMA
+// work.  The epilogue transposes each 32-row chunk into two boxes.
+template <bool kSwiglu, bool kReplay = false, bool kT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
+  static_assert(!kT || (!kSwiglu && !kReplay), "transposed form: down only");
   constexpr bool kBf16Out = !kSwiglu || kReplay;
   constexpr int STAGES = mx_stages(kBf16Out);
   extern __shared__ uint8_t smem_raw[];
@@ -185,11 +192,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
           uint8_t* st = smem + stage * CODE_BYTES;
           uint8_t* sf = sf_smem + stage * SF_BYTES;
-          tma_load_2d_pair(st, &P.tmA, kb * BKB, arow, lbar);
-          tma_load_2d_pair(st + A_BYTES, tmB, kb * BKB, brow, lbar);
-          tma_load_2d_pair(sf, &P.tmSA, sfrow, kb, lbar);
-          tma_load_2d_pair(sf + SF_BLOCK, &P.tmSB0, brow0, kb, lbar);
-          tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSB1, brow0 + P.b1_off, kb, lbar);
+          if (kT) {
+            const int wrow = brow0 + static_cast<int>(rank) * 128;  // this CTA's weight rows (A)
+            const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
+            const int gb = static_cast<int>(mx_group_row0(c.row0, c.g)) + c.mt * 256;  // the tile's scale blocks
+            tma_load_2d_pair(st, &P.tmB0, kb * BKB, wrow, lbar);
+            tma_load_2d_pair(st + A_BYTES, &P.tmA, kb * BKB, xrow, lbar);
+            tma_load_2d_pair(sf, &P.tmSB0, wrow, kb, lbar);
+            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kb, lbar);
+            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kb, lbar);
+          } else {
+            tma_load_2d_pair(st, &P.tmA, kb * BKB, arow, lbar);
+            tma_load_2d_pair(st + A_BYTES, tmB, kb * BKB, brow, lbar);
+            tma_load_2d_pair(sf, &P.tmSA, sfrow, kb, lbar);
+            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSB0, brow0, kb, lbar);
+            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSB1, brow0 + P.b1_off, kb, lbar);
+          }
           issued[stage] = true;
           issued_parity[stage] = phase;
           if (++stage == STAGES) {
@@ -216,6 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       TileWalker walk(P.sched, tstart);
       for (int tile = cid; tile < total && ok; tile += ncl, ++it) {
         const TileCoord c = walk.at(tile);
+        const uint32_t ncols = kT ? static_cast<uint32_t>(t_ncols(c)) : 256u;
         ok = __all_sync(0xffffffffu, mbar_wait(tempty, (it & 1) ^ 1, abort_flag, P.status, SITE_MMA));
         if (!ok) break;
         tc_fence_after();
@@ -234,7 +253,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_mx2(tmem_base, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024),
-                      idesc_mx(k), sft, sft + 4, (kb | k) != 0);
+                      idesc_mx(k, ncols), sft, sft + 4, (kb | k) != 0);
             commit2(&empty[stage], 0x3);
             any = true;
           }
@@ -257,6 +276,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     }
+  } else if (kT && warp >= 4) {
+    // ---------------- epilogue, transposed form (both CTAs) ----------------
+    // Warp 4 + 4 h + q: TMEM lane quarter q (output columns 32 q .. of the
+    // CTA's 128), accumulator columns (routed rows) [128 h, 128 h + 128).
+    // Half h stages its up to four 32-row chunks in boxes of its own (two
+    // [32 rows][64 columns] boxes per chunk: quarters 0, 1 fill the first,
+    // 2, 3 the second), releases the accumulator once they are written and
+    // then stores them, so the next tile's MMAs overlap the stores.  The
+    // half's four warps meet at named barrier 1 + h twice per tile; all
+    // eight first combine their accumulator waits at barrier 3.
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    uint8_t* hstage = staging + half * (4 * 2 * 4096);
+    const bool issuer = q == 2 && lane == 0;  // issues (and waits for) this half's TMA stores
+    const uint32_t bar = 1 + half;
+    int it = 0;
+    TileWalker walk(P.sched, tstart);
+    for (int tile = cid; tile < total; tile += ncl, ++it) {
+      const TileCoord c = walk.at(tile);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(tfull, it & 1, abort_flag, P.status, SITE_EPILOGUE));
+      ok = named_bar_and(3, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const int nrows = min(c.rows - c.mt * 256, 256);
+      const int row0 = c.row0 + c.mt * 256;
+      const int dcol = c.nt * P.b_tile_rows + static_cast<int>(rank) * 128;
+      const int ch0 = 4 * half;
+      const int ch_end = min((t_ncols(c) + 31) / 32, ch0 + 4);
+      if (issuer) bulk_wait_read0();  // the previous tile's stores have read the boxes
+      named_bar(bar, 128);
+#pragma unroll 1
+      for (int ch = ch0; ch < ch_end; ++ch) {
+        const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
+        uint32_t v[32];
+        tmem_ld32(taddr + ch * 32, v);
+        tmem_ld_wait();
+        if (nv == 32) {
+          // row j, column 32 (q & 1) + lane of the box (128-byte swizzle);
+          // lanes pair up so that each store writes two neighbouring columns
+          uint8_t* box = hstage + (ch - ch0) * 8192 + (q >> 1) * 4096;
+          const bool odd = lane & 1;
+          const int c2 = 32 * (q & 1) + (lane & ~1);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? v[j] : v[j + 1]), 1);
+            const int r = odd ? j + 1 : j;
+            const uint32_t w = odd ? pack_bf16x2(recv, __uint_as_float(v[j + 1]))
+                                   : pack_bf16x2(__uint_as_float(v[j]), recv);
+            st_shared_b32(box + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2, w);
+          }
+        } else {
+          __nv_bfloat16* o = P.y + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) o[static_cast<int64_t>(j) * P.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      if (leader) mbar_arrive(tempty);  // the accumulator is free for the next tile
+      else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+      named_bar(bar, 128);  // every box of the half written
+      if (issuer) {
+        for (int ch = ch0; ch < ch_end; ++ch) {
+          if (nrows - ch * 32 < 32) continue;  // written row by row above
+          uint8_t* boxes = hstage + (ch - ch0) * 8192;
+          tma_store_2d(&P.tmO0, boxes, dcol, row0 + ch * 32);
+          tma_store_2d(&P.tmO0, boxes + 4096, dcol + 64, row0 + ch * 32);
+        }
+        bulk_commit();
+      }
+    }
+    if (issuer) bulk_wait0();  // this half's stores have landed before the CTA exits
+    __syncwarp();
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
     const int q = warp & 3;             // TMEM lane quarter of this warp
@@ -385,11 +479,11 @@ size_t mx_smem_bytes(int G, bool bf16_out) {
          (bf16_out ? STAGING_BYTES : 0) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
-template <bool kSwiglu, bool kReplay = false>
+template <bool kSwiglu, bool kReplay = false, bool kT = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st) {
   const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay>;
+  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
@@ -509,6 +603,9 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   P.out_ld = D;
   if (!out_map(&P.tmO0, y, rows, D)) return MOK_ERR_CUDA;
   P.tmO1 = P.tmO0;
+  // fewer than 512 routed rows per group on average: the routed rows as the
+  // MMA's N dimension (no padding rows in the MMAs)
+  if (rows < static_cast<int64_t>(512) * G) return run_mx<false, false, true>(P, st);
   return run_mx<false>(P, st);
 }
 

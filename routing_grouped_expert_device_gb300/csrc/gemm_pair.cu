@@ -558,31 +558,6 @@ struct PairTParams {
 constexpr int T_OUT_BYTES = 32 * 128;       // one [32 rows][64 columns] bf16 box of a
 constexpr int T_XBUF_BYTES = 2 * 32 * 32 * 4;  // u of two warps for one 32-column chunk, fp32
 
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-// AND of p over the n threads of named barrier id (all of them must call it).
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool p) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "bar.red.and.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void st_shared_b32(void* p, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-
-// N of a tile: its routed rows (at most 256) rounded up to 16.
-__device__ __forceinline__ int t_ncols(const TileCoord& c) {
-  const int n = min(c.rows - c.mt * 256, 256);
-  return (n + 15) & ~15;
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_upgate_t(const __grid_constant__ PairTParams P) {

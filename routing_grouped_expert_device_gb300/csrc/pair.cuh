@@ -2,6 +2,7 @@
 // two SMs, tcgen05 cta_group::2).
 #pragma once
 #include "common.cuh"
+#include "gemm_core.cuh"  // TileCoord
 
 namespace mok {
 
@@ -64,6 +65,35 @@ __device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
 __device__ __forceinline__ void tmem_cp_block2(uint32_t taddr, uint32_t saddr) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc_rows16(saddr))
                : "memory");
+}
+
+// Named barrier id for n threads (a multiple of 32; every thread of each
+// participating warp calls it).
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// AND of p over the n threads of named barrier id (all of them must call it).
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void st_shared_b32(void* p, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+
+// N of a tile whose routed rows are the MMA's N dimension: the tile's rows
+// (at most 256) rounded up to 16.
+__device__ __forceinline__ int t_ncols(const TileCoord& c) {
+  const int n = min(c.rows - c.mt * 256, 256);
+  return (n + 15) & ~15;
 }
 
 }  // namespace mok

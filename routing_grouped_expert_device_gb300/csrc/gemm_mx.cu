@@ -110,16 +110,19 @@ struct MxParams {
   CUtensorMap tmO0, tmO1;
 };
 
-// kT (down form only): the routed rows are the MMA's N dimension.  A is 128
-// weight rows per CTA (B0's rows, scale block of those rows), B is half of
-// the tile's N routed rows per CTA, and B's scales are the two grouped
-// 128-row blocks of the tile (every CTA copies both); N = the tile's rows
-// rounded up to 16, so the padding rows of a group's last tile cost no MMA
-// work.  The epilogue transposes each 32-row chunk into two boxes.
+// kT (the forms with bf16 outputs: down, replay): the routed rows are the
+// MMA's N dimension.  A is 128 weight rows per CTA with the scale block of
+// those rows (down: rows 128 r .. of the tile's 256 W_down rows; replay:
+// the tile's 128 W_gate rows in CTA 0 and the same W_up rows in CTA 1, so
+// CTA 0 produces h and CTA 1 u), B is half of the tile's N routed rows per
+// CTA, and B's scales are the two grouped 128-row blocks of the tile (every
+// CTA copies both); N = the tile's rows rounded up to 16, so the padding
+// rows of a group's last tile cost no MMA work.  The epilogue transposes
+// each 32-row chunk into two boxes.
 template <bool kSwiglu, bool kReplay = false, bool kT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
-  static_assert(!kT || (!kSwiglu && !kReplay), "transposed form: down only");
+  static_assert(!kT || !kSwiglu || kReplay, "transposed form: bf16 outputs only");
   constexpr bool kBf16Out = !kSwiglu || kReplay;
   constexpr int STAGES = mx_stages(kBf16Out);
   extern __shared__ uint8_t smem_raw[];
@@ -193,12 +196,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           uint8_t* st = smem + stage * CODE_BYTES;
           uint8_t* sf = sf_smem + stage * SF_BYTES;
           if (kT) {
-            const int wrow = brow0 + static_cast<int>(rank) * 128;  // this CTA's weight rows (A)
+            // this CTA's weight rows (A): down rows 128 r .. of the tile, replay
+            // the tile's rows of W_gate (CTA 0) or W_up (CTA 1)
+            const int wrow = brow0 + (kReplay ? 0 : static_cast<int>(rank) * 128);
             const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
             const int gb = static_cast<int>(mx_group_row0(c.row0, c.g)) + c.mt * 256;  // the tile's scale blocks
-            tma_load_2d_pair(st, &P.tmB0, kb * BKB, wrow, lbar);
+            tma_load_2d_pair(st, kReplay ? tmB : &P.tmB0, kb * BKB, wrow, lbar);
             tma_load_2d_pair(st + A_BYTES, &P.tmA, kb * BKB, xrow, lbar);
-            tma_load_2d_pair(sf, &P.tmSB0, wrow, kb, lbar);
+            tma_load_2d_pair(sf, kReplay && rank ? &P.tmSB1 : &P.tmSB0, wrow, kb, lbar);
             tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kb, lbar);
             tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kb, lbar);
           } else {
@@ -302,7 +307,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const int nrows = min(c.rows - c.mt * 256, 256);
       const int row0 = c.row0 + c.mt * 256;
-      const int dcol = c.nt * P.b_tile_rows + static_cast<int>(rank) * 128;
+      // first output column of this CTA; the replay's CTA 1 writes u, CTA 0 h
+      const int dcol = c.nt * P.b_tile_rows + (kReplay ? 0 : static_cast<int>(rank) * 128);
+      const CUtensorMap* tmOut = kReplay && rank ? &P.tmO1 : &P.tmO0;
+      __nv_bfloat16* outp = kReplay ? (rank ? P.u_out : P.h_out) : P.y;
       const int ch0 = 4 * half;
       const int ch_end = min((t_ncols(c) + 31) / 32, ch0 + 4);
       if (issuer) bulk_wait_read0();  // the previous tile's stores have read the boxes
@@ -328,7 +336,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             st_shared_b32(box + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2, w);
           }
         } else {
-          __nv_bfloat16* o = P.y + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
+          __nv_bfloat16* o = outp + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (j < nv) o[static_cast<int64_t>(j) * P.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
@@ -343,8 +351,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int ch = ch0; ch < ch_end; ++ch) {
           if (nrows - ch * 32 < 32) continue;  // written row by row above
           uint8_t* boxes = hstage + (ch - ch0) * 8192;
-          tma_store_2d(&P.tmO0, boxes, dcol, row0 + ch * 32);
-          tma_store_2d(&P.tmO0, boxes + 4096, dcol + 64, row0 + ch * 32);
+          tma_store_2d(tmOut, boxes, dcol, row0 + ch * 32);
+          tma_store_2d(tmOut, boxes + 4096, dcol + 64, row0 + ch * 32);
         }
         bulk_commit();
       }
@@ -573,6 +581,8 @@ mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const
   P.h_out = static_cast<__nv_bfloat16*>(h);
   P.u_out = static_cast<__nv_bfloat16*>(u);
   if (!out_map(&P.tmO0, h, rows, I) || !out_map(&P.tmO1, u, rows, I)) return MOK_ERR_CUDA;
+  // as the down form: the routed rows as N for groups under 512 rows on average
+  if (rows < static_cast<int64_t>(512) * G) return run_mx<true, true, true>(P, st);
   return run_mx<true, true>(P, st);
 }
 

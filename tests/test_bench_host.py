@@ -1,0 +1,43 @@
+"""Host logic of bench.py that decides what the JSON line reports, on CPU.
+
+The roofline's `traffic` comes from a committed ncu record only while the
+record was taken on the current kernel sources and on the bench's workload;
+otherwise it is null."""
+import importlib.util
+import os
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_host_mod", os.path.join(ROOT, "bench.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    return b
+
+
+def _record(path, sha, workload, nbytes):
+    with open(path, "w") as f:
+        f.write(f"kernel: test\nworkload: {workload}\nsource_sha256: {sha}\n"
+                f"dram_bytes_per_launch: {nbytes}\nderivation: test\n")
+
+
+def test_traffic_reported_only_for_current_sources_and_workload(tmp_path):
+    b = _bench()
+    path = str(tmp_path / "traffic.txt")
+    b.TRAFFIC_FILE = path
+    assert b.recorded_traffic("dsv3_bf16_fwd") is None  # no record
+    sha = b.source_hash()
+    _record(path, sha, "dsv3_bf16_fwd", 16209799168)
+    assert b.recorded_traffic("dsv3_bf16_fwd") == 16209799168.0
+    assert b.recorded_traffic("dsv3_mxfp8_fwd") is None  # another workload
+    _record(path, "0" * 16, "dsv3_bf16_fwd", 16209799168)
+    assert b.recorded_traffic("dsv3_bf16_fwd") is None  # taken on other sources
+
+
+def test_source_hash_covers_the_up_gate_kernel_sources():
+    b = _bench()
+    assert "gemm_pair.cu" in b.KERNEL_SOURCES and "pair.cuh" in b.KERNEL_SOURCES
+    h = b.source_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+    assert b.source_hash() == h  # deterministic

@@ -41,3 +41,37 @@ def test_source_hash_covers_the_up_gate_kernel_sources():
     h = b.source_hash()
     assert len(h) == 16 and int(h, 16) >= 0
     assert b.source_hash() == h  # deterministic
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampled(b, tmp_path, lines):
+    cs = b.ClockSampler(0)
+    cs.proc = _DoneProc()
+    cs.path = str(tmp_path / "clocks.csv")
+    with open(cs.path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    return cs.stop()
+
+
+def test_clock_samples_median_and_throttle_reasons(tmp_path):
+    """The clocks key: median SM clock under load, the maximum, and every
+    throttle reason seen active in any sample (nvidia-smi csv, no units)."""
+    b = _bench()
+    na = "Not Active"
+    got = _sampled(b, tmp_path, [
+        f"0, 2070, 2070, 900.5, 0x0000000000000000, {na}, {na}, {na}, {na}",
+        f"0, 1500, 2070, 1400.2, 0x0000000000000004, {na}, {na}, {na}, Active",
+        f"0, 1400, 2070, 1398.0, 0x0000000000000004, {na}, {na}, {na}, Active",
+        f"0, [N/A], [N/A], [N/A], [N/A], {na}, {na}, {na}, {na}",
+    ])
+    assert got == {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0, "samples": 4, "reasons": ["sw_power_cap"]}
+    got = _sampled(b, tmp_path, [f"0, 1200, 2070, 700.0, 0x0000000000000048, {na}, Active, {na}, {na}"])
+    assert got["reasons"] == ["hw_thermal_slowdown"]  # a run the timing rules reject
+    assert _sampled(b, tmp_path, ["garbage"]) is None

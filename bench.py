@@ -593,12 +593,14 @@ def run_reference(args, world, rank, local):
 
 def main():
     args = parse_args()
+    if args.impl == "reference":
+        # the oracle runs on the host cores: rank 0 alone, no process group
+        env = lambda k: int(os.environ.get(k, "0"))
+        run_reference(args, max(1, env("WORLD_SIZE")), env("RANK"), env("LOCAL_RANK"))
+        return
     world, rank, local = dist_setup(args.gpus)
     try:
-        if args.impl == "reference":
-            run_reference(args, world, rank, local)
-        else:
-            run_ours(args, world, rank, local)
+        run_ours(args, world, rank, local)
     finally:
         if world > 1:
             import torch.distributed as dist

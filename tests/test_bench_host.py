@@ -75,3 +75,32 @@ def test_clock_samples_median_and_throttle_reasons(tmp_path):
     got = _sampled(b, tmp_path, [f"0, 1200, 2070, 700.0, 0x0000000000000048, {na}, Active, {na}, {na}"])
     assert got["reasons"] == ["hw_thermal_slowdown"]  # a run the timing rules reject
     assert _sampled(b, tmp_path, ["garbage"]) is None
+
+
+def _run_reference(env_extra):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_line_on_host_cores():
+    """bench.py --impl reference times the oracle on the host: one JSON line
+    with the contract's keys, its own e2e (no copies) and cpu_baseline."""
+    (line,) = _run_reference({"WORLD_SIZE": "1", "RANK": "0"})
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["steps"] == 3 and line["warmup"] == 3 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny"
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    assert _run_reference({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}) == []

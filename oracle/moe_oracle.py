@@ -51,8 +51,8 @@ __all__ = [
     "silu", "softmax_rows", "router_scores", "route", "pull_schedule", "plan", "gather",
     "expert_ffn_rows", "expert_ffn", "shared_ffn", "combine", "moe_forward",
     "HostWeights", "moe_forward_tokens",
-    "route_backward_rows", "moe_backward", "router_grad", "router_grad_slack",
-    "e4m3_code_values", "e4m3_encode", "mx_scale_exponent", "mxfp8_quantize",
+    "route_backward_rows", "rounding_ranges", "sum_range", "moe_backward", "moe_backward_tokens", "router_grad",
+    "e4m3_code_values", "e4m3_encode", "e4m3_round", "mx_scale_exponent", "mxfp8_quantize",
     "mxfp8_dequantize", "expert_ffn_rows_mxfp8", "moe_forward_mxfp8",
     "mxfp8_roundtrip", "route_backward_rows_mxfp8", "moe_backward_mxfp8",
 ]
@@ -335,10 +335,14 @@ class HostWeights:
 
 
 def moe_forward_tokens(tokens: Sequence[int], x_rows, s_rows, weights: HostWeights, K: int,
-                       num: Numerics = FP32):
+                       num: Numerics = FP32, mxfp8: bool = False, map_fn: Callable = map):
     """The forward for a sample of tokens, one route at a time (routing is
-    per token, so the sampled rows need no other token).  Returns
-    topk_idx, g, per-route a [n][K][I], y [n][K][D], ys and out [n][D]."""
+    per token, so the sampled rows need no other token).  mxfp8: the routed
+    experts as expert_ffn_rows_mxfp8 (x quantised per token row, so a
+    sampled row is quantised as in the whole layer); the shared expert stays
+    BF16.  map_fn maps the per-expert evaluations (e.g. a thread pool's map;
+    the arithmetic is the same).  Returns topk_idx, g, per-route
+    a [n][K][I], y [n][K][D], ys and out [n][D]."""
     n = len(tokens)
     topk_idx, g, _ = route(s_rows, K, num)
     X = num.w(x_rows)
@@ -346,11 +350,18 @@ def moe_forward_tokens(tokens: Sequence[int], x_rows, s_rows, weights: HostWeigh
     for j in range(n):
         for k in range(K):
             by_expert.setdefault(int(topk_idx[j, k]), []).append((j, k))
-    a = y = None
-    for e, lst in sorted(by_expert.items()):
+    def one_expert(item):
+        e, lst = item
         Wg, Wu, Wd = weights.fetch(e)
         rows = np.array([j for j, _ in lst])
-        _, _, ae, ye = expert_ffn_rows(X[rows], Wg, Wu, Wd, num)
+        if mxfp8:
+            rr = expert_ffn_rows_mxfp8(X[rows], Wg, Wu, Wd)
+            return rr["a"], rr["y"]
+        return expert_ffn_rows(X[rows], Wg, Wu, Wd, num)[2:]
+
+    items = sorted(by_expert.items())
+    a = y = None
+    for (e, lst), (ae, ye) in zip(items, map_fn(one_expert, items)):
         if a is None:
             a = np.zeros((n, K, ae.shape[1]), dtype=num.dtype)
             y = np.zeros((n, K, ye.shape[1]), dtype=num.dtype)
@@ -370,19 +381,85 @@ def moe_forward_tokens(tokens: Sequence[int], x_rows, s_rows, weights: HostWeigh
 # --------------------------------------------------------------------------
 # backward
 # --------------------------------------------------------------------------
-def route_backward_rows(xrows, dyrows, g, Wg, Wu, Wd, num: Numerics = FP32):
+# Bounds on how far another correct evaluation of the backward's products
+# (a different fp32 summation order: the tensor cores' K-serial accumulation)
+# and of its exponential and division can land from this oracle's, used to
+# mark the bf16 rounding points whose decision the arithmetic does not fix.
+#   products: |delta| <= sqrt(K) 2^-24 sum_k |a_k b_k| (an fp32 sum of K
+#             terms in another order; measured on the GPU: at most 0.18 of it
+#             at K = 512 and K = 7168);
+#   sigma = 1 / (1 + exp(-h)): relative (8 + 1.2 |h|) 2^-24 (fast exponential
+#             and reciprocal on the GPU, libm here);
+#   each further product / sum: 8 ulp relative.
+_U32 = 2.0 ** -24
+
+
+def _bf16_range(v, dv):
+    """bf16 values that rounding v + e, |e| <= dv, can give: (lo, hi) in
+    float32 (equal to round_bf16(v) where the decision is fixed)."""
+    v = np.asarray(v, dtype=np.float64)
+    lo = round_bf16((v - dv).astype(np.float32))
+    hi = round_bf16((v + dv).astype(np.float32))
+    return np.minimum(lo, hi), np.maximum(lo, hi)
+
+
+def rounding_ranges(X, dY, g, Wg, Wu, Wd, h, u, t, a):
+    """For rows of one expert: the admissible bf16 values of dh, du, a and
+    a_g under the bounds above, as (lo, hi) pairs (lo == hi == the oracle's
+    value where the rounding decision is fixed).  All inputs float32 as the
+    oracle computed them (Wd is [D][I])."""
+    f = lambda z: np.asarray(z, dtype=np.float64)
+    X, dY, Wg, Wu, Wd, h, u, t, a = map(f, (X, dY, Wg, Wu, Wd, h, u, t, a))
+    gcol = f(g).reshape(-1, 1)
+    eps = np.sqrt(X.shape[1]) * _U32
+    dh_ = eps * (np.abs(X) @ np.abs(Wg).T)
+    du_ = eps * (np.abs(X) @ np.abs(Wu).T)
+    dt_ = eps * (np.abs(dY) @ np.abs(Wd))
+    sig = 1.0 / (1.0 + np.exp(-h))
+    dsig = sig * (8.0 + 1.2 * np.abs(h)) * _U32
+    silu_v = h * sig
+    dsilu = np.abs(sig * (1.0 + h * (1.0 - sig))) * dh_ + np.abs(h) * dsig
+    a_pre = silu_v * u
+    da_pre = np.abs(u) * dsilu + np.abs(silu_v) * du_ + 8 * _U32 * np.abs(a_pre)
+    sp = sig * (1.0 + h * (1.0 - sig))                       # SiLU'(h)
+    dsp = np.abs(sig * (1.0 - sig) * (2.0 + h * (1.0 - 2.0 * sig))) * dh_ + np.abs(1.0 + h - 2.0 * h * sig) * dsig
+    dh_pre = gcol * t * u * sp
+    ddh = np.abs(gcol) * (np.abs(u * sp) * dt_ + np.abs(t * sp) * du_ + np.abs(t * u) * dsp) + 8 * _U32 * np.abs(dh_pre)
+    du_pre = gcol * t * silu_v
+    ddu = np.abs(gcol) * (np.abs(silu_v) * dt_ + np.abs(t) * dsilu) + 8 * _U32 * np.abs(du_pre)
+    a_lo, a_hi = _bf16_range(a_pre, da_pre)
+    ag_ends = np.stack([gcol * a_lo, gcol * a_hi])
+    ag_lo, _ = _bf16_range(ag_ends.min(0), 8 * _U32 * np.abs(ag_ends).max(0))
+    _, ag_hi = _bf16_range(ag_ends.max(0), 8 * _U32 * np.abs(ag_ends).max(0))
+    return dict(dh=_bf16_range(dh_pre, ddh), du=_bf16_range(du_pre, ddu), a=(a_lo, a_hi), a_g=(ag_lo, ag_hi))
+
+
+def sum_range(vals, rng, other):
+    """Range of bf16(sum_p v[p, i] * other[p, j]) shifts when each v[p, i]
+    may be any bf16 value in [lo, hi] (rng) instead of vals: returns
+    (lo_shift, hi_shift) [I][J] of the fp32 sum before its final rounding."""
+    v = np.asarray(vals, dtype=np.float64)
+    lo = np.asarray(rng[0], dtype=np.float64) - v
+    hi = np.asarray(rng[1], dtype=np.float64) - v
+    o = np.asarray(other, dtype=np.float64)
+    op, on = np.maximum(o, 0.0), np.minimum(o, 0.0)
+    return lo.T @ op + hi.T @ on, hi.T @ op + lo.T @ on
+
+
+def route_backward_rows(xrows, dyrows, g, Wg, Wu, Wd, num: Numerics = FP32, ranges: bool = False):
     """Backward of g * E_i(x) for a batch of rows of one expert.
 
     Recomputes h, u (forward replay), t = W_down^T dY; the router-weight
-    gradient is dg = <t, a> ([note] "The production details": SonicMoE's inner
-    product of the gated activation with the down-projection input gradient;
-    the down-projection output is never formed).  With da = g t and
+    gradient is dg = <t, SiLU(h) u> ([note] "The production details":
+    SonicMoE's inner product of the gated activation with the
+    down-projection input gradient; the down-projection output is never
+    formed), with the gated activation taken unrounded: the pages put no
+    rounding point inside the inner product.  With da = g t and
     SiLU'(h) = sig(h) (1 + h (1 - sig(h))):
         dh = bf16(da * u * SiLU'(h)),  du = bf16(da * SiLU(h)),
-        a_g = bf16(g * a),  dx = bf16(dh W_gate + du W_up).
-    Returns dict(h, u, a, t, dg, dh, du, a_g, dx) and, under the fp32
-    numerics, flip_dh / flip_du / flip_ag: bf16_flip_ulp of each rounding
-    point (a_g also inherits g times the flip of a)."""
+        a = bf16(SiLU(h) u), a_g = bf16(g * a),  dx = bf16(dh W_gate + du W_up).
+    Returns dict(h, u, a, t, dg, dh, du, a_g, dx); ranges (fp32 numerics):
+    also "ranges", rounding_ranges of dh, du, a, a_g."""
     X = num.w(xrows)
     dY = num.w(dyrows)
     gcol = np.asarray(g, dtype=num.dtype).reshape(-1, 1)
@@ -392,41 +469,18 @@ def route_backward_rows(xrows, dyrows, g, Wg, Wu, Wd, num: Numerics = FP32):
     a_pre = silu(h) * u
     a = num.rnd(a_pre).astype(num.dtype)
     t = dY @ Wd_
-    dg = np.sum(t * a, axis=1)
+    dg = np.sum(t * a_pre, axis=1)
     da = gcol * t
     one = num.dtype(1)
     with np.errstate(over="ignore"):
         sig = one / (one + np.exp(-h))
-    dh_pre = da * u * sig * (one + h * (one - sig))
-    du_pre = da * h * sig
-    ag_pre = gcol * a
-    dh = num.rnd(dh_pre).astype(num.dtype)
-    du = num.rnd(du_pre).astype(num.dtype)
-    a_g = num.rnd(ag_pre).astype(num.dtype)
-    dx_pre = dh @ Wg_ + du @ Wu_
-    dx = num.rnd(dx_pre).astype(num.dtype)
+    dh = num.rnd(da * u * sig * (one + h * (one - sig))).astype(num.dtype)
+    du = num.rnd(da * h * sig).astype(num.dtype)
+    a_g = num.rnd(gcol * a).astype(num.dtype)
+    dx = num.rnd(dh @ Wg_ + du @ Wu_).astype(num.dtype)
     out = dict(h=h, u=u, a=a, t=t, dg=dg, dh=dh, du=du, a_g=a_g, dx=dx)
-    if num.round_points:
-        flip_a = bf16_flip_ulp(a_pre)
-        out["flip_dh"] = bf16_flip_ulp(dh_pre)
-        out["flip_du"] = bf16_flip_ulp(du_pre)
-        out["flip_ag"] = bf16_flip_ulp(ag_pre) + np.abs(gcol) * flip_a
-        out["flip_dg"] = np.sum(flip_a * np.abs(t), axis=1)
-        out["flip_dx"] = (bf16_flip_ulp(dx_pre) + out["flip_dh"] @ np.abs(Wg_.astype(np.float64))
-                          + out["flip_du"] @ np.abs(Wu_.astype(np.float64)))
-    return out
-
-
-def router_grad_slack(flip_dg, g, den, topk_idx, E):
-    """Bound on ds from ambiguous roundings inside dg (see router_grad):
-    (flip_dg_k + sum_k' |g_k'| flip_dg_k') / den at the selected experts."""
-    flip_dg = np.asarray(flip_dg, dtype=np.float64)
-    gg = np.abs(np.asarray(g, dtype=np.float64))
-    T, K = gg.shape
-    dot = np.sum(gg * flip_dg, axis=1)
-    out = np.zeros((T, E))
-    val = (flip_dg + dot[:, None]) / np.abs(np.asarray(den, dtype=np.float64))[:, None]
-    np.put_along_axis(out, np.asarray(topk_idx, dtype=np.int64), val, axis=1)
+    if ranges:
+        out["ranges"] = rounding_ranges(X, dY, g, Wg_, Wu_, Wd_, h, u, t, a)
     return out
 
 
@@ -448,8 +502,7 @@ def router_grad(dg, g, den, topk_idx, E, num: Numerics = FP32):
 
 def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
                  fwd: Optional[Dict[str, np.ndarray]] = None,
-                 with_slack: bool = False,
-                 routed_rows: Optional[Callable] = None) -> Dict[str, np.ndarray]:
+                 routed_rows: Optional[Callable] = None, ranges: bool = False) -> Dict[str, np.ndarray]:
     """Gradients of L = <dY, MoE(x, s)> w.r.t. x, every weight and s.
 
     Routing is recomputed (or taken from ``fwd``); gradients do not flow
@@ -459,15 +512,15 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
     the shared expert likewise with g = 1 over all tokens;
     dX[t] = bf16(dx_shared[t] + sum_k dx[route_dst[t,k]]) in k order.
 
-    with_slack (fp32 numerics): also return out["slack"][name], per weight
-    gradient element the sum over rows of |other operand| times the
-    bf16_flip_ulp of the rounded factor (dh, du or a_g): how far another
-    correct evaluation, which may round those ambiguous factors the other
-    way, can land from this one.
-
     routed_rows: the per-expert backward of the routed experts (default
     route_backward_rows; moe_backward_mxfp8 passes the MXFP8 one), called
-    as routed_rows(x_rows, dy_rows, g_rows, W_gate[e], W_up[e], W_down[e])."""
+    as routed_rows(x_rows, dy_rows, g_rows, W_gate[e], W_up[e], W_down[e],
+    ranges=...).
+
+    ranges (fp32 numerics): also out["range"][name] = (lo_shift, hi_shift)
+    of each weight gradient: how far its fp32 sum can move when the dh, du
+    or a_g points whose bf16 rounding the arithmetic does not fix
+    (rounding_ranges) round the other way, term by term (sum_range)."""
     if fwd is None:
         s = inp["s"]
         topk_idx, g, den = route(s, K, num)
@@ -486,14 +539,10 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
     g_route = np.asarray(g, dtype=num.dtype)[src_tok, src_k]
     dx_r = np.zeros((R, D), dtype=num.dtype)
     dg_route = np.zeros(R, dtype=num.dtype)
-    flip_dg_route = np.zeros(R)
-    flip_dx_r = np.zeros((R, D)) if with_slack else None
     dW_gate = np.zeros((E, I, D), dtype=num.dtype)
     dW_up = np.zeros((E, I, D), dtype=num.dtype)
     dW_down = np.zeros((E, D, I), dtype=num.dtype)
-    slack = {}
-    if with_slack:
-        slack = dict(dW_gate=np.zeros((E, I, D)), dW_up=np.zeros((E, I, D)), dW_down=np.zeros((E, D, I)))
+    rng: Dict[str, tuple] = {}
     for e in range(E):
         p0, p1 = int(offsets[e]), int(offsets[e + 1])
         if p0 == p1:
@@ -501,55 +550,96 @@ def moe_backward(inp: Dict[str, np.ndarray], dy, K: int, num: Numerics = FP32,
         rows = src_tok[p0:p1]
         if routed_rows is None:
             b = route_backward_rows(x[rows], dY[rows], g_route[p0:p1],
-                                    inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], num)
+                                    inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], num, ranges=ranges)
         else:
-            b = routed_rows(x[rows], dY[rows], g_route[p0:p1], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+            b = routed_rows(x[rows], dY[rows], g_route[p0:p1], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e],
+                            ranges=ranges)
         dx_r[p0:p1] = b["dx"]
         dg_route[p0:p1] = b["dg"]
         dW_down[e] = num.rnd(dY[rows].T @ b["a_g"])
         dW_gate[e] = num.rnd(b["dh"].T @ x[rows])
         dW_up[e] = num.rnd(b["du"].T @ x[rows])
-        if with_slack:
-            flip_dg_route[p0:p1] = b["flip_dg"]
-            flip_dx_r[p0:p1] = b["flip_dx"]
-            ax, ady = np.abs(x[rows]).astype(np.float64), np.abs(dY[rows]).astype(np.float64)
-            slack["dW_down"][e] = ady.T @ b["flip_ag"]
-            slack["dW_gate"][e] = b["flip_dh"].T @ ax
-            slack["dW_up"][e] = b["flip_du"].T @ ax
+        if ranges:
+            rg = b["ranges"]
+            for name, (lo, hi) in (("dW_down", sum_range(b["a_g"], rg["a_g"], dY[rows])),
+                                   ("dW_gate", sum_range(b["dh"], rg["dh"], x[rows])),
+                                   ("dW_up", sum_range(b["du"], rg["du"], x[rows]))):
+                if name == "dW_down":
+                    lo, hi = lo.T, hi.T
+                rng.setdefault(name, (np.zeros(dW_down.shape if name == "dW_down" else dW_gate.shape),
+                                      np.zeros(dW_down.shape if name == "dW_down" else dW_gate.shape)))
+                rng[name][0][e], rng[name][1][e] = lo, hi
     out = dict(dW_gate=dW_gate, dW_up=dW_up, dW_down=dW_down, dx_r=dx_r)
     acc = np.zeros((T, D), dtype=num.dtype)
-    slack_dx = np.zeros((T, D)) if with_slack else None
     if inp.get("ws_gate") is not None:
         bs = route_backward_rows(x, dY, np.ones(T, dtype=num.dtype),
-                                 inp["ws_gate"], inp["ws_up"], inp["ws_down"], num)
+                                 inp["ws_gate"], inp["ws_up"], inp["ws_down"], num, ranges=ranges)
         acc = bs["dx"].copy()
         out["dWs_down"] = num.rnd(dY.T @ bs["a_g"]).astype(num.dtype)
         out["dWs_gate"] = num.rnd(bs["dh"].T @ x).astype(num.dtype)
         out["dWs_up"] = num.rnd(bs["du"].T @ x).astype(num.dtype)
-        if with_slack:
-            slack_dx += bs["flip_dx"]
-            ax, ady = np.abs(x).astype(np.float64), np.abs(dY).astype(np.float64)
-            slack["dWs_down"] = ady.T @ bs["flip_ag"]
-            slack["dWs_gate"] = bs["flip_dh"].T @ ax
-            slack["dWs_up"] = bs["flip_du"].T @ ax
+        if ranges:
+            rg = bs["ranges"]
+            lo, hi = sum_range(bs["a_g"], rg["a_g"], dY)
+            rng["dWs_down"] = (lo.T, hi.T)
+            rng["dWs_gate"] = sum_range(bs["dh"], rg["dh"], x)
+            rng["dWs_up"] = sum_range(bs["du"], rg["du"], x)
     rd = np.asarray(route_dst).reshape(T, K)
     for k in range(K):
         acc = acc + dx_r[rd[:, k]]
-        if with_slack:
-            slack_dx += flip_dx_r[rd[:, k]]
     out["dX"] = num.rnd(acc).astype(num.dtype)
     dg = np.zeros((T, K), dtype=num.dtype)
     dg[src_tok, src_k] = dg_route
     out["dg"] = dg
     out["ds"] = router_grad(dg, g, den, topk_idx, E, num)
-    if with_slack:
-        fdg = np.zeros((T, K))
-        fdg[src_tok, src_k] = flip_dg_route
-        slack["dX"] = slack_dx + bf16_flip_ulp(acc)
-        slack["dg"] = fdg
-        slack["ds"] = router_grad_slack(fdg, g, den, topk_idx, E)
-        out["slack"] = slack
+    if ranges:
+        for name in ("dW_gate", "dW_up", "dW_down"):
+            rng.setdefault(name, (np.zeros(out[name].shape), np.zeros(out[name].shape)))
+        out["range"] = rng
     return out
+
+
+def moe_backward_tokens(x_rows, dy_rows, s_rows, weights: HostWeights, K: int, mxfp8: bool = False,
+                        map_fn: Callable = map) -> Dict[str, np.ndarray]:
+    """The backward restricted to a sample of tokens: dX rows, dg and ds of
+    those tokens (each depends only on its own routes), the same steps as
+    moe_backward.  Every route of the sample runs route_backward_rows (or
+    route_backward_rows_mxfp8) with its expert's weights, grouped by expert;
+    the shared expert (BF16, g = 1) runs over the sampled rows; then
+    dX = bf16(dx_shared + sum_k dx_k) in k order and ds from dg.  map_fn
+    maps the per-expert evaluations.  Returns dX [n][D], dg [n][K], ds [n][E]."""
+    num = FP32
+    topk_idx, g, den = route(s_rows, K, num)
+    n = topk_idx.shape[0]
+    X = num.w(x_rows)
+    dY = num.w(dy_rows)
+    by_expert: Dict[int, list] = {}
+    for j in range(n):
+        for k in range(K):
+            by_expert.setdefault(int(topk_idx[j, k]), []).append((j, k))
+    rows_fn = route_backward_rows_mxfp8 if mxfp8 else route_backward_rows
+
+    def one_expert(item):
+        e, lst = item
+        rows = np.array([j for j, _ in lst])
+        ks = np.array([k for _, k in lst])
+        b = rows_fn(X[rows], dY[rows], g[rows, ks], *weights.fetch(e))
+        return b["dx"], b["dg"]
+
+    items = sorted(by_expert.items())
+    dx_route = np.zeros((n, K, X.shape[1]), dtype=np.float32)
+    dg = np.zeros((n, K), dtype=np.float32)
+    for (e, lst), (dxe, dge) in zip(items, map_fn(one_expert, items)):
+        for q, (j, k) in enumerate(lst):
+            dx_route[j, k] = dxe[q]
+            dg[j, k] = dge[q]
+    acc = np.zeros_like(X)
+    if weights.shared is not None:
+        acc = route_backward_rows(X, dY, np.ones(n, dtype=np.float32), *weights.shared)["dx"].copy()
+    for k in range(K):
+        acc = acc + dx_route[:, k]
+    dX = round_bf16(acc)
+    return dict(topk_idx=topk_idx, g=g, dX=dX, dg=dg, ds=router_grad(dg, g, den, topk_idx, s_rows.shape[1]))
 
 
 # --------------------------------------------------------------------------
@@ -586,6 +676,23 @@ def e4m3_encode(v) -> np.ndarray:
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
     code = np.where(pick_hi, hi, lo).astype(np.uint8)
     return code | (np.signbit(v).astype(np.uint8) << np.uint8(7))
+
+
+def e4m3_round(v) -> np.ndarray:
+    """The value e4m3_encode picks, computed without codes: E4M3 keeps 3
+    mantissa bits, so in binade [2^q, 2^(q+1)) (q >= -6) its values are
+    n 2^(q-3) for integers n in [8, 16), and below 2^-6 the subnormals are
+    n 2^-9 (n in [0, 8)).  Rounding |v| / step to the nearest integer with
+    ties to even is ties to the even mantissa in both cases (n even iff the
+    mantissa is even; n = 16 is the next binade's even mantissa 0).
+    |v| <= 448; float64 out, sign kept."""
+    v = np.asarray(v, dtype=np.float64)
+    mag = np.abs(v)
+    if np.any(mag > 448.0) or np.any(np.isnan(v)):
+        raise ValueError("e4m3_round: |v| must be <= 448")
+    _, q = np.frexp(mag)  # mag = m 2^q with m in [0.5, 1): binade 2^(q - 1)
+    step = np.ldexp(1.0, np.maximum(q - 1, -6) - 3)
+    return np.copysign(np.rint(mag / step) * step, v)
 
 
 def mx_scale_exponent(amax) -> np.ndarray:
@@ -629,8 +736,7 @@ def expert_ffn_rows_mxfp8(xrows, Wg, Wu, Wd):
     along D, W_down along I, a = bf16(SiLU(h) u) quantised along I; every
     GEMM contracts the exactly dequantised values in fp32.  Inputs are bf16
     bits (or float values).  Returns dict(a_pre, a, aq, asc, y)."""
-    deq = lambda v: mxfp8_dequantize(*mxfp8_quantize(FP32.w(v))).astype(np.float32)
-    X, Wgd, Wud, Wdd = deq(xrows), deq(Wg), deq(Wu), deq(Wd)
+    X, Wgd, Wud, Wdd = (mxfp8_roundtrip(FP32.w(v)) for v in (xrows, Wg, Wu, Wd))
     h = X @ Wgd.T
     u = X @ Wud.T
     a_pre = silu(h) * u
@@ -677,9 +783,9 @@ def moe_forward_mxfp8(inp: Dict[str, np.ndarray], K: int, quant: Optional[Dict[s
             Wu = mxfp8_dequantize(quant["w_up"][0][e], quant["w_up"][1][e])
             Wd = mxfp8_dequantize(quant["w_down"][0][e], quant["w_down"][1][e])
         else:
-            Wg = mxfp8_dequantize(*mxfp8_quantize(bf16_to_f32(inp["w_gate"][e])))
-            Wu = mxfp8_dequantize(*mxfp8_quantize(bf16_to_f32(inp["w_up"][e])))
-            Wd = mxfp8_dequantize(*mxfp8_quantize(bf16_to_f32(inp["w_down"][e])))
+            Wg = mxfp8_roundtrip(bf16_to_f32(inp["w_gate"][e]))
+            Wu = mxfp8_roundtrip(bf16_to_f32(inp["w_up"][e]))
+            Wd = mxfp8_roundtrip(bf16_to_f32(inp["w_down"][e]))
         X = xg_d[p0:p1]
         h = X @ Wg.astype(np.float32).T
         u = X @ Wu.astype(np.float32).T
@@ -697,11 +803,19 @@ def moe_forward_mxfp8(inp: Dict[str, np.ndarray], K: int, quant: Optional[Dict[s
 
 def mxfp8_roundtrip(v) -> np.ndarray:
     """Quantise along the last axis and dequantise exactly, as float32: the
-    values a block-scaled GEMM contracts."""
-    return mxfp8_dequantize(*mxfp8_quantize(np.asarray(v, dtype=np.float64))).astype(np.float32)
+    values a block-scaled GEMM contracts.  The same values as
+    mxfp8_dequantize(*mxfp8_quantize(v)), taken through e4m3_round (no codes)."""
+    v = np.asarray(v, dtype=np.float64)
+    n = v.shape[-1]
+    if n % 32:
+        raise ValueError("last dim must be a multiple of 32")
+    blocks = v.reshape(v.shape[:-1] + (n // 32, 32))
+    e = mx_scale_exponent(np.max(np.abs(blocks), axis=-1))[..., None]
+    vals = np.ldexp(e4m3_round(np.ldexp(blocks, -e)), e)
+    return vals.reshape(v.shape).astype(np.float32)
 
 
-def route_backward_rows_mxfp8(xrows, dyrows, g, Wg, Wu, Wd, deq: Optional[Callable] = None):
+def route_backward_rows_mxfp8(xrows, dyrows, g, Wg, Wu, Wd, deq: Optional[Callable] = None, ranges: bool = False):
     """Backward of g * E_i(x) for rows of one expert with MXFP8 routed GEMMs
     ([note] "The production details": MXFP8 with quantisation fused into the
     dispatch, the grouped GEMMs and the gated activation; the router gradient
@@ -709,27 +823,31 @@ def route_backward_rows_mxfp8(xrows, dyrows, g, Wg, Wu, Wd, deq: Optional[Callab
     input gradient).  Each GEMM contracts operands quantised along its own
     reduction dim, exactly dequantised, in fp32:
       replay  h = X W_gate^T, u = X W_up^T : x, W_gate, W_up along D (the
-              forward's quantisation); h and u are kept as bf16;
+              forward's quantisation);
       t = dY W_down                        : dY along D, W_down^T along D;
-              t is kept as bf16;
       dx = [dh | du] [W_gate ; W_up]       : [dh | du] along 2I,
               [W_gate^T | W_up^T] along 2I; dx = bf16.
-    The activation gradient is the BF16 backward's, on the bf16 h, u, t:
-      a = bf16(SiLU(h) u), dg = <t, a>, da = g t,
+    h, u and t stay the fp32 products: the pages put no rounding point
+    there.  The activation gradient is the BF16 backward's, on those values:
+      a = bf16(SiLU(h) u), dg = <t, SiLU(h) u> (unrounded), da = g t,
       dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)), a_g = bf16(g a).
     ``deq`` is the quantise-dequantise step along the last axis (default
     mxfp8_roundtrip); the identity turns the quantisation off.  Inputs are
-    bf16 bits or float values.  Returns dict(h, u, a, t, dg, dh, du, a_g, dx)."""
+    bf16 bits or float values.  Returns dict(h, u, a, t, dg, dh, du, a_g, dx)
+    and with ranges also rounding_ranges of dh, du, a, a_g (products of the
+    quantised operands)."""
     deq = mxfp8_roundtrip if deq is None else deq
     X = deq(FP32.w(xrows))
     dY = deq(FP32.w(dyrows))
     gcol = np.asarray(g, dtype=np.float32).reshape(-1, 1)
     Wg_, Wu_, Wd_ = FP32.w(Wg), FP32.w(Wu), FP32.w(Wd)
-    h = round_bf16(X @ deq(Wg_).T)
-    u = round_bf16(X @ deq(Wu_).T)
-    t = round_bf16(dY @ deq(np.ascontiguousarray(Wd_.T)).T)
-    a = round_bf16(silu(h) * u)
-    dg = np.sum(t * a, axis=1, dtype=np.float32)
+    Wgq, Wuq, WdqT = deq(Wg_), deq(Wu_), deq(np.ascontiguousarray(Wd_.T))
+    h = X @ Wgq.T
+    u = X @ Wuq.T
+    t = dY @ WdqT.T
+    a_pre = silu(h) * u
+    a = round_bf16(a_pre)
+    dg = np.sum(t * a_pre, axis=1, dtype=np.float32)
     da = gcol * t
     one = np.float32(1)
     with np.errstate(over="ignore"):
@@ -740,15 +858,18 @@ def route_backward_rows_mxfp8(xrows, dyrows, g, Wg, Wu, Wd, deq: Optional[Callab
     dhu = deq(np.concatenate([dh, du], axis=1))
     wgu_t = deq(np.concatenate([Wg_.T, Wu_.T], axis=1))  # [D][2I]
     dx = round_bf16(dhu @ wgu_t.T)
-    return dict(h=h, u=u, a=a, t=t, dg=dg, dh=dh, du=du, a_g=a_g, dx=dx)
+    out = dict(h=h, u=u, a=a, t=t, dg=dg, dh=dh, du=du, a_g=a_g, dx=dx)
+    if ranges:
+        out["ranges"] = rounding_ranges(X, dY, g, Wgq, Wuq, np.ascontiguousarray(WdqT.T), h, u, t, a)
+    return out
 
 
 def moe_backward_mxfp8(inp: Dict[str, np.ndarray], dy, K: int,
                        fwd: Optional[Dict[str, np.ndarray]] = None,
-                       deq: Optional[Callable] = None) -> Dict[str, np.ndarray]:
+                       deq: Optional[Callable] = None, ranges: bool = False) -> Dict[str, np.ndarray]:
     """The backward with the routed experts' GEMMs in MXFP8
     (route_backward_rows_mxfp8); the weight gradients are BF16 products of
     the bf16 x, dY and the MXFP8 path's bf16 dh, du, a_g, as in moe_backward;
     the shared expert is BF16 ([note] "The production details")."""
-    return moe_backward(inp, dy, K, FP32, fwd=fwd,
-                        routed_rows=lambda *a: route_backward_rows_mxfp8(*a, deq=deq))
+    return moe_backward(inp, dy, K, FP32, fwd=fwd, ranges=ranges,
+                        routed_rows=lambda *a, ranges=False: route_backward_rows_mxfp8(*a, deq=deq, ranges=ranges))

@@ -48,6 +48,12 @@ class MoEConfig:
     skew: float = 0.0            # logit bias b_e = -skew * ln(e + 1)
     backward: bool = False
     chunks: Tuple[int, ...] = ()
+    # "normal": the distributions above.  "grid": x, dY and every weight are
+    # small integers times a power of two of the same scale (x, dY: j / 2;
+    # W_gate, W_up, W_shared_gate/up: j 2^-7; W_down, W_shared_down: j 2^-6;
+    # j uniform in -3..3), so every product sum of the layer's GEMMs over
+    # D or I is exact in fp32 whatever the summation order.
+    values: str = "normal"
 
     @property
     def R(self) -> int:
@@ -109,6 +115,19 @@ def _draw(gen: torch.Generator, shape, std: float, device, out_dtype=torch.bfloa
     return out
 
 
+def _draw_grid(gen: torch.Generator, shape, scale: float, device) -> torch.Tensor:
+    """Integers uniform in -3..3 times `scale` (a power of two), bf16."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(shape[0], -1)
+    row = flat.shape[1]
+    rows_per = max(1, _SLAB // max(row, 1))
+    for r0 in range(0, shape[0], rows_per):
+        r1 = min(shape[0], r0 + rows_per)
+        v = torch.randint(-3, 4, (r1 - r0, row), generator=gen, device=device).to(torch.float32)
+        flat[r0:r1].copy_(v * scale)  # exact in bf16
+    return out
+
+
 def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, with_dy: Optional[bool] = None) -> Dict[str, torch.Tensor]:
     """Draw one layer's inputs on ``device``.
 
@@ -121,14 +140,20 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, with_dy: Optional[b
     gen.manual_seed(seed)
     T, D, I, E, Is = cfg.T, cfg.D, cfg.I, cfg.E, cfg.I_shared
     out: Dict[str, torch.Tensor] = {}
-    out["x"] = _draw(gen, (T, D), 1.0, device)
-    out["w_gate"] = _draw(gen, (E, I, D), 1.0 / math.sqrt(D), device)
-    out["w_up"] = _draw(gen, (E, I, D), 1.0 / math.sqrt(D), device)
-    out["w_down"] = _draw(gen, (E, D, I), 1.0 / math.sqrt(I), device)
+    if cfg.values == "grid":
+        draw = lambda shape, scale: _draw_grid(gen, shape, scale, device)
+        sx, sgu, sd = 0.5, 2.0 ** -7, 2.0 ** -6
+    else:
+        draw = lambda shape, std: _draw(gen, shape, std, device)
+        sx, sgu, sd = 1.0, 1.0 / math.sqrt(D), None
+    out["x"] = draw((T, D), sx)
+    out["w_gate"] = draw((E, I, D), sgu)
+    out["w_up"] = draw((E, I, D), sgu)
+    out["w_down"] = draw((E, D, I), sd if sd else 1.0 / math.sqrt(I))
     if Is > 0:
-        out["ws_gate"] = _draw(gen, (Is, D), 1.0 / math.sqrt(D), device)
-        out["ws_up"] = _draw(gen, (Is, D), 1.0 / math.sqrt(D), device)
-        out["ws_down"] = _draw(gen, (D, Is), 1.0 / math.sqrt(Is), device)
+        out["ws_gate"] = draw((Is, D), sgu)
+        out["ws_up"] = draw((Is, D), sgu)
+        out["ws_down"] = draw((D, Is), sd if sd else 1.0 / math.sqrt(Is))
     logits = torch.randn((T, E), generator=gen, dtype=torch.float32, device=device)
     if cfg.skew != 0.0:
         bias = -cfg.skew * torch.log(torch.arange(1, E + 1, dtype=torch.float32, device=device))
@@ -137,7 +162,7 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, with_dy: Optional[b
     if with_dy is None:
         with_dy = cfg.backward
     if with_dy:
-        out["dy"] = _draw(gen, (T, D), 1.0, device)
+        out["dy"] = draw((T, D), sx)
     return out
 
 

@@ -108,23 +108,107 @@ def test_fp32_backward_close_to_fp64():
         assert err.max() < 0.05, k
 
 
-def test_fp32_and_fp64_roundings_agree_within_slack():
-    """Two correct evaluations (fp32 and fp64 sums, same bf16 rounding
-    points) may round ambiguous dh/du/a_g/a/dx the other way; they must agree
-    within 2e-2 * max(1, |ref|) plus the oracle's ambiguity slack."""
+def test_fp32_and_fp64_roundings_agree_at_the_bare_tolerance():
+    """Two correct evaluations of the same rounding points (fp32 sums in
+    numpy's order, and fp64 sums) may round a bf16 point the other way where
+    the sum lands next to a midpoint; the parity tolerance must absorb that
+    by itself: every output within 2e-2 * max(1, |ref|), with room to spare
+    (the worst seen is under 0.8 of it on these shapes)."""
     import sys, os
     sys.path.insert(0, os.path.dirname(__file__))
-    from helpers import assert_close, host
+    from helpers import host, rel_err
+    from routing_grouped_expert_device_gb300 import workloads as W
+    for cfg in (W.MoEConfig("r", T=300, D=512, I=256, E=5, K=3, I_shared=128),
+                W.MoEConfig("s", T=700, D=512, I=256, E=32, K=4, I_shared=256, skew=2.0)):
+        h = host(W.make_inputs(cfg, "cpu", with_dy=True))
+        a = O.moe_backward(h, h["dy"], cfg.K)
+        b = O.moe_backward(h, h["dy"], cfg.K, O.Numerics(np.float64, True))
+        for k in ["dX", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down", "dg", "ds"]:
+            assert rel_err(b[k], a[k]).max() <= 0.9 * 2e-2, (cfg.name, k)
+
+
+def test_sampled_token_backward_matches_full_backward():
+    """moe_backward_tokens (routes grouped by expert over a token sample)
+    gives the whole layer's dX rows, dg and ds of those tokens."""
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from helpers import host
     from routing_grouped_expert_device_gb300 import workloads as W
     cfg = W.MoEConfig("r", T=300, D=512, I=256, E=5, K=3, I_shared=128)
     h = host(W.make_inputs(cfg, "cpu", with_dy=True))
-    a = O.moe_backward(h, h["dy"], cfg.K, with_slack=True)
-    b = O.moe_backward(h, h["dy"], cfg.K, O.Numerics(np.float64, True))
-    for k in ["dX", "dW_gate", "dW_up", "dW_down", "dWs_gate", "dWs_up", "dWs_down", "dg", "ds"]:
-        assert_close(b[k], a[k], 2e-2, k, a["slack"][k])
-    # the ambiguous rounding decisions are a small fraction of all of them
-    x = O.bf16_to_f32(h["x"])
-    r = O.route_backward_rows(x[:200], O.bf16_to_f32(h["dy"])[:200], np.full(200, 0.3, np.float32),
-                              h["w_gate"][0], h["w_up"][0], h["w_down"][0])
-    for f in ("flip_dh", "flip_du", "flip_ag"):
-        assert np.mean(r[f] > 0) < 0.05, f
+    full = O.moe_backward(h, h["dy"], cfg.K)
+    toks = np.array([0, 3, 150, 299])
+    part = O.moe_backward_tokens(h["x"][toks], h["dy"][toks], h["s"][toks], O.HostWeights.from_arrays(h), cfg.K)
+    # the per-route products run in other row batches (another matmul
+    # blocking, so a bf16 point may round the other way): a tenth of the
+    # parity tolerance
+    from helpers import rel_err
+    for k in ("dX", "dg", "ds"):
+        assert rel_err(part[k], full[k][toks]).max() <= 2e-3, k
+    assert np.array_equal(part["ds"] == 0, full["ds"][toks] == 0)
+
+
+def test_rounding_ranges_cover_another_evaluation_and_stay_tight():
+    """rounding_ranges marks the bf16 points of dh, du, a, a_g whose decision
+    another correct evaluation could take the other way.  An fp64 evaluation
+    with the same rounding points (closer to exact than fp32) must land in
+    the range at every point; unmarked points are the oracle's value; and
+    most points are unmarked."""
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from helpers import host
+    from routing_grouped_expert_device_gb300 import workloads as W
+    cfg = W.MoEConfig("r", T=300, D=512, I=256, E=5, K=3, I_shared=0)
+    h = host(W.make_inputs(cfg, "cpu", with_dy=True))
+    idx, g, _ = O.route(h["s"], cfg.K)
+    F64R = O.Numerics(np.float64, True)
+    marked = total = 0
+    for e in range(cfg.E):
+        rows, ks = np.nonzero(idx == e)
+        if len(rows) == 0:
+            continue
+        args = (h["x"][rows], h["dy"][rows], g[rows, ks], h["w_gate"][e], h["w_up"][e], h["w_down"][e])
+        b = O.route_backward_rows(*args, ranges=True)
+        c = O.route_backward_rows(*args, num=F64R)
+        for k in ("dh", "du", "a", "a_g"):
+            lo, hi = b["ranges"][k]
+            assert np.all(lo <= b[k]) and np.all(b[k] <= hi), k
+            other = np.asarray(c[k], dtype=np.float32)
+            assert np.all(lo <= other) and np.all(other <= hi), k
+            fixed = lo == hi
+            assert np.array_equal(lo[fixed], b[k][fixed])
+            marked += int(np.count_nonzero(~fixed))
+            total += fixed.size
+    # the bounds are worst cases (about 5x the largest accumulation error
+    # measured on the GPU): some 7 % of the points are marked on this shape
+    assert 0 < marked < 0.15 * total
+
+
+def test_sum_range_is_the_extreme_choice_brute_force():
+    """sum_range's shifts are the least and greatest fp32-exact sums over
+    every choice of the marked values (2^n combinations, n small)."""
+    rng = np.random.default_rng(9)
+    v = O.round_bf16(rng.standard_normal((6, 2)).astype(np.float32))
+    lo, hi = v.copy(), v.copy()
+    ulp = np.abs(O.round_bf16(v * (1 + 2.0 ** -7)) - v)
+    pick = [(0, 0), (2, 0), (5, 0), (1, 1), (3, 1)]
+    for i, (p, c) in enumerate(pick):
+        if i % 2:
+            hi[p, c] += ulp[p, c]
+        else:
+            lo[p, c] -= ulp[p, c]
+    other = rng.standard_normal((6, 3))
+    slo, shi = O.sum_range(v, (lo, hi), other)
+    base = v.T.astype(np.float64) @ other
+    import itertools
+    for c in range(2):
+        marks = [p for (p, cc) in pick if cc == c]
+        sums = []
+        for choice in itertools.product([0, 1], repeat=len(marks)):
+            w = v[:, c].astype(np.float64).copy()
+            for p, ch in zip(marks, choice):
+                if ch:
+                    w[p] = lo[p, c] if lo[p, c] != v[p, c] else hi[p, c]
+            sums.append(w @ other)
+        sums = np.array(sums)
+        assert np.allclose(slo[c], sums.min(0) - base[c]) and np.allclose(shi[c], sums.max(0) - base[c])

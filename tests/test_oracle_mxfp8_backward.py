@@ -2,17 +2,18 @@
 moe_backward_mxfp8).
 
 * With the quantiser switched off and small-integer inputs (every product
-  exact, so keeping h, u, t in bf16 rounds nothing), it is the BF16
-  backward: the same dh, du, a_g, dg, weight gradients and ds bit for bit,
-  dX within one bf16 ulp (the fp32 sum over [dh | du] runs in another order).
-* Quantisation axes: inputs whose 1x32 blocks along the intended reduction
-  dim hold one binade each (exact in E4M3 at the block's scale) while the
-  other axis mixes binades 2^14 apart (inexact there).  The replay h, u and
-  t then equal the exact products rounded to bf16, and a quantiser along the
-  other axis would not (checked, so the construction has teeth); likewise
-  the weights of the dX product along 2I.  Activations that E4M3 does not
-  hold exactly enter the replay and t quantised per row (and unquantised
-  they would give other h, t).
+  exact), it is the BF16 backward: the same dh, du, a_g, dg, weight
+  gradients and ds bit for bit, dX within one bf16 ulp (the fp32 sum over
+  [dh | du] runs in another order).
+* Quantisation axes: inputs whose rows are each one binade (so every 1x32
+  block along the row is exact in E4M3 at the block's scale, and every
+  fp32 sum of a row pair's products is exact) while the other axis mixes
+  binades 2^14 apart (inexact there).  The replay h, u and t then equal the
+  exact products, bit for bit and unrounded (the pages put no rounding point
+  on them), and a quantiser along the other axis would not (checked, so the
+  construction has teeth); likewise the weights of the dX product along 2I.
+  Activations that E4M3 does not hold exactly enter the replay and t
+  quantised per row (and unquantised they would give other h, t).
 * Random inputs: within the MXFP8 error of the BF16 backward.
 """
 import numpy as np
@@ -53,14 +54,14 @@ def test_quantiser_off_is_the_bf16_backward():
         assert np.abs(b["dX"]).max() > 1.0  # not a trivially zero case
 
 
-def _exact_bf16(a, b_t):
-    """bf16 of the fp64 product a @ b_t.T."""
-    return O.round_bf16((a.astype(np.float64) @ b_t.astype(np.float64).T).astype(np.float32))
+def _exact(a, b_t):
+    """The fp64 product a @ b_t.T as float32 (exact for one-binade rows)."""
+    return (a.astype(np.float64) @ b_t.astype(np.float64).T).astype(np.float32)
 
 
 def test_replay_and_t_quantised_along_d():
     rng = np.random.default_rng(7)
-    n, D, I = 40, 64, 64
+    n, D, I = 64, 64, 64
     x = _rows_binades(rng, n, D)
     dy = _rows_binades(rng, n, D)
     Wg = _rows_binades(rng, I, D)
@@ -69,23 +70,29 @@ def test_replay_and_t_quantised_along_d():
     Wd = np.ascontiguousarray(WdT.T)      # [D][I]
     g = np.full(n, 0.5, np.float32)
     r = O.route_backward_rows_mxfp8(x, dy, g, Wg, Wu, Wd)
-    assert np.array_equal(r["h"], _exact_bf16(x, Wg))
-    assert np.array_equal(r["u"], _exact_bf16(x, Wu))
-    assert np.array_equal(r["t"], _exact_bf16(dy, WdT))
+    assert r["h"].dtype == np.float32 and r["t"].dtype == np.float32
+    assert np.array_equal(r["h"], _exact(x, Wg))
+    assert np.array_equal(r["u"], _exact(x, Wu))
+    assert np.array_equal(r["t"], _exact(dy, WdT))
+    # not rounded to bf16 anywhere: the exact products carry more than 8 bits
+    assert not np.array_equal(r["h"], O.round_bf16(r["h"]))
+    assert not np.array_equal(r["t"], O.round_bf16(r["t"]))
     # the same operands quantised along the other axis lose the small binade
+    close = lambda a, b: np.allclose(a, b, rtol=2.0 ** -12, atol=0)
     wrong = O.mxfp8_roundtrip(Wg.T).T
-    assert not np.array_equal(O.round_bf16(x @ wrong.T), r["h"])
+    assert not close(x @ wrong.T, r["h"])
     wrong_d = O.mxfp8_roundtrip(Wd)       # W_down along I
-    assert not np.array_equal(O.round_bf16(dy @ wrong_d), r["t"])
+    assert not close(dy @ wrong_d, r["t"])
+    wrong_x = O.mxfp8_roundtrip(x.T).T    # x along the token axis
+    assert not close(wrong_x @ Wg.T, r["h"])
     # activations that E4M3 does not hold exactly enter quantised per row
     xr = O.round_bf16(rng.standard_normal((n, D)).astype(np.float32))
     dyr = O.round_bf16(rng.standard_normal((n, D)).astype(np.float32))
     r2 = O.route_backward_rows_mxfp8(xr, dyr, g, Wg, Wu, Wd)
-    close = lambda a, b: np.allclose(a, b, rtol=2.0 ** -7, atol=0)
-    assert close(r2["h"], _exact_bf16(O.mxfp8_roundtrip(xr), Wg))
-    assert close(r2["t"], _exact_bf16(O.mxfp8_roundtrip(dyr), WdT))
-    assert not close(r2["h"], _exact_bf16(xr, Wg))
-    assert not close(r2["t"], _exact_bf16(dyr, WdT))
+    assert close(r2["h"], _exact(O.mxfp8_roundtrip(xr), Wg))
+    assert close(r2["t"], _exact(O.mxfp8_roundtrip(dyr), WdT))
+    assert not close(r2["h"], _exact(xr, Wg))
+    assert not close(r2["t"], _exact(dyr, WdT))
 
 
 def test_dx_weights_quantised_along_2i():

@@ -75,6 +75,31 @@ def test_e4m3_encode_vs_nearest_search():
         assert int(c) == want, (x, c, want)
 
 
+def test_e4m3_round_is_the_encoders_value():
+    """The closed form (3 mantissa bits, ties to even) against the value of
+    the code e4m3_encode picks: every bf16 value up to 448, both signs,
+    scaled by powers of two into the subnormal range, and the exact
+    midpoints between neighbouring codes."""
+    vals = O.e4m3_code_values()
+    v = _all_bf16_values_upto(448.0).astype(np.float64)
+    mids = (vals[1:126] + vals[2:127]) / 2
+    cases = [v, v * 2.0 ** -7, v * 2.0 ** -12, mids, -mids]
+    for c in cases:
+        c = c[np.abs(c) <= 448.0]
+        want = vals[O.e4m3_encode(c)]
+        got = O.e4m3_round(c)
+        assert np.array_equal(got, want)
+        assert np.array_equal(np.signbit(got[want == 0]), np.signbit(c[want == 0]))
+
+
+def test_mxfp8_roundtrip_is_quantize_then_dequantize():
+    rng = np.random.default_rng(5)
+    v = O.round_bf16((rng.standard_normal((96, 256)) * 10.0 ** rng.uniform(-5, 5, (96, 1))).astype(np.float32))
+    v[3, 64:96] = 0.0
+    want = O.mxfp8_dequantize(*O.mxfp8_quantize(v)).astype(np.float32)
+    assert np.array_equal(O.mxfp8_roundtrip(v), want)
+
+
 @pytest.mark.parametrize("k", range(-20, 21, 3))
 def test_mx_scale_rule_boundaries(k):
     b = 448.0 * 2.0 ** k

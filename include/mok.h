@@ -124,18 +124,42 @@ typedef struct {
   const uint8_t *sct_gu;
 } mok_weights;
 
-/* Routing and plan state saved by the forward for the backward.
+/* State saved by the forward for the backward.
  * topk_idx int32 [T][K]; g fp32 [T][K]; counts int32 [E]; offsets int32
- * [E+1]; table int32 [R][3]; route_dst int32 [R]. */
+ * [E+1]; table int32 [R][3]; route_dst int32 [R].
+ *
+ * act, act_rows (optional; paper note, "A ring buffer instead of a host
+ * round-trip": the backward replays only the forward activations it no
+ * longer has): a caller-owned fp32 store of act_rows rows of 2I floats.
+ * The forward writes h = W_gate x (columns [0, I)) and u = W_up x (columns
+ * [I, 2I)), unrounded, for the routed rows of every expert whose rows all
+ * lie below act_rows in expert order (offsets[e+1] <= act_rows), at row
+ * offsets[e] + j.  The backward reads them for those experts and replays
+ * h, u (streaming W_gate and W_up again) only for the others.  act = NULL
+ * or act_rows = 0 keeps nothing: the backward replays every expert.  With
+ * act_rows >= T*K every expert is kept.  act must be 16-byte aligned and
+ * stay untouched between the forward and the backward. */
 typedef struct {
   int32_t *topk_idx;
   float *g;
   int32_t *counts, *offsets, *table, *route_dst;
+  float *act;
+  int64_t act_rows;
 } mok_plan_buf;
 
 /* Bytes of caller-provided device workspace `op` needs for `shape`
  * (0 for an invalid shape).  The workspace needs 256-byte alignment. */
 size_t mok_workspace_bytes(const mok_shape *shape, int op);
+
+/* Intermediates of mok_moe_bwd that stay in its workspace after the call,
+ * for inspection (the pages have no counterpart; the parity tests read
+ * them): dh, du and a_g = bf16(g a) of the routed experts, each bf16
+ * [T*K][I] in expert order (row = mok_plan's dst). */
+typedef enum { MOK_WS_BWD_DH = 1, MOK_WS_BWD_DU = 2, MOK_WS_BWD_AG = 3 } mok_ws_region;
+/* Byte offset of `region` in the MOK_OP_BWD workspace of `shape`, or
+ * (size_t)-1 for an invalid shape or region.  The contents are those of the
+ * last mok_moe_bwd that used the workspace, until the next call writes it. */
+size_t mok_workspace_offset(const mok_shape *shape, int region);
 
 /* Top-K routing (blog, "Overlapping computation and communication in MoE":
  * the router selects the top-k routed experts and their weights).
@@ -177,8 +201,11 @@ mok_status mok_plan(const int32_t *topk_idx, int32_t T, int32_t E, int32_t K,
  * (held on every GPU that loads the library until the process exits); it
  * allows ceil(T*K / 1024) * E <= 262144, else MOK_ERR_WORKSPACE and nothing
  * is enqueued.  Nothing is allocated.  The first call on a device looks up
- * the array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  All calls share the one array, so
+ * the array's device address (cudaGetSymbolAddress) and caches it with the
+ * id of the current context; a call under another context (after
+ * cudaDeviceReset the device gets a new one, and the library's module is
+ * reloaded) looks it up again.  Make the first call in each context before
+ * any stream capture.  All calls share the one array, so
  * calls that overlap on the GPU (different streams, no ordering between
  * them) race and give wrong plans; order them.  Arguments and errors
  * otherwise as mok_plan. */
@@ -299,13 +326,14 @@ mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void 
  * when I_shared = 0); ds fp32 [T][E] (zero outside the top-k);
  * dg fp32 [T][K] (nullable) = <t, a> per route with t = W_down^T dy (paper
  * note, "The production details": the router-gradient inner product; the
- * down-projection output is not formed).  h and u are recomputed.  Weight
+ * down-projection output is not formed).  h and u are read from saved->act
+ * for the experts the forward kept there and recomputed for the rest.  Weight
  * gradients of experts with no routes are written as zeros.
  * With shape.dtype = MOK_MXFP8 the routed experts' replay (h, u), t and dX
  * products run in MXFP8, each operand quantised along that product's
  * reduction dim (x, dY per row along D; w's q_gate, q_up, qt_down; the
  * activation gradient quantises [dh | du] along 2I for qt_gu); h, u and t
- * are kept as bf16 between the products and the activation gradient.  The
+ * stay fp32 between the products and the activation gradient.  The
  * weight gradients are BF16 products (of bf16 x, dY, dh, du, g a) and the
  * shared expert is BF16.  MXFP8 needs I % 256 == 0 (the t and dX products
  * run on 256-column tiles; MOK_ERR_UNSUPPORTED otherwise) and w's q_* and

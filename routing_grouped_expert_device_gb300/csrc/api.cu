@@ -99,9 +99,9 @@ BwdLayout bwd_layout(const mok_shape& s) {
   L.xq_sc = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
   L.dyq = c.take(mx ? R * D : 0);
   L.dyq_sc = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
-  L.hh = c.take(mx ? R * I * 2 : 0);
-  L.uu = c.take(mx ? R * I * 2 : 0);
-  L.tt = c.take(mx ? R * I * 2 : 0);
+  L.hh = c.take(mx ? R * I * 4 : 0);  // fp32 h, u, t: no rounding point there
+  L.uu = c.take(mx ? R * I * 4 : 0);
+  L.tt = c.take(mx ? R * I * 4 : 0);
   L.dhu_q = c.take(mx ? R * 2 * I : 0);
   L.dhu_sc = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), 2 * I, s.E) : 0);
   L.total = c.off;
@@ -175,6 +175,17 @@ extern "C" size_t mok_workspace_bytes(const mok_shape* shape, int op) {
     }
   }
   return 0;
+}
+
+extern "C" size_t mok_workspace_offset(const mok_shape* shape, int region) {
+  if (!shape_ok(shape)) return static_cast<size_t>(-1);
+  const BwdLayout L = bwd_layout(*shape);
+  switch (region) {
+    case MOK_WS_BWD_DH: return L.dh;
+    case MOK_WS_BWD_DU: return L.du;
+    case MOK_WS_BWD_AG: return L.ag;
+  }
+  return static_cast<size_t>(-1);
 }
 
 extern "C" mok_status mok_dispatch(const mok_shape* shape, const void* x, const int32_t* table,
@@ -374,7 +385,12 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     pb.offsets = at<int32_t>(ws, L.offsets);
     pb.table = at<int32_t>(ws, L.table);
     pb.route_dst = at<int32_t>(ws, L.route_dst);
+    pb.act = nullptr;
+    pb.act_rows = 0;
   }
+  if (pb.act_rows < 0 || (pb.act && !aligned16(pb.act))) return MOK_ERR_INVALID_ARG;
+  // h, u of the groups that fit in the caller's store, kept for the backward
+  const KeptAct kept{pb.act_rows > 0 ? pb.act : nullptr, pb.act_rows};
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mok_status r;
@@ -415,7 +431,7 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
       return fail(r);
     void* asc = at<void>(ws, L.a_scale);
     if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
-                              w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st)) != MOK_OK)
+                              w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st, kept)) != MOK_OK)
       return fail(r);
     if ((r = launch_down_mx(a, asc, R, w->q_down, w->sc_down, pb.offsets, s.E, s.D, s.I, yg, st)) !=
         MOK_OK)
@@ -426,13 +442,13 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
       const int64_t b = ring_chunk(s.chunk_rows);
       if ((r = launch_upgate_ring(x, pb.table, s.K, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, xg,
                                   ring_rows_for(R, b), static_cast<int>(b), at<int32_t>(ws, L.ring_counters),
-                                  st)) != MOK_OK)
+                                  st, kept)) != MOK_OK)
         return fail(r);
     } else {
       if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
         return fail(r);
-      if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr)) !=
-          MOK_OK)
+      if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr,
+                                  kept)) != MOK_OK)
         return fail(r);
     }
   }
@@ -502,9 +518,15 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
     return MOK_ERR_INVALID_ARG;
   if (s.I_shared && (!w->ws_gate || !w->ws_up || !w->ws_down || !dws_gate || !dws_up || !dws_down))
     return MOK_ERR_INVALID_ARG;
+  if (pb.act_rows < 0 || (pb.act && !aligned16(pb.act))) return MOK_ERR_INVALID_ARG;
   const BwdLayout L = bwd_layout(s);
   if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOK_ERR_WORKSPACE;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
+  // the groups whose h, u the forward kept (rows below kept_rows) skip the
+  // replay; with every row kept no replay runs at all
+  const KeptAct kept{pb.act_rows > 0 ? pb.act : nullptr, pb.act_rows};
+  const int32_t kept_rows = kept.limit();
+  const bool replay = kept_rows < R;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* xg = at<void>(ws, L.xg);
   void* dyg = at<void>(ws, L.dyg);
@@ -532,27 +554,32 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
     void* tt = at<void>(ws, L.tt);
     void* dhu_q = at<void>(ws, L.dhu_q);
     uint8_t* dhu_sc = at<uint8_t>(ws, L.dhu_sc);
-    if ((r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xq, xq_sc, st)) !=
-        MOK_OK)
+    if (replay && (r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xq,
+                                             xq_sc, st)) != MOK_OK)
       return r;
     if ((r = launch_dispatch_mxfp8(dy, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, dyq, dyq_sc, st)) !=
         MOK_OK)
       return r;
-    if ((r = launch_replay_mx(xq, xq_sc, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, pb.offsets, s.E, s.D, s.I,
-                              hh, uu, st)) != MOK_OK)
+    if (replay && (r = launch_replay_mx(xq, xq_sc, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, pb.offsets, s.E,
+                                        s.D, s.I, hh, uu, st, kept_rows)) != MOK_OK)
       return r;
-    if ((r = launch_down_mx(dyq, dyq_sc, R, w->qt_down, w->sct_down, pb.offsets, s.E, s.I, s.D, tt, st)) != MOK_OK)
+    if ((r = launch_down_mx(dyq, dyq_sc, R, w->qt_down, w->sct_down, pb.offsets, s.E, s.I, s.D, tt, st,
+                            /*f32_out=*/true)) != MOK_OK)
       return r;
     if ((r = launch_act_grad_mx(hh, uu, tt, g_route, pb.table, pb.offsets, R, s.I, s.E, dh, du, ag, dhu_q, dhu_sc,
-                                dgp, st)) != MOK_OK)
+                                dgp, st, kept)) != MOK_OK)
       return r;
     if ((r = launch_down_mx(dhu_q, dhu_sc, R, w->qt_gu, w->sct_gu, pb.offsets, s.E, s.D, 2 * s.I, dxr, st)) !=
         MOK_OK)
       return r;
   } else {
-    // replay h, u; t = dY W_down; dh, du, g*a, <t, a> partials
-    if ((r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,
-                              g_route, dh, du, ag, dgp, st)) != MOK_OK)
+    // t = dY W_down with the kept h, u; replay h, u for the other groups;
+    // dh, du, g*a, <t, a> partials
+    if (kept_rows > 0 && (r = launch_bwd_dgrad_kept(dyg, R, w->w_down, pb.offsets, s.E, s.D, s.I, g_route,
+                                                    kept.act, kept_rows, dh, du, ag, dgp, st)) != MOK_OK)
+      return r;
+    if (replay && (r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,
+                                        g_route, dh, du, ag, dgp, st, kept_rows)) != MOK_OK)
       return r;
     if ((r = launch_bwd_dx(dh, du, R, w->w_gate, w->w_up, pb.offsets, s.E, s.D, s.I, dxr, st)) != MOK_OK)
       return r;

@@ -171,17 +171,21 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
 // Activation gradient of the MXFP8 backward (paper note, "The production
 // details": MXFP8 with quantisation fused into the gated activation; the
 // router-gradient inner product).  One warp per routed row p, 8 columns per
-// lane: from the bf16 replay h, u and t = dY W_down it forms
+// lane: from fp32 h, u (the replay's, or for rows of a group that ends at or
+// below kept_rows the forward's kept store act [R][2I]) and t = dY W_down
+// it forms
 // a = bf16(SiLU(h) u), da = g t, dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)),
 // a_g = bf16(g a) (bf16 [R][I], for the weight gradients), the E4M3 codes of
 // [dh | du] [R][2I] with their scale words in the grouped layout of expert
-// table[p].e (for dX), and dgp[p] = <t, a> (per-lane sums in column order,
-// then a fixed butterfly over the lanes).  g_route null: weight 1.
+// table[p].e (for dX), and dgp[p] = <t, SiLU(h) u> with the activation
+// unrounded (per-lane sums in column order, then a fixed butterfly over the
+// lanes).  g_route null: weight 1.
 __global__ void __launch_bounds__(256) act_grad_mx_kernel(
-    const uint4* __restrict__ h, const uint4* __restrict__ u, const uint4* __restrict__ t,
+    const float4* __restrict__ h, const float4* __restrict__ u, const float4* __restrict__ t,
     const float* __restrict__ g_route, const int32_t* __restrict__ table, const int32_t* __restrict__ offsets,
     int64_t R, int I, int64_t ld, uint4* __restrict__ dh, uint4* __restrict__ du, uint4* __restrict__ ag,
-    uint2* __restrict__ dhu_q, uint32_t* __restrict__ dhu_sc, float* __restrict__ dgp) {
+    uint2* __restrict__ dhu_q, uint32_t* __restrict__ dhu_sc, float* __restrict__ dgp,
+    const float4* __restrict__ act, int32_t kept_rows) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int I8 = I / 8;
@@ -189,16 +193,23 @@ __global__ void __launch_bounds__(256) act_grad_mx_kernel(
     const int e = __ldg(table + p * 3 + 1);
     const int64_t off = __ldg(offsets + e);
     const int64_t pos = mx_scale_pos(mx_group_row0(off, e) + (p - off));
+    // h, u of this row: the kept store (float4 units: h at p*2*I8*2, u I/4 later) or the replay's
+    const bool kept = act && __ldg(offsets + e + 1) <= kept_rows;
+    const float4* hsrc = kept ? act + p * (4 * I8) : h + p * (2 * I8);
+    const float4* usrc = kept ? act + p * (4 * I8) + 2 * I8 : u + p * (2 * I8);
     const float g = g_route ? g_route[p] : 1.0f;
     float dot = 0.0f;
 #pragma unroll 1
     for (int v0 = 0; v0 < I8; v0 += 32) {
       const int vi = v0 + lane;
       const bool in = vi < I8;  // warp-uniform per 16 lanes: I is a multiple of 128
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      const uint4 hv = in ? h[p * I8 + vi] : z, uv = in ? u[p * I8 + vi] : z, tv = in ? t[p * I8 + vi] : z;
-      const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w},
-                     tw[4] = {tv.x, tv.y, tv.z, tv.w};
+      const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int64_t at = (p * I8 + vi) * 2;  // two float4 per 8 columns
+      const float4 h0 = in ? hsrc[2 * vi] : z, h1 = in ? hsrc[2 * vi + 1] : z, u0 = in ? usrc[2 * vi] : z,
+                   u1 = in ? usrc[2 * vi + 1] : z, t0 = in ? t[at] : z, t1 = in ? t[at + 1] : z;
+      const float hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      const float uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      const float tw[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
       float dhf[8], duf[8];
       uint32_t pdh[4], pdu[4], pag[4];
 #pragma unroll
@@ -206,12 +217,11 @@ __global__ void __launch_bounds__(256) act_grad_mx_kernel(
         float agv[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          const float hf = q ? bf16hi(hw[j]) : bf16lo(hw[j]);
-          const float uf = q ? bf16hi(uw[j]) : bf16lo(uw[j]);
-          const float tf = q ? bf16hi(tw[j]) : bf16lo(tw[j]);
+          const float hf = hw[2 * j + q], uf = uw[2 * j + q], tf = tw[2 * j + q];
           const float sig = sigmoid_f(hf);
-          const float a = __bfloat162float(__float2bfloat16_rn((hf * sig) * uf));  // = bf16(silu_f(h) * u)
-          dot = __fmaf_rn(tf, a, dot);
+          const float a_pre = (hf * sig) * uf;  // = silu_f(h) * u
+          const float a = __bfloat162float(__float2bfloat16_rn(a_pre));
+          dot = __fmaf_rn(tf, a_pre, dot);  // the router gradient takes the unrounded activation
           const float da = g * tf;
           dhf[2 * j + q] = __bfloat162float(__float2bfloat16_rn(da * uf * sig * (1.0f + hf * (1.0f - sig))));
           duf[2 * j + q] = __bfloat162float(__float2bfloat16_rn(da * hf * sig));
@@ -428,13 +438,15 @@ mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, vo
 
 mok_status launch_act_grad_mx(const void* h, const void* u, const void* t, const float* g_route,
                               const int32_t* table, const int32_t* offsets, int64_t R, int I, int E, void* dh,
-                              void* du, void* ag, void* dhu_q, uint8_t* dhu_sc, float* dgp, cudaStream_t st) {
+                              void* du, void* ag, void* dhu_q, uint8_t* dhu_sc, float* dgp, cudaStream_t st,
+                              KeptAct kept) {
   if (R == 0) return MOK_OK;
   if (I % 128) return MOK_ERR_UNSUPPORTED;
   act_grad_mx_kernel<<<grid_for(R, 8), 256, 0, st>>>(
-      static_cast<const uint4*>(h), static_cast<const uint4*>(u), static_cast<const uint4*>(t), g_route, table,
+      static_cast<const float4*>(h), static_cast<const float4*>(u), static_cast<const float4*>(t), g_route, table,
       offsets, R, I, mx_scale_ld(R, E), static_cast<uint4*>(dh), static_cast<uint4*>(du), static_cast<uint4*>(ag),
-      static_cast<uint2*>(dhu_q), reinterpret_cast<uint32_t*>(dhu_sc), dgp);
+      static_cast<uint2*>(dhu_q), reinterpret_cast<uint32_t*>(dhu_sc), dgp,
+      reinterpret_cast<const float4*>(kept.act), kept.limit());
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

@@ -8,6 +8,12 @@
 //                 (paper note "The production details": the down-projection
 //                 output is never formed), da = g t,
 //                 dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)), a_g = bf16(g a).
+//  dgrad, kept  : the same for the experts whose h, u the forward kept
+//                 (paper note, "A ring buffer instead of a host round-trip":
+//                 the backward replays only what it no longer has): only
+//                 t^T = W_down^T dYg^T is accumulated (W_gate and W_up are
+//                 not streamed), and the epilogue reads h, u fp32 from the
+//                 kept store.
 //  dx           : dx = bf16(dh W_gate + du W_up), K = 2I, weights MN-major.
 //  wgrad        : dW[e] = bf16(sum over the expert's rows of P^T Q) with both
 //                 operands MN-major and K running over rows; the last K block
@@ -28,6 +34,54 @@ constexpr int MNCHUNK = 64 * 128;   // 8 KB: 64 K-rows x 64 MN elements, MN-majo
 // 64-wide MN chunk = 8 KB, SBO 1024).
 __device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sdesc_sw128(a, 16, 1024); }
 __device__ __forceinline__ uint64_t mndesc(uint32_t a) { return sdesc_sw128(a, MNCHUNK, 1024); }
+
+// ---------------------------------------------------------------------------
+// The fused epilogue of row a9 for one 32-row chunk of a dgrad tile.  Lane l
+// owns I column icol = nt*128 + 32 ew + l; h[j], u[j], t[j] are row
+// row0 + j's values of that column (fp32 bits).  Per row it forms
+// a = bf16(SiLU(h) u), da = g t, dh = bf16(da u SiLU'(h)),
+// du = bf16(da SiLU(h)), a_g = bf16(g a) (each row's 32 columns of the warp
+// are one 64-byte store), and the warp's partial of the router-gradient
+// inner product <t, SiLU(h) u> of each row over its 32 columns, with the
+// gated activation unrounded (fp32), by a butterfly that leaves row j = l's
+// sum in lane l, stored at dgp[row][nt*4 + ew].  nv: valid rows of the chunk.
+template <class Params>
+__device__ __forceinline__ void dgrad_chunk(const Params& P, const TileCoord& c, int64_t row0, int nv, int ew,
+                                            int lane, const uint32_t* hv, const uint32_t* uv, const uint32_t* tv) {
+  const int icol = c.nt * 128 + ew * 32 + lane;
+  const int nI32 = P.I / 32;
+  const float gl = (P.g_route && lane < nv) ? P.g_route[row0 + lane] : 1.0f;
+  float dots[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float g = __shfl_sync(0xffffffffu, gl, j);
+    const float h = __uint_as_float(hv[j]);
+    const float u = __uint_as_float(uv[j]);
+    const float t = __uint_as_float(tv[j]);
+    const float sig = sigmoid_f(h);
+    const float a_pre = (h * sig) * u;  // = silu_f(h) * u
+    const float a = __bfloat162float(__float2bfloat16_rn(a_pre));
+    dots[j] = t * a_pre;
+    const float da = g * t;
+    if (j < nv) {
+      const size_t o = static_cast<size_t>(row0 + j) * P.I + icol;
+      P.dh[o] = __float2bfloat16_rn(da * u * sig * (1.0f + h * (1.0f - sig)));
+      P.du[o] = __float2bfloat16_rn(da * h * sig);
+      P.ag[o] = __float2bfloat16_rn(g * a);
+    }
+  }
+#pragma unroll
+  for (int sh = 16; sh >= 1; sh >>= 1) {
+    const bool upper = (lane & sh) != 0;
+#pragma unroll
+    for (int j = 0; j < sh; ++j) {
+      const float send = upper ? dots[j] : dots[j + sh];
+      const float keep = upper ? dots[j + sh] : dots[j];
+      dots[j] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
+    }
+  }
+  if (P.dgp && lane < nv) P.dgp[(row0 + lane) * nI32 + c.nt * 4 + ew] = dots[0];
+}
 
 // ---------------------------------------------------------------------------
 struct DgradCfg {
@@ -116,18 +170,12 @@ struct DgradCfg {
     }
   }
 
-  // Lane l of warp w owns I column nt*128 + 32w + l; per chunk of 32 rows it
-  // loads h, u, t of those rows, forms a = bf16(SiLU(h) u), da = g t,
-  // dh = bf16(da u SiLU'(h)), du = bf16(da SiLU(h)), a_g = bf16(g a) (each
-  // row's 32 columns of the warp are one 64-byte store), and the warp's
-  // partial <t, a> of each row over its 32 columns (a butterfly that leaves
-  // row 32 c + l's sum in lane l), stored at dgp[row][nt*4 + w].
+  // Lane l of warp w owns I column nt*128 + 32w + l; per chunk of 32 rows
+  // it loads h, u, t of those rows and runs dgrad_chunk.
   __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
                                   int lane, bool, uint8_t*) {
     const int nrows = tile_rows(c);
     const int64_t row0 = c.row0 + c.mt * ROWS;
-    const int icol = c.nt * 128 + ew * 32 + lane;
-    const int nI32 = P.I / 32;
 #pragma unroll 1
     for (int cc = 0; cc * 32 < nrows; ++cc) {
       uint32_t hv[32], uv[32], tv[32];
@@ -135,37 +183,90 @@ struct DgradCfg {
       tmem_ld32(taddr + ROWS + cc * 32, uv);
       tmem_ld32(taddr + 2 * ROWS + cc * 32, tv);
       tmem_ld_wait();
-      const int jr = cc * 32 + lane;
-      const float gl = (P.g_route && jr < nrows) ? P.g_route[row0 + jr] : 1.0f;
-      float dots[32];
+      dgrad_chunk(P, c, row0 + cc * 32, min(nrows - cc * 32, 32), ew, lane, hv, uv, tv);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// dgrad of the experts whose h, u the forward kept: t^T = W_down^T dYg^T
+// only (TMEM lane = I column, column = row, as DgradCfg), 64-wide K blocks
+// (W_down MN-major, dY K-major, both 128-byte swizzle), two accumulators so
+// that a tile's epilogue overlaps the next tile's loads and MMAs.  The
+// epilogue reads the kept h, u (fp32, [rows][2I]: h then u) of its rows:
+// per row the warp's 32 lanes read 128 contiguous bytes of each.
+struct DgradKeptCfg {
+  static constexpr int BKD = 64;
+  static constexpr int ROWS = 160;                // rows per tile (N = rows rounded up to 16)
+  static constexpr int WDCHUNK = BKD * 128;       // 8 KB: 64 K rows x 64 I columns, MN-major
+  static constexpr int RT = ROWS * BKD * 2;       // 20 KB: 160 rows x 64 bf16, K-major
+  static constexpr int OFF_DY = 2 * WDCHUNK;
+  static constexpr int STAGES = 5;
+  static constexpr int STAGE_BYTES = OFF_DY + RT;  // 36 KB: W_down, dY
+  static constexpr int EPI_SMEM_BYTES = 0;
+  static constexpr int NUM_ACC = 2;
+  static constexpr int ACC_COLS = ROWS;
+  static constexpr uint32_t TMEM_COLS = 512;
+
+  struct Params {
+    SchedArgs sched;         // bm = ROWS; split_side 1: the kept groups only
+    int* status;
+    CUtensorMap tmDy;        // [rows][D], K-major boxes 160 x 64
+    CUtensorMap tmWd;        // [G*D][I], MN-major boxes 64 x 64
+    int32_t I, D;
+    const float* g_route;    // [rows] or null (weight 1)
+    const float* act;        // kept h, u [rows][2I]
+    __nv_bfloat16 *dh, *du, *ag;  // [rows][I]
+    float* dgp;              // [rows][I/32] or null
+  };
+
+  __device__ static uint32_t full_arrivals(const Params&) { return 1; }
+  __device__ static uint32_t tx_bytes(const Params&) { return STAGE_BYTES; }
+
+  __device__ static void load(const Params& P, const TileCoord& c, int kb, uint8_t* st,
+                              uint64_t* bar, int lane) {
+    if (lane != 0) return;
+    const int k0 = kb * BKD;
+    const int drow = c.g * P.D + k0;
+    tma_load_2d(st, &P.tmWd, c.nt * 128, drow, bar);
+    tma_load_2d(st + WDCHUNK, &P.tmWd, c.nt * 128 + 64, drow, bar);
+    tma_load_2d(st + OFF_DY, &P.tmDy, k0, c.row0 + c.mt * ROWS, bar);
+  }
+
+  __device__ static void fixup(const Params&, const TileCoord&, int, uint8_t*, int) {}
+
+  __device__ static int tile_rows(const TileCoord& c) {
+    const int n = c.rows - c.mt * ROWS;
+    return n < ROWS ? n : ROWS;
+  }
+
+  __device__ static void mma(const Params&, const TileCoord& c, int kb, uint8_t* st, uint32_t d) {
+    const uint32_t s = smem_u32(st);
+    const uint32_t id_t = idesc_bf16(128, (tile_rows(c) + 15) & ~15, true, false);
+#pragma unroll
+    for (int k = 0; k < BKD / 16; ++k)
+      mma_bf16(d, sdesc_sw128(s + k * 2048, WDCHUNK, 1024), kdesc(s + OFF_DY + k * 32), id_t, (kb | k) != 0);
+  }
+
+  __device__ static void epilogue(const Params& P, const TileCoord& c, uint32_t taddr, int ew,
+                                  int lane, bool, uint8_t*) {
+    const int nrows = tile_rows(c);
+    const int64_t row0 = c.row0 + c.mt * ROWS;
+    const int64_t ld = 2 * static_cast<int64_t>(P.I);
+    const float* hp = P.act + row0 * ld + c.nt * 128 + ew * 32 + lane;
+#pragma unroll 1
+    for (int cc = 0; cc * 32 < nrows; ++cc) {
+      const int nv = min(nrows - cc * 32, 32);
+      uint32_t hv[32], uv[32], tv[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float g = __shfl_sync(0xffffffffu, gl, j);
-        const float h = __uint_as_float(hv[j]);
-        const float u = __uint_as_float(uv[j]);
-        const float t = __uint_as_float(tv[j]);
-        const float sig = sigmoid_f(h);
-        const float a = __bfloat162float(__float2bfloat16_rn((h * sig) * u));  // = bf16(silu_f(h) * u)
-        dots[j] = t * a;
-        const float da = g * t;
-        if (cc * 32 + j < nrows) {
-          const size_t o = static_cast<size_t>(row0 + cc * 32 + j) * P.I + icol;
-          P.dh[o] = __float2bfloat16_rn(da * u * sig * (1.0f + h * (1.0f - sig)));
-          P.du[o] = __float2bfloat16_rn(da * h * sig);
-          P.ag[o] = __float2bfloat16_rn(g * a);
-        }
+        const float* q = hp + (cc * 32 + j) * ld;
+        hv[j] = j < nv ? __float_as_uint(__ldg(q)) : 0u;
+        uv[j] = j < nv ? __float_as_uint(__ldg(q + P.I)) : 0u;
       }
-#pragma unroll
-      for (int s = 16; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
-#pragma unroll
-        for (int j = 0; j < s; ++j) {
-          const float send = upper ? dots[j] : dots[j + s];
-          const float keep = upper ? dots[j + s] : dots[j];
-          dots[j] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-        }
-      }
-      if (P.dgp && jr < nrows) P.dgp[(row0 + jr) * nI32 + c.nt * 4 + ew] = dots[0];
+      tmem_ld32(taddr + cc * 32, tv);
+      tmem_ld_wait();
+      dgrad_chunk(P, c, row0 + cc * 32, nv, ew, lane, hv, uv, tv);
     }
   }
 };
@@ -400,11 +501,15 @@ bool mnmap(CUtensorMap* m, const void* p, int64_t rows, int cols) {
 mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
                             const void* w_up, const void* w_down, const int32_t* offsets, int G,
                             int D, int I, const float* g_route, void* dh, void* du, void* ag,
-                            float* dgp, cudaStream_t st) {
+                            float* dgp, cudaStream_t st, int32_t skip_rows_below) {
   if (rows == 0) return MOK_OK;
   DgradCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradCfg::BKD);
   P.sched.bm = DgradCfg::ROWS;
+  if (skip_rows_below > 0 && offsets) {  // the groups the forward kept are another launch's
+    P.sched.row_split = skip_rows_below;
+    P.sched.split_side = 2;
+  }
   P.status = status_ptr();
   if (!P.status) return MOK_ERR_CUDA;
   const int groups = offsets ? G : 1;
@@ -426,6 +531,33 @@ mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const
   P.ag = static_cast<__nv_bfloat16*>(ag);
   P.dgp = dgp;
   return run<DgradCfg>(P, st);
+}
+
+mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_down, const int32_t* offsets, int G,
+                                 int D, int I, const float* g_route, const float* act, int32_t kept_rows, void* dh,
+                                 void* du, void* ag, float* dgp, cudaStream_t st) {
+  if (rows == 0 || kept_rows <= 0 || !offsets) return MOK_OK;
+  DgradKeptCfg::Params P;
+  P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradKeptCfg::BKD);
+  P.sched.bm = DgradKeptCfg::ROWS;
+  P.sched.row_split = kept_rows;
+  P.sched.split_side = 1;
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  if (!make_tmap_2d(&P.tmDy, dyg, kBF16, rows, D, static_cast<uint64_t>(D) * 2, DgradKeptCfg::ROWS,
+                    DgradKeptCfg::BKD, true) ||
+      !make_tmap_2d(&P.tmWd, w_down, kBF16, static_cast<int64_t>(G) * D, I, static_cast<uint64_t>(I) * 2,
+                    DgradKeptCfg::BKD, 64, true))
+    return MOK_ERR_CUDA;
+  P.I = I;
+  P.D = D;
+  P.g_route = g_route;
+  P.act = act;
+  P.dh = static_cast<__nv_bfloat16*>(dh);
+  P.du = static_cast<__nv_bfloat16*>(du);
+  P.ag = static_cast<__nv_bfloat16*>(ag);
+  P.dgp = dgp;
+  return run<DgradKeptCfg>(P, st);
 }
 
 mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,

@@ -43,6 +43,11 @@ struct SchedArgs {
   // tiles that share a weight tile run together), or M tile outer (rows are
   // consumed in order, as a ring dispatch needs).
   int32_t m_outer = 0;
+  // Optional split of the groups at a row limit: split_side 1 keeps only the
+  // groups whose rows all lie below row_split (offsets[g + 1] <= row_split),
+  // split_side 2 only the others; the rest get no tiles.  0: every group.
+  int32_t row_split = 0;
+  int32_t split_side = 0;
 };
 
 struct TileCoord {
@@ -60,6 +65,13 @@ __device__ __forceinline__ int sched_k_blocks(const SchedArgs& s, int rows) {
   return s.k_blocks_fixed > 0 ? s.k_blocks_fixed : (rows + s.bk_rows - 1) / s.bk_rows;
 }
 
+// Tiles of a group with rows [r0, r1), after the optional row split.
+__device__ __forceinline__ int group_tiles(const SchedArgs& s, int r0, int r1) {
+  if (s.split_side == 1 && r1 > s.row_split) return 0;
+  if (s.split_side == 2 && r1 <= s.row_split) return 0;
+  return sched_m_tiles(s, r1 - r0) * s.n_tiles;
+}
+
 __device__ __forceinline__ int extra_tiles(const SchedArgs& s) {
   return s.extra_rows > 0 ? ((s.extra_rows + s.bm - 1) / s.bm) * s.extra_n_tiles : 0;
 }
@@ -75,7 +87,7 @@ __device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart,
   for (int g = g0; g < g0 + per && g < G; ++g) {
     int r0 = s.offsets ? s.offsets[g] : 0;
     int r1 = s.offsets ? s.offsets[g + 1] : s.m_total;
-    local += sched_m_tiles(s, r1 - r0) * s.n_tiles;
+    local += group_tiles(s, r0, r1);
   }
   int incl = local;
 #pragma unroll
@@ -88,7 +100,7 @@ __device__ __forceinline__ int build_tile_table(const SchedArgs& s, int* tstart,
     tstart[g] = run;
     int r0 = s.offsets ? s.offsets[g] : 0;
     int r1 = s.offsets ? s.offsets[g + 1] : s.m_total;
-    run += sched_m_tiles(s, r1 - r0) * s.n_tiles;
+    run += group_tiles(s, r0, r1);
   }
   int total = __shfl_sync(0xffffffffu, incl, 31);
   if (lane == 0) tstart[G] = total;

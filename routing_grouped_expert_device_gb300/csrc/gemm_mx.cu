@@ -28,8 +28,8 @@
 // up/gate : the epilogue forms a = bf16(SiLU(h) u) and quantises it to E4M3
 //           per 32 columns (one TMEM load of 32 columns is one block),
 //           writing a's scale words in the grouped layout.
-// replay  : the up/gate products of the backward, h and u written as bf16.
-// down    : y = bf16(acc).
+// replay  : the up/gate products of the backward, h and u written as fp32.
+// down    : y = bf16(acc), or the fp32 accumulator (the backward's t).
 #include <cuda_fp8.h>
 
 #include "gemm_core.cuh"
@@ -102,8 +102,13 @@ struct MxParams {
   uint32_t* asc;  // up/gate: a scale words, grouped layout [I/128][a_ld]
   int64_t a_ld;
   __nv_bfloat16* y;  // down: y [rows][D]
-  __nv_bfloat16* h_out;  // replay: h, u [rows][I]
+  __nv_bfloat16* h_out;  // bf16 replay outputs h, u [rows][I] (unused: the replay stores fp32)
   __nv_bfloat16* u_out;
+  float* h32;  // kF32: replay h, u [rows][I], or y [rows][D]
+  float* u32;
+  float* y32;
+  float* act;  // up/gate: kept h, u fp32 [rows][2 out_ld] of groups ending at or below act_rows
+  int32_t act_rows;
   int32_t out_ld;
   // bf16 outputs as [rows][out_ld], boxes 32 rows x 64 columns, 128-byte
   // swizzle: y (down), or h and u (replay)
@@ -119,11 +124,18 @@ struct MxParams {
 // CTA copies both); N = the tile's rows rounded up to 16, so the padding
 // rows of a group's last tile cost no MMA work.  The epilogue transposes
 // each 32-row chunk into two boxes.
-template <bool kSwiglu, bool kReplay = false, bool kT = false>
+//
+// kF32 (forms with bf16 outputs): the accumulator is stored unrounded as
+// fp32 (h32 / u32 for the replay, y32 for down) straight from registers;
+// in the transposed form each warp store writes 32 consecutive columns of
+// one row (128 bytes), in the row-major form each thread 128 bytes of its
+// row.
+template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
   static_assert(!kT || !kSwiglu || kReplay, "transposed form: bf16 outputs only");
   constexpr bool kBf16Out = !kSwiglu || kReplay;
+  static_assert(!kF32 || kBf16Out, "fp32 outputs replace the bf16 ones");
   constexpr int STAGES = mx_stages(kBf16Out);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -313,6 +325,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       __nv_bfloat16* outp = kReplay ? (rank ? P.u_out : P.h_out) : P.y;
       const int ch0 = 4 * half;
       const int ch_end = min((t_ncols(c) + 31) / 32, ch0 + 4);
+      if constexpr (kF32) {
+        // lane = output column 32 q + lane; register j = row ch * 32 + j
+        float* out32 = kReplay ? (rank ? P.u32 : P.h32) : P.y32;
+#pragma unroll 1
+        for (int ch = ch0; ch < ch_end; ++ch) {
+          const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
+          uint32_t v[32];
+          tmem_ld32(taddr + ch * 32, v);
+          tmem_ld_wait();
+          float* o = out32 + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) o[static_cast<int64_t>(j) * P.out_ld] = __uint_as_float(v[j]);
+        }
+        tc_fence_before();
+        if (leader) mbar_arrive(tempty);  // the accumulator is free for the next tile
+        else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+        continue;
+      }
       if (issuer) bulk_wait_read0();  // the previous tile's stores have read the boxes
       named_bar(bar, 128);
 #pragma unroll 1
@@ -373,6 +404,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int local = c.mt * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;  // row within the group
       const bool valid = local < c.rows;
       const int64_t row = c.row0 + local;
+      if (kF32) {
+        // 256 fp32 columns per row: y (down), or h then u (replay); this
+        // warp drains 128 of them, 32 per TMEM load, each thread storing its
+        // row's 128 bytes
+#pragma unroll 1
+        for (int ch = 4 * half; ch < 4 * half + 4; ++ch) {
+          uint32_t v[32];
+          tmem_ld32(taddr + ch * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            float* dst = kReplay ? (ch < 4 ? P.h32 : P.u32) + row * P.out_ld + c.nt * 128 + (ch & 3) * 32
+                                 : P.y32 + row * P.out_ld + c.nt * 256 + ch * 32;
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+              st_global_v4(dst + qq * 4, v[4 * qq], v[4 * qq + 1], v[4 * qq + 2], v[4 * qq + 3]);
+          }
+        }
+        tc_fence_before();
+        if (leader) mbar_arrive(tempty);
+        else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+        continue;
+      }
       if (kBf16Out) {
         // 256 bf16 columns per row: y (down), or h then u (replay); this
         // warp drains 128 of them.  A full 32-row slab is drained into the
@@ -431,12 +484,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       if (kSwiglu) {
         uint32_t words = 0;
+        const bool keep = P.act && valid && c.row0 + c.rows <= P.act_rows;
 #pragma unroll 1
         for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
           uint32_t hv[32], uv[32];
           tmem_ld32(taddr + ch * 32, hv);
           tmem_ld32(taddr + 128 + ch * 32, uv);
           tmem_ld_wait();
+          if (keep) {  // this row's 32 columns of h and of u, unrounded
+            float* ar = P.act + row * (2 * P.out_ld) + c.nt * 128 + ch * 32;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              st_global_v4(ar + 4 * q, hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+              st_global_v4(ar + P.out_ld + 4 * q, uv[4 * q], uv[4 * q + 1], uv[4 * q + 2], uv[4 * q + 3]);
+            }
+          }
           float av[32];
           float amax = 0.0f;
 #pragma unroll
@@ -487,11 +549,11 @@ size_t mx_smem_bytes(int G, bool bf16_out) {
          (bf16_out ? STAGING_BYTES : 0) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
-template <bool kSwiglu, bool kReplay = false, bool kT = false>
+template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st) {
   const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT>;
+  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
@@ -552,6 +614,11 @@ mok_status upgate_mx_params(MxParams& P, const void* xq, const void* xsc, int64_
   P.y = nullptr;
   P.h_out = nullptr;
   P.u_out = nullptr;
+  P.h32 = nullptr;
+  P.u32 = nullptr;
+  P.y32 = nullptr;
+  P.act = nullptr;
+  P.act_rows = 0;
   P.out_ld = I;
   return MOK_OK;
 }
@@ -559,7 +626,7 @@ mok_status upgate_mx_params(MxParams& P, const void* xq, const void* xsc, int64_
 
 mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
                             const void* sg, const void* qu, const void* su, const int32_t* offsets,
-                            int G, int D, int I, void* aq, void* asc, cudaStream_t st) {
+                            int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept) {
   if (rows == 0) return MOK_OK;
   if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
@@ -567,28 +634,33 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
   if (r != MOK_OK) return r;
   P.aq = static_cast<uint8_t*>(aq);
   P.asc = static_cast<uint32_t*>(asc);
+  P.act = kept.act;
+  P.act_rows = kept.limit();
   return run_mx<true>(P, st);
 }
 
 mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const void* qg, const void* sg,
                             const void* qu, const void* su, const int32_t* offsets, int G, int D, int I, void* h,
-                            void* u, cudaStream_t st) {
+                            void* u, cudaStream_t st, int32_t skip_rows_below) {
   if (rows == 0) return MOK_OK;
   if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
   mok_status r = upgate_mx_params(P, xq, xsc, rows, qg, sg, qu, su, offsets, G, D, I);
   if (r != MOK_OK) return r;
-  P.h_out = static_cast<__nv_bfloat16*>(h);
-  P.u_out = static_cast<__nv_bfloat16*>(u);
-  if (!out_map(&P.tmO0, h, rows, I) || !out_map(&P.tmO1, u, rows, I)) return MOK_ERR_CUDA;
+  if (skip_rows_below > 0) {  // the groups the forward kept need no replay
+    P.sched.row_split = skip_rows_below;
+    P.sched.split_side = 2;
+  }
+  P.h32 = static_cast<float*>(h);
+  P.u32 = static_cast<float*>(u);
   // as the down form: the routed rows as N for groups under 512 rows on average
-  if (rows < static_cast<int64_t>(512) * G) return run_mx<true, true, true>(P, st);
-  return run_mx<true, true>(P, st);
+  if (rows < static_cast<int64_t>(512) * G) return run_mx<true, true, true, true>(P, st);
+  return run_mx<true, true, false, true>(P, st);
 }
 
 mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
                           const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool f32_out) {
   if (rows == 0) return MOK_OK;
   if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
@@ -606,16 +678,27 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   P.b1_off = 128;
   P.aq = nullptr;
   P.asc = nullptr;
+  P.act = nullptr;
+  P.act_rows = 0;
   P.a_ld = 0;
-  P.y = static_cast<__nv_bfloat16*>(y);
   P.h_out = nullptr;
   P.u_out = nullptr;
+  P.h32 = nullptr;
+  P.u32 = nullptr;
   P.out_ld = D;
+  const bool by_rows = rows < static_cast<int64_t>(512) * G;
+  if (f32_out) {
+    P.y = nullptr;
+    P.y32 = static_cast<float*>(y);
+    return by_rows ? run_mx<false, false, true, true>(P, st) : run_mx<false, false, false, true>(P, st);
+  }
+  P.y = static_cast<__nv_bfloat16*>(y);
+  P.y32 = nullptr;
   if (!out_map(&P.tmO0, y, rows, D)) return MOK_ERR_CUDA;
   P.tmO1 = P.tmO0;
   // fewer than 512 routed rows per group on average: the routed rows as the
   // MMA's N dimension (no padding rows in the MMAs)
-  if (rows < static_cast<int64_t>(512) * G) return run_mx<false, false, true>(P, st);
+  if (by_rows) return run_mx<false, false, true>(P, st);
   return run_mx<false>(P, st);
 }
 

@@ -72,6 +72,11 @@ struct PairParams {
   // valid; s_out [rows][E] fp32.
   float* s_out;
   int32_t E;
+  // Kept activations (kSwiglu, optional): h, u fp32 of the routed rows of
+  // every group whose rows end at or below act_rows, as [rows][2 * act_i]
+  // (h in columns [0, act_i), u in [act_i, 2 act_i)).
+  float* act;
+  int32_t act_rows, act_i;
 };
 
 // ---------------------------------------------------------------------------
@@ -398,6 +403,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         continue;
       }
       const int y = (c.extra ? 0 : c.row0) + slab;  // its row in the output tensor
+      // h, u of this group go to the kept-activation store
+      const bool keep = kSwiglu && P.act && !c.extra && c.row0 + c.rows <= P.act_rows;
       const CUtensorMap* tmOut = c.extra ? &P.tmOut_s : &P.tmOut;
       __nv_bfloat16* orow = c.extra ? P.out_s + static_cast<size_t>(y + lane) * P.out_ld_s
                                     : P.out + static_cast<size_t>(y + lane) * P.out_ld;
@@ -414,6 +421,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
             tmem_ld32(taddr + ch * 32, h);
             tmem_ld32(taddr + 128 + ch * 32, u);
             tmem_ld_wait();
+            if (keep && lane < nvalid) {
+              float* ar = P.act + static_cast<int64_t>(y + lane) * (2 * P.act_i) + c.nt * 128 + ch * 32;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                st_global_v4(ar + 4 * q, h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+                st_global_v4(ar + P.act_i + 4 * q, u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+              }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               pk[hh * 16 + j] = pack_bf16x2(silu_f(__uint_as_float(h[2 * j])) * __uint_as_float(u[2 * j]),
@@ -553,6 +568,8 @@ struct PairTParams {
   CUtensorMap tmOut;     // a [rows][I], boxes 32 rows x 64 columns, 128-byte swizzle
   __nv_bfloat16* out;
   int32_t I;
+  float* act;            // kept h, u (as PairParams::act), or null
+  int32_t act_rows;
 };
 
 constexpr int T_OUT_BYTES = 32 * 128;       // one [32 rows][64 columns] bf16 box of a
@@ -729,12 +746,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       const int nrows = min(c.rows - c.mt * 256, 256);  // valid routed rows of the tile
       const int row0 = c.row0 + c.mt * 256;             // the tile's first row of a
       const int ocol = c.nt * 128 + static_cast<int>(rank) * 64;  // first column of a of this CTA
+      // kept activations: lane = column ocol + 32 hq + lane of h (h warps) or
+      // u (u warps), register j = row; each store writes 128 bytes of a row
+      const bool keep = P.act && c.row0 + c.rows <= P.act_rows;
+      float* kept = keep ? P.act + static_cast<int64_t>(row0) * (2 * P.I) + (hwarp ? 0 : P.I) + ocol + 32 * hq + lane
+                         : nullptr;
 #pragma unroll 1
       for (int ch = 0; ch * 32 < n; ++ch) {
         const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
         uint32_t v[32];
         tmem_ld32(taddr + ch * 32, v);
         tmem_ld_wait();
+        if (keep) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) kept[static_cast<int64_t>(ch * 32 + j) * (2 * P.I)] = __uint_as_float(v[j]);
+        }
         if (!hwarp) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) xb[j * 32 + lane] = __uint_as_float(v[j]);
@@ -794,7 +821,7 @@ size_t pair_t_smem_bytes(int G) {
 
 mok_status launch_upgate_pair_t(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                                 const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                                cudaStream_t st) {
+                                cudaStream_t st, KeptAct kept) {
   PairTParams P{};
   P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
   P.status = status_ptr();
@@ -808,6 +835,8 @@ mok_status launch_upgate_pair_t(const void* A, int64_t a_rows, const void* w_gat
     return MOK_ERR_CUDA;
   P.out = static_cast<__nv_bfloat16*>(a_out);
   P.I = I;
+  P.act = kept.act;
+  P.act_rows = kept.limit();
   const size_t smem = pair_t_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(gemm_pair_upgate_t, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1108,7 +1137,7 @@ mok_status launch_down_pair_t(const void* a, int64_t a_rows, const void* w_down,
 
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                              cudaStream_t st, const SharedOperands* sh) {
+                              cudaStream_t st, const SharedOperands* sh, KeptAct kept) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
   // Routed rows alone, fewer than 512 per expert on average: the transposed
   // kernel, whose MMAs skip the padding rows of each expert's last tile
@@ -1116,7 +1145,7 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
   // padding, and the row-major kernel's lighter epilogue measured 0.3-0.6 %
   // faster (the skewed 16384-token layer).
   if (offsets && !(sh && sh->rows) && m_total < static_cast<int64_t>(512) * G)
-    return launch_upgate_pair_t(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st);
+    return launch_upgate_pair_t(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st, kept);
   PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
   P.status = status_ptr();
@@ -1150,6 +1179,11 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
     P.sched.extra_k_blocks = D / BK;
     P.out_s = static_cast<__nv_bfloat16*>(sh->out);
     P.out_ld_s = Is;
+  }
+  if (offsets) {
+    P.act = kept.act;
+    P.act_rows = kept.limit();
+    P.act_i = I;
   }
   if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
   return run_pair<true>(P, st);
@@ -1238,7 +1272,8 @@ mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, in
 
 mok_status launch_upgate_ring(const void* x, const int32_t* table, int K, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t R, int D, int I, void* a_out, void* ring,
-                              int64_t ring_rows, int chunk_rows, int32_t* counters, cudaStream_t st) {
+                              int64_t ring_rows, int chunk_rows, int32_t* counters, cudaStream_t st,
+                              KeptAct kept) {
   if (R == 0) return MOK_OK;
   if (!offsets || chunk_rows < 128 || ring_rows < chunk_rows || ring_rows % chunk_rows) return MOK_ERR_INVALID_ARG;
   const int64_t nchunks = (R + chunk_rows - 1) / chunk_rows;
@@ -1276,6 +1311,9 @@ mok_status launch_upgate_ring(const void* x, const int32_t* table, int K, const 
   P.n_tiles = I / 128;
   P.ready = counters;
   P.done = counters + nchunks;
+  P.act = kept.act;
+  P.act_rows = kept.limit();
+  P.act_i = I;
   if (!set_out_maps(P, R)) return MOK_ERR_CUDA;
   return run_pair<true, true>(P, st);
 }

@@ -1,6 +1,8 @@
 // Host-side launchers shared between the translation units of libmok.
 #pragma once
 
+#include <climits>
+
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -42,6 +44,17 @@ mok_status launch_combine(const void* rows, const void* base, const float* w,
                           const int32_t* route_dst, int T, int K, int D, void* out,
                           cudaStream_t st);
 
+// Kept activations of the forward's routed up/gate (mok_plan_buf::act): h, u
+// fp32 [rows][2I] of every group whose rows end at or below `rows`; null /
+// 0: none kept.
+struct KeptAct {
+  float* act = nullptr;
+  int64_t rows = 0;
+  int32_t limit() const {  // the row limit as the kernels compare it
+    return act ? static_cast<int32_t>(rows < INT32_MAX ? rows : INT32_MAX) : 0;
+  }
+};
+
 // Forward grouped GEMMs (CTA pairs, gemm_pair.cu).  offsets == nullptr: one
 // group of m_total rows.
 //  up/gate: a[rows][I] = bf16(SiLU(A W_gate^T) * (A W_up^T)), A [rows][D]
@@ -65,7 +78,7 @@ struct SharedOperands {
 // routed launch (cta_group::2, 256-row tiles).
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                              cudaStream_t st, const SharedOperands* sh = nullptr);
+                              cudaStream_t st, const SharedOperands* sh = nullptr, KeptAct kept = {});
 // Router scores s = softmax(x W_r^T) [T][E] fp32 (E <= 256): x [T][D], W_r
 // [E][D] bf16, on CTA pairs with the softmax in the epilogue.
 mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, int E, int D, float* s_out,
@@ -75,7 +88,8 @@ mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, in
 // chunks of chunk_rows routed rows; counters: 2 * ceil(R / chunk_rows) ints.
 mok_status launch_upgate_ring(const void* x, const int32_t* table, int K, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t R, int D, int I, void* a_out, void* ring,
-                              int64_t ring_rows, int chunk_rows, int32_t* counters, cudaStream_t st);
+                              int64_t ring_rows, int chunk_rows, int32_t* counters, cudaStream_t st,
+                              KeptAct kept = {});
 // Ring geometry for R routed rows and chunk b (0: 2048): 4 slots of b rows,
 // or fewer when that already holds every row (then no slot is reused).
 constexpr int64_t kRingSlots = 4;
@@ -95,11 +109,17 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
 
 // Backward.  dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
 // non-null, dgp [rows][I/32] partials of <t, a> (32 I columns each);
-// g_route null = weight 1.
+// g_route null = weight 1.  skip_rows_below > 0: only the groups with a row
+// at or above it (the others were kept by the forward).
 mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
                             const void* w_up, const void* w_down, const int32_t* offsets, int G,
                             int D, int I, const float* g_route, void* dh, void* du, void* ag,
-                            float* dgp, cudaStream_t st);
+                            float* dgp, cudaStream_t st, int32_t skip_rows_below = 0);
+// The same outputs for the groups whose rows all lie below kept_rows, from
+// the forward's kept h, u (act fp32 [rows][2I]) and t = dYg W_down.
+mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_down, const int32_t* offsets, int G,
+                                 int D, int I, const float* g_route, const float* act, int32_t kept_rows, void* dh,
+                                 void* du, void* ag, float* dgp, cudaStream_t st);
 // dx [rows][D] = bf16(dh W_gate + du W_up)
 mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,
                          const void* w_up, const int32_t* offsets, int G, int D, int I, void* dx,
@@ -107,17 +127,20 @@ mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const voi
 // dw [G][M][N] = bf16(sum over each group's rows of pm[p][m] qn[p][n])
 mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
                         int G, int M, int N, void* dw, cudaStream_t st);
-// MXFP8 backward.  Replay: h, u bf16 [rows][I] from the up/gate pair GEMM
-// (operands as launch_upgate_mx).  Activation gradient: from bf16 h, u, t
-// [R][I] and g_route (null = 1): dh, du, a_g bf16 [R][I], the codes of
-// [dh | du] [R][2I] with grouped scale words (ld = mx_scale_ld(R, E)) and
-// dgp [R] = <t, a>.
+// MXFP8 backward.  Replay: h, u fp32 [rows][I] from the up/gate pair GEMM
+// (operands as launch_upgate_mx); skip_rows_below > 0: only the groups with
+// a row at or above it.  Activation gradient: from fp32 h, u, t [R][I] and
+// g_route (null = 1): dh, du, a_g bf16 [R][I], the codes of [dh | du]
+// [R][2I] with grouped scale words (ld = mx_scale_ld(R, E)) and dgp [R] =
+// <t, a>; the rows of groups that end at or below kept.rows read h, u from
+// kept.act ([rows][2I]) instead.
 mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const void* qg, const void* sg,
                             const void* qu, const void* su, const int32_t* offsets, int G, int D, int I, void* h,
-                            void* u, cudaStream_t st);
+                            void* u, cudaStream_t st, int32_t skip_rows_below = 0);
 mok_status launch_act_grad_mx(const void* h, const void* u, const void* t, const float* g_route,
                               const int32_t* table, const int32_t* offsets, int64_t R, int I, int E, void* dh,
-                              void* du, void* ag, void* dhu_q, uint8_t* dhu_sc, float* dgp, cudaStream_t st);
+                              void* du, void* ag, void* dhu_q, uint8_t* dhu_sc, float* dgp, cudaStream_t st,
+                              KeptAct kept = {});
 // Codes of src^T per matrix: src bf16 [G][M][N]; output row g N + n holds
 // src[g][:, n] quantised along M at columns [col0, col0 + M) of out_cols,
 // plain scale layout of G*N rows (M, col0, out_cols multiples of 128, N of 64).
@@ -150,14 +173,27 @@ inline int64_t mx_scale_ld(int64_t rows, int groups = 0) {
 inline size_t mx_scale_bytes(int64_t rows, int64_t K, int groups = 0) {
   return static_cast<size_t>(K / 128) * static_cast<size_t>(mx_scale_ld(rows, groups)) * 4;
 }
-// MXFP8 grouped GEMMs: a codes [rows][I] + scales, y bf16 [rows][D]
+// MXFP8 grouped GEMMs: a codes [rows][I] + scales, y [rows][D] (bf16, or
+// fp32 when f32_out: the backward's t)
 mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
                             const void* sg, const void* qu, const void* su, const int32_t* offsets,
-                            int G, int D, int I, void* aq, void* asc, cudaStream_t st);
+                            int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept = {});
 mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
                           const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
-                          cudaStream_t st);
+                          cudaStream_t st, bool f32_out = false);
 
 bool shape_ok(const mok_shape* s);
+
+// Device address of a __device__ variable (its host-side stand-in `symbol`)
+// on the current device.  cudaGetSymbolAddress is called once per device and
+// context: the result is cached with the id of the context it was made in
+// and looked up again when another context is current (for instance the new
+// primary context after cudaDeviceReset, which reloads the module), so a
+// stale address is never handed out.  Null on failure.
+struct SymbolCache {
+  void* addr[64] = {};
+  unsigned long long ctx[64] = {};
+};
+void* symbol_address(const void* symbol, SymbolCache& cache);
 
 }  // namespace mok

@@ -12,9 +12,9 @@
 // The array is `static __device__`, so every GPU that loads the library holds
 // kStaticPlanScratchInts * 4 bytes (1 MiB) until the process exits.  In host
 // code the name g_plan_scratch is only a host-side stand-in: the kernels get
-// its device address, looked up once per device with cudaGetSymbolAddress.
-#include <mutex>
-
+// its device address, looked up with cudaGetSymbolAddress once per device
+// and context (again after a cudaDeviceReset, whose new context reloads the
+// module and may place the array elsewhere).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -25,23 +25,13 @@ constexpr int kStaticPlanScratchInts = 1 << 18;
 
 static __device__ __align__(256) int g_plan_scratch[kStaticPlanScratchInts];
 
-constexpr int kMaxDevices = 64;
-int* g_scratch_addr[kMaxDevices];
-std::mutex g_scratch_mu;
+mok::SymbolCache g_scratch_cache;
 
-// Device address of g_plan_scratch on the current device.  The first call on
-// a device performs the lookup (with that device current) and caches it.
+// Device address of g_plan_scratch on the current device (with that device
+// current): looked up on the first call in each context, then cached.
 mok_status scratch_address(int** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOK_ERR_CUDA;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_plan_scratch) != cudaSuccess || !p) return MOK_ERR_CUDA;
-    g_scratch_addr[dev] = static_cast<int*>(p);
-  }
-  *out = g_scratch_addr[dev];
-  return MOK_OK;
+  *out = static_cast<int*>(mok::symbol_address(g_plan_scratch, g_scratch_cache));
+  return *out ? MOK_OK : MOK_ERR_CUDA;
 }
 
 }  // namespace

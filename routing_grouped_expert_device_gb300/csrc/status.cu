@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kernels.h"
 
 namespace {
 
@@ -12,11 +13,35 @@ namespace {
 __device__ int g_status_word;
 
 constexpr int kMaxDevices = 64;
-int* g_status_addr[kMaxDevices];
+mok::SymbolCache g_status_cache;
 int g_num_sms[kMaxDevices];
 std::mutex g_mu;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+template <class F>
+bool driver_fn(const char* name, int version, F* out) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  *out = reinterpret_cast<F>(fn);
+  return true;
+}
+
+// Id of the context current on this thread (unique for the life of the
+// process; a context made after cudaDeviceReset gets a new one).  Called
+// with g_mu held.
+bool current_context_id(unsigned long long* id) {
+  if (!g_ctx_current && !driver_fn("cuCtxGetCurrent", 4000, &g_ctx_current)) return false;
+  if (!g_ctx_id && !driver_fn("cuCtxGetId", 12000, &g_ctx_id)) return false;
+  CUcontext c = nullptr;
+  if (g_ctx_current(&c) != CUDA_SUCCESS || !c) return false;
+  return g_ctx_id(c, id) == CUDA_SUCCESS;
+}
 
 int current_device() {
   int d = 0;
@@ -28,17 +53,24 @@ int current_device() {
 
 namespace mok {
 
-int* status_ptr() {
+void* symbol_address(const void* symbol, SymbolCache& cache) {
   int d = current_device();
   if (d < 0 || d >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_addr[d]) {
+  unsigned long long ctx = 0;
+  const bool known = current_context_id(&ctx);
+  if (!known || !cache.addr[d] || cache.ctx[d] != ctx) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    g_status_addr[d] = static_cast<int*>(p);
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+    // the lookup made the device's context current if none was
+    if (!known && !current_context_id(&ctx)) ctx = 0;
+    cache.addr[d] = p;
+    cache.ctx[d] = ctx;
   }
-  return g_status_addr[d];
+  return cache.addr[d];
 }
+
+int* status_ptr() { return static_cast<int*>(symbol_address(&g_status_word, g_status_cache)); }
 
 int num_sms() {
   int d = current_device();

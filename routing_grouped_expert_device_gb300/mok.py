@@ -42,7 +42,8 @@ class Weights(ctypes.Structure):
 
 
 class PlanBuf(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst")]
+    _fields_ = ([(n, ctypes.c_void_p) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst", "act")]
+                + [("act_rows", ctypes.c_int64)])
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -53,6 +54,7 @@ _SZ = ctypes.c_size_t
 
 _SIGS = {
     "mok_workspace_bytes": (_SZ, [ctypes.POINTER(Shape), ctypes.c_int]),
+    "mok_workspace_offset": (_SZ, [ctypes.POINTER(Shape), ctypes.c_int]),
     "mok_route": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "mok_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "mok_plan_static": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
@@ -147,11 +149,27 @@ def make_weights(t: Dict[str, object]) -> Weights:
 
 
 def make_plan_buf(t: Dict[str, object]) -> PlanBuf:
-    return PlanBuf(*(_ptr(t[n]) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst")))
+    """The forward's saved state; optional "act" (fp32 [rows][2I]) keeps h, u
+    of the experts whose rows lie below its row count for the backward."""
+    act = t.get("act")
+    rows = int(act.shape[0]) if act is not None else 0
+    return PlanBuf(*(_ptr(t[n]) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst")),
+                   _ptr(act), rows)
 
 
 def workspace_bytes(shape: Shape, op: int) -> int:
     return int(_lib_handle().mok_workspace_bytes(ctypes.byref(shape), op))
+
+
+WS_BWD_DH, WS_BWD_DU, WS_BWD_AG = 1, 2, 3
+
+
+def workspace_offset(shape: Shape, region: int) -> int:
+    """Byte offset of a backward intermediate (WS_BWD_*) in the MOK_OP_BWD workspace."""
+    off = int(_lib_handle().mok_workspace_offset(ctypes.byref(shape), region))
+    if off == ctypes.c_size_t(-1).value:
+        raise ValueError("invalid shape or region")
+    return off
 
 
 def route(s, K, topk_idx, g, stream=None):

@@ -25,3 +25,20 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """With MOK_PARITY_REPORT set: the largest |gpu - oracle| / tolerance of
+    every named float check that ran, printed and written as JSON to the
+    path the variable names."""
+    path = os.environ.get("MOK_PARITY_REPORT")
+    if not path:
+        return
+    import json
+    from helpers import PARITY_RATIOS
+    terminalreporter.write_line("parity: max |gpu - oracle| / tolerance per check")
+    for k in sorted(PARITY_RATIOS):
+        v = PARITY_RATIOS[k]
+        terminalreporter.write_line(f"  {k:64s} {v:.4f}" if isinstance(v, float) else f"  {k:64s} {v}")
+    with open(path, "w") as f:
+        json.dump(PARITY_RATIOS, f, indent=1, sort_keys=True)

@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import MXFP8_TOL, alloc_plan, assert_close, host, mok
+from helpers import (MXFP8_TOL, alloc_plan, assert_close, assert_close_ranged, device_weights_fetch, host, mok,
+                     sample_experts, sample_tokens)
 from routing_grouped_expert_device_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -165,7 +166,7 @@ def test_moe_fwd_mxfp8_elementwise_and_deterministic(m, name):
         outs.append(out)
     ref = O.moe_forward_mxfp8(h, cfg.K)
     assert np.array_equal(saved["table"][:cfg.R].cpu().numpy(), ref["table"])
-    assert_close(outs[0].float().cpu().numpy(), ref["out"], MXFP8_TOL, "out")
+    assert_close(outs[0].float().cpu().numpy(), ref["out"], MXFP8_TOL, f"mxfp8 fwd out [{name}]")
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 
@@ -200,6 +201,28 @@ def test_mxfp8_full_size_sampled_rows(m):
                                       W.bf16_bits(d["w_down"][e]))
         assert_close(yg[torch.from_numpy(picks).to(DEV)].float().cpu().numpy(), ref["y"], MXFP8_TOL,
                      f"y expert {e}")
+
+
+def test_moe_fwd_mxfp8_full_size_sampled_tokens(m):
+    """The DSV3 MXFP8 forward through mok_moe_fwd: out rows of 512 seeded
+    tokens against the oracle's MXFP8 forward of those tokens."""
+    from concurrent.futures import ThreadPoolExecutor
+    cfg = W.CONFIGS["dsv3_mxfp8_fwd"]
+    d = mx_weights(m, W.make_inputs(cfg, DEV))
+    shape = m.shape_of(cfg)
+    out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+    saved = alloc_plan(cfg, DEV)
+    m.moe_fwd(shape, m.make_weights(d), d["x"], d["s"], out, ws, m.make_plan_buf(saved))
+    m.check_device_status()
+    s_host = d["s"].cpu().numpy()
+    toks = sample_tokens(cfg.T, 512, seed=3)
+    x_rows = W.bf16_bits(d["x"][torch.from_numpy(toks).to(DEV)])
+    with ThreadPoolExecutor(max_workers=16) as pool:
+        ref = O.moe_forward_tokens(toks, x_rows, s_host[toks], device_weights_fetch(d), cfg.K, mxfp8=True,
+                                   map_fn=pool.map)
+    assert_close(out[torch.from_numpy(toks).to(DEV)].float().cpu().numpy(), ref["out"], MXFP8_TOL,
+                 "mxfp8 fwd out [full]")
 
 
 # ---------------------------------------------------------------- backward
@@ -244,13 +267,15 @@ def test_bwd_weight_copies_bitexact(m):
     assert np.array_equal(words_to_bytes(d["sct_gu"], E * D, 2 * I), sc)
 
 
-def _mx_fwd_bwd(m, cfg, d):
+def _mx_fwd_bwd(m, cfg, d, act_rows=None):
     shape = m.shape_of(cfg)
     w = m.make_weights(d)
     ws = torch.empty(max(m.workspace_bytes(shape, m.OP_FWD), m.workspace_bytes(shape, m.OP_BWD)),
                      dtype=torch.uint8, device=DEV)
     out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
     saved = alloc_plan(cfg, DEV)
+    if act_rows is not None:
+        saved["act"] = torch.full((act_rows, 2 * cfg.I), float("nan"), dtype=torch.float32, device=DEV)
     pb = m.make_plan_buf(saved)
     m.moe_fwd(shape, w, d["x"], d["s"], out, ws, pb)
     bf = torch.bfloat16
@@ -275,14 +300,15 @@ def test_backward_mxfp8_elementwise_and_deterministic(m, name):
     h = host(inp)
     d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
     got = _mx_fwd_bwd(m, cfg, d)
-    ref = O.moe_backward_mxfp8(h, h["dy"], cfg.K)
+    ref = O.moe_backward_mxfp8(h, h["dy"], cfg.K, ranges=True)
     f = lambda t: t.float().cpu().numpy()
-    pairs = [("dx", "dX"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down"),
-             ("dg", "dg"), ("ds", "ds")]
+    for k, r in (("dx", "dX"), ("dg", "dg"), ("ds", "ds")):
+        assert_close(f(got[k]), ref[r], MXFP8_TOL, f"mxfp8 bwd {r} [{name}]")
+    pairs = [("dw_gate", "dW_gate"), ("dw_up", "dW_up"), ("dw_down", "dW_down")]
     if cfg.I_shared:
         pairs += [("dws_gate", "dWs_gate"), ("dws_up", "dWs_up"), ("dws_down", "dWs_down")]
     for k, r in pairs:
-        assert_close(f(got[k]), ref[r], MXFP8_TOL, k)
+        assert_close_ranged(f(got[k]), ref[r], ref["range"][r], MXFP8_TOL, f"mxfp8 bwd {r} [{name}]")
     if name == "skew":
         empty = np.flatnonzero(np.bincount(O.route(h["s"], cfg.K)[0].reshape(-1), minlength=cfg.E) == 0)
         assert len(empty) > 0 and torch.all(got["dw_gate"][torch.from_numpy(empty).to(DEV)] == 0)
@@ -293,13 +319,28 @@ def test_backward_mxfp8_elementwise_and_deterministic(m, name):
 
 
 
+@pytest.mark.parametrize("name", ["ragged", "skew"])
+def test_backward_mxfp8_kept_activations(m, name):
+    """MXFP8: the forward keeps h, u (fp32, from its block-scaled up/gate) of
+    the experts that fit; the backward replays only the others.  Every
+    capacity gives the all-replay path's bytes."""
+    cfg = BWD[name]
+    inp = W.make_inputs(cfg, "cpu", with_dy=True)
+    d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
+    base = _mx_fwd_bwd(m, cfg, d)
+    for rows in (cfg.R, cfg.R // 2):
+        got = _mx_fwd_bwd(m, cfg, d, act_rows=rows)
+        for k, v in base.items():
+            bits = (lambda t: t.view(torch.int16)) if v.dtype == torch.bfloat16 else (lambda t: t.view(torch.int32))
+            assert torch.equal(bits(v), bits(got[k])), (rows, k)
+
+
 def test_backward_mxfp8_full_size_sampled(m):
     """The DSV3 fwd+bwd layer (T 4096, 256 experts) with MXFP8 routed experts:
-    one token's dX, dg and ds (its 8 routes), and whole weight gradients of
-    two experts (the fullest and a middle one), each from the oracle's MXFP8
-    backward of that expert's rows.  The oracle quantises each expert's
-    full weights (about 10 s per expert on one core), so the calls run on a
-    thread pool."""
+    dX, dg and ds of 512 seeded tokens, and whole weight gradients of four
+    experts (the fullest, the emptiest and two seeded ones), each from the
+    oracle's MXFP8 backward of those rows.  The oracle quantises every
+    touched expert's weights, so the calls run on a thread pool."""
     from concurrent.futures import ThreadPoolExecutor
     cfg = W.CONFIGS["dsv3_mxfp8_fwdbwd"]
     d = bwd_weights(m, cfg, W.make_inputs(cfg, DEV))
@@ -308,39 +349,55 @@ def test_backward_mxfp8_full_size_sampled(m):
     idx, g, den = O.route(s_host, cfg.K)
     counts, offsets, table, _ = O.plan(idx, cfg.E)
     f = lambda t: t.float().cpu().numpy()
-    Wsh = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
+    hw = device_weights_fetch(d)
     x_all = W.bf16_bits(d["x"])
     dy_all = W.bf16_bits(d["dy"])
+    toks = sample_tokens(cfg.T, 512, seed=2)
+    sel = torch.from_numpy(toks).to(DEV)
+    with ThreadPoolExecutor(max_workers=16) as pool:
+        ref = O.moe_backward_tokens(x_all[toks], dy_all[toks], s_host[toks], hw, cfg.K, mxfp8=True,
+                                    map_fn=pool.map)
+        assert_close(f(got["dx"][sel]), ref["dX"], MXFP8_TOL, "mxfp8 bwd dX [full]")
+        assert_close(f(got["dg"][sel]), ref["dg"], MXFP8_TOL, "mxfp8 bwd dg [full]")
+        assert_close(f(got["ds"][sel]), ref["ds"], MXFP8_TOL, "mxfp8 bwd ds [full]")
+        experts = sample_experts(counts, 4, seed=4)
 
-    def ew(e):
-        return W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e])
-
-    t = int(np.random.default_rng(2).integers(cfg.T))
-    experts = [int(np.argmax(counts)), cfg.E // 2]
-    jobs = [(t, k, int(idx[t, k])) for k in range(cfg.K)]
-    with ThreadPoolExecutor(max_workers=len(jobs) + len(experts)) as pool:
-        tok = [pool.submit(O.route_backward_rows_mxfp8, x_all[t:t + 1], dy_all[t:t + 1], g[t:t + 1, k], *ew(e))
-               for _, k, e in jobs]
-        rows = {}
-        for e in experts:
+        def expert_grads(e):
             p0, p1 = int(offsets[e]), int(offsets[e + 1])
+            if p0 == p1:
+                return None
             toks_e = table[p0:p1, 0] // cfg.K
             gr = g[toks_e, table[p0:p1, 0] % cfg.K]
-            rows[e] = (toks_e, pool.submit(O.route_backward_rows_mxfp8, x_all[toks_e], dy_all[toks_e], gr, *ew(e)))
-        acc = O.route_backward_rows(x_all[t:t + 1], dy_all[t:t + 1], np.ones(1, np.float32), *Wsh)["dx"][0].copy()
-        dg_t = np.zeros(cfg.K, np.float32)
-        for k, fut in enumerate(tok):
-            b = fut.result()
-            acc = acc + b["dx"][0]
-            dg_t[k] = b["dg"][0]
-        assert_close(f(got["dx"][t]), O.round_bf16(acc), MXFP8_TOL, f"dX[{t}]")
-        assert_close(f(got["dg"][t]), dg_t, MXFP8_TOL, f"dg[{t}]")
-        ds_ref = O.router_grad(dg_t[None], g[t:t + 1], den[t:t + 1], idx[t:t + 1], cfg.E)[0]
-        assert_close(f(got["ds"][t]), ds_ref, MXFP8_TOL, f"ds[{t}]")
-        for e, (toks_e, fut) in rows.items():
-            b = fut.result()
+            b = O.route_backward_rows_mxfp8(x_all[toks_e], dy_all[toks_e], gr, *hw.fetch(e), ranges=True)
             X = O.bf16_to_f32(x_all[toks_e])
             dY = O.bf16_to_f32(dy_all[toks_e])
-            assert_close(f(got["dw_down"][e]), O.round_bf16(dY.T @ b["a_g"]), MXFP8_TOL, f"dW_down[{e}]")
-            assert_close(f(got["dw_gate"][e]), O.round_bf16(b["dh"].T @ X), MXFP8_TOL, f"dW_gate[{e}]")
-            assert_close(f(got["dw_up"][e]), O.round_bf16(b["du"].T @ X), MXFP8_TOL, f"dW_up[{e}]")
+            rg = b["ranges"]
+            lo, hi = O.sum_range(b["a_g"], rg["a_g"], dY)
+            return {"dW_down": (O.round_bf16(dY.T @ b["a_g"]), (lo.T, hi.T)),
+                    "dW_gate": (O.round_bf16(b["dh"].T @ X), O.sum_range(b["dh"], rg["dh"], X)),
+                    "dW_up": (O.round_bf16(b["du"].T @ X), O.sum_range(b["du"], rg["du"], X))}
+
+        for e, res in zip(experts, pool.map(expert_grads, experts)):
+            if counts[e] == 0:
+                assert torch.all(got["dw_down"][e] == 0) and torch.all(got["dw_gate"][e] == 0)
+                continue
+            for k, r in (("dw_down", "dW_down"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up")):
+                assert_close_ranged(f(got[k][e]), res[r][0], res[r][1], MXFP8_TOL, f"mxfp8 bwd {r} [full, expert {e}]")
+
+
+@pytest.mark.parametrize("name", ["ragged", "skew"])
+def test_backward_mxfp8_grid_inputs_bare_tolerance(m, name):
+    """MXFP8 on grid inputs (x, dY, weights exact in E4M3 at their block
+    scales; exact fp32 product sums): every output within 6e-2 * max(1,
+    |oracle|) with no other allowance."""
+    cfg = BWD[name].replace(values="grid")
+    inp = W.make_inputs(cfg, "cpu", with_dy=True)
+    h = host(inp)
+    d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
+    got = _mx_fwd_bwd(m, cfg, d, act_rows=cfg.R)
+    ref = O.moe_backward_mxfp8(h, h["dy"], cfg.K)
+    f = lambda t: t.float().cpu().numpy()
+    pairs = [("dx", "dX"), ("dg", "dg"), ("ds", "ds"), ("dw_gate", "dW_gate"), ("dw_up", "dW_up"),
+             ("dw_down", "dW_down"), ("dws_gate", "dWs_gate"), ("dws_up", "dWs_up"), ("dws_down", "dWs_down")]
+    for k, r in pairs:
+        assert_close(f(got[k]), ref[r], MXFP8_TOL, f"mxfp8 bwd grid {r} [{name}]")

@@ -6,7 +6,8 @@ libmok.  This file is collected last so that a run stopping at the first
 failure has already run every other test; it also passes on its own in a
 fresh process.  Each case calls the new entry point twice in a row through
 the C ABI, on different inputs, and requires the same bytes as mok_plan
-(plan outputs are integers: bit-exact).
+(plan outputs are integers: bit-exact); further cases sit exactly at the
+array's size limit and at zero tokens.
 """
 import ctypes
 
@@ -79,3 +80,38 @@ def test_plan_static_rejects_oversize():
     # ceil(R / 1024) * E = 300 * 1024 > 262144: refused before any launch
     st = lib.mok_plan_static(None, 300 * 1024 // 8, 1024, 8, None, None, None, None, None)
     assert st == m.MOK_ERR_WORKSPACE
+
+
+def test_plan_static_at_the_exact_limit():
+    """ceil(T*K / 1024) * E == 262144 (E 256, T*K = 1,048,576) is accepted and
+    gives mok_plan's bytes; one more route is refused."""
+    m = mok()
+    T, E, K = 131072, 256, 8
+    topk = _topk(T, E, K, seed=21)
+    want = _plan_with_ws(m, topk, E)
+    got = _plan_static_cabi(m, topk, E)
+    torch.cuda.synchronize()
+    assert m.get_error() == m.MOK_OK
+    for w, g in zip(want, got):
+        assert torch.equal(w, g)
+    lib = m._lib_handle()
+    st = lib.mok_plan_static(None, T + 1, E, K, None, None, None, None, None)
+    assert st == m.MOK_ERR_WORKSPACE
+
+
+def test_plan_static_zero_tokens():
+    """T = 0: every count and offset is zero and nothing else is written."""
+    m = mok()
+    E, K = 64, 4
+    counts, offsets, table, route_dst = _outputs(0, E, K)
+    lib = m._lib_handle()
+    for _ in range(2):
+        counts.fill_(-7)
+        offsets.fill_(-7)
+        st = lib.mok_plan_static(None, 0, E, K, ctypes.c_void_p(counts.data_ptr()),
+                                 ctypes.c_void_p(offsets.data_ptr()), None, None,
+                                 ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == m.MOK_OK, m.status_string(st)
+        torch.cuda.synchronize()
+        assert m.get_error() == m.MOK_OK
+        assert torch.all(counts == 0) and torch.all(offsets == 0)

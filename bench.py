@@ -43,6 +43,7 @@ from routing_grouped_expert_device_gb300 import workloads as W  # noqa: E402
 METRIC = "MoE layer fwd/bwd tokens/s and TFLOP/s (% dense tensor peak), 1×GB300"
 KERNEL_SOURCES = ["common.cuh", "gemm_core.cuh", "pair.cuh", "gemm_pair.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "upgate_gemm_dsv3_bf16_fwd_traffic.txt")
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 datasheet figure (no 2:4 sparsity)
 
 
 # ---------------------------------------------------------------------------
@@ -53,11 +54,15 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=30)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="dsv3_bf16_fwd")
-    p.add_argument("--cpu-sample-tokens", type=int, default=160)
+    p.add_argument("--cpu-slice-experts", type=int, default=0,
+                   help="experts in the cpu_baseline slice (0 = a per-workload default)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk-rows", type=int, default=0,
                    help="BF16 forward: gather through a ring of chunks of this many routed rows "
                         "(512..32768; 0 = whole-batch dispatch)")
+    p.add_argument("--act-rows", type=int, default=-1,
+                   help="fwd+bwd: rows of the forward's kept h, u store (-1 = every routed row, "
+                        "0 = none: the backward replays every expert)")
     p.add_argument("--protocol-warmup", type=int, default=500,
                    help="the pages' protocol: warm-up calls of the public entry point")
     p.add_argument("--protocol-runs", type=int, default=100,
@@ -202,28 +207,147 @@ def blas_threads() -> int:
 
 
 # ---------------------------------------------------------------------------
-def oracle_tokens_per_s(cfg, d, n_tokens: int, first: int = 0):
-    """Time the CPU oracle on n_tokens tokens of the workload (host cores).
+class OracleSlice:
+    """The CPU oracle on a batched slice of the workload (host cores).
 
-    The timed work is what the oracle does per token as it stands: top-k
-    routing of the token, then for each selected expert and the shared expert
-    the bf16 -> fp32 conversion of the weights and the SwiGLU FFN, then the
-    combine.  The expert weights are copied to host memory beforehand."""
-    import oracle as O
-    s_host = d["s"].cpu().numpy()
-    toks = [(first + 997 * i) % cfg.T for i in range(n_tokens)]
-    idx, _, _ = O.route(s_host[toks], cfg.K)
-    need = sorted(set(int(e) for e in idx.reshape(-1)))
-    cache = {e: (W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e])) for e in need}
-    shared = None
-    if cfg.I_shared:
-        shared = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
-    weights = O.HostWeights(lambda e: cache[e], shared)
-    x_rows = W.bf16_bits(d["x"][toks])
-    t0 = time.perf_counter()
-    O.moe_forward_tokens(toks, x_rows, s_host[toks], weights, cfg.K)
-    dt = time.perf_counter() - t0
-    return n_tokens / dt, dt
+    A slice is every routed row of a few experts of the full workload, plus
+    the shared expert on the same fraction of the tokens: per expert the
+    oracle's own per-expert steps as the layer functions run them (the
+    bf16 -> fp32 weight conversion inside, MXFP8 quantisation of the weights
+    and rows for MXFP8 experts, the SwiGLU FFN; for fwd+bwd also the
+    backward of those rows and the expert's weight gradients).  Routing is
+    computed once beforehand.  Its work is scaled to layer tokens by FLOPs:
+    tokens = T * slice FLOPs / layer FLOPs."""
+
+    def __init__(self, cfg, d):
+        import oracle as O
+        self.O, self.cfg = O, cfg
+        self.mx = cfg.dtype == "mxfp8"
+        s_host = d["s"].cpu().numpy()
+        self.idx, self.g, _ = O.route(s_host, cfg.K)
+        self.counts = np.bincount(self.idx.reshape(-1), minlength=cfg.E)
+        self.nonempty = [int(e) for e in np.flatnonzero(self.counts)]
+        self.x = W.bf16_bits(d["x"])
+        self.dy = W.bf16_bits(d["dy"]) if cfg.backward else None
+        self.d = d
+        self.shared = None
+        if cfg.I_shared:
+            self.shared = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
+        self.layer_flops = cfg.fwd_flops() + (cfg.bwd_flops() if cfg.backward else 0.0)
+
+    def weights(self, e):
+        d = self.d
+        return W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e])
+
+    def _expert(self, rows, g_rows, wts, shared=False):
+        O, cfg = self.O, self.cfg
+        mx = self.mx and not shared
+        if mx:
+            O.expert_ffn_rows_mxfp8(self.x[rows], *wts)
+        else:
+            O.expert_ffn_rows(self.x[rows], *wts)
+        if cfg.backward:
+            fn = O.route_backward_rows_mxfp8 if mx else O.route_backward_rows
+            b = fn(self.x[rows], self.dy[rows], g_rows, *wts)
+            X = O.bf16_to_f32(self.x[rows])
+            dY = O.bf16_to_f32(self.dy[rows])
+            O.round_bf16(dY.T @ b["a_g"])
+            O.round_bf16(b["dh"].T @ X)
+            O.round_bf16(b["du"].T @ X)
+
+    def run(self, experts):
+        """Time the slice of the given experts: (layer tokens, seconds)."""
+        cfg = self.cfg
+        jobs = []
+        for e in experts:
+            hit = self.idx == e
+            rows = np.flatnonzero(hit.any(1))
+            jobs.append((rows, self.g[hit], self.weights(e)))  # host copies before the clock starts
+        routed = sum(len(r) for r, _, _ in jobs)
+        n_sh = 0
+        if self.shared is not None:
+            n_sh = max(1, round(cfg.T * len(experts) / max(1, len(self.nonempty))))
+        t0 = time.perf_counter()
+        for rows, g_rows, wts in jobs:
+            self._expert(rows, g_rows, wts)
+        if n_sh:
+            self._expert(np.arange(n_sh), np.ones(n_sh, np.float32), self.shared, shared=True)
+        dt = time.perf_counter() - t0
+        per = 3.0 if cfg.backward else 1.0  # backward = twice the forward
+        flops = per * (6.0 * routed * cfg.D * cfg.I + 6.0 * n_sh * cfg.D * cfg.I_shared)
+        return cfg.T * flops / self.layer_flops, dt
+
+    def describe(self, experts, dt):
+        cfg = self.cfg
+        what = ("MXFP8 " if self.mx else "") + ("forward+backward incl. weight gradients" if cfg.backward
+                                                else "forward")
+        sh = " + the shared expert on the same fraction of tokens" if self.shared is not None else ""
+        return (f"all routed rows of {len(experts)} of {len(self.nonempty)} non-empty experts of {cfg.name}{sh}, "
+                f"oracle {what}, {dt:.1f} s; scaled to layer tokens by FLOPs")
+
+
+def slice_experts(sl, n, seed=0):
+    rng = np.random.default_rng(seed)
+    return [int(e) for e in rng.choice(sl.nonempty, min(n, len(sl.nonempty)), replace=False)]
+
+
+# experts per cpu_baseline slice (about 10-30 s on 16 host cores)
+CPU_SLICE_EXPERTS = {("bf16", False): 24, ("bf16", True): 8, ("mxfp8", False): 8, ("mxfp8", True): 4}
+
+
+def roofline_of(cfg, nonempty: int, part_ms: float, peaks: dict, capped: bool, chunk_rows: int = 0,
+                traffic=None):
+    """The roofline object of the bench line for the timed kernel (the routed
+    up/gate launch of a forward, the whole mok_moe_bwd call of fwd+bwd):
+    algorithmic bytes and FLOPs per launch, its bound (arithmetic intensity
+    against the ridge point of the measured peaks), achieved / peak / frac
+    against that bound, and the other figure beside it.  Returns
+    (roofline, tensor_peak, burst_peak, bf16_peak) in TFLOP/s."""
+    mx = cfg.dtype == "mxfp8"
+    ring = chunk_rows > 0
+    T, D, I, Is, R = cfg.T, cfg.D, cfg.I, cfg.I_shared, cfg.R
+    bf16_peak = peaks["bf16_sustained"] if (capped and peaks.get("bf16_sustained")) else peaks["bf16"]
+    # fp8 dense rate is twice bf16 on this part (nominal 4.5 vs 2.25 PFLOP/s)
+    tensor_peak = bf16_peak * (2.0 if mx else 1.0)
+    burst_peak = peaks["bf16"] * (2.0 if mx else 1.0)
+    wbytes = 1 if mx else 2  # bytes per weight / activation element on the routed path
+    if cfg.backward:
+        # the whole backward call: ideal bytes = every weight read once (the
+        # routed ones as fp8 codes + scales for MXFP8) + every weight
+        # gradient written once (bf16) + x, dY, dX
+        wread = nonempty * 3 * I * D * (wbytes + (1 / 32 if mx else 0.0)) + 3 * Is * D * 2
+        alg_bytes = int(wread + (nonempty * 3 * I * D + 3 * Is * D) * 2 + 3 * T * D * 2)
+        kernel = "backward (mok_moe_bwd: gathers, dgrad+replay, dx, combine, wgrad, router grad)"
+        part_flops = cfg.bwd_flops()
+    else:
+        # grouped up/gate + SwiGLU: each expert's W_gate/W_up tile is read once
+        # per 128..256 routed rows
+        scale_b = (1 / 32) if mx else 0.0
+        # (with the ring: x read once instead of xg; the ring itself stays on chip)
+        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + (T if ring else R) * D * wbytes * (1 + scale_b)
+                        + R * I * wbytes * (1 + scale_b))
+        part_flops = 4.0 * R * D * I
+        kernel = (f"grouped up/gate + SwiGLU GEMM (tcgen05 cta_group::2"
+                  f"{', MXFP8 block-scaled' if mx else ''}, routed experts"
+                  f"{f', ring dispatch in the same launch, chunk {chunk_rows} rows' if ring else ''})")
+    part_tflops = part_flops / (part_ms / 1e3) / 1e12
+    achieved = alg_bytes / (part_ms / 1e3) / 1e9
+    if ring:
+        traffic = None
+    intensity = part_flops / alg_bytes
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity > ridge:
+        roofline = {"kernel": kernel, "bound": "tensor", "achieved": round(part_tflops, 1), "peak": tensor_peak,
+                    "unit": "TFLOP/s", "frac": round(part_tflops / tensor_peak, 4), "traffic": traffic,
+                    "gbs": round(achieved, 1), "hbm_frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        roofline = {"kernel": kernel, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                    "tflops": round(part_tflops, 1), "tensor_frac": round(part_tflops / tensor_peak, 4)}
+    roofline.update({"algorithmic_bytes": alg_bytes, "algorithmic_flops": part_flops,
+                     "intensity_flop_per_byte": round(intensity, 1), "ridge_flop_per_byte": round(ridge, 1),
+                     "avg_launch_ms": round(part_ms, 4), "peak_source": peaks["source"]})
+    return roofline, tensor_peak, burst_peak, bf16_peak
 
 
 # ---------------------------------------------------------------------------
@@ -283,6 +407,11 @@ def run_ours(args, world, rank, local):
         bws = torch.empty(max(M.workspace_bytes(shape, M.OP_FWD), M.workspace_bytes(shape, M.OP_BWD)),
                           dtype=u8, device=dev)
         saved = dict(topk_idx=topk, g=g, counts=counts, offsets=offsets, table=table, route_dst=route_dst)
+        act_rows = R if args.act_rows < 0 else min(args.act_rows, R)
+        if act_rows > 0:
+            # the forward keeps h, u (fp32) of the experts that fit; the
+            # backward replays only the others
+            saved["act"] = torch.empty(act_rows, 2 * I, dtype=f32, device=dev)
         pb = M.make_plan_buf(saved)
         gr = dict(dx=torch.empty(T, D, dtype=bf, device=dev), dw_gate=torch.empty(E, I, D, dtype=bf, device=dev),
                   dw_up=torch.empty(E, I, D, dtype=bf, device=dev), dw_down=torch.empty(E, D, I, dtype=bf, device=dev),
@@ -292,11 +421,15 @@ def run_ours(args, world, rank, local):
                   ds=torch.empty(T, E, dtype=f32, device=dev), dg=torch.empty(T, K, dtype=f32, device=dev))
         # forward: route, plan (3), dispatch, up/gate, down, combine, the
         # shared expert's up/gate (BF16) or FFN (MXFP8); backward: gathers
-        # (2), dgrad + dx (BF16) or 2 quantising dispatches, replay, t,
-        # activation gradient, dX (MXFP8), reverse combine, 3 wgrad, router
-        # grad, and the shared expert's dgrad, dx and 3 wgrad
+        # (2), dgrad of the kept experts and / or dgrad with replay, dx
+        # (BF16), or the quantising dispatch of dY (and of x with a replay),
+        # the replay, t, activation gradient, dX (MXFP8); reverse combine,
+        # 3 wgrad, router grad, and the shared expert's dgrad, dx and 3 wgrad
+        all_kept = act_rows >= R
+        some_kept = act_rows > 0
+        bwd_routed = (4 if all_kept else 6) if mx else ((1 if all_kept else 2 if some_kept else 1) + 1)
         launches_per_step = ((1 + 3 + 1 + 2 + 1 + ((2 if mx else 1) if Is else 0))
-                             + (2 + (6 if mx else 2) + 1 + 3 + 1 + (5 if Is else 0)))
+                             + (2 + bwd_routed + 1 + 3 + 1 + (5 if Is else 0)))
 
     def step(ev0=None, ev1=None):
         if cfg.backward:
@@ -381,39 +514,8 @@ def run_ours(args, world, rank, local):
     # the SM clock near its maximum is compared with the burst figure.
     ck = clk or {}
     capped = bool(ck.get("sm_mhz") and ck.get("sm_max_mhz") and ck["sm_mhz"] < 0.95 * ck["sm_max_mhz"])
-    bf16_peak = peaks["bf16_sustained"] if (capped and peaks.get("bf16_sustained")) else peaks["bf16"]
-    # fp8 dense rate is twice bf16 on this part (nominal 4.5 vs 2.25 PFLOP/s)
-    tensor_peak = bf16_peak * (2.0 if mx else 1.0)
-    burst_peak = peaks["bf16"] * (2.0 if mx else 1.0)
-    wbytes = 1 if mx else 2  # bytes per weight / activation element on the routed path
-
-    if cfg.backward:
-        # the whole backward call: ideal bytes = every weight read once (the
-        # routed ones as fp8 codes + scales for MXFP8) + every weight
-        # gradient written once (bf16) + x, dY, dX
-        wread = nonempty * 3 * I * D * (wbytes + (1 / 32 if mx else 0.0)) + 3 * Is * D * 2
-        alg_bytes = int(wread + (nonempty * 3 * I * D + 3 * Is * D) * 2 + 3 * T * D * 2)
-        kernel = "backward (mok_moe_bwd: gathers, dgrad+replay, dx, combine, wgrad, router grad)"
-        part_tflops = cfg.bwd_flops() / (part_ms / 1e3) / 1e12
-    else:
-        # grouped up/gate + SwiGLU: each expert's W_gate/W_up tile is read once
-        # per 128..256 routed rows (HBM-bound below ~290 FLOP/B for bf16)
-        scale_b = (1 / 32) if mx else 0.0
-        # (with the ring: x read once instead of xg; the ring itself stays on chip)
-        alg_bytes = int(nonempty * 2 * I * D * wbytes * (1 + scale_b) + (T if ring else R) * D * wbytes * (1 + scale_b)
-                        + R * I * wbytes * (1 + scale_b))
-        part_flops = 4.0 * R * D * I
-        kernel = (f"grouped up/gate + SwiGLU GEMM (tcgen05 cta_group::2"
-                  f"{', MXFP8 block-scaled' if mx else ''}, routed experts"
-                  f"{f', ring dispatch in the same launch, chunk {args.chunk_rows} rows' if ring else ''})")
-        part_tflops = part_flops / (part_ms / 1e3) / 1e12
-    achieved = alg_bytes / (part_ms / 1e3) / 1e9
-    traffic = None if ring else recorded_traffic(cfg.name)
-    roofline = {"kernel": kernel, "bound": "hbm",
-                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "algorithmic_bytes": alg_bytes, "avg_launch_ms": round(part_ms, 4),
-                "peak_source": peaks["source"], "tflops": round(part_tflops, 1)}
+    roofline, tensor_peak, burst_peak, bf16_peak = roofline_of(
+        cfg, nonempty, part_ms, peaks, capped, args.chunk_rows if ring else 0, recorded_traffic(cfg.name))
 
     # end to end through the public entry points with pinned host buffers:
     # every step copies its inputs in and reads its result back.  The copies
@@ -508,11 +610,12 @@ def run_ours(args, world, rank, local):
         "entry": "mok_moe_fwd + mok_moe_bwd" if cfg.backward else "mok_moe_fwd"}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not cfg.backward and not mx:
-        tps, dt = oracle_tokens_per_s(cfg, d, args.cpu_sample_tokens)
-        cpu = {"value": round(tps, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{args.cpu_sample_tokens} tokens of {cfg.name} (route, {K} routed + shared "
-                         f"SwiGLU experts incl. bf16->fp32 weight conversion, combine), {dt:.1f} s"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sl = OracleSlice(cfg, d)
+        ex = slice_experts(sl, args.cpu_slice_experts or CPU_SLICE_EXPERTS[(cfg.dtype, cfg.backward)])
+        toks, dt = sl.run(ex)
+        cpu = {"value": round(toks / dt, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": sl.describe(ex, dt)}
 
     if rank == 0:
         line = {
@@ -524,6 +627,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": cfg.name, "T": T, "D": D, "I": I, "E": E, "K": K, "I_shared": Is,
                        "global_batch": world * T, "parallelism": f"replicas x{world}",
                        "chunk_rows": args.chunk_rows if ring else 0,
+                       "kept_act_rows": (act_rows if cfg.backward else None),
                        "l2": "inputs larger than L2: every step streams all expert weights "
                              f"({(nonempty * 3 * I * D + 3 * Is * D) * 2 / 1e9:.1f} GB)"},
             "tflops": round(tflops, 1), "tensor_frac": round(tflops / tensor_peak, 4),
@@ -532,6 +636,8 @@ def run_ours(args, world, rank, local):
                                   + (" bf16 x 2 (fp8)" if mx else " bf16")
                                   + (" (SM clock below 95 % of max under load: power cap)" if capped else ""),
             "tensor_frac_burst": round(tflops / burst_peak, 4),
+            # against the datasheet's dense peak (2.25 PFLOP/s bf16, 4.5 fp8)
+            "tensor_frac_nominal": round(tflops / (NOMINAL_BF16_TFLOPS * (2.0 if mx else 1.0)), 4),
             "pass": "fwd+bwd" if cfg.backward else "fwd",
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "pages_protocol": protocol,
@@ -544,48 +650,35 @@ def run_ours(args, world, rank, local):
 
 
 def run_reference(args, world, rank, local):
-    """The CPU oracle as the reference arm.  Each step is one of the K + 1
-    expert FFN evaluations of one token (its top-k routing, the bf16 -> fp32
-    conversion of that expert's weights, the SwiGLU FFN), cycling over the
-    token's routed experts and the shared expert, so a step counts as
-    1 / (K + 1) token.  Only rank 0 works; other ranks exit."""
+    """The CPU oracle as the reference arm, on the host cores.  Each step is
+    the oracle on every routed row of one expert of the workload (plus the
+    shared expert on the same fraction of tokens), as OracleSlice runs it,
+    cycling over the non-empty experts; its work counts as the layer tokens
+    of the same FLOPs.  Only rank 0 works; other ranks exit."""
     if rank != 0:
         return
-    import oracle as O
     cfg = W.CONFIGS[args.config]
     dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
     d = W.make_inputs(cfg, dev, seed=0)
-    s_host = d["s"].cpu().numpy()
-    parts = cfg.K + (1 if cfg.I_shared else 0)
-
-    def one(i):
-        t = (997 * (i // parts)) % cfg.T
-        j = i % parts
-        x_row = W.bf16_bits(d["x"][t:t + 1])
-        idx, _, _ = O.route(s_host[t:t + 1], cfg.K)
-        if j < cfg.K:
-            e = int(idx[0, j])
-            wts = (W.bf16_bits(d["w_gate"][e]), W.bf16_bits(d["w_up"][e]), W.bf16_bits(d["w_down"][e]))
-        else:
-            wts = (W.bf16_bits(d["ws_gate"]), W.bf16_bits(d["ws_up"]), W.bf16_bits(d["ws_down"]))
-        t0 = time.perf_counter()
-        O.route(s_host[t:t + 1], cfg.K)
-        O.expert_ffn_rows(x_row, *wts)
-        return time.perf_counter() - t0
-
+    sl = OracleSlice(cfg, d)
+    order = slice_experts(sl, len(sl.nonempty), seed=1)
     for i in range(args.warmup):
-        one(i)
-    total = sum(one(args.warmup + i) for i in range(args.steps))
-    tokens = args.steps / parts
-    value = tokens / total
+        sl.run([order[i % len(order)]])
+    toks = total = 0.0
+    for i in range(args.steps):
+        t, dt = sl.run([order[(args.warmup + i) % len(order)]])
+        toks += t
+        total += dt
+    value = toks / total
     line = {
         "metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (oracle" + (", MXFP8 operands)" if cfg.dtype == "mxfp8" else ")"),
         "data": "synthetic (seeded)", "config": {"workload": cfg.name, "T": cfg.T, "D": cfg.D, "I": cfg.I,
                                                  "E": cfg.E, "K": cfg.K, "I_shared": cfg.I_shared},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": f"one of the {parts} expert FFNs of one {cfg.name} token per step"},
+                         "sample": "per step: " + sl.describe([0], total / max(1, args.steps))},
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

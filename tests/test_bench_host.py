@@ -104,3 +104,57 @@ def test_reference_arm_line_on_host_cores():
 
 def test_reference_arm_other_ranks_exit_without_work():
     assert _run_reference({"WORLD_SIZE": "2", "RANK": "1", "LOCAL_RANK": "1"}) == []
+
+
+PEAKS = dict(hbm_gbs=6781.1, bf16=1887.9, bf16_sustained=1649.2, source="measured")
+
+
+def test_roofline_bound_per_workload():
+    """The bench line's roofline is judged against the kernel's own bound:
+    the skewed layer's up/gate (about 1100 FLOP per algorithmic byte) against
+    the tensor peak, the DSV3 up/gate (BF16 and MXFP8) and the backward call
+    against HBM; every line names both figures."""
+    from routing_grouped_expert_device_gb300 import workloads as W
+    b = _bench()
+    cases = {"skewed_bf16_fwd": (57, 1.9, "tensor"), "dsv3_bf16_fwd": (256, 2.5, "hbm"),
+             "dsv3_mxfp8_fwd": (256, 1.5, "hbm"), "dsv3_bf16_fwdbwd": (256, 11.4, "hbm"),
+             "dsv3_mxfp8_fwdbwd": (256, 9.4, "hbm")}
+    for name, (nonempty, ms, bound) in cases.items():
+        cfg = W.CONFIGS[name]
+        r, tensor_peak, burst, bf16 = b.roofline_of(cfg, nonempty, ms, PEAKS, capped=False)
+        assert r["bound"] == bound, name
+        if bound == "tensor":
+            assert r["unit"] == "TFLOP/s" and r["peak"] == tensor_peak and "gbs" in r
+            assert r["intensity_flop_per_byte"] > r["ridge_flop_per_byte"]
+        else:
+            assert r["unit"] == "GB/s" and r["peak"] == PEAKS["hbm_gbs"] and "tflops" in r
+            assert r["intensity_flop_per_byte"] <= r["ridge_flop_per_byte"]
+        assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+        assert tensor_peak == PEAKS["bf16"] * (2.0 if cfg.dtype == "mxfp8" else 1.0)
+    # under the power cap the sustained figure is the denominator
+    _, tp, burst, bf16 = b.roofline_of(W.CONFIGS["skewed_bf16_fwd"], 57, 1.9, PEAKS, capped=True)
+    assert tp == PEAKS["bf16_sustained"] and burst == PEAKS["bf16"]
+    # the DSV3 up/gate's algorithmic bytes: weights of non-empty experts + xg + a
+    r, *_ = b.roofline_of(W.CONFIGS["dsv3_bf16_fwd"], 256, 2.5, PEAKS, capped=False)
+    assert r["algorithmic_bytes"] == 16089350144
+
+
+def test_oracle_slice_every_kind_of_workload():
+    """The cpu_baseline / reference-arm slice runs the oracle for BF16 and
+    MXFP8, forward and forward+backward, and scales its work by FLOPs."""
+    from routing_grouped_expert_device_gb300 import workloads as W
+    b = _bench()
+    base = W.MoEConfig("t", T=128, D=128, I=64, E=8, K=2, I_shared=64)
+    for cfg in (base, base.replace(backward=True), base.replace(dtype="mxfp8"),
+                base.replace(dtype="mxfp8", backward=True)):
+        d = W.make_inputs(cfg, "cpu", with_dy=cfg.backward)
+        sl = b.OracleSlice(cfg, d)
+        ex = b.slice_experts(sl, 2)
+        toks, dt = sl.run(ex)
+        rows = sum(int(sl.counts[e]) for e in ex)
+        n_sh = round(cfg.T * 2 / len(sl.nonempty))
+        per = 3.0 if cfg.backward else 1.0
+        want = cfg.T * per * (6.0 * rows * cfg.D * cfg.I + 6.0 * n_sh * cfg.D * cfg.I_shared) / (
+            cfg.fwd_flops() + (cfg.bwd_flops() if cfg.backward else 0.0))
+        assert abs(toks - want) < 1e-9 * want and dt > 0
+        assert "scaled to layer tokens by FLOPs" in sl.describe(ex, dt)

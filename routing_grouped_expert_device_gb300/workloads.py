@@ -49,10 +49,11 @@ class MoEConfig:
     backward: bool = False
     chunks: Tuple[int, ...] = ()
     # "normal": the distributions above.  "grid": x, dY and every weight are
-    # small integers times a power of two of the same scale (x, dY: j / 2;
-    # W_gate, W_up, W_shared_gate/up: j 2^-7; W_down, W_shared_down: j 2^-6;
-    # j uniform in -3..3), so every product sum of the layer's GEMMs over
-    # D or I is exact in fp32 whatever the summation order.
+    # small integers times a power of two (x, dY: j / 2; W_gate, W_up,
+    # W_shared_gate/up: j 2^-8; W_down, W_shared_down: j 2^-7; j uniform in
+    # -3..3: at D = 7168, I = 2048 standard deviations of 1 and 0.66-0.7 of
+    # the normal weights'), so every product sum of the layer's GEMMs over D
+    # or I is exact in fp32 whatever the summation order.
     values: str = "normal"
 
     @property
@@ -142,7 +143,7 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, with_dy: Optional[b
     out: Dict[str, torch.Tensor] = {}
     if cfg.values == "grid":
         draw = lambda shape, scale: _draw_grid(gen, shape, scale, device)
-        sx, sgu, sd = 0.5, 2.0 ** -7, 2.0 ** -6
+        sx, sgu, sd = 0.5, 2.0 ** -8, 2.0 ** -7
     else:
         draw = lambda shape, std: _draw(gen, shape, std, device)
         sx, sgu, sd = 1.0, 1.0 / math.sqrt(D), None

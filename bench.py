@@ -60,6 +60,9 @@ def parse_args():
     p.add_argument("--chunk-rows", type=int, default=0,
                    help="BF16 forward: gather through a ring of chunks of this many routed rows "
                         "(512..32768; 0 = whole-batch dispatch)")
+    p.add_argument("--producer-sms", type=int, default=0,
+                   help="SMs left to route, plan and the dispatch while the shared expert's up/gate "
+                        "runs on the others (mok_shape.producer_sms; 0 = the shared expert takes every SM)")
     p.add_argument("--act-rows", type=int, default=-1,
                    help="fwd+bwd: rows of the forward's kept h, u store (-1 = every routed row, "
                         "0 = none: the backward replays every expert)")
@@ -361,7 +364,7 @@ def run_ours(args, world, rank, local):
     d = W.make_inputs(cfg, dev, seed=rank)
     T, D, I, E, K, Is, R = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, cfg.R
     ring = args.chunk_rows > 0 and not mx and not cfg.backward
-    shape = M.shape_of(cfg, chunk_rows=args.chunk_rows if ring else 0)
+    shape = M.shape_of(cfg, chunk_rows=args.chunk_rows if ring else 0, producer_sms=args.producer_sms)
     i32, f32, bf, u8 = torch.int32, torch.float32, torch.bfloat16, torch.uint8
     if mx:
         # weights are model parameters: quantised once, outside the timed region
@@ -627,7 +630,7 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), logits~N(0,1) softmax; bf16)",
             "config": {"workload": cfg.name, "T": T, "D": D, "I": I, "E": E, "K": K, "I_shared": Is,
                        "global_batch": world * T, "parallelism": f"replicas x{world}",
-                       "chunk_rows": args.chunk_rows if ring else 0,
+                       "chunk_rows": args.chunk_rows if ring else 0, "producer_sms": args.producer_sms,
                        "kept_act_rows": (act_rows if cfg.backward else None),
                        "l2": "inputs larger than L2: every step streams all expert weights "
                              f"({(nonempty * 3 * I * D + 3 * Is * D) * 2 / 1e9:.1f} GB)"},

@@ -73,7 +73,15 @@ typedef enum {
  * dispatch gathers the whole batch before the expert GEMMs; 512..32768 =
  * the BF16 forward gathers through a ring of 4 chunks that producer warps
  * fill while the up/gate GEMM consumes it (mok_expert_upgate_ring).
- * producer_sms: reserved, must be 0. */
+ * producer_sms: the split of the GPU between the dispatch (producers) and
+ * the shared expert in the first dispatch window (paper note, "The
+ * production details": the shared expert fills the first dispatch window).
+ * mok_moe_fwd runs the shared expert's launches on a side stream next to
+ * route, plan and the dispatch; with producer_sms > 0 those launches take
+ * every SM but producer_sms (at least 2), which stay free so that the
+ * dispatch runs beside them instead of queueing behind; 0 = the shared
+ * expert's launches take every SM.  The same holds for mok_shared_ffn and
+ * the shared-only call of mok_expert_upgate.  0..4096. */
 typedef struct {
   int32_t T, D, I, E, K, I_shared;
   int32_t dtype;

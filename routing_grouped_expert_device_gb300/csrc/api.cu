@@ -15,8 +15,14 @@ bool shape_ok(const mok_shape* s) {
   if (static_cast<int64_t>(s->T) * s->K >= (int64_t(1) << 31)) return false;
   if (s->dtype != MOK_BF16 && s->dtype != MOK_MXFP8) return false;
   if (s->chunk_rows != 0 && (s->chunk_rows < 512 || s->chunk_rows > 32768)) return false;
-  if (s->producer_sms != 0) return false;
+  if (s->producer_sms < 0 || s->producer_sms > 4096) return false;
   return true;
+}
+
+int shared_expert_sms(const mok_shape& s) {
+  if (s.producer_sms <= 0) return 0;
+  const int left = num_sms() - s.producer_sms;
+  return left >= 2 ? left : 2;
 }
 
 namespace {
@@ -252,9 +258,10 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
   if (with_shared && (!w->ws_gate || !w->ws_up || !aligned16(x_shared) || !aligned16(a_shared)))
     return MOK_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!xg && !offsets && !a) {  // the shared expert's up/gate alone
+  if (!xg && !offsets && !a) {  // the shared expert's up/gate alone (a side stream's work)
     if (!with_shared) return MOK_ERR_INVALID_ARG;
-    return launch_upgate(x_shared, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, a_shared, st);
+    return launch_upgate(x_shared, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, a_shared, st,
+                         shared_expert_sms(s));
   }
   if (s.dtype == MOK_MXFP8) {
     if (!xg || !xg_scale || !offsets || !a || !a_scale || !mx_weights_ok(w) || !aligned16(xg) ||
@@ -343,10 +350,11 @@ extern "C" mok_status mok_shared_ffn(const mok_shape* shape, const mok_weights* 
     return MOK_ERR_INVALID_ARG;
   if (!ws || ws_bytes < static_cast<size_t>(s.T) * s.I_shared * 2) return MOK_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = shared_expert_sms(s);
   mok_status r =
-      launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, ws, st);
+      launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, ws, st, sms);
   if (r != MOK_OK) return r;
-  return launch_down(ws, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st);
+  return launch_down(ws, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, st, sms);
 }
 
 extern "C" mok_status mok_combine(const mok_shape* shape, const void* yg, const void* ys,
@@ -415,8 +423,10 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     if (!(side = side_stream())) return MOK_ERR_CUDA;
     if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
       return MOK_ERR_CUDA;
-    r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, side->s);
-    if (r == MOK_OK && mx) r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, side->s);
+    const int sms = shared_expert_sms(s);
+    r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, side->s, sms);
+    if (r == MOK_OK && mx)
+      r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, side->s, sms);
     if (cudaEventRecord(side->join, side->s) != cudaSuccess) return MOK_ERR_CUDA;
     joined = false;
     if (r != MOK_OK) return fail(r);

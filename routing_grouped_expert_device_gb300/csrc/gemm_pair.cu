@@ -480,14 +480,17 @@ size_t pair_smem_bytes(int G) {
          static_cast<size_t>(G + 1) * sizeof(int);
 }
 
+// max_sms > 0: the persistent grid takes at most that many SMs (clusters
+// of two), leaving the rest to kernels of other streams.
 template <bool kSwiglu, bool kRing = false, bool kSoftmax = false>
-mok_status run_pair(const PairParams& P, cudaStream_t st) {
+mok_status run_pair(const PairParams& P, cudaStream_t st, int max_sms = 0) {
   const size_t smem = pair_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   auto kern = gemm_pair_persistent<kSwiglu, kRing, kSoftmax>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return MOK_ERR_CUDA;
-  const int grid = (num_sms() / 2) * 2;
+  const int sms = max_sms > 0 && max_sms < num_sms() ? max_sms : num_sms();
+  const int grid = sms >= 2 ? (sms / 2) * 2 : 2;
   if (!kRing) {
     kern<<<grid, 256, smem, st>>>(P);
     MOK_CHECK_LAUNCH();
@@ -1137,7 +1140,7 @@ mok_status launch_down_pair_t(const void* a, int64_t a_rows, const void* w_down,
 
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                              cudaStream_t st, const SharedOperands* sh, KeptAct kept) {
+                              cudaStream_t st, const SharedOperands* sh, KeptAct kept, int max_sms) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
   // Routed rows alone, fewer than 512 per expert on average: the transposed
   // kernel, whose MMAs skip the padding rows of each expert's last tile
@@ -1186,12 +1189,12 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
     P.act_i = I;
   }
   if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
-  return run_pair<true>(P, st);
+  return run_pair<true>(P, st, max_sms);
 }
 
 mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
-                            const SharedOperands* sh) {
+                            const SharedOperands* sh, int max_sms) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
   // routed groups of fewer than 512 rows on average: the transposed kernel
   // (no padding rows in the MMAs), as for the up/gate
@@ -1231,19 +1234,19 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
     P.out_ld_s = D;
   }
   if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
-  return run_pair<false>(P, st);
+  return run_pair<false>(P, st, max_sms);
 }
 
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st) {
+                         cudaStream_t st, int max_sms) {
   if (a_rows == 0 || m_total == 0) return MOK_OK;
-  return launch_upgate_pair(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st);
+  return launch_upgate_pair(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st, nullptr, {}, max_sms);
 }
 
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
-                       int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st) {
-  return launch_down_pair(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st);
+                       int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st, int max_sms) {
+  return launch_down_pair(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st, nullptr, max_sms);
 }
 
 mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, int E, int D, float* s_out,

@@ -59,11 +59,13 @@ struct KeptAct {
 // group of m_total rows.
 //  up/gate: a[rows][I] = bf16(SiLU(A W_gate^T) * (A W_up^T)), A [rows][D]
 //  down   : y[rows][D] = bf16(a W_down^T)
+// max_sms > 0: the grid takes at most that many SMs (the rest stay free for
+// kernels of other streams).
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st);
+                         cudaStream_t st, int max_sms = 0);
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
-                       int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st);
+                       int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st, int max_sms = 0);
 // The shared expert as an extra group of a routed launch: A [rows][K],
 // weights w0 (, w1) with `inner` = I_shared, output [rows][N].
 struct SharedOperands {
@@ -78,7 +80,8 @@ struct SharedOperands {
 // routed launch (cta_group::2, 256-row tiles).
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                              cudaStream_t st, const SharedOperands* sh = nullptr, KeptAct kept = {});
+                              cudaStream_t st, const SharedOperands* sh = nullptr, KeptAct kept = {},
+                              int max_sms = 0);
 // Router scores s = softmax(x W_r^T) [T][E] fp32 (E <= 256): x [T][D], W_r
 // [E][D] bf16, on CTA pairs with the softmax in the epilogue.
 mok_status launch_router_pair(const void* x, int64_t T, const void* w_router, int E, int D, float* s_out,
@@ -105,7 +108,7 @@ inline size_t ring_bytes(int64_t R, int64_t D, int64_t b) {
 inline size_t ring_counter_bytes(int64_t R, int64_t b) { return static_cast<size_t>((R + b - 1) / b) * 8; }
 mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
-                            const SharedOperands* sh = nullptr);
+                            const SharedOperands* sh = nullptr, int max_sms = 0);
 
 // Backward.  dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
 // non-null, dgp [rows][I/32] partials of <t, a> (32 I columns each);
@@ -183,6 +186,9 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
                           cudaStream_t st, bool f32_out = false);
 
 bool shape_ok(const mok_shape* s);
+// SMs the shared expert's side-stream launches may take (0: all): every SM
+// but shape.producer_sms, which stay free for route, plan and the dispatch.
+int shared_expert_sms(const mok_shape& s);
 
 // Device address of a __device__ variable (its host-side stand-in `symbol`)
 // on the current device.  cudaGetSymbolAddress is called once per device and

@@ -133,9 +133,9 @@ def make_shape(T, D, I, E, K, I_shared=0, dtype=MOK_BF16, chunk_rows=0, producer
     return Shape(T, D, I, E, K, I_shared, dtype, chunk_rows, producer_sms)
 
 
-def shape_of(cfg, dtype=None, chunk_rows=0) -> Shape:
+def shape_of(cfg, dtype=None, chunk_rows=0, producer_sms=0) -> Shape:
     dt = MOK_MXFP8 if (dtype or cfg.dtype) == "mxfp8" else MOK_BF16
-    return make_shape(cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, dt, chunk_rows)
+    return make_shape(cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, dt, chunk_rows, producer_sms)
 
 
 def make_weights(t: Dict[str, object]) -> Weights:

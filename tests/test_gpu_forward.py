@@ -365,3 +365,25 @@ def test_moe_fwd_ring_full_size_bitexact(m, config, chunks):
         del ws
     for o in outs[1:]:
         assert torch.equal(outs[0].view(torch.int16), o.view(torch.int16))
+
+
+@pytest.mark.parametrize("name,producer_sms", [("tiny", 8), ("dsv3_bf16_fwd", 40), ("dsv3_mxfp8_fwd", 40)])
+def test_producer_sms_split_is_bitexact(m, name, producer_sms):
+    """shape.producer_sms leaves SMs free for route, plan and the dispatch
+    while the shared expert's launches run on the rest: a different grid,
+    the same tiles, the same bytes."""
+    cfg = W.CONFIGS[name]
+    d = W.make_inputs(cfg, DEV if cfg.T > 1024 else "cpu")
+    d = {k: v.to(DEV) for k, v in d.items()}
+    if cfg.dtype == "mxfp8":
+        from test_gpu_mxfp8 import mx_weights
+        d = mx_weights(m, d)
+    outs = []
+    for ps in (0, producer_sms):
+        shape = m.shape_of(cfg, producer_sms=ps)
+        ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+        out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+        m.moe_fwd(shape, m.make_weights(d), d["x"], d["s"], out, ws)
+        m.check_device_status()
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))

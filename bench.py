@@ -63,6 +63,9 @@ def parse_args():
     p.add_argument("--producer-sms", type=int, default=0,
                    help="SMs left to route, plan and the dispatch while the shared expert's up/gate "
                         "runs on the others (mok_shape.producer_sms; 0 = the shared expert takes every SM)")
+    p.add_argument("--mx-pair-scales", action="store_true",
+                   help="MXFP8: give the paired W_up / W_gate scale blocks, so that the up/gate takes the "
+                        "routed rows as N (measured slower than the row-major up/gate on GB300)")
     p.add_argument("--act-rows", type=int, default=-1,
                    help="fwd+bwd: rows of the forward's kept h, u store (-1 = every routed row, "
                         "0 = none: the backward replays every expert)")
@@ -374,6 +377,10 @@ def run_ours(args, world, rank, local):
             sc = torch.empty(M.mx_scale_words(*wt.shape), dtype=i32, device=dev)
             M.quantize_mxfp8(wt, q, sc)
             d["q_" + name], d["sc_" + name] = q, sc
+        if args.mx_pair_scales:
+            # the paired W_up / W_gate scale blocks: the up/gate with the routed rows as N
+            d["sc_gu_pair"] = torch.empty(M.mx_scale_words(2 * E * I, D), dtype=i32, device=dev)
+            M.mxfp8_pair_scales(shape, M.make_weights(d), d["sc_gu_pair"])
         if cfg.backward:
             # the backward's copies: W_down^T along D, [W_gate^T | W_up^T] along 2I
             d["qt_down"] = torch.empty(E * I, D, dtype=u8, device=dev)

@@ -130,6 +130,7 @@ typedef struct {
   const uint8_t *sct_down;
   const void *qt_gu;
   const uint8_t *sct_gu;
+  const uint8_t *sc_gu_pair;
 } mok_weights;
 
 /* State saved by the forward for the backward.
@@ -357,6 +358,24 @@ mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void 
  * MXFP8 layout above).  0 for invalid sizes (cols not a positive multiple
  * of 128, negative rows or groups).  Host-only. */
 size_t mok_mxfp8_scale_bytes(int64_t rows, int64_t cols, int32_t groups);
+
+/* The MXFP8 routed up/gate with the routed rows as the MMA's N dimension
+ * (no padding rows in its MMAs; used when w->sc_gu_pair is given and the
+ * experts average fewer than 512 routed rows) takes each CTA's A operand as
+ * 64 W_up rows followed by the same 64 W_gate rows, whose scales it reads
+ * from one 512-byte block of this paired copy: block b of expert e =
+ * b / (I/64), s = b % (I/64), holds the scale words of W_up rows 64 s ..
+ * 64 s + 63 and then of the same W_gate rows, in the plain layout of 2 E I
+ * rows (the block order of the 32x128b copy).  Writes sc_gu_pair
+ * (mok_mxfp8_scale_bytes(2*E*I, D, 0) bytes) from w->sc_gate and w->sc_up
+ * (mok_quantize_mxfp8's words); a permutation, no arithmetic.  Weights are
+ * parameters: call once after quantising them.  The pages have no
+ * counterpart; the layout serves the tensor cores' scale placement.  The
+ * routed-rows-as-N up/gate gives the row-major one's bytes; on a GB300 it
+ * measured slower (DSV3 MXFP8 up/gate 1.89 vs 1.55 ms): its quantising
+ * epilogue holds the single accumulator longer than the MMAs it saves. */
+mok_status mok_mxfp8_pair_scales(const mok_shape *shape, const mok_weights *w, uint8_t *sc_gu_pair,
+                                 void *stream);
 
 /* The MXFP8 weight copies of the backward, from the bf16 w_gate, w_up,
  * w_down of `w`: qt_down = codes of W_down^T [E][I][D] quantised along D

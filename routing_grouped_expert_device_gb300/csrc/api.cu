@@ -122,7 +122,8 @@ bool mx_bwd_weights_ok(const mok_weights* w) {
 bool mx_weights_ok(const mok_weights* w) {
   return w->q_gate && w->q_up && w->q_down && w->sc_gate && w->sc_up && w->sc_down &&
          aligned16(w->q_gate) && aligned16(w->q_up) && aligned16(w->q_down) &&
-         aligned16(w->sc_gate) && aligned16(w->sc_up) && aligned16(w->sc_down);
+         aligned16(w->sc_gate) && aligned16(w->sc_up) && aligned16(w->sc_down) &&
+         (!w->sc_gu_pair || aligned16(w->sc_gu_pair));
 }
 
 // Workspace of mok_expert_ffn: a (bf16), or a codes + scale words (MXFP8).
@@ -227,7 +228,7 @@ extern "C" mok_status mok_expert_ffn(const mok_shape* shape, const mok_weights* 
     void* asc = static_cast<uint8_t*>(ws) + round_up(static_cast<size_t>(R) * s.I);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     mok_status r = launch_upgate_mx(xg, xg_scale, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up,
-                                    offsets, s.E, s.D, s.I, aq, asc, st);
+                                    offsets, s.E, s.D, s.I, aq, asc, st, {}, w->sc_gu_pair);
     if (r != MOK_OK) return r;
     return launch_down_mx(aq, asc, R, w->q_down, w->sc_down, offsets, s.E, s.D, s.I, yg, st);
   }
@@ -268,7 +269,7 @@ extern "C" mok_status mok_expert_upgate(const mok_shape* shape, const mok_weight
         !aligned16(xg_scale) || !aligned16(a) || !aligned16(a_scale))
       return MOK_ERR_INVALID_ARG;
     mok_status r = launch_upgate_mx(xg, xg_scale, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, offsets,
-                                    s.E, s.D, s.I, a, a_scale, st);
+                                    s.E, s.D, s.I, a, a_scale, st, {}, w->sc_gu_pair);
     if (r != MOK_OK || !with_shared) return r;
     return launch_upgate(x_shared, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared,
                          a_shared, st);
@@ -441,7 +442,7 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
       return fail(r);
     void* asc = at<void>(ws, L.a_scale);
     if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
-                              w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st, kept)) != MOK_OK)
+                              w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st, kept, w->sc_gu_pair)) != MOK_OK)
       return fail(r);
     if ((r = launch_down_mx(a, asc, R, w->q_down, w->sc_down, pb.offsets, s.E, s.D, s.I, yg, st)) !=
         MOK_OK)
@@ -487,6 +488,16 @@ extern "C" mok_status mok_quantize_mxfp8(const void* src, int64_t rows, int64_t 
   if (rows == 0) return MOK_OK;
   if (!src || !q || !scale || !aligned16(src) || !aligned16(q)) return MOK_ERR_INVALID_ARG;
   return launch_quantize_mxfp8(src, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mok_status mok_mxfp8_pair_scales(const mok_shape* shape, const mok_weights* w, uint8_t* sc_gu_pair,
+                                            void* stream) {
+  if (!shape_ok(shape) || !w) return MOK_ERR_INVALID_ARG;
+  const mok_shape& s = *shape;
+  if (!w->sc_gate || !w->sc_up || !sc_gu_pair || !aligned16(w->sc_gate) || !aligned16(w->sc_up) ||
+      !aligned16(sc_gu_pair))
+    return MOK_ERR_INVALID_ARG;
+  return launch_pair_scales(w->sc_gate, w->sc_up, s.E, s.I, s.D, sc_gu_pair, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" mok_status mok_quantize_mxfp8_bwd_weights(const mok_shape* shape, const mok_weights* w, void* qt_down,

@@ -252,6 +252,28 @@ __global__ void __launch_bounds__(256) act_grad_mx_kernel(
   }
 }
 
+// Paired scale blocks for the MXFP8 up/gate with the routed rows as N: the
+// virtual row v = 128 b + m of block b = e (I / 64) + s is W_up row
+// e I + 64 s + m (m < 64) or W_gate row e I + 64 s + m - 64, so that one
+// 512-byte block holds the scales of a CTA's A operand (64 W_up rows, then
+// the same W_gate rows) in the order the block-scaled MMA reads them.  For
+// every 128-column group k of K: dst[k][pos(v)] = src[k][pos(row)].
+__global__ void __launch_bounds__(256) pair_scales_kernel(const uint32_t* __restrict__ sg,
+                                                          const uint32_t* __restrict__ su, int64_t ld_src,
+                                                          int64_t ld_dst, int64_t vrows, int I, int kgroups,
+                                                          uint32_t* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < vrows; v += stride) {
+    const int64_t b = v >> 7;
+    const int m = static_cast<int>(v & 127);
+    const int64_t slices = I / 64;
+    const int64_t r = (b / slices) * I + 64 * (b % slices) + (m & 63);
+    const uint32_t* src = m < 64 ? su : sg;
+    const int64_t ps = mx_scale_pos(r), pd = mx_scale_pos(v);
+    for (int k = 0; k < kgroups; ++k) dst[k * ld_dst + pd] = src[k * ld_src + ps];
+  }
+}
+
 // MXFP8 codes of transposed weights: output row (g, n) holds the M values
 // src[g][m][n] (src bf16 [G][M][N]), quantised along m in 1x32 blocks:
 // codes at q[(g N + n) * out_cols + col0 + m], scale words in the plain
@@ -432,6 +454,17 @@ mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, vo
   quant_rows_kernel<<<grid_for(rows, 8), 256, 0, st>>>(static_cast<const uint4*>(src), nullptr, nullptr, nullptr, 1,
                                                        rows, cols, mx_scale_ld(rows), static_cast<uint2*>(q),
                                                        reinterpret_cast<uint32_t*>(scale));
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_pair_scales(const void* sg, const void* su, int G, int I, int D, void* sp, cudaStream_t st) {
+  if (G == 0) return MOK_OK;
+  if (I % 128 || D % 128) return MOK_ERR_UNSUPPORTED;
+  const int64_t vrows = 2 * static_cast<int64_t>(G) * I;
+  pair_scales_kernel<<<grid_for(vrows, 256), 256, 0, st>>>(
+      static_cast<const uint32_t*>(sg), static_cast<const uint32_t*>(su), mx_scale_ld(static_cast<int64_t>(G) * I),
+      mx_scale_ld(vrows), vrows, I, D / 128, static_cast<uint32_t*>(sp));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

@@ -46,6 +46,11 @@ constexpr int BKB = 128;  // K columns (bytes) per stage
 // MMAs while TMA stores write the tile out.
 constexpr int kMaxStages = 6;
 constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 rows x 64 bf16
+// The quantising up/gate with the routed rows as N passes u from the warps
+// that drain it to the warps that drain h through shared memory: 32 rows x
+// 32 columns of fp32 for each of the 2 x 2 (column half, lane-quarter pair)
+// warp pairs.
+constexpr int XCH_BYTES = 4 * 32 * 32 * 4;
 __host__ __device__ constexpr int mx_stages(bool bf16_out) { return bf16_out ? 4 : kMaxStages; }
 constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows
 constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B
@@ -109,12 +114,26 @@ struct MxParams {
   float* y32;
   float* act;  // up/gate: kept h, u fp32 [rows][2 out_ld] of groups ending at or below act_rows
   int32_t act_rows;
+  // up/gate with the routed rows as N: W_up, W_gate codes in 64-row boxes
+  // and the paired scale blocks (mok_mxfp8_pair_scales: block b of expert
+  // e = b / (I / 64) holds the scale words of W_up rows 64 s .. 64 s + 63
+  // and then of the same W_gate rows, s = b % (I / 64))
+  CUtensorMap tmU64, tmG64, tmSP;
   int32_t out_ld;
   // bf16 outputs as [rows][out_ld], boxes 32 rows x 64 columns, 128-byte
   // swizzle: y (down), or h and u (replay)
   CUtensorMap tmO0, tmO1;
 };
 
+// kT with kSwiglu (the quantising up/gate): A is the tile's 64 W_up rows
+// (A rows 0-63) and the same 64 W_gate rows (64-127) of this CTA's half of
+// the tile's 128 I columns, with their paired scale block; TMEM lane
+// quarters 0, 1 then hold u and 2, 3 the matching h, one column per routed
+// row.  The u warps pass their chunk to the h warps through shared memory;
+// the h warps form a = bf16(SiLU(h) u), find each row's amax over their 32
+// columns (one 1x32 block of a) with a transposing butterfly, and write the
+// codes (32 bytes of a row per warp) and the scale byte of their block.
+//
 // kT (the forms with bf16 outputs: down, replay): the routed rows are the
 // MMA's N dimension.  A is 128 weight rows per CTA with the scale block of
 // those rows (down: rows 128 r .. of the tile's 256 W_down rows; replay:
@@ -133,8 +152,8 @@ struct MxParams {
 template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
-  static_assert(!kT || !kSwiglu || kReplay, "transposed form: bf16 outputs only");
   constexpr bool kBf16Out = !kSwiglu || kReplay;
+  constexpr bool kSwigluT = kT && kSwiglu && !kReplay;
   static_assert(!kF32 || kBf16Out, "fp32 outputs replace the bf16 ones");
   constexpr int STAGES = mx_stages(kBf16Out);
   extern __shared__ uint8_t smem_raw[];
@@ -142,7 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sf_smem = smem + STAGES * CODE_BYTES;
   uint8_t* staging = sf_smem + STAGES * SF_BYTES;  // 1024-byte aligned; STAGING_BYTES when kBf16Out
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + (kBf16Out ? STAGING_BYTES : 0));
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + (kBf16Out ? STAGING_BYTES : (kSwigluT ? XCH_BYTES : 0)));
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
@@ -207,7 +226,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
           uint8_t* st = smem + stage * CODE_BYTES;
           uint8_t* sf = sf_smem + stage * SF_BYTES;
-          if (kT) {
+          if (kSwigluT) {
+            // A: 64 W_up rows then the same 64 W_gate rows (this CTA's half of
+            // the tile's I columns) with their paired scale block; B: half of
+            // the tile's routed rows, scales from the tile's two grouped blocks
+            const int urow = brow0 + static_cast<int>(rank) * 64;
+            const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
+            const int gb = static_cast<int>(mx_group_row0(c.row0, c.g)) + c.mt * 256;
+            const int pblk = (brow0 / 64 + static_cast<int>(rank)) * 128;  // virtual row of the paired block
+            tma_load_2d_pair(st, &P.tmU64, kb * BKB, urow, lbar);
+            tma_load_2d_pair(st + 64 * BKB, &P.tmG64, kb * BKB, urow, lbar);
+            tma_load_2d_pair(st + A_BYTES, &P.tmA, kb * BKB, xrow, lbar);
+            tma_load_2d_pair(sf, &P.tmSP, pblk, kb, lbar);
+            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kb, lbar);
+            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kb, lbar);
+          } else if (kT) {
             // this CTA's weight rows (A): down rows 128 r .. of the tile, replay
             // the tile's rows of W_gate (CTA 0) or W_up (CTA 1)
             const int wrow = brow0 + (kReplay ? 0 : static_cast<int>(rank) * 128);
@@ -293,6 +326,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     }
+  } else if (kSwigluT && warp >= 4) {
+    // ---------------- epilogue, quantising up/gate with the routed rows as N ----------------
+    // Warp 4 + 4 h + q: TMEM lane quarter q, accumulator columns (routed
+    // rows) [128 h, 128 h + 128).  Quarters 0, 1 hold u of I columns
+    // i0 + 64 r + 32 q + lane, quarters 2, 3 h of the same columns; warp
+    // pair (q & 1, half) meets at named barrier 4 + 2 half + (q & 1).
+    const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
+    const bool hwarp = q >= 2;
+    const int pair = 2 * half + (q & 1);
+    float* xb = reinterpret_cast<float*>(staging) + pair * 1024;  // [32 rows][32 columns]
+    const uint32_t pbar = 4 + pair;
+    int it = 0;
+    TileWalker walk(P.sched, tstart);
+    for (int tile = cid; tile < total; tile += ncl, ++it) {
+      const TileCoord c = walk.at(tile);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(tfull, it & 1, abort_flag, P.status, SITE_EPILOGUE));
+      ok = named_bar_and(3, 256, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const int nrows = min(c.rows - c.mt * 256, 256);
+      const int64_t row0 = c.row0 + c.mt * 256;
+      const int icol = c.nt * 128 + static_cast<int>(rank) * 64 + 32 * (q & 1) + lane;  // this lane's I column
+      const int ch0 = 4 * half;
+      const int ch_end = min((t_ncols(c) + 31) / 32, ch0 + 4);
+      const bool keep = P.act && c.row0 + c.rows <= P.act_rows;
+      float* kept = keep ? P.act + row0 * (2 * P.out_ld) + (hwarp ? 0 : P.out_ld) + icol : nullptr;
+      // the scale word of grouped row g, byte of this warp pair's 32-column block
+      uint8_t* scb = reinterpret_cast<uint8_t*>(P.asc + static_cast<int64_t>(c.nt) * P.a_ld) +
+                     (2 * static_cast<int>(rank) + (q & 1));
+      const int64_t grow0 = mx_group_row0(c.row0, c.g) + c.mt * 256;
+#pragma unroll 1
+      for (int ch = ch0; ch < ch_end; ++ch) {
+        const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
+        uint32_t v[32];
+        tmem_ld32(taddr + ch * 32, v);
+        tmem_ld_wait();
+        if (keep) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) kept[static_cast<int64_t>(ch * 32 + j) * (2 * P.out_ld)] = __uint_as_float(v[j]);
+        }
+        if (!hwarp) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) xb[j * 32 + lane] = __uint_as_float(v[j]);
+        }
+        named_bar(pbar, 64);  // u of the chunk in shared memory
+        if (hwarp) {
+          float a[32], m[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            a[j] = __bfloat162float(__float2bfloat16_rn(silu_f(__uint_as_float(v[j])) * xb[j * 32 + lane]));
+            m[j] = fabsf(a[j]);
+          }
+          // m[0] of lane l = amax over the 32 columns of row l
+#pragma unroll
+          for (int sh = 16; sh >= 1; sh >>= 1) {
+            const bool upper = (lane & sh) != 0;
+#pragma unroll
+            for (int j = 0; j < sh; ++j) {
+              const float send = upper ? m[j] : m[j + sh];
+              const float keepv = upper ? m[j + sh] : m[j];
+              m[j] = fmaxf(keepv, __shfl_xor_sync(0xffffffffu, send, sh));
+            }
+          }
+          const int e = mx_exp(m[0]);
+          uint8_t* arow = P.aq + (row0 + ch * 32) * P.out_ld + icol;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, e, j);
+            const float inv = __uint_as_float(static_cast<uint32_t>(127 - ej) << 23);  // 2^-e
+            if (j < nv)
+              arow[static_cast<int64_t>(j) * P.out_ld] =
+                  static_cast<uint8_t>(__nv_cvt_float_to_fp8(a[j] * inv, __NV_SATFINITE, __NV_E4M3));
+          }
+          if (lane < nv) scb[4 * mx_scale_pos(grow0 + ch * 32 + lane)] = static_cast<uint8_t>(e + 127);
+        }
+        named_bar(pbar, 64);  // the chunk's u consumed
+      }
+      tc_fence_before();
+      if (leader) mbar_arrive(tempty);  // the accumulator is free for the next tile
+      else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+    }
+    __syncwarp();
   } else if (kT && warp >= 4) {
     // ---------------- epilogue, transposed form (both CTAs) ----------------
     // Warp 4 + 4 h + q: TMEM lane quarter q (output columns 32 q .. of the
@@ -544,14 +662,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 2) tmem_dealloc2(tmem_base, 512);
 }
 
-size_t mx_smem_bytes(int G, bool bf16_out) {
+size_t mx_smem_bytes(int G, bool bf16_out, bool swiglu_t = false) {
   return 1024 + static_cast<size_t>(mx_stages(bf16_out)) * (CODE_BYTES + SF_BYTES) +
-         (bf16_out ? STAGING_BYTES : 0) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
+         (bf16_out ? STAGING_BYTES : (swiglu_t ? XCH_BYTES : 0)) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st) {
-  const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay);
+  const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay, kT && kSwiglu && !kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
@@ -571,8 +689,8 @@ bool out_map(CUtensorMap* m, const void* p, int64_t rows, int cols) {
                       static_cast<uint64_t>(cols) * 2, 32, 64, true);
 }
 
-bool code_map(CUtensorMap* m, const void* p, int64_t rows, int K) {
-  return make_tmap_2d(m, p, kU8, rows, K, static_cast<uint64_t>(K), 128, BKB, true);
+bool code_map(CUtensorMap* m, const void* p, int64_t rows, int K, int box_rows = 128) {
+  return make_tmap_2d(m, p, kU8, rows, K, static_cast<uint64_t>(K), box_rows, BKB, true);
 }
 // scale words [K/128][ld] as a 2D tensor of K/128 rows of ld words (ld is a
 // multiple of 128), boxes of one 128-row block
@@ -626,7 +744,8 @@ mok_status upgate_mx_params(MxParams& P, const void* xq, const void* xsc, int64_
 
 mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
                             const void* sg, const void* qu, const void* su, const int32_t* offsets,
-                            int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept) {
+                            int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept,
+                            const void* sp) {
   if (rows == 0) return MOK_OK;
   if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
@@ -636,6 +755,16 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
   P.asc = static_cast<uint32_t*>(asc);
   P.act = kept.act;
   P.act_rows = kept.limit();
+  // fewer than 512 routed rows per group on average and the paired scale
+  // blocks given: the routed rows as the MMA's N dimension (no padding rows
+  // in the MMAs)
+  if (sp && rows < static_cast<int64_t>(512) * G) {
+    const int64_t wrows = static_cast<int64_t>(G) * I;
+    if (!code_map(&P.tmU64, qu, wrows, D, 64) || !code_map(&P.tmG64, qg, wrows, D, 64) ||
+        !scale_map(&P.tmSP, sp, mx_scale_ld(2 * wrows), D))
+      return MOK_ERR_CUDA;
+    return run_mx<true, false, true>(P, st);
+  }
   return run_mx<true>(P, st);
 }
 

@@ -180,7 +180,13 @@ inline size_t mx_scale_bytes(int64_t rows, int64_t K, int groups = 0) {
 // fp32 when f32_out: the backward's t)
 mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const void* qg,
                             const void* sg, const void* qu, const void* su, const int32_t* offsets,
-                            int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept = {});
+                            int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept = {},
+                            const void* sp = nullptr);
+// Paired scale blocks of W_up / W_gate (plain-layout scale words sg, su of
+// G*I rows, K = D) for the up/gate with the routed rows as N: block
+// b = e (I / 64) + s holds the words of W_up rows e I + 64 s .. + 63, then
+// of the same W_gate rows; plain layout of 2 G I virtual rows.
+mok_status launch_pair_scales(const void* sg, const void* su, int G, int I, int D, void* sp, cudaStream_t st);
 mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
                           const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
                           cudaStream_t st, bool f32_out = false);

@@ -38,7 +38,7 @@ class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_gate", "w_up", "w_down", "q_gate", "q_up", "q_down",
                  "sc_gate", "sc_up", "sc_down", "ws_gate", "ws_up", "ws_down",
-                 "qt_down", "sct_down", "qt_gu", "sct_gu")]
+                 "qt_down", "sct_down", "qt_gu", "sct_gu", "sc_gu_pair")]
 
 
 class PlanBuf(ctypes.Structure):
@@ -77,6 +77,7 @@ _SIGS = {
     "mok_quantize_mxfp8_bwd_weights": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P, _P,
                                                       _P, _P]),
     "mok_mxfp8_scale_bytes": (ctypes.c_size_t, [_I64, _I64, ctypes.c_int32]),
+    "mok_mxfp8_pair_scales": (ctypes.c_int, [ctypes.POINTER(Shape), ctypes.POINTER(Weights), _P, _P]),
     "mok_check_wait_timeout": (ctypes.c_int, [_P]),
     "mok_router": (ctypes.c_int, [ctypes.POINTER(Shape), _P, _P, _P, _P, _P, _P]),
     "mok_plan_ranks_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int32] * 4),
@@ -142,7 +143,7 @@ def make_weights(t: Dict[str, object]) -> Weights:
     w = Weights()
     for name in ("w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down",
                  "q_gate", "q_up", "q_down", "sc_gate", "sc_up", "sc_down",
-                 "qt_down", "sct_down", "qt_gu", "sct_gu"):
+                 "qt_down", "sct_down", "qt_gu", "sct_gu", "sc_gu_pair"):
         if t.get(name) is not None:
             setattr(w, name, _ptr(t[name]))
     return w
@@ -267,6 +268,13 @@ def quantize_mxfp8_bwd_weights(shape: Shape, weights: Weights, qt_down, sct_down
     _check(_lib_handle().mok_quantize_mxfp8_bwd_weights(ctypes.byref(shape), ctypes.byref(weights), _ptr(qt_down),
                                                         _ptr(sct_down), _ptr(qt_gu), _ptr(sct_gu),
                                                         _stream(stream)), "mok_quantize_mxfp8_bwd_weights")
+
+
+def mxfp8_pair_scales(shape: Shape, weights: Weights, sc_gu_pair, stream=None):
+    """The paired W_up / W_gate scale blocks of the MXFP8 up/gate with the
+    routed rows as N (mok_mxfp8_pair_scales), from weights' sc_gate, sc_up."""
+    _check(_lib_handle().mok_mxfp8_pair_scales(ctypes.byref(shape), ctypes.byref(weights), _ptr(sc_gu_pair),
+                                               _stream(stream)), "mok_mxfp8_pair_scales")
 
 
 def mx_scale_words(rows: int, cols: int, groups: int = 0) -> int:

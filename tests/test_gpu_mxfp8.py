@@ -62,13 +62,20 @@ def quantize(m, t: torch.Tensor):
     return q, sc
 
 
-def mx_weights(m, d):
+def mx_weights(m, d, pair=False):
+    """The forward's MXFP8 weight copies; pair: also the paired W_up / W_gate
+    scale blocks, so that the up/gate takes the routed rows as N when the
+    experts average fewer than 512 rows (the library's other up/gate form;
+    test_upgate_routed_rows_as_n_bitexact holds it to this one's bytes)."""
     out = dict(d)
     E, I, D = d["w_gate"].shape
     for name, key in (("gate", "w_gate"), ("up", "w_up"), ("down", "w_down")):
         w = d[key]
         q, sc = quantize(m, w.reshape(-1, w.shape[-1]))
         out["q_" + name], out["sc_" + name] = q, sc
+    if pair:
+        out["sc_gu_pair"] = torch.empty(m.mx_scale_words(2 * E * I, D), dtype=torch.int32, device=DEV)
+        m.mxfp8_pair_scales(m.make_shape(T=1, D=D, I=I, E=E, K=1), m.make_weights(out), out["sc_gu_pair"])
     return out
 
 
@@ -401,3 +408,62 @@ def test_backward_mxfp8_grid_inputs_bare_tolerance(m, name):
              ("dw_down", "dW_down"), ("dws_gate", "dWs_gate"), ("dws_up", "dWs_up"), ("dws_down", "dWs_down")]
     for k, r in pairs:
         assert_close(f(got[k]), ref[r], MXFP8_TOL, f"mxfp8 bwd grid {r} [{name}]")
+
+
+def test_pair_scales_are_the_permutation():
+    """mok_mxfp8_pair_scales: block b = e (I/64) + s of the paired copy holds
+    the scale words of W_up rows e I + 64 s .. + 63, then of the same W_gate
+    rows, in the 128-row block order (row 32 c + l at word 4 l + c)."""
+    m = mok()
+    cfg = BWD["ragged"]
+    d = mx_weights(m, {k: v.to(DEV) for k, v in W.make_inputs(cfg, "cpu").items()})
+    E, I, D = cfg.E, cfg.I, cfg.D
+    pos = lambda r: (r & ~127) | ((r & 31) << 2) | ((r >> 5) & 3)
+    sg = d["sc_gate"].cpu().numpy().reshape(D // 128, -1)
+    su = d["sc_up"].cpu().numpy().reshape(D // 128, -1)
+    sp = d["sc_gu_pair"].cpu().numpy().reshape(D // 128, -1)
+    v = np.arange(2 * E * I)
+    b, mm = v >> 7, v & 127
+    r = (b // (I // 64)) * I + 64 * (b % (I // 64)) + (mm & 63)
+    want = np.where(mm[None, :] < 64, su[:, pos(r)], sg[:, pos(r)])
+    assert np.array_equal(sp[:, pos(v)], want)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "skew_small", "dsv3_mxfp8_fwd", "dsv3_mxfp8_fwdbwd"])
+def test_upgate_routed_rows_as_n_bitexact(m, name):
+    """The MXFP8 up/gate with the routed rows as N (paired scales) gives the
+    row-major kernel's bytes: a codes, a scale words, y and the forward's
+    out; on the fwd+bwd layer also the kept h, u and every gradient."""
+    if name in CONFIG_NAMES:
+        cfg = W.CONFIGS[name]
+        inp = W.make_inputs(cfg, DEV)
+    else:
+        cfg = SMALL[name].replace(dtype="mxfp8")
+        inp = {k: v.to(DEV) for k, v in W.make_inputs(cfg, "cpu").items()}
+    dp = mx_weights(m, inp, pair=True)
+    dr = mx_weights(m, inp, pair=False)
+    shape = m.shape_of(cfg)
+    res = []
+    for d in (dp, dr):
+        ws = torch.zeros(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+        out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+        saved = alloc_plan(cfg, DEV)
+        saved["act"] = torch.zeros(cfg.R, 2 * cfg.I, dtype=torch.float32, device=DEV)
+        m.moe_fwd(shape, m.make_weights(d), inp["x"], inp["s"], out, ws, m.make_plan_buf(saved))
+        m.check_device_status()
+        res.append((out, saved["act"], ws))
+    assert torch.equal(res[0][0].view(torch.int16), res[1][0].view(torch.int16)), "out"
+    assert torch.equal(res[0][1].view(torch.int32), res[1][1].view(torch.int32)), "kept h, u"
+    assert torch.equal(res[0][2], res[1][2]), "workspace (a codes, a scales, y)"
+    if cfg.backward:
+        dp = bwd_weights(m, cfg, inp)
+        dr = dict(dp)
+        del dr["sc_gu_pair"]
+        gp = _mx_fwd_bwd(m, cfg, dp, act_rows=cfg.R)
+        gr = _mx_fwd_bwd(m, cfg, dr, act_rows=cfg.R)
+        for k, v in gp.items():
+            bits = (lambda t: t.view(torch.int16)) if v.dtype == torch.bfloat16 else (lambda t: t.view(torch.int32))
+            assert torch.equal(bits(v), bits(gr[k])), k
+
+
+CONFIG_NAMES = ("dsv3_mxfp8_fwd", "dsv3_mxfp8_fwdbwd")

@@ -243,10 +243,10 @@ BWD = {
 }
 
 
-def bwd_weights(m, cfg, d):
+def bwd_weights(m, cfg, d, pair=False):
     """The forward's MXFP8 copies plus the backward's (W_down^T along D,
     [W_gate^T | W_up^T] along 2I) from mok_quantize_mxfp8_bwd_weights."""
-    out = mx_weights(m, d)
+    out = mx_weights(m, d, pair=pair)
     E, I, D = cfg.E, cfg.I, cfg.D
     out["qt_down"] = torch.empty(E * I, D, dtype=torch.uint8, device=DEV)
     out["sct_down"] = torch.empty(m.mx_scale_words(E * I, D), dtype=torch.int32, device=DEV)
@@ -416,7 +416,7 @@ def test_pair_scales_are_the_permutation():
     rows, in the 128-row block order (row 32 c + l at word 4 l + c)."""
     m = mok()
     cfg = BWD["ragged"]
-    d = mx_weights(m, {k: v.to(DEV) for k, v in W.make_inputs(cfg, "cpu").items()})
+    d = mx_weights(m, {k: v.to(DEV) for k, v in W.make_inputs(cfg, "cpu").items()}, pair=True)
     E, I, D = cfg.E, cfg.I, cfg.D
     pos = lambda r: (r & ~127) | ((r & 31) << 2) | ((r >> 5) & 3)
     sg = d["sc_gate"].cpu().numpy().reshape(D // 128, -1)
@@ -456,7 +456,7 @@ def test_upgate_routed_rows_as_n_bitexact(m, name):
     assert torch.equal(res[0][1].view(torch.int32), res[1][1].view(torch.int32)), "kept h, u"
     assert torch.equal(res[0][2], res[1][2]), "workspace (a codes, a scales, y)"
     if cfg.backward:
-        dp = bwd_weights(m, cfg, inp)
+        dp = bwd_weights(m, cfg, inp, pair=True)
         dr = dict(dp)
         del dr["sc_gu_pair"]
         gp = _mx_fwd_bwd(m, cfg, dp, act_rows=cfg.R)

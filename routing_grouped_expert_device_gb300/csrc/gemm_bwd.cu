@@ -18,9 +18,12 @@
 //  wgrad        : dW[e] = bf16(sum over the expert's rows of P^T Q) with both
 //                 operands MN-major and K running over rows; the last K block
 //                 of an expert stops at its end (16-row MMA steps, the few
-//                 rows past the end zeroed in A).
+//                 rows past the end zeroed in A).  Clusters of two CTAs take
+//                 neighbouring M tiles and share B: each loads half of it
+//                 and multicasts that half into both CTAs' stages.
 #include "gemm_core.cuh"
 #include "kernels.h"
+#include "pair.cuh"
 
 namespace mok {
 namespace {
@@ -462,6 +465,216 @@ struct WgradCfg {
   }
 };
 
+
+// ---------------------------------------------------------------------------
+// The weight gradient on clusters of two CTAs that share B.
+//
+// A wgrad tile writes 64 KB of dW and reads 96 KB of operand rows from L2
+// (K over an expert's ~128 rows is short, so the operand reads are not
+// amortised), and those L2 reads share the memory system with the dW write
+// stream: the more bytes a kernel reads from L2 per byte it writes to DRAM,
+// the lower its write rate.  Here the two CTAs
+// of a cluster take M tiles 2p and 2p + 1 of the same (expert, N tile): each
+// loads its own A chunks and one half of B (chunks rank * NB / 2 ..), the
+// latter with a cluster multicast into the same stage of both CTAs, so every
+// CTA requests 32 KB per 64-row stage instead of 48 KB and issues four TMA
+// loads instead of six.  The MMAs stay per CTA (cta_group::1), so the rows
+// past an expert's end are zeroed in each CTA's own A as before, and TMEM,
+// the accumulators and the epilogue are the single-CTA kernel's.
+//
+// Barriers: a stage's full barrier counts its own producer's arrival and
+// 48 KB (its A, its half of B, the peer's half of B); its empty barrier
+// counts two arrivals, the MMA commits of both CTAs (multicast), since a
+// producer refills its half of B in both CTAs.  Both CTAs walk the same
+// sequence of (expert, M tile pair, N tile) units and K blocks, so their
+// stage and phase counters stay in step; every wait is bounded, and the
+// CTAs meet at a cluster barrier before either exits, so no multicast or
+// remote arrival reaches a CTA that has left.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* m, int32_t x, int32_t y,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+// Arrive on `bar` (same offset) in every CTA of `mask` once this thread's
+// earlier tcgen05 operations have completed (single-CTA MMAs).
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+template <int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
+    wgrad_cluster(const __grid_constant__ typename WgradCfg<BN>::Params P) {
+  using Cfg = WgradCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* epi_smem = smem + Cfg::STAGES * Cfg::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi_smem + Cfg::EPI_SMEM_BYTES);
+  uint64_t* empty = full + Cfg::STAGES;
+  uint64_t* tfull = empty + Cfg::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* total_holder = reinterpret_cast<int*>(tmem_holder + 2);
+  int* tstart = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(full) + 256);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  constexpr uint16_t kBoth = 0x3;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 2);  // the MMA commits of both CTAs
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) tmem_alloc(tmem_holder, Cfg::TMEM_COLS);
+  if (warp == 3) {
+    const int total = build_tile_table(P.sched, tstart, lane);
+    if (lane == 0) *total_holder = total;
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers initialised before any multicast or remote commit
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int total = *total_holder;
+  const int cid = blockIdx.x >> 1;
+  const int ncl = gridDim.x >> 1;
+  // this CTA's M tile of a unit: the schedule counts M tile pairs
+  auto own = [rank](TileCoord c) {
+    c.mt = 2 * c.mt + rank;
+    return c;
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    uint32_t stage = 0, phase = 0;
+    uint32_t issued_parity[Cfg::STAGES];
+    bool issued[Cfg::STAGES];
+    for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = false;
+    bool ok = true;
+    TileWalker walk(P.sched, tstart);
+    for (int unit = cid; unit < total && ok; unit += ncl) {
+      const TileCoord c = own(walk.at(unit));
+      for (int kb = 0; kb < c.kblocks; ++kb) {
+        bool got = false;
+        if (lane == 0) got = mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER);
+        ok = __shfl_sync(0xffffffffu, got, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* st = smem + stage * Cfg::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], Cfg::STAGE_BYTES);
+          const int rk = c.row0 + kb * Cfg::BKW;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) tma_load_2d(st + j * Cfg::CH, &P.tmA, c.mt * 128 + 64 * j, rk, &full[stage]);
+#pragma unroll
+          for (int h = 0; h < Cfg::NB / 2; ++h) {
+            const int j = rank * (Cfg::NB / 2) + h;
+            tma_load_2d_mc(st + (2 + j) * Cfg::CH, &P.tmB, c.nt * BN + 64 * j, rk, &full[stage], kBoth);
+          }
+        }
+        __syncwarp();
+        issued[stage] = true;
+        issued_parity[stage] = phase;
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      for (int i = 0; i < Cfg::STAGES; ++i) {
+        if (!issued[i]) continue;
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&full[i], issued_parity[i]) && globaltimer() - t0 < kWaitBudgetNs) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    uint32_t stage = 0, phase = 0;
+    bool ok = true, any = false;
+    int it = 0;
+    TileWalker walk(P.sched, tstart);
+    for (int unit = cid; unit < total && ok; unit += ncl, ++it) {
+      const TileCoord c = own(walk.at(unit));
+      const uint32_t acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, P.status, SITE_MMA));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * Cfg::ACC_COLS;
+      for (int kb = 0; kb < c.kblocks; ++kb) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA));
+        if (!ok) break;
+        tc_fence_after();
+        Cfg::fixup(P, c, kb, smem + stage * Cfg::STAGE_BYTES, lane);
+        __syncwarp();
+        if (lane == 0) {
+          Cfg::mma(P, c, kb, smem + stage * Cfg::STAGE_BYTES, d_tmem);
+          mma_commit_mc(&empty[stage], kBoth);  // both producers may refill the stage
+          any = true;
+        }
+        __syncwarp();
+        if (++stage == Cfg::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&tfull[acc]);
+      __syncwarp();
+    }
+    any = __shfl_sync(0xffffffffu, any, 0);
+    if (any) {
+      if (lane == 0) mma_commit(drain);
+      __syncwarp();
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitBudgetNs) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 4;
+    int it = 0;
+    TileWalker walk(P.sched, tstart);
+    for (int unit = cid; unit < total; unit += ncl, ++it) {
+      const TileCoord c = own(walk.at(unit));
+      const uint32_t acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort_flag, P.status, SITE_EPILOGUE)))
+        break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + acc * Cfg::ACC_COLS + (static_cast<uint32_t>(ew * 32) << 16);
+      Cfg::epilogue(P, c, taddr, ew, lane, c.kblocks > 0, epi_smem + ew * (Cfg::EPI_SMEM_BYTES / 4));
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+    if (lane == 0) bulk_wait0();
+  }
+
+  tc_fence_before();
+  cluster_sync();  // no multicast load or remote commit still targets either CTA
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
 template <class Cfg>
 mok_status run(const typename Cfg::Params& P, cudaStream_t st) {
   const size_t smem = gemm_smem_bytes<Cfg>(P.sched.G);
@@ -610,7 +823,19 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
   P.M = M;
   P.N = N;
   P.out = static_cast<__nv_bfloat16*>(dw);
-  return run<WgradCfg<BN>>(P, st);
+  const int sms = num_sms();
+  if ((M / 128) % 2 != 0 || sms < 2) return run<WgradCfg<BN>>(P, st);
+  // clusters of two CTAs on neighbouring M tiles sharing B: the schedule
+  // counts M tile pairs
+  P.sched.m_tiles_fixed = M / 256;
+  const size_t smem = gemm_smem_bytes<WgradCfg<BN>>(P.sched.G);
+  if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(wgrad_cluster<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  wgrad_cluster<BN><<<(sms / 2) * 2, 256, smem, st>>>(P);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
 }
 
 mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,

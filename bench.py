@@ -63,6 +63,10 @@ def parse_args():
     p.add_argument("--producer-sms", type=int, default=0,
                    help="SMs left to route, plan and the dispatch while the shared expert's up/gate "
                         "runs on the others (mok_shape.producer_sms; 0 = the shared expert takes every SM)")
+    p.add_argument("--bwd-shared-sms", type=int, default=0,
+                   help="fwd+bwd: SMs the shared expert's backward takes on a side stream while the routed "
+                        "dgrad and dX run on the others (mok_shape.bwd_shared_sms; 0 = no side stream, which "
+                        "measured fastest)")
     p.add_argument("--mx-pair-scales", action="store_true",
                    help="MXFP8: give the paired W_up / W_gate scale blocks, so that the up/gate takes the "
                         "routed rows as N (measured slower than the row-major up/gate on GB300)")
@@ -367,7 +371,8 @@ def run_ours(args, world, rank, local):
     d = W.make_inputs(cfg, dev, seed=rank)
     T, D, I, E, K, Is, R = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, cfg.R
     ring = args.chunk_rows > 0 and not mx and not cfg.backward
-    shape = M.shape_of(cfg, chunk_rows=args.chunk_rows if ring else 0, producer_sms=args.producer_sms)
+    shape = M.shape_of(cfg, chunk_rows=args.chunk_rows if ring else 0, producer_sms=args.producer_sms,
+                       bwd_shared_sms=args.bwd_shared_sms)
     i32, f32, bf, u8 = torch.int32, torch.float32, torch.bfloat16, torch.uint8
     if mx:
         # weights are model parameters: quantised once, outside the timed region
@@ -639,6 +644,7 @@ def run_ours(args, world, rank, local):
                        "global_batch": world * T, "parallelism": f"replicas x{world}",
                        "chunk_rows": args.chunk_rows if ring else 0, "producer_sms": args.producer_sms,
                        "kept_act_rows": (act_rows if cfg.backward else None),
+                       "bwd_shared_sms": (M.bwd_shared_sms(shape) if cfg.backward else None),
                        "l2": "inputs larger than L2: every step streams all expert weights "
                              f"({(nonempty * 3 * I * D + 3 * Is * D) * 2 / 1e9:.1f} GB)"},
             "tflops": round(tflops, 1), "tensor_frac": round(tflops / tensor_peak, 4),

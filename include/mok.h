@@ -81,12 +81,23 @@ typedef enum {
  * every SM but producer_sms (at least 2), which stay free so that the
  * dispatch runs beside them instead of queueing behind; 0 = the shared
  * expert's launches take every SM.  The same holds for mok_shared_ffn and
- * the shared-only call of mok_expert_upgate.  0..4096. */
+ * the shared-only call of mok_expert_upgate.  0..4096.
+ * bwd_shared_sms: the split of the GPU in mok_moe_bwd.  The shared expert's
+ * backward (its dgrad, dX and three weight gradients) needs only x, dY and
+ * its own weights; with bwd_shared_sms > 0 it runs on a side stream on that
+ * many SMs (at most a third of them) while the routed experts' dgrad and dX
+ * run on the others, and the caller's stream waits for it before the
+ * reverse combine, the first launch that reads its output.  0 = no side
+ * stream: the shared expert's backward runs after the routed dX on every
+ * SM, which measured faster on a GB300 at every split (the routed dgrad and
+ * dX lose more bandwidth on fewer SMs than the overlap hides).  0..4096;
+ * every setting gives the same bits. */
 typedef struct {
   int32_t T, D, I, E, K, I_shared;
   int32_t dtype;
   int32_t chunk_rows;
   int32_t producer_sms;
+  int32_t bwd_shared_sms;
 } mok_shape;
 
 /* MXFP8 tensors (paper note, "The production details").  A [rows][cols]
@@ -346,12 +357,23 @@ mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void 
  * weight gradients are BF16 products (of bf16 x, dY, dh, du, g a) and the
  * shared expert is BF16.  MXFP8 needs I % 256 == 0 (the t and dX products
  * run on 256-column tiles; MOK_ERR_UNSUPPORTED otherwise) and w's q_* and
- * qt_* copies (MOK_ERR_INVALID_ARG without them). */
+ * qt_* copies (MOK_ERR_INVALID_ARG without them).  With
+ * shape.bwd_shared_sms > 0 the shared expert's backward runs on the side
+ * stream of mok_moe_fwd, on mok_bwd_shared_sms SMs, while the routed dgrad
+ * and dX take the others; the caller's stream waits for it before the
+ * reverse combine, so on return all work is queued on `stream` as for a
+ * single-stream call. */
 mok_status mok_moe_bwd(const mok_shape *shape, const mok_weights *w, const void *x,
                        const float *s, const mok_plan_buf *saved, const void *dy, void *dx,
                        void *dw_gate, void *dw_up, void *dw_down, void *dws_gate,
                        void *dws_up, void *dws_down, float *ds, float *dg, void *ws,
                        size_t ws_bytes, void *stream);
+
+/* SMs that mok_moe_bwd gives the shared expert's backward on its side
+ * stream on the current device: shape.bwd_shared_sms, at most a third of the
+ * SMs; 0 when the backward runs without a side stream (I_shared = 0, T = 0,
+ * or shape.bwd_shared_sms under 2); -1 for an invalid shape.  Host-only. */
+int32_t mok_bwd_shared_sms(const mok_shape *shape);
 
 /* Bytes of MXFP8 scale storage for a [rows][cols] tensor: plain layout
  * when groups = 0, grouped layout over `groups` experts otherwise (see the

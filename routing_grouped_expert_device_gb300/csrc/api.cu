@@ -16,6 +16,7 @@ bool shape_ok(const mok_shape* s) {
   if (s->dtype != MOK_BF16 && s->dtype != MOK_MXFP8) return false;
   if (s->chunk_rows != 0 && (s->chunk_rows < 512 || s->chunk_rows > 32768)) return false;
   if (s->producer_sms < 0 || s->producer_sms > 4096) return false;
+  if (s->bwd_shared_sms < 0 || s->bwd_shared_sms > 4096) return false;
   return true;
 }
 
@@ -23,6 +24,13 @@ int shared_expert_sms(const mok_shape& s) {
   if (s.producer_sms <= 0) return 0;
   const int left = num_sms() - s.producer_sms;
   return left >= 2 ? left : 2;
+}
+
+int bwd_shared_split(const mok_shape& s) {
+  if (!s.I_shared || s.bwd_shared_sms <= 0 || s.T == 0) return 0;
+  const int cap = num_sms() / 3;
+  const int k = s.bwd_shared_sms < cap ? s.bwd_shared_sms : cap;
+  return k >= 2 ? k : 0;
 }
 
 namespace {
@@ -518,6 +526,11 @@ extern "C" mok_status mok_quantize_mxfp8_bwd_weights(const mok_shape* shape, con
   return launch_quantize_cols_mxfp8(w->w_up, s.E, s.I, s.D, qt_gu, sct_gu, 2 * s.I, s.I, st);
 }
 
+extern "C" int32_t mok_bwd_shared_sms(const mok_shape* shape) {
+  if (!shape_ok(shape)) return -1;
+  return bwd_shared_split(*shape);
+}
+
 extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, const void* x,
                                   const float* s_in, const mok_plan_buf* saved, const void* dy,
                                   void* dx, void* dw_gate, void* dw_up, void* dw_down,
@@ -558,10 +571,51 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
   float* dgp = at<float>(ws, L.dgp);
   void* dxr = at<void>(ws, L.dxr);
   mok_status r;
+  // The shared expert's backward (paper note, "The production details": the
+  // shared expert needs no dispatch) reads x, dY and its own weights only.
+  // With shape.bwd_shared_sms it runs on a side stream on `ksh` SMs while
+  // the routed dgrad and dX run on the rest, and the caller's stream joins
+  // it before the reverse combine, the first launch that reads its dX;
+  // without (the default, faster on a GB300: the routed dgrad and dX need
+  // every SM for their bandwidth) it runs after the routed dX.
+  const int ksh = bwd_shared_split(s);
+  const int routed_sms = ksh > 0 ? num_sms() - ksh : 0;
+  void* dxs = s.I_shared ? at<void>(ws, L.dxs) : nullptr;
+  auto shared_bwd = [&](cudaStream_t ss, int sms) -> mok_status {
+    void* dhs = at<void>(ws, L.dhs);
+    void* dus = at<void>(ws, L.dus);
+    void* ags = at<void>(ws, L.ags);
+    mok_status e;
+    if ((e = launch_bwd_dgrad(x, dy, s.T, w->ws_gate, w->ws_up, w->ws_down, nullptr, 1, s.D, s.I_shared, nullptr,
+                              dhs, dus, ags, nullptr, ss, 0, sms)) != MOK_OK)
+      return e;
+    if ((e = launch_bwd_dx(dhs, dus, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.D, s.I_shared, dxs, ss, sms)) !=
+        MOK_OK)
+      return e;
+    if ((e = launch_wgrad(dy, ags, s.T, nullptr, 1, s.D, s.I_shared, dws_down, ss, sms)) != MOK_OK) return e;
+    if ((e = launch_wgrad(dhs, x, s.T, nullptr, 1, s.I_shared, s.D, dws_gate, ss, sms)) != MOK_OK) return e;
+    return launch_wgrad(dus, x, s.T, nullptr, 1, s.I_shared, s.D, dws_up, ss, sms);
+  };
+  SideStream* side = nullptr;
+  bool joined = true;
+  // on an error after the fork, the caller's stream still waits for the side stream
+  auto fail = [&](mok_status e) {
+    if (!joined) cudaStreamWaitEvent(st, side->join, 0);
+    return e;
+  };
+  if (ksh > 0) {
+    if (!(side = side_stream())) return MOK_ERR_CUDA;
+    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+      return MOK_ERR_CUDA;
+    r = shared_bwd(side->s, ksh);
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess) return MOK_ERR_CUDA;
+    joined = false;
+    if (r != MOK_OK) return fail(r);
+  }
   // gather x, dY and the route weights into expert order (the forward's plan)
-  if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, pb.g, g_route, st)) != MOK_OK) return r;
+  if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, pb.g, g_route, st)) != MOK_OK) return fail(r);
   if ((r = launch_dispatch_bf16(dy, pb.route_dst, s.T, s.K, s.D, dyg, nullptr, nullptr, st)) != MOK_OK)
-    return r;
+    return fail(r);
   if (mx) {
     // MXFP8: quantising dispatches of x and dY; replay h, u; t = dY W_down
     // (W_down^T quantised along D); the activation gradient with [dh | du]
@@ -577,49 +631,39 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
     uint8_t* dhu_sc = at<uint8_t>(ws, L.dhu_sc);
     if (replay && (r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xq,
                                              xq_sc, st)) != MOK_OK)
-      return r;
+      return fail(r);
     if ((r = launch_dispatch_mxfp8(dy, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, dyq, dyq_sc, st)) !=
         MOK_OK)
-      return r;
+      return fail(r);
     if (replay && (r = launch_replay_mx(xq, xq_sc, R, w->q_gate, w->sc_gate, w->q_up, w->sc_up, pb.offsets, s.E,
                                         s.D, s.I, hh, uu, st, kept_rows)) != MOK_OK)
-      return r;
+      return fail(r);
     if ((r = launch_down_mx(dyq, dyq_sc, R, w->qt_down, w->sct_down, pb.offsets, s.E, s.I, s.D, tt, st,
-                            /*f32_out=*/true)) != MOK_OK)
-      return r;
+                            /*f32_out=*/true, routed_sms)) != MOK_OK)
+      return fail(r);
     if ((r = launch_act_grad_mx(hh, uu, tt, g_route, pb.table, pb.offsets, R, s.I, s.E, dh, du, ag, dhu_q, dhu_sc,
                                 dgp, st, kept)) != MOK_OK)
-      return r;
-    if ((r = launch_down_mx(dhu_q, dhu_sc, R, w->qt_gu, w->sct_gu, pb.offsets, s.E, s.D, 2 * s.I, dxr, st)) !=
-        MOK_OK)
-      return r;
+      return fail(r);
+    if ((r = launch_down_mx(dhu_q, dhu_sc, R, w->qt_gu, w->sct_gu, pb.offsets, s.E, s.D, 2 * s.I, dxr, st,
+                            /*f32_out=*/false, routed_sms)) != MOK_OK)
+      return fail(r);
   } else {
     // t = dY W_down with the kept h, u; replay h, u for the other groups;
     // dh, du, g*a, <t, a> partials
     if (kept_rows > 0 && (r = launch_bwd_dgrad_kept(dyg, R, w->w_down, pb.offsets, s.E, s.D, s.I, g_route,
-                                                    kept.act, kept_rows, dh, du, ag, dgp, st)) != MOK_OK)
-      return r;
+                                                    kept.act, kept_rows, dh, du, ag, dgp, st, routed_sms)) != MOK_OK)
+      return fail(r);
     if (replay && (r = launch_bwd_dgrad(xg, dyg, R, w->w_gate, w->w_up, w->w_down, pb.offsets, s.E, s.D, s.I,
-                                        g_route, dh, du, ag, dgp, st, kept_rows)) != MOK_OK)
-      return r;
-    if ((r = launch_bwd_dx(dh, du, R, w->w_gate, w->w_up, pb.offsets, s.E, s.D, s.I, dxr, st)) != MOK_OK)
-      return r;
+                                        g_route, dh, du, ag, dgp, st, kept_rows, routed_sms)) != MOK_OK)
+      return fail(r);
+    if ((r = launch_bwd_dx(dh, du, R, w->w_gate, w->w_up, pb.offsets, s.E, s.D, s.I, dxr, st, routed_sms)) !=
+        MOK_OK)
+      return fail(r);
   }
-  void* dxs = nullptr;
-  if (s.I_shared) {
-    void* dhs = at<void>(ws, L.dhs);
-    void* dus = at<void>(ws, L.dus);
-    void* ags = at<void>(ws, L.ags);
-    dxs = at<void>(ws, L.dxs);
-    if ((r = launch_bwd_dgrad(x, dy, s.T, w->ws_gate, w->ws_up, w->ws_down, nullptr, 1, s.D,
-                              s.I_shared, nullptr, dhs, dus, ags, nullptr, st)) != MOK_OK)
-      return r;
-    if ((r = launch_bwd_dx(dhs, dus, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.D, s.I_shared, dxs,
-                           st)) != MOK_OK)
-      return r;
-    if ((r = launch_wgrad(dy, ags, s.T, nullptr, 1, s.D, s.I_shared, dws_down, st)) != MOK_OK) return r;
-    if ((r = launch_wgrad(dhs, x, s.T, nullptr, 1, s.I_shared, s.D, dws_gate, st)) != MOK_OK) return r;
-    if ((r = launch_wgrad(dus, x, s.T, nullptr, 1, s.I_shared, s.D, dws_up, st)) != MOK_OK) return r;
+  if (s.I_shared && ksh == 0 && (r = shared_bwd(st, 0)) != MOK_OK) return r;
+  if (!joined) {
+    joined = true;
+    if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return MOK_ERR_CUDA;
   }
   // reverse combine in fixed k order
   if ((r = launch_combine(dxr, dxs, nullptr, pb.route_dst, s.T, s.K, s.D, dx, st)) != MOK_OK) return r;

@@ -675,14 +675,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
   if (warp == 2) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
+// SMs a persistent launch takes: every SM, or at most max_sms > 0 of them
+// (the rest stay free for another stream's kernels).
+int grid_sms(int max_sms) {
+  const int n = num_sms();
+  return max_sms > 0 && max_sms < n ? max_sms : n;
+}
+
 template <class Cfg>
-mok_status run(const typename Cfg::Params& P, cudaStream_t st) {
+mok_status run(const typename Cfg::Params& P, cudaStream_t st, int max_sms = 0) {
   const size_t smem = gemm_smem_bytes<Cfg>(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   if (cudaFuncSetAttribute(gemm_persistent<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MOK_ERR_CUDA;
-  gemm_persistent<Cfg><<<num_sms(), 256, smem, st>>>(P);
+  gemm_persistent<Cfg><<<grid_sms(max_sms), 256, smem, st>>>(P);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -714,7 +721,7 @@ bool mnmap(CUtensorMap* m, const void* p, int64_t rows, int cols) {
 mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
                             const void* w_up, const void* w_down, const int32_t* offsets, int G,
                             int D, int I, const float* g_route, void* dh, void* du, void* ag,
-                            float* dgp, cudaStream_t st, int32_t skip_rows_below) {
+                            float* dgp, cudaStream_t st, int32_t skip_rows_below, int max_sms) {
   if (rows == 0) return MOK_OK;
   DgradCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradCfg::BKD);
@@ -743,12 +750,12 @@ mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const
   P.du = static_cast<__nv_bfloat16*>(du);
   P.ag = static_cast<__nv_bfloat16*>(ag);
   P.dgp = dgp;
-  return run<DgradCfg>(P, st);
+  return run<DgradCfg>(P, st, max_sms);
 }
 
 mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_down, const int32_t* offsets, int G,
                                  int D, int I, const float* g_route, const float* act, int32_t kept_rows, void* dh,
-                                 void* du, void* ag, float* dgp, cudaStream_t st) {
+                                 void* du, void* ag, float* dgp, cudaStream_t st, int max_sms) {
   if (rows == 0 || kept_rows <= 0 || !offsets) return MOK_OK;
   DgradKeptCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradKeptCfg::BKD);
@@ -770,12 +777,12 @@ mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_do
   P.du = static_cast<__nv_bfloat16*>(du);
   P.ag = static_cast<__nv_bfloat16*>(ag);
   P.dgp = dgp;
-  return run<DgradKeptCfg>(P, st);
+  return run<DgradKeptCfg>(P, st, max_sms);
 }
 
 mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,
                          const void* w_up, const int32_t* offsets, int G, int D, int I, void* dx,
-                         cudaStream_t st) {
+                         cudaStream_t st, int max_sms) {
   if (rows == 0) return MOK_OK;
   DxCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, D / 256, 2 * (I / BK));
@@ -790,12 +797,12 @@ mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const voi
   P.half_kb = I / BK;
   P.out = static_cast<__nv_bfloat16*>(dx);
   P.out_ld = D;
-  return run<DxCfg>(P, st);
+  return run<DxCfg>(P, st, max_sms);
 }
 
 template <int BN>
 mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t* offsets, int G,
-                    int M, int N, void* dw, cudaStream_t st) {
+                    int M, int N, void* dw, cudaStream_t st, int max_sms) {
   typename WgradCfg<BN>::Params P;
   SchedArgs s;
   s.offsets = offsets;
@@ -823,8 +830,8 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
   P.M = M;
   P.N = N;
   P.out = static_cast<__nv_bfloat16*>(dw);
-  const int sms = num_sms();
-  if ((M / 128) % 2 != 0 || sms < 2) return run<WgradCfg<BN>>(P, st);
+  const int sms = grid_sms(max_sms);
+  if ((M / 128) % 2 != 0 || sms < 2) return run<WgradCfg<BN>>(P, st, max_sms);
   // clusters of two CTAs on neighbouring M tiles sharing B: the schedule
   // counts M tile pairs
   P.sched.m_tiles_fixed = M / 256;
@@ -839,12 +846,12 @@ mok_status wgrad_bn(const void* pm, const void* qn, int64_t rows, const int32_t*
 }
 
 mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
-                        int G, int M, int N, void* dw, cudaStream_t st) {
+                        int G, int M, int N, void* dw, cudaStream_t st, int max_sms) {
   // 256-wide tiles unless their shared memory (which grows with the
   // number of groups) does not fit
   if (N % 256 == 0 && gemm_smem_bytes<WgradCfg<256>>(offsets ? G : 1) <= 227 * 1024)
-    return wgrad_bn<256>(pm, qn, rows, offsets, G, M, N, dw, st);
-  return wgrad_bn<128>(pm, qn, rows, offsets, G, M, N, dw, st);
+    return wgrad_bn<256>(pm, qn, rows, offsets, G, M, N, dw, st, max_sms);
+  return wgrad_bn<128>(pm, qn, rows, offsets, G, M, N, dw, st, max_sms);
 }
 
 }  // namespace mok

@@ -668,14 +668,15 @@ size_t mx_smem_bytes(int G, bool bf16_out, bool swiglu_t = false) {
 }
 
 template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
-mok_status run_mx(const MxParams& P, cudaStream_t st) {
+mok_status run_mx(const MxParams& P, cudaStream_t st, int max_sms = 0) {
   const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay, kT && kSwiglu && !kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
-  kern<<<(num_sms() / 2) * 2, THREADS, smem, st>>>(P);
+  const int sms = max_sms > 0 && max_sms < num_sms() ? max_sms : num_sms();
+  kern<<<sms >= 2 ? (sms / 2) * 2 : 2, THREADS, smem, st>>>(P);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -789,7 +790,7 @@ mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const
 
 mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
                           const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
-                          cudaStream_t st, bool f32_out) {
+                          cudaStream_t st, bool f32_out, int max_sms) {
   if (rows == 0) return MOK_OK;
   if (!offsets || G < 1) return MOK_ERR_INVALID_ARG;
   MxParams P;
@@ -819,7 +820,7 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   if (f32_out) {
     P.y = nullptr;
     P.y32 = static_cast<float*>(y);
-    return by_rows ? run_mx<false, false, true, true>(P, st) : run_mx<false, false, false, true>(P, st);
+    return by_rows ? run_mx<false, false, true, true>(P, st, max_sms) : run_mx<false, false, false, true>(P, st, max_sms);
   }
   P.y = static_cast<__nv_bfloat16*>(y);
   P.y32 = nullptr;
@@ -827,8 +828,8 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   P.tmO1 = P.tmO0;
   // fewer than 512 routed rows per group on average: the routed rows as the
   // MMA's N dimension (no padding rows in the MMAs)
-  if (by_rows) return run_mx<false, false, true>(P, st);
-  return run_mx<false>(P, st);
+  if (by_rows) return run_mx<false, false, true>(P, st, max_sms);
+  return run_mx<false>(P, st, max_sms);
 }
 
 }  // namespace mok

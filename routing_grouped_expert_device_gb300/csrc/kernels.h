@@ -110,26 +110,27 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
                             const SharedOperands* sh = nullptr, int max_sms = 0);
 
-// Backward.  dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
+// Backward (max_sms > 0: the persistent grid takes at most that many SMs).
+// dgrad+replay: dh, du, ag [rows][I] bf16 and, when dgp is
 // non-null, dgp [rows][I/32] partials of <t, a> (32 I columns each);
 // g_route null = weight 1.  skip_rows_below > 0: only the groups with a row
 // at or above it (the others were kept by the forward).
 mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const void* w_gate,
                             const void* w_up, const void* w_down, const int32_t* offsets, int G,
                             int D, int I, const float* g_route, void* dh, void* du, void* ag,
-                            float* dgp, cudaStream_t st, int32_t skip_rows_below = 0);
+                            float* dgp, cudaStream_t st, int32_t skip_rows_below = 0, int max_sms = 0);
 // The same outputs for the groups whose rows all lie below kept_rows, from
 // the forward's kept h, u (act fp32 [rows][2I]) and t = dYg W_down.
 mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_down, const int32_t* offsets, int G,
                                  int D, int I, const float* g_route, const float* act, int32_t kept_rows, void* dh,
-                                 void* du, void* ag, float* dgp, cudaStream_t st);
+                                 void* du, void* ag, float* dgp, cudaStream_t st, int max_sms = 0);
 // dx [rows][D] = bf16(dh W_gate + du W_up)
 mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,
                          const void* w_up, const int32_t* offsets, int G, int D, int I, void* dx,
-                         cudaStream_t st);
+                         cudaStream_t st, int max_sms = 0);
 // dw [G][M][N] = bf16(sum over each group's rows of pm[p][m] qn[p][n])
 mok_status launch_wgrad(const void* pm, const void* qn, int64_t rows, const int32_t* offsets,
-                        int G, int M, int N, void* dw, cudaStream_t st);
+                        int G, int M, int N, void* dw, cudaStream_t st, int max_sms = 0);
 // MXFP8 backward.  Replay: h, u fp32 [rows][I] from the up/gate pair GEMM
 // (operands as launch_upgate_mx); skip_rows_below > 0: only the groups with
 // a row at or above it.  Activation gradient: from fp32 h, u, t [R][I] and
@@ -189,12 +190,16 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
 mok_status launch_pair_scales(const void* sg, const void* su, int G, int I, int D, void* sp, cudaStream_t st);
 mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const void* qd,
                           const void* sd, const int32_t* offsets, int G, int D, int I, void* y,
-                          cudaStream_t st, bool f32_out = false);
+                          cudaStream_t st, bool f32_out = false, int max_sms = 0);
 
 bool shape_ok(const mok_shape* s);
 // SMs the shared expert's side-stream launches may take (0: all): every SM
 // but shape.producer_sms, which stay free for route, plan and the dispatch.
 int shared_expert_sms(const mok_shape& s);
+// SMs the shared expert's backward takes on mok_moe_bwd's side stream
+// (0: no side stream, it runs after the routed dX on every SM):
+// shape.bwd_shared_sms, at most a third of the SMs.
+int bwd_shared_split(const mok_shape& s);
 
 // Device address of a __device__ variable (its host-side stand-in `symbol`)
 // on the current device.  cudaGetSymbolAddress is called once per device and

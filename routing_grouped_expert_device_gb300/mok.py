@@ -31,7 +31,7 @@ class MokError(RuntimeError):
 
 class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("T", "D", "I", "E", "K", "I_shared", "dtype", "chunk_rows", "producer_sms")]
+                ("T", "D", "I", "E", "K", "I_shared", "dtype", "chunk_rows", "producer_sms", "bwd_shared_sms")]
 
 
 class Weights(ctypes.Structure):
@@ -55,6 +55,7 @@ _SZ = ctypes.c_size_t
 _SIGS = {
     "mok_workspace_bytes": (_SZ, [ctypes.POINTER(Shape), ctypes.c_int]),
     "mok_workspace_offset": (_SZ, [ctypes.POINTER(Shape), ctypes.c_int]),
+    "mok_bwd_shared_sms": (ctypes.c_int32, [ctypes.POINTER(Shape)]),
     "mok_route": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P]),
     "mok_plan": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "mok_plan_static": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P, _P, _P, _P]),
@@ -130,13 +131,13 @@ def _check(status: int, where: str):
         raise MokError(status, where)
 
 
-def make_shape(T, D, I, E, K, I_shared=0, dtype=MOK_BF16, chunk_rows=0, producer_sms=0) -> Shape:
-    return Shape(T, D, I, E, K, I_shared, dtype, chunk_rows, producer_sms)
+def make_shape(T, D, I, E, K, I_shared=0, dtype=MOK_BF16, chunk_rows=0, producer_sms=0, bwd_shared_sms=0) -> Shape:
+    return Shape(T, D, I, E, K, I_shared, dtype, chunk_rows, producer_sms, bwd_shared_sms)
 
 
-def shape_of(cfg, dtype=None, chunk_rows=0, producer_sms=0) -> Shape:
+def shape_of(cfg, dtype=None, chunk_rows=0, producer_sms=0, bwd_shared_sms=0) -> Shape:
     dt = MOK_MXFP8 if (dtype or cfg.dtype) == "mxfp8" else MOK_BF16
-    return make_shape(cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, dt, chunk_rows, producer_sms)
+    return make_shape(cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, dt, chunk_rows, producer_sms, bwd_shared_sms)
 
 
 def make_weights(t: Dict[str, object]) -> Weights:
@@ -163,6 +164,14 @@ def workspace_bytes(shape: Shape, op: int) -> int:
 
 
 WS_BWD_DH, WS_BWD_DU, WS_BWD_AG = 1, 2, 3
+
+
+def bwd_shared_sms(shape: Shape) -> int:
+    """SMs mok_moe_bwd gives the shared expert's backward on its side stream (0: none)."""
+    n = int(_lib_handle().mok_bwd_shared_sms(ctypes.byref(shape)))
+    if n < 0:
+        raise ValueError("invalid shape")
+    return n
 
 
 def workspace_offset(shape: Shape, region: int) -> int:

@@ -56,10 +56,11 @@ def weight_grads(b, x_bits, dy_bits):
             "dW_up": (O.round_bf16(b["du"].T @ X), O.sum_range(b["du"], rg["du"], X))}
 
 
-def _fwd_bwd(m, cfg, d, act_rows=None):
+def _fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0):
     """Forward + backward through the C ABI.  act_rows: rows of the kept
-    h, u store (None: no store, the backward replays every expert)."""
-    shape = m.shape_of(cfg)
+    h, u store (None: no store, the backward replays every expert);
+    bwd_shared_sms: shape.bwd_shared_sms."""
+    shape = m.shape_of(cfg, bwd_shared_sms=bwd_shared_sms)
     ws = torch.empty(max(m.workspace_bytes(shape, m.OP_FWD), m.workspace_bytes(shape, m.OP_BWD)),
                      dtype=torch.uint8, device=DEV)
     out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
@@ -338,3 +339,47 @@ def test_backward_grid_inputs_full_size(m):
     assert_close(_f(got["dws_gate"][i0:i1]), res["dW_gate"][0], BF16_TOL, "bf16 bwd grid dWs_gate [full]")
     assert_close(_f(got["dws_up"][i0:i1]), res["dW_up"][0], BF16_TOL, "bf16 bwd grid dWs_up [full]")
     assert_close(_f(got["dws_down"][:, i0:i1]), res["dW_down"][0], BF16_TOL, "bf16 bwd grid dWs_down [full]")
+
+
+@pytest.mark.parametrize("name", ["ragged", "skew_256", "one_token", "k_equals_e"])
+def test_backward_shared_side_stream_is_bitexact(m, name):
+    """shape.bwd_shared_sms runs the shared expert's backward on a side
+    stream on that many SMs while the routed dgrad and dX take the others:
+    other grids, the same tiles, the same bits as the single-stream
+    backward (bwd_shared_sms = 0), with and without the kept store."""
+    cfg = SMALL[name]
+    inp = W.make_inputs(cfg, "cpu", with_dy=True)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    for act_rows in (cfg.R, None):
+        base, _ = _fwd_bwd(m, cfg, d, act_rows=act_rows)
+        for k in (2, 9, 40):
+            got, _ = _fwd_bwd(m, cfg, d, act_rows=act_rows, bwd_shared_sms=k)
+            for key, v in base.items():
+                if v is not None:
+                    assert torch.equal(_bits(v), _bits(got[key])), (k, act_rows, key)
+
+
+def test_bwd_shared_sms_rule(m):
+    """The split mok_moe_bwd uses: none by default or without a shared
+    expert, an explicit count capped at a third of the SMs."""
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    c4 = W.CONFIGS["dsv3_bf16_fwdbwd"]
+    assert m.bwd_shared_sms(m.shape_of(c4)) == 0
+    assert m.bwd_shared_sms(m.shape_of(c4.replace(I_shared=0), bwd_shared_sms=20)) == 0
+    assert m.bwd_shared_sms(m.shape_of(c4, bwd_shared_sms=1)) == 0
+    assert m.bwd_shared_sms(m.shape_of(c4, bwd_shared_sms=4096)) == n // 3
+    assert m.bwd_shared_sms(m.shape_of(c4, bwd_shared_sms=20)) == min(20, n // 3)
+    with pytest.raises(ValueError):
+        m.bwd_shared_sms(m.shape_of(c4, bwd_shared_sms=-1))
+
+
+def test_backward_shared_side_stream_full_size(m):
+    """The DSV3 fwd+bwd layer (T 4096, h, u kept) with the shared expert's
+    backward on 40 SMs of a side stream gives the single-stream bits."""
+    cfg = W.CONFIGS["dsv3_bf16_fwdbwd"]
+    d = W.make_inputs(cfg, DEV, with_dy=True)
+    base, _ = _fwd_bwd(m, cfg, d, act_rows=cfg.R)
+    base = {k: _bits(v).clone() for k, v in base.items() if v is not None}
+    got, _ = _fwd_bwd(m, cfg, d, act_rows=cfg.R, bwd_shared_sms=40)
+    for key, v in base.items():
+        assert torch.equal(v, _bits(got[key])), key

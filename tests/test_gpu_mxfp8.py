@@ -274,8 +274,8 @@ def test_bwd_weight_copies_bitexact(m):
     assert np.array_equal(words_to_bytes(d["sct_gu"], E * D, 2 * I), sc)
 
 
-def _mx_fwd_bwd(m, cfg, d, act_rows=None):
-    shape = m.shape_of(cfg)
+def _mx_fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0):
+    shape = m.shape_of(cfg, bwd_shared_sms=bwd_shared_sms)
     w = m.make_weights(d)
     ws = torch.empty(max(m.workspace_bytes(shape, m.OP_FWD), m.workspace_bytes(shape, m.OP_BWD)),
                      dtype=torch.uint8, device=DEV)
@@ -467,3 +467,19 @@ def test_upgate_routed_rows_as_n_bitexact(m, name):
 
 
 CONFIG_NAMES = ("dsv3_mxfp8_fwd", "dsv3_mxfp8_fwdbwd")
+
+
+@pytest.mark.parametrize("name", ["ragged", "skew"])
+def test_backward_mxfp8_shared_side_stream_is_bitexact(m, name):
+    """The MXFP8 backward with the shared expert's backward on a side stream
+    (t, the activation gradient and dX of the routed experts on the other
+    SMs) gives the single-stream bits."""
+    cfg = BWD[name]
+    inp = W.make_inputs(cfg, "cpu", with_dy=True)
+    d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
+    base = _mx_fwd_bwd(m, cfg, d, act_rows=cfg.R)
+    for k in (10, 40):
+        got = _mx_fwd_bwd(m, cfg, d, act_rows=cfg.R, bwd_shared_sms=k)
+        for key, v in base.items():
+            bits = (lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32))
+            assert torch.equal(bits(v), bits(got[key])), (k, key)

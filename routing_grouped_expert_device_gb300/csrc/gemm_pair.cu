@@ -858,16 +858,26 @@ mok_status launch_upgate_pair_t(const void* A, int64_t a_rows, const void* w_gat
 // [32 rows][64 columns] boxes of each 32-row chunk, and one thread stores
 // both.  The shared expert's down tiles (the schedule's extra group, its
 // T rows in tiles of 256) run in the same launch.
+//
+// kDx: the backward's dX per route, dx = dh W_gate + du W_up, on the same
+// tiles: the weight operand has the MMA's M = 256 D columns and K = 2I, the
+// first I from W_gate and the rest from W_up, each stored [I][D] and so
+// MN-major (128-row K boxes of 64 D columns, one 16-row K step every 2 KB,
+// the two 64-column halves of a CTA's 128 D columns a box apart); B is the
+// tile's routed rows of dh, then of du, K-major as a.
 struct PairTDownParams {
   SchedArgs sched;  // bm = 256 routed rows, n_tiles = D / 256
   int* status;
   CUtensorMap tmW, tmA, tmOut;     // W_down [G * D][I], a [rows][I] (boxes 128 x 64), y [rows][D]
   CUtensorMap tmWs, tmAs, tmOut_s;  // the extra group: W_sd [D][I_s], a_s [T][I_s], ys [T][D]
+  CUtensorMap tmW2, tmA2;          // kDx: W_up [G * I][D], du [rows][I] (tmW, tmA: W_gate, dh)
   __nv_bfloat16* out;
   __nv_bfloat16* out_s;
   int32_t D;
+  int32_t I;                       // kDx: K blocks below I / BK read W_gate and dh
 };
 
+template <bool kDx>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
     gemm_pair_down_t(const __grid_constant__ PairTDownParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -928,8 +938,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const TileCoord c = walk.at(tile);
         const int wrow = c.g * P.D + c.nt * 256 + static_cast<int>(rank) * 128;  // this CTA's W_down rows
         const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
-        const CUtensorMap* tmW = c.extra ? &P.tmWs : &P.tmW;
-        const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
+        const int dcol = c.nt * 256 + static_cast<int>(rank) * 128;  // kDx: this CTA's D columns
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
             ok = false;
@@ -938,11 +947,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE_BYTES);
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
           uint8_t* st = smem + stage * STAGE_BYTES;
+          if constexpr (kDx) {
+            const bool up = kb * BK >= P.I;  // the second half of K: W_up and du
+            const int k0 = up ? kb * BK - P.I : kb * BK;
 #pragma unroll
-          for (int j = 0; j < BK / BOX_K; ++j) {
-            const int kx = kb * BK + j * BOX_K;
-            tma_load_2d_pair(st + j * BOX_BYTES, tmW, kx, wrow, lbar);
-            tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, tmA, kx, xrow, lbar);
+            for (int j = 0; j < BK / BOX_K; ++j) {
+              tma_load_2d_pair(st + j * BOX_BYTES, up ? &P.tmW2 : &P.tmW, dcol + 64 * j, c.g * P.I + k0, lbar);
+              tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, up ? &P.tmA2 : &P.tmA, k0 + j * BOX_K, xrow, lbar);
+            }
+          } else {
+            const CUtensorMap* tmW = c.extra ? &P.tmWs : &P.tmW;
+            const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
+#pragma unroll
+            for (int j = 0; j < BK / BOX_K; ++j) {
+              const int kx = kb * BK + j * BOX_K;
+              tma_load_2d_pair(st + j * BOX_BYTES, tmW, kx, wrow, lbar);
+              tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, tmA, kx, xrow, lbar);
+            }
           }
           issued[stage] = true;
           issued_parity[stage] = phase;
@@ -972,7 +993,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
         const TileCoord c = walk.at(tile);
         const uint32_t acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
-        const uint32_t idesc = idesc_bf16(256, t_ncols(c), false, false);
+        const uint32_t idesc = idesc_bf16(256, t_ncols(c), kDx, false);
         ok = __all_sync(0xffffffffu, mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, P.status, SITE_MMA));
         if (!ok) break;
         tc_fence_after();
@@ -987,10 +1008,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               const uint32_t off = (k / (BOX_K / 16)) * BOX_BYTES + (k % (BOX_K / 16)) * 32;
+              // kDx: A MN-major, K step k at 16 rows x 128 B, the 64-column halves a box apart
+              const uint64_t adesc = kDx ? sdesc_sw128(a + k * 2048, BOX_BYTES, 1024) : sdesc_sw128(a + off, 16, 1024);
               asm volatile(
                   "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                   "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-                  "l"(sdesc_sw128(a + off, 16, 1024)), "l"(sdesc_sw128(b + off, 16, 1024)), "r"(idesc),
+                  "l"(adesc), "l"(sdesc_sw128(b + off, 16, 1024)), "r"(idesc),
                   "r"(static_cast<uint32_t>((kb | k) != 0))
                   : "memory");
             }
@@ -1128,15 +1151,55 @@ mok_status launch_down_pair_t(const void* a, int64_t a_rows, const void* w_down,
   }
   const size_t smem = pair_t_down_smem_bytes(P.sched.G);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(gemm_pair_down_t, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_pair_down_t<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                           static_cast<int>(smem)) != cudaSuccess)
     return MOK_ERR_CUDA;
-  gemm_pair_down_t<<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
+  gemm_pair_down_t<false><<<(num_sms() / 2) * 2, 256, smem, st>>>(P);
+  MOK_CHECK_LAUNCH();
+  return MOK_OK;
+}
+
+mok_status launch_dx_pair_t_impl(const void* dh, const void* du, int64_t rows, const void* w_gate, const void* w_up,
+                                 const int32_t* offsets, int G, int D, int I, void* dx, cudaStream_t st, int max_sms) {
+  PairTDownParams P{};
+  P.sched = pair_sched(offsets, G, rows, D / 256, 2 * I / BK);
+  P.status = status_ptr();
+  if (!P.status) return MOK_ERR_CUDA;
+  const uint64_t wrows = static_cast<uint64_t>(G) * I;
+  // dh, du K-major (128 routed rows x 64 K per box); W_gate, W_up [G I][D]
+  // MN-major (128 K rows x 64 D columns per box)
+  if (!make_tmap_2d(&P.tmA, dh, kBF16, rows, I, static_cast<uint64_t>(I) * 2, 128, BOX_K, true) ||
+      !make_tmap_2d(&P.tmA2, du, kBF16, rows, I, static_cast<uint64_t>(I) * 2, 128, BOX_K, true) ||
+      !make_tmap_2d(&P.tmW, w_gate, kBF16, wrows, D, static_cast<uint64_t>(D) * 2, BK, 64, true) ||
+      !make_tmap_2d(&P.tmW2, w_up, kBF16, wrows, D, static_cast<uint64_t>(D) * 2, BK, 64, true) ||
+      !out_map(&P.tmOut, dx, rows, D))
+    return MOK_ERR_CUDA;
+  P.out = static_cast<__nv_bfloat16*>(dx);
+  P.out_s = nullptr;
+  P.tmWs = P.tmW;
+  P.tmAs = P.tmA;
+  P.tmOut_s = P.tmOut;
+  P.D = D;
+  P.I = I;
+  const size_t smem = pair_t_down_smem_bytes(P.sched.G);
+  if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(gemm_pair_down_t<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOK_ERR_CUDA;
+  const int sms = max_sms > 0 && max_sms < num_sms() ? max_sms : num_sms();
+  gemm_pair_down_t<true><<<sms >= 2 ? (sms / 2) * 2 : 2, 256, smem, st>>>(P);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
 
 }  // namespace
+
+mok_status launch_dx_pair_t(const void* dh, const void* du, int64_t rows, const void* w_gate, const void* w_up,
+                            const int32_t* offsets, int G, int D, int I, void* dx, cudaStream_t st, int max_sms) {
+  if (rows == 0) return MOK_OK;
+  if (!offsets || G < 1 || D % 256 || I % BK) return MOK_ERR_INVALID_ARG;
+  return launch_dx_pair_t_impl(dh, du, rows, w_gate, w_up, offsets, G, D, I, dx, st, max_sms);
+}
 
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                               const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,

@@ -933,6 +933,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
       bool issued[STAGES];
       for (int i = 0; i < STAGES; ++i) issued[i] = false;
       bool ok = true;
+      const uint64_t keep_policy = policy_evict_last();     // re-read operands
+      const uint64_t stream_policy = policy_evict_first();  // read-once weights
       TileWalker walk(P.sched, tstart);
       for (int tile = cid; tile < total && ok; tile += ncl) {
         const TileCoord c = walk.at(tile);
@@ -955,14 +957,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(256, 1)
               tma_load_2d_pair(st + j * BOX_BYTES, up ? &P.tmW2 : &P.tmW, dcol + 64 * j, c.g * P.I + k0, lbar);
               tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, up ? &P.tmA2 : &P.tmA, k0 + j * BOX_K, xrow, lbar);
             }
-          } else {
-            const CUtensorMap* tmW = c.extra ? &P.tmWs : &P.tmW;
-            const CUtensorMap* tmA = c.extra ? &P.tmAs : &P.tmA;
+          } else if (c.extra) {
+            // the shared expert's W_sd and a_s are re-read by all of its
+            // tiles, which are spread through the launch: keep them in L2
+            // while the routed weights stream through
 #pragma unroll
             for (int j = 0; j < BK / BOX_K; ++j) {
               const int kx = kb * BK + j * BOX_K;
-              tma_load_2d_pair(st + j * BOX_BYTES, tmW, kx, wrow, lbar);
-              tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, tmA, kx, xrow, lbar);
+              tma_load_2d_pair_hint(st + j * BOX_BYTES, &P.tmWs, kx, wrow, lbar, keep_policy);
+              tma_load_2d_pair_hint(st + A_BYTES + j * BOX_BYTES, &P.tmAs, kx, xrow, lbar, keep_policy);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < BK / BOX_K; ++j) {
+              const int kx = kb * BK + j * BOX_K;
+              tma_load_2d_pair_hint(st + j * BOX_BYTES, &P.tmW, kx, wrow, lbar, stream_policy);
+              tma_load_2d_pair(st + A_BYTES + j * BOX_BYTES, &P.tmA, kx, xrow, lbar);
             }
           }
           issued[stage] = true;

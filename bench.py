@@ -71,7 +71,8 @@ def parse_args():
                    help="MXFP8: give the paired W_up / W_gate scale blocks, so that the up/gate takes the "
                         "routed rows as N (measured slower than the row-major up/gate on GB300)")
     p.add_argument("--act-rows", type=int, default=-1,
-                   help="fwd+bwd: rows of the forward's kept h, u store (-1 = every routed row, "
+                   help="fwd+bwd: rows of the forward's kept h, u store (-1 = every routed row, and the "
+                        "shared expert's h, u kept too; "
                         "0 = none: the backward replays every expert)")
     p.add_argument("--protocol-warmup", type=int, default=500,
                    help="the pages' protocol: warm-up calls of the public entry point")
@@ -425,9 +426,11 @@ def run_ours(args, world, rank, local):
         saved = dict(topk_idx=topk, g=g, counts=counts, offsets=offsets, table=table, route_dst=route_dst)
         act_rows = R if args.act_rows < 0 else min(args.act_rows, R)
         if act_rows > 0:
-            # the forward keeps h, u (fp32) of the experts that fit; the
-            # backward replays only the others
+            # the forward keeps h, u (fp32) of the experts that fit, and the
+            # shared expert's; the backward replays only the others
             saved["act"] = torch.empty(act_rows, 2 * I, dtype=f32, device=dev)
+            if Is:
+                saved["act_shared"] = torch.empty(T, 2 * Is, dtype=f32, device=dev)
         pb = M.make_plan_buf(saved)
         gr = dict(dx=torch.empty(T, D, dtype=bf, device=dev), dw_gate=torch.empty(E, I, D, dtype=bf, device=dev),
                   dw_up=torch.empty(E, I, D, dtype=bf, device=dev), dw_down=torch.empty(E, D, I, dtype=bf, device=dev),

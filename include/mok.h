@@ -158,13 +158,20 @@ typedef struct {
  * h, u (streaming W_gate and W_up again) only for the others.  act = NULL
  * or act_rows = 0 keeps nothing: the backward replays every expert.  With
  * act_rows >= T*K every expert is kept.  act must be 16-byte aligned and
- * stay untouched between the forward and the backward. */
+ * stay untouched between the forward and the backward.
+ *
+ * act_shared (optional): the same for the shared expert, fp32 [T][2 I_shared]
+ * (h in columns [0, I_shared), u in [I_shared, 2 I_shared), row = token);
+ * with it the backward's shared dgrad reads h, u there instead of
+ * recomputing them from x.  NULL: the backward replays them.  16-byte
+ * aligned; ignored when I_shared = 0. */
 typedef struct {
   int32_t *topk_idx;
   float *g;
   int32_t *counts, *offsets, *table, *route_dst;
   float *act;
   int64_t act_rows;
+  float *act_shared;
 } mok_plan_buf;
 
 /* Bytes of caller-provided device workspace `op` needs for `shape`

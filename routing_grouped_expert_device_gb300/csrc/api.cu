@@ -404,10 +404,13 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     pb.route_dst = at<int32_t>(ws, L.route_dst);
     pb.act = nullptr;
     pb.act_rows = 0;
+    pb.act_shared = nullptr;
   }
-  if (pb.act_rows < 0 || (pb.act && !aligned16(pb.act))) return MOK_ERR_INVALID_ARG;
+  if (pb.act_rows < 0 || (pb.act && !aligned16(pb.act)) || (pb.act_shared && !aligned16(pb.act_shared)))
+    return MOK_ERR_INVALID_ARG;
   // h, u of the groups that fit in the caller's store, kept for the backward
   const KeptAct kept{pb.act_rows > 0 ? pb.act : nullptr, pb.act_rows};
+  const KeptAct kept_shared{s.I_shared ? pb.act_shared : nullptr, s.T};
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   mok_status r;
@@ -433,7 +436,8 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
       return MOK_ERR_CUDA;
     const int sms = shared_expert_sms(s);
-    r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, side->s, sms);
+    r = launch_upgate(x, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.T, s.D, s.I_shared, as, side->s, sms,
+                      kept_shared);
     if (r == MOK_OK && mx)
       r = launch_down(as, s.T, w->ws_down, nullptr, 1, s.T, s.D, s.I_shared, ys, side->s, sms);
     if (cudaEventRecord(side->join, side->s) != cudaSuccess) return MOK_ERR_CUDA;
@@ -552,7 +556,8 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
     return MOK_ERR_INVALID_ARG;
   if (s.I_shared && (!w->ws_gate || !w->ws_up || !w->ws_down || !dws_gate || !dws_up || !dws_down))
     return MOK_ERR_INVALID_ARG;
-  if (pb.act_rows < 0 || (pb.act && !aligned16(pb.act))) return MOK_ERR_INVALID_ARG;
+  if (pb.act_rows < 0 || (pb.act && !aligned16(pb.act)) || (pb.act_shared && !aligned16(pb.act_shared)))
+    return MOK_ERR_INVALID_ARG;
   const BwdLayout L = bwd_layout(s);
   if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOK_ERR_WORKSPACE;
   const int64_t R = static_cast<int64_t>(s.T) * s.K;
@@ -586,9 +591,15 @@ extern "C" mok_status mok_moe_bwd(const mok_shape* shape, const mok_weights* w, 
     void* dus = at<void>(ws, L.dus);
     void* ags = at<void>(ws, L.ags);
     mok_status e;
-    if ((e = launch_bwd_dgrad(x, dy, s.T, w->ws_gate, w->ws_up, w->ws_down, nullptr, 1, s.D, s.I_shared, nullptr,
-                              dhs, dus, ags, nullptr, ss, 0, sms)) != MOK_OK)
+    // h, u from the forward's store when it kept them, else replayed from x
+    if (pb.act_shared) {
+      if ((e = launch_bwd_dgrad_kept(dy, s.T, w->ws_down, nullptr, 1, s.D, s.I_shared, nullptr, pb.act_shared, s.T,
+                                     dhs, dus, ags, nullptr, ss, sms)) != MOK_OK)
+        return e;
+    } else if ((e = launch_bwd_dgrad(x, dy, s.T, w->ws_gate, w->ws_up, w->ws_down, nullptr, 1, s.D, s.I_shared,
+                                     nullptr, dhs, dus, ags, nullptr, ss, 0, sms)) != MOK_OK) {
       return e;
+    }
     if ((e = launch_bwd_dx(dhs, dus, s.T, w->ws_gate, w->ws_up, nullptr, 1, s.D, s.I_shared, dxs, ss, sms)) !=
         MOK_OK)
       return e;

@@ -756,7 +756,7 @@ mok_status launch_bwd_dgrad(const void* xg, const void* dyg, int64_t rows, const
 mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_down, const int32_t* offsets, int G,
                                  int D, int I, const float* g_route, const float* act, int32_t kept_rows, void* dh,
                                  void* du, void* ag, float* dgp, cudaStream_t st, int max_sms) {
-  if (rows == 0 || kept_rows <= 0 || !offsets) return MOK_OK;
+  if (rows == 0 || kept_rows <= 0) return MOK_OK;
   DgradKeptCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, I / 128, D / DgradKeptCfg::BKD);
   P.sched.bm = DgradKeptCfg::ROWS;

@@ -1256,11 +1256,11 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
     P.out_s = static_cast<__nv_bfloat16*>(sh->out);
     P.out_ld_s = Is;
   }
-  if (offsets) {
-    P.act = kept.act;
-    P.act_rows = kept.limit();
-    P.act_i = I;
-  }
+  // kept h, u: every group whose rows end at or below kept.rows (offsets
+  // null: the one group of m_total rows)
+  P.act = kept.act;
+  P.act_rows = kept.limit();
+  P.act_i = I;
   if (!set_out_maps(P, m_total)) return MOK_ERR_CUDA;
   return run_pair<true>(P, st, max_sms);
 }
@@ -1312,9 +1312,9 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
 
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st, int max_sms) {
+                         cudaStream_t st, int max_sms, KeptAct kept) {
   if (a_rows == 0 || m_total == 0) return MOK_OK;
-  return launch_upgate_pair(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st, nullptr, {}, max_sms);
+  return launch_upgate_pair(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st, nullptr, kept, max_sms);
 }
 
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,

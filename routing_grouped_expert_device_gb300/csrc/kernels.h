@@ -63,7 +63,7 @@ struct KeptAct {
 // kernels of other streams).
 mok_status launch_upgate(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,
                          const int32_t* offsets, int G, int64_t m_total, int D, int I, void* a_out,
-                         cudaStream_t st, int max_sms = 0);
+                         cudaStream_t st, int max_sms = 0, KeptAct kept = {});
 mok_status launch_down(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets,
                        int G, int64_t m_total, int D, int I, void* y_out, cudaStream_t st, int max_sms = 0);
 // The shared expert as an extra group of a routed launch: A [rows][K],

@@ -43,7 +43,7 @@ class Weights(ctypes.Structure):
 
 class PlanBuf(ctypes.Structure):
     _fields_ = ([(n, ctypes.c_void_p) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst", "act")]
-                + [("act_rows", ctypes.c_int64)])
+                + [("act_rows", ctypes.c_int64), ("act_shared", ctypes.c_void_p)])
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -152,11 +152,12 @@ def make_weights(t: Dict[str, object]) -> Weights:
 
 def make_plan_buf(t: Dict[str, object]) -> PlanBuf:
     """The forward's saved state; optional "act" (fp32 [rows][2I]) keeps h, u
-    of the experts whose rows lie below its row count for the backward."""
+    of the experts whose rows lie below its row count for the backward, and
+    optional "act_shared" (fp32 [T][2 I_shared]) the shared expert's."""
     act = t.get("act")
     rows = int(act.shape[0]) if act is not None else 0
     return PlanBuf(*(_ptr(t[n]) for n in ("topk_idx", "g", "counts", "offsets", "table", "route_dst")),
-                   _ptr(act), rows)
+                   _ptr(act), rows, _ptr(t.get("act_shared")))
 
 
 def workspace_bytes(shape: Shape, op: int) -> int:

@@ -56,10 +56,11 @@ def weight_grads(b, x_bits, dy_bits):
             "dW_up": (O.round_bf16(b["du"].T @ X), O.sum_range(b["du"], rg["du"], X))}
 
 
-def _fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0):
+def _fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0, act_shared=False):
     """Forward + backward through the C ABI.  act_rows: rows of the kept
     h, u store (None: no store, the backward replays every expert);
-    bwd_shared_sms: shape.bwd_shared_sms."""
+    act_shared: also keep the shared expert's h, u; bwd_shared_sms:
+    shape.bwd_shared_sms."""
     shape = m.shape_of(cfg, bwd_shared_sms=bwd_shared_sms)
     ws = torch.empty(max(m.workspace_bytes(shape, m.OP_FWD), m.workspace_bytes(shape, m.OP_BWD)),
                      dtype=torch.uint8, device=DEV)
@@ -67,6 +68,8 @@ def _fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0):
     saved = alloc_plan(cfg, DEV)
     if act_rows is not None:
         saved["act"] = torch.full((act_rows, 2 * cfg.I), float("nan"), dtype=torch.float32, device=DEV)
+    if act_shared and cfg.I_shared:
+        saved["act_shared"] = torch.full((cfg.T, 2 * cfg.I_shared), float("nan"), dtype=torch.float32, device=DEV)
     pb = m.make_plan_buf(saved)
     w = m.make_weights(d)
     m.moe_fwd(shape, w, d["x"], d["s"], out, ws, pb)
@@ -185,9 +188,10 @@ def test_backward_kept_activations(m, name):
     """The forward keeps h, u (fp32) for every expert that fits in the store;
     the backward reads them there and replays only the other experts.  With
     the store holding every row, half the rows, or one row less than the
-    first expert, the gradients equal the all-replay path bit for bit (the
-    kept h, u are the same tensor-core sums the replay forms) and the oracle
-    at the bare tolerance."""
+    first expert, and with or without the shared expert's own store, the
+    gradients equal the all-replay path bit for bit (the kept h, u are the
+    same tensor-core sums the replay forms) and the oracle at the bare
+    tolerance."""
     cfg = SMALL[name]
     inp = W.make_inputs(cfg, "cpu", with_dy=True)
     h = host(inp)
@@ -196,8 +200,8 @@ def test_backward_kept_activations(m, name):
     offsets = saved["offsets"].cpu().numpy()
     first = int(offsets[np.flatnonzero(np.diff(offsets) > 0)[0] + 1])  # end of the first non-empty expert
     ref = O.moe_backward(h, h["dy"], cfg.K)
-    for rows in (cfg.R, cfg.R // 2, max(first - 1, 1)):
-        got, sv = _fwd_bwd(m, cfg, d, act_rows=rows)
+    for rows, keep_shared in ((cfg.R, True), (cfg.R, False), (cfg.R // 2, True), (max(first - 1, 1), False)):
+        got, sv = _fwd_bwd(m, cfg, d, act_rows=rows, act_shared=keep_shared)
         for k, v in base.items():
             if v is not None:
                 assert torch.equal(_bits(v), _bits(got[k])), (rows, k)
@@ -207,6 +211,8 @@ def test_backward_kept_activations(m, name):
         act = sv["act"].cpu().numpy()
         kept_end = int(offsets[np.searchsorted(offsets, rows, side="right") - 1])
         assert np.all(np.isfinite(act[:kept_end])) and np.all(np.isnan(act[kept_end:]))
+        if keep_shared and cfg.I_shared:  # the shared expert's h, u: every token's row written
+            assert torch.isfinite(sv["act_shared"]).all()
 
 
 @pytest.mark.parametrize("name", ["ragged", "skew_256", "tiny"])

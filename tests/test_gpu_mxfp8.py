@@ -274,7 +274,7 @@ def test_bwd_weight_copies_bitexact(m):
     assert np.array_equal(words_to_bytes(d["sct_gu"], E * D, 2 * I), sc)
 
 
-def _mx_fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0):
+def _mx_fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0, act_shared=False):
     shape = m.shape_of(cfg, bwd_shared_sms=bwd_shared_sms)
     w = m.make_weights(d)
     ws = torch.empty(max(m.workspace_bytes(shape, m.OP_FWD), m.workspace_bytes(shape, m.OP_BWD)),
@@ -283,6 +283,8 @@ def _mx_fwd_bwd(m, cfg, d, act_rows=None, bwd_shared_sms=0):
     saved = alloc_plan(cfg, DEV)
     if act_rows is not None:
         saved["act"] = torch.full((act_rows, 2 * cfg.I), float("nan"), dtype=torch.float32, device=DEV)
+    if act_shared and cfg.I_shared:
+        saved["act_shared"] = torch.full((cfg.T, 2 * cfg.I_shared), float("nan"), dtype=torch.float32, device=DEV)
     pb = m.make_plan_buf(saved)
     m.moe_fwd(shape, w, d["x"], d["s"], out, ws, pb)
     bf = torch.bfloat16
@@ -330,13 +332,14 @@ def test_backward_mxfp8_elementwise_and_deterministic(m, name):
 def test_backward_mxfp8_kept_activations(m, name):
     """MXFP8: the forward keeps h, u (fp32, from its block-scaled up/gate) of
     the experts that fit; the backward replays only the others.  Every
-    capacity gives the all-replay path's bytes."""
+    capacity, with or without the shared expert's store, gives the
+    all-replay path's bytes."""
     cfg = BWD[name]
     inp = W.make_inputs(cfg, "cpu", with_dy=True)
     d = bwd_weights(m, cfg, {k: v.to(DEV) for k, v in inp.items()})
     base = _mx_fwd_bwd(m, cfg, d)
-    for rows in (cfg.R, cfg.R // 2):
-        got = _mx_fwd_bwd(m, cfg, d, act_rows=rows)
+    for rows, keep_shared in ((cfg.R, True), (cfg.R, False), (cfg.R // 2, True)):
+        got = _mx_fwd_bwd(m, cfg, d, act_rows=rows, act_shared=keep_shared)
         for k, v in base.items():
             bits = (lambda t: t.view(torch.int16)) if v.dtype == torch.bfloat16 else (lambda t: t.view(torch.int32))
             assert torch.equal(bits(v), bits(got[k])), (rows, k)

@@ -601,10 +601,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         continue;
       }
       if (kSwiglu) {
-        uint32_t words = 0;
         const bool keep = P.act && valid && c.row0 + c.rows <= P.act_rows;
-#pragma unroll 1
-        for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
+        // a = bf16(SiLU(h) u) of this warp's two 32-column chunks, as bf16
+        // pairs (exact: a is rounded to bf16 before it is quantised), and
+        // each chunk's amax; then the accumulator is released, so the next
+        // tile's MMAs run while this tile's codes are formed and stored
+        uint32_t apk[2][16];
+        float amax[2];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int ch = 2 * half + cc;
           uint32_t hv[32], uv[32];
           tmem_ld32(taddr + ch * 32, hv);
           tmem_ld32(taddr + 128 + ch * 32, uv);
@@ -617,28 +623,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               st_global_v4(ar + P.out_ld + 4 * q, uv[4 * q], uv[4 * q + 1], uv[4 * q + 2], uv[4 * q + 3]);
             }
           }
-          float av[32];
-          float amax = 0.0f;
+          float am = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            av[j] = __bfloat162float(
-                __float2bfloat16_rn(silu_f(__uint_as_float(hv[j])) * __uint_as_float(uv[j])));
-            amax = fmaxf(amax, fabsf(av[j]));
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = __bfloat162float(
+                __float2bfloat16_rn(silu_f(__uint_as_float(hv[2 * j])) * __uint_as_float(uv[2 * j])));
+            const float a1 = __bfloat162float(
+                __float2bfloat16_rn(silu_f(__uint_as_float(hv[2 * j + 1])) * __uint_as_float(uv[2 * j + 1])));
+            am = fmaxf(am, fmaxf(fabsf(a0), fabsf(a1)));
+            apk[cc][j] = pack_bf16x2(a0, a1);
           }
-          const int e = mx_exp(amax);
+          amax[cc] = am;
+        }
+        tc_fence_before();
+        if (leader) mbar_arrive(tempty);
+        else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+        uint32_t words = 0;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int e = mx_exp(amax[cc]);
           const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
           uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
+            const uint32_t w0 = apk[cc][2 * i], w1 = apk[cc][2 * i + 1];
             const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                make_float2(av[4 * i] * inv, av[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+                make_float2(bf16lo(w0) * inv, bf16hi(w0) * inv), __NV_SATFINITE, __NV_E4M3);
             const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                make_float2(av[4 * i + 2] * inv, av[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+                make_float2(bf16lo(w1) * inv, bf16hi(w1) * inv), __NV_SATFINITE, __NV_E4M3);
             pk[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
           }
-          words |= static_cast<uint32_t>(e + 127) << (8 * (ch - 2 * half));
+          words |= static_cast<uint32_t>(e + 127) << (8 * cc);
           if (valid) {
-            uint8_t* dst = P.aq + row * P.out_ld + c.nt * 128 + ch * 32;
+            uint8_t* dst = P.aq + row * P.out_ld + c.nt * 128 + (2 * half + cc) * 32;
             st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
             st_global_v4(dst + 16, pk[4], pk[5], pk[6], pk[7]);
           }
@@ -647,6 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (valid)
           reinterpret_cast<uint16_t*>(P.asc + c.nt * P.a_ld + mx_scale_pos(mx_group_row0(c.row0, c.g) + local))[half] =
               static_cast<uint16_t>(words);
+        continue;  // the accumulator was released above
       }
       tc_fence_before();
       if (leader) mbar_arrive(tempty);

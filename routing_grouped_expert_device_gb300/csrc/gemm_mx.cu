@@ -39,12 +39,15 @@
 namespace mok {
 namespace {
 
-constexpr int BKB = 128;  // K columns (bytes) per stage
-// The quantising up/gate keeps six stages in flight.  The modes with bf16
-// outputs (down, replay) keep four and use 64 KB per CTA to drain the
-// accumulator into shared memory, so that it is free for the next tile's
-// MMAs while TMA stores write the tile out.
-constexpr int kMaxStages = 6;
+constexpr int BKB = 128;  // K columns (bytes) of one K block: one 128-byte swizzled box
+// The quantising up/gate keeps three stages of two K blocks (eight MMAs per
+// stage: the MMA thread's wait, fences and commit per stage cost about a
+// third of one K block's MMA time; six stages of one K block took 1.55 ms
+// at DSV3 size against 1.47-1.49 ms).  The modes with bf16
+// outputs (down, replay) keep four stages of one K block and use 64 KB per
+// CTA to drain the accumulator into shared memory, so that it is free for
+// the next tile's MMAs while TMA stores write the tile out.
+constexpr int kMaxStages = 3;
 constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 rows x 64 bf16
 // The quantising up/gate with the routed rows as N passes u from the warps
 // that drain it to the warps that drain h through shared memory: 32 rows x
@@ -52,14 +55,15 @@ constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 
 // warp pairs.
 constexpr int XCH_BYTES = 4 * 32 * 32 * 4;
 __host__ __device__ constexpr int mx_stages(bool bf16_out) { return bf16_out ? 4 : kMaxStages; }
-constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows
-constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B
+// K blocks (of BKB bytes) per stage
+__host__ __device__ constexpr int mx_ksub(bool bf16_out) { return bf16_out ? 1 : 2; }
+constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows, one K block
+constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B, one K block
 constexpr int CODE_BYTES = A_BYTES + B_BYTES;
 constexpr int SF_BLOCK = 512;           // one 128-row block of scale words
-constexpr int SF_BYTES = 3 * SF_BLOCK;  // A's block, B's two halves
-constexpr uint32_t TX_BYTES = 2 * (CODE_BYTES + SF_BYTES);
+constexpr int SF_BYTES = 3 * SF_BLOCK;  // A's block, B's two halves (one K block)
 constexpr uint32_t ACC_COLS = 256;
-constexpr uint32_t SF_COLS = 12;  // per stage: A 4, B 8
+constexpr uint32_t SF_COLS = 12;  // per K block: A 4, B 8
 // Eight epilogue warps: warps 4 + 4h + q drain TMEM lane quarter q (the
 // hardware ties a warp to quarter warp % 4), columns of half h of the
 // accumulator, so each warp holds the accumulator for half as long.
@@ -156,11 +160,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   constexpr bool kSwigluT = kT && kSwiglu && !kReplay;
   static_assert(!kF32 || kBf16Out, "fp32 outputs replace the bf16 ones");
   constexpr int STAGES = mx_stages(kBf16Out);
+  // a stage holds KSUB K blocks: A's KSUB boxes, then B's, then KSUB sets of
+  // three scale blocks, copied to KSUB sets of SF_COLS TMEM columns
+  constexpr int KSUB = mx_ksub(kBf16Out);
+  constexpr int STAGE_CODE = KSUB * CODE_BYTES;
+  constexpr int STAGE_SF = KSUB * SF_BYTES;
+  constexpr uint32_t STAGE_TX = 2 * (STAGE_CODE + STAGE_SF);
+  constexpr uint32_t STAGE_SF_COLS = KSUB * SF_COLS;
+  static_assert(ACC_COLS + STAGES * STAGE_SF_COLS <= 512, "accumulator and scale ring in TMEM");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sf_smem = smem + STAGES * CODE_BYTES;
-  uint8_t* staging = sf_smem + STAGES * SF_BYTES;  // 1024-byte aligned; STAGING_BYTES when kBf16Out
+  uint8_t* sf_smem = smem + STAGES * STAGE_CODE;
+  uint8_t* staging = sf_smem + STAGES * STAGE_SF;  // 1024-byte aligned; STAGING_BYTES when kBf16Out
   uint64_t* full = reinterpret_cast<uint64_t*>(staging + (kBf16Out ? STAGING_BYTES : (kSwigluT ? XCH_BYTES : 0)));
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -222,10 +234,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[stage], TX_BYTES);
+          if (leader) mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
-          uint8_t* st = smem + stage * CODE_BYTES;
-          uint8_t* sf = sf_smem + stage * SF_BYTES;
+#pragma unroll
+          for (int sub = 0; sub < KSUB; ++sub) {
+          const int kk = kb * KSUB + sub;  // the K block
+          uint8_t* st = smem + stage * STAGE_CODE + sub * A_BYTES;  // A of K block kk; B at + KSUB A_BYTES
+          uint8_t* sf = sf_smem + stage * STAGE_SF + sub * SF_BYTES;
           if (kSwigluT) {
             // A: 64 W_up rows then the same 64 W_gate rows (this CTA's half of
             // the tile's I columns) with their paired scale block; B: half of
@@ -234,29 +249,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
             const int gb = static_cast<int>(mx_group_row0(c.row0, c.g)) + c.mt * 256;
             const int pblk = (brow0 / 64 + static_cast<int>(rank)) * 128;  // virtual row of the paired block
-            tma_load_2d_pair(st, &P.tmU64, kb * BKB, urow, lbar);
-            tma_load_2d_pair(st + 64 * BKB, &P.tmG64, kb * BKB, urow, lbar);
-            tma_load_2d_pair(st + A_BYTES, &P.tmA, kb * BKB, xrow, lbar);
-            tma_load_2d_pair(sf, &P.tmSP, pblk, kb, lbar);
-            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kb, lbar);
-            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kb, lbar);
+            tma_load_2d_pair(st, &P.tmU64, kk * BKB, urow, lbar);
+            tma_load_2d_pair(st + 64 * BKB, &P.tmG64, kk * BKB, urow, lbar);
+            tma_load_2d_pair(st + KSUB * A_BYTES, &P.tmA, kk * BKB, xrow, lbar);
+            tma_load_2d_pair(sf, &P.tmSP, pblk, kk, lbar);
+            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kk, lbar);
+            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kk, lbar);
           } else if (kT) {
             // this CTA's weight rows (A): down rows 128 r .. of the tile, replay
             // the tile's rows of W_gate (CTA 0) or W_up (CTA 1)
             const int wrow = brow0 + (kReplay ? 0 : static_cast<int>(rank) * 128);
             const int xrow = c.row0 + c.mt * 256 + static_cast<int>(rank) * (t_ncols(c) / 2);
             const int gb = static_cast<int>(mx_group_row0(c.row0, c.g)) + c.mt * 256;  // the tile's scale blocks
-            tma_load_2d_pair(st, kReplay ? tmB : &P.tmB0, kb * BKB, wrow, lbar);
-            tma_load_2d_pair(st + A_BYTES, &P.tmA, kb * BKB, xrow, lbar);
-            tma_load_2d_pair(sf, kReplay && rank ? &P.tmSB1 : &P.tmSB0, wrow, kb, lbar);
-            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kb, lbar);
-            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kb, lbar);
+            tma_load_2d_pair(st, kReplay ? tmB : &P.tmB0, kk * BKB, wrow, lbar);
+            tma_load_2d_pair(st + KSUB * A_BYTES, &P.tmA, kk * BKB, xrow, lbar);
+            tma_load_2d_pair(sf, kReplay && rank ? &P.tmSB1 : &P.tmSB0, wrow, kk, lbar);
+            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kk, lbar);
+            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kk, lbar);
           } else {
-            tma_load_2d_pair(st, &P.tmA, kb * BKB, arow, lbar);
-            tma_load_2d_pair(st + A_BYTES, tmB, kb * BKB, brow, lbar);
-            tma_load_2d_pair(sf, &P.tmSA, sfrow, kb, lbar);
-            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSB0, brow0, kb, lbar);
-            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSB1, brow0 + P.b1_off, kb, lbar);
+            tma_load_2d_pair(st, &P.tmA, kk * BKB, arow, lbar);
+            tma_load_2d_pair(st + KSUB * A_BYTES, tmB, kk * BKB, brow, lbar);
+            tma_load_2d_pair(sf, &P.tmSA, sfrow, kk, lbar);
+            tma_load_2d_pair(sf + SF_BLOCK, &P.tmSB0, brow0, kk, lbar);
+            tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSB1, brow0 + P.b1_off, kk, lbar);
+          }
           }
           issued[stage] = true;
           issued_parity[stage] = phase;
@@ -293,17 +309,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t sft = tmem_base + ACC_COLS + stage * SF_COLS;
-            const uint32_t sfs = smem_u32(sf_smem + stage * SF_BYTES);
-            tmem_cp_block2(sft, sfs);                     // A: columns sft .. sft + 3
-            tmem_cp_block2(sft + 4, sfs + SF_BLOCK);      // B rows 0..127: sft + 4 .. sft + 7
-            tmem_cp_block2(sft + 8, sfs + 2 * SF_BLOCK);  // B rows 128..255: sft + 8 .. sft + 11
-            const uint32_t a = smem_u32(smem + stage * CODE_BYTES);
-            const uint32_t b = a + A_BYTES;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_mx2(tmem_base, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024),
-                      idesc_mx(k, ncols), sft, sft + 4, (kb | k) != 0);
+            for (int sub = 0; sub < KSUB; ++sub) {
+              const uint32_t sft = tmem_base + ACC_COLS + stage * STAGE_SF_COLS + sub * SF_COLS;
+              const uint32_t sfs = smem_u32(sf_smem + stage * STAGE_SF + sub * SF_BYTES);
+              tmem_cp_block2(sft, sfs);                     // A: columns sft .. sft + 3
+              tmem_cp_block2(sft + 4, sfs + SF_BLOCK);      // B rows 0..127: sft + 4 .. sft + 7
+              tmem_cp_block2(sft + 8, sfs + 2 * SF_BLOCK);  // B rows 128..255: sft + 8 .. sft + 11
+              const uint32_t a = smem_u32(smem + stage * STAGE_CODE + sub * A_BYTES);
+              const uint32_t b = a + KSUB * A_BYTES;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_mx2(tmem_base, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024),
+                        idesc_mx(k, ncols), sft, sft + 4, (kb | sub | k) != 0);
+            }
             commit2(&empty[stage], 0x3);
             any = true;
           }
@@ -681,7 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 size_t mx_smem_bytes(int G, bool bf16_out, bool swiglu_t = false) {
-  return 1024 + static_cast<size_t>(mx_stages(bf16_out)) * (CODE_BYTES + SF_BYTES) +
+  return 1024 + static_cast<size_t>(mx_stages(bf16_out)) * mx_ksub(bf16_out) * (CODE_BYTES + SF_BYTES) +
          (bf16_out ? STAGING_BYTES : (swiglu_t ? XCH_BYTES : 0)) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
@@ -693,8 +712,13 @@ mok_status run_mx(const MxParams& P, cudaStream_t st, int max_sms = 0) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
+  // the schedule counts stages of mx_ksub K blocks each
+  constexpr int ksub = mx_ksub(!kSwiglu || kReplay);
+  if (P.sched.k_blocks_fixed % ksub) return MOK_ERR_UNSUPPORTED;
+  MxParams Q = P;
+  Q.sched.k_blocks_fixed = P.sched.k_blocks_fixed / ksub;
   const int sms = max_sms > 0 && max_sms < num_sms() ? max_sms : num_sms();
-  kern<<<sms >= 2 ? (sms / 2) * 2 : 2, THREADS, smem, st>>>(P);
+  kern<<<sms >= 2 ? (sms / 2) * 2 : 2, THREADS, smem, st>>>(Q);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

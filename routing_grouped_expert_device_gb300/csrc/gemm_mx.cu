@@ -43,10 +43,11 @@ constexpr int BKB = 128;  // K columns (bytes) of one K block: one 128-byte swiz
 // The quantising up/gate keeps three stages of two K blocks (eight MMAs per
 // stage: the MMA thread's wait, fences and commit per stage cost about a
 // third of one K block's MMA time; six stages of one K block took 1.55 ms
-// at DSV3 size against 1.47-1.49 ms).  The modes with bf16
-// outputs (down, replay) keep four stages of one K block and use 64 KB per
-// CTA to drain the accumulator into shared memory, so that it is free for
-// the next tile's MMAs while TMA stores write the tile out.
+// at DSV3 size against 1.47-1.49 ms), and so do the modes with fp32
+// outputs (stored straight from registers).  The modes with bf16 outputs
+// (down, dX) keep four stages of one K block and use 64 KB per CTA to drain
+// the accumulator into shared memory, so that it is free for the next
+// tile's MMAs while TMA stores write the tile out.
 constexpr int kMaxStages = 3;
 constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 rows x 64 bf16
 // The quantising up/gate with the routed rows as N passes u from the warps
@@ -54,9 +55,11 @@ constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 
 // 32 columns of fp32 for each of the 2 x 2 (column half, lane-quarter pair)
 // warp pairs.
 constexpr int XCH_BYTES = 4 * 32 * 32 * 4;
-__host__ __device__ constexpr int mx_stages(bool bf16_out) { return bf16_out ? 4 : kMaxStages; }
+// `staged`: the modes that drain a bf16 tile through STAGING_BYTES of
+// shared memory
+__host__ __device__ constexpr int mx_stages(bool staged) { return staged ? 4 : kMaxStages; }
 // K blocks (of BKB bytes) per stage
-__host__ __device__ constexpr int mx_ksub(bool bf16_out) { return bf16_out ? 1 : 2; }
+__host__ __device__ constexpr int mx_ksub(bool staged) { return staged ? 1 : 2; }
 constexpr int A_BYTES = 128 * BKB;  // this CTA's 128 rows, one K block
 constexpr int B_BYTES = 128 * BKB;  // this CTA's half of B, one K block
 constexpr int CODE_BYTES = A_BYTES + B_BYTES;
@@ -159,10 +162,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   constexpr bool kBf16Out = !kSwiglu || kReplay;
   constexpr bool kSwigluT = kT && kSwiglu && !kReplay;
   static_assert(!kF32 || kBf16Out, "fp32 outputs replace the bf16 ones");
-  constexpr int STAGES = mx_stages(kBf16Out);
+  constexpr bool kStaged = kBf16Out && !kF32;  // bf16 tiles drained through shared memory
+  constexpr int STAGES = mx_stages(kStaged);
   // a stage holds KSUB K blocks: A's KSUB boxes, then B's, then KSUB sets of
   // three scale blocks, copied to KSUB sets of SF_COLS TMEM columns
-  constexpr int KSUB = mx_ksub(kBf16Out);
+  constexpr int KSUB = mx_ksub(kStaged);
   constexpr int STAGE_CODE = KSUB * CODE_BYTES;
   constexpr int STAGE_SF = KSUB * SF_BYTES;
   constexpr uint32_t STAGE_TX = 2 * (STAGE_CODE + STAGE_SF);
@@ -172,8 +176,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sf_smem = smem + STAGES * STAGE_CODE;
-  uint8_t* staging = sf_smem + STAGES * STAGE_SF;  // 1024-byte aligned; STAGING_BYTES when kBf16Out
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + (kBf16Out ? STAGING_BYTES : (kSwigluT ? XCH_BYTES : 0)));
+  uint8_t* staging = sf_smem + STAGES * STAGE_SF;  // 1024-byte aligned; STAGING_BYTES when kStaged
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + (kStaged ? STAGING_BYTES : (kSwigluT ? XCH_BYTES : 0)));
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
@@ -699,21 +703,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   if (warp == 2) tmem_dealloc2(tmem_base, 512);
 }
 
-size_t mx_smem_bytes(int G, bool bf16_out, bool swiglu_t = false) {
-  return 1024 + static_cast<size_t>(mx_stages(bf16_out)) * mx_ksub(bf16_out) * (CODE_BYTES + SF_BYTES) +
-         (bf16_out ? STAGING_BYTES : (swiglu_t ? XCH_BYTES : 0)) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
+size_t mx_smem_bytes(int G, bool staged, bool swiglu_t = false) {
+  return 1024 + static_cast<size_t>(mx_stages(staged)) * mx_ksub(staged) * (CODE_BYTES + SF_BYTES) +
+         (staged ? STAGING_BYTES : (swiglu_t ? XCH_BYTES : 0)) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st, int max_sms = 0) {
-  const size_t smem = mx_smem_bytes(P.sched.G, !kSwiglu || kReplay, kT && kSwiglu && !kReplay);
+  constexpr bool staged = (!kSwiglu || kReplay) && !kF32;
+  const size_t smem = mx_smem_bytes(P.sched.G, staged, kT && kSwiglu && !kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
   // the schedule counts stages of mx_ksub K blocks each
-  constexpr int ksub = mx_ksub(!kSwiglu || kReplay);
+  constexpr int ksub = mx_ksub(staged);
   if (P.sched.k_blocks_fixed % ksub) return MOK_ERR_UNSUPPORTED;
   MxParams Q = P;
   Q.sched.k_blocks_fixed = P.sched.k_blocks_fixed / ksub;

@@ -35,6 +35,9 @@ SMALL = {
     "one_token": W.MoEConfig("one_token", T=1, D=256, I=128, E=8, K=2, I_shared=128),
     "k_equals_e": W.MoEConfig("k_equals_e", T=65, D=256, I=128, E=8, K=8, I_shared=128),
     "max_e_k": W.MoEConfig("max_e_k", T=40, D=256, I=128, E=1024, K=32, I_shared=0),
+    # experts of 512 or more routed rows on average: the routed dX on the
+    # 128-row single-CTA tiles instead of the CTA pairs
+    "big_experts": W.MoEConfig("big_experts", T=1100, D=256, I=256, E=2, K=1, I_shared=128),
 }
 
 

@@ -27,6 +27,8 @@ SMALL = {
     "ragged": W.MoEConfig("ragged", T=301, D=512, I=256, E=5, K=3, I_shared=128, dtype="mxfp8"),
     "skew_small": W.MoEConfig("skew_small", T=700, D=256, I=128, E=16, K=4, I_shared=0, skew=2.0,
                               dtype="mxfp8"),
+    # experts of 512 or more routed rows on average: the row-major down form
+    "big_experts": W.MoEConfig("big_experts", T=1100, D=256, I=256, E=2, K=1, I_shared=128, dtype="mxfp8"),
 }
 
 
@@ -240,6 +242,9 @@ BWD = {
     "one_token": W.MoEConfig("one_token_bwd", T=1, D=256, I=256, E=8, K=2, I_shared=256, dtype="mxfp8"),
     # the largest E and K the boundary accepts: most experts empty
     "max_e_k": W.MoEConfig("max_e_k_bwd", T=40, D=256, I=256, E=1024, K=32, I_shared=0, dtype="mxfp8"),
+    # experts of 512 or more routed rows on average: t and dX in the
+    # row-major form (t with its fp32 outputs on stages of two K blocks)
+    "big_experts": W.MoEConfig("big_experts_bwd", T=1100, D=256, I=256, E=2, K=1, I_shared=256, dtype="mxfp8"),
 }
 
 

@@ -43,11 +43,12 @@ constexpr int BKB = 128;  // K columns (bytes) of one K block: one 128-byte swiz
 // The quantising up/gate keeps three stages of two K blocks (eight MMAs per
 // stage: the MMA thread's wait, fences and commit per stage cost about a
 // third of one K block's MMA time; six stages of one K block took 1.55 ms
-// at DSV3 size against 1.47-1.49 ms), and so do the modes with fp32
-// outputs (stored straight from registers).  The modes with bf16 outputs
-// (down, dX) keep four stages of one K block and use 64 KB per CTA to drain
-// the accumulator into shared memory, so that it is free for the next
-// tile's MMAs while TMA stores write the tile out.
+// at DSV3 size against 1.47-1.49 ms), and so do the modes that store their
+// output straight from registers: fp32 (t, the replay) and the bf16 down
+// and dX with the routed rows as N, each warp store 32 consecutive columns
+// of one row.  The row-major bf16 down keeps four stages of one K block and
+// uses 64 KB per CTA to drain the accumulator into shared memory, so that
+// it is free for the next tile's MMAs while TMA stores write the tile out.
 constexpr int kMaxStages = 3;
 constexpr int STAGING_BYTES = 4 * 4 * 4096;  // 4 lane quarters x 4 boxes of 32 rows x 64 bf16
 // The quantising up/gate with the routed rows as N passes u from the warps
@@ -162,7 +163,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   constexpr bool kBf16Out = !kSwiglu || kReplay;
   constexpr bool kSwigluT = kT && kSwiglu && !kReplay;
   static_assert(!kF32 || kBf16Out, "fp32 outputs replace the bf16 ones");
-  constexpr bool kStaged = kBf16Out && !kF32;  // bf16 tiles drained through shared memory
+  // the bf16 down / dX with the routed rows as N store from registers too
+  constexpr bool kDirect16 = kT && kBf16Out && !kF32 && !kReplay;
+  constexpr bool kStaged = kBf16Out && !kF32 && !kDirect16;  // bf16 tiles drained through shared memory
+  static_assert(!kT || kSwigluT || kDirect16 || kF32, "the transposed down and replay store from registers");
   constexpr int STAGES = mx_stages(kStaged);
   // a stage holds KSUB K blocks: A's KSUB boxes, then B's, then KSUB sets of
   // three scale blocks, copied to KSUB sets of SF_COLS TMEM columns
@@ -438,17 +442,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // ---------------- epilogue, transposed form (both CTAs) ----------------
     // Warp 4 + 4 h + q: TMEM lane quarter q (output columns 32 q .. of the
     // CTA's 128), accumulator columns (routed rows) [128 h, 128 h + 128).
-    // Half h stages its up to four 32-row chunks in boxes of its own (two
-    // [32 rows][64 columns] boxes per chunk: quarters 0, 1 fill the first,
-    // 2, 3 the second), releases the accumulator once they are written and
-    // then stores them, so the next tile's MMAs overlap the stores.  The
-    // half's four warps meet at named barrier 1 + h twice per tile; all
-    // eight first combine their accumulator waits at barrier 3.
+    // Each warp stores its chunks straight from registers (lane = column,
+    // one row per store: 32 neighbouring columns, bf16 or fp32) and the
+    // accumulator is released once every chunk is out; the eight warps
+    // first combine their accumulator waits at barrier 3.
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;
-    uint8_t* hstage = staging + half * (4 * 2 * 4096);
-    const bool issuer = q == 2 && lane == 0;  // issues (and waits for) this half's TMA stores
-    const uint32_t bar = 1 + half;
     int it = 0;
     TileWalker walk(P.sched, tstart);
     for (int tile = cid; tile < total; tile += ncl, ++it) {
@@ -462,10 +461,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int row0 = c.row0 + c.mt * 256;
       // first output column of this CTA; the replay's CTA 1 writes u, CTA 0 h
       const int dcol = c.nt * P.b_tile_rows + (kReplay ? 0 : static_cast<int>(rank) * 128);
-      const CUtensorMap* tmOut = kReplay && rank ? &P.tmO1 : &P.tmO0;
-      __nv_bfloat16* outp = kReplay ? (rank ? P.u_out : P.h_out) : P.y;
       const int ch0 = 4 * half;
       const int ch_end = min((t_ncols(c) + 31) / 32, ch0 + 4);
+      if constexpr (kDirect16) {
+        // lane = output column 32 q + lane; register j = row ch * 32 + j:
+        // each warp store writes 32 neighbouring bf16 columns of one row
+#pragma unroll 1
+        for (int ch = ch0; ch < ch_end; ++ch) {
+          const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
+          uint32_t v[32];
+          tmem_ld32(taddr + ch * 32, v);
+          tmem_ld_wait();
+          __nv_bfloat16* o = P.y + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nv) o[static_cast<int64_t>(j) * P.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+        tc_fence_before();
+        if (leader) mbar_arrive(tempty);  // the accumulator is free for the next tile
+        else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+        continue;
+      }
       if constexpr (kF32) {
         // lane = output column 32 q + lane; register j = row ch * 32 + j
         float* out32 = kReplay ? (rank ? P.u32 : P.h32) : P.y32;
@@ -485,51 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         else remote_arrive(map_to_rank(smem_u32(tempty), 0));
         continue;
       }
-      if (issuer) bulk_wait_read0();  // the previous tile's stores have read the boxes
-      named_bar(bar, 128);
-#pragma unroll 1
-      for (int ch = ch0; ch < ch_end; ++ch) {
-        const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
-        uint32_t v[32];
-        tmem_ld32(taddr + ch * 32, v);
-        tmem_ld_wait();
-        if (nv == 32) {
-          // row j, column 32 (q & 1) + lane of the box (128-byte swizzle);
-          // lanes pair up so that each store writes two neighbouring columns
-          uint8_t* box = hstage + (ch - ch0) * 8192 + (q >> 1) * 4096;
-          const bool odd = lane & 1;
-          const int c2 = 32 * (q & 1) + (lane & ~1);
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float recv = __shfl_xor_sync(0xffffffffu, __uint_as_float(odd ? v[j] : v[j + 1]), 1);
-            const int r = odd ? j + 1 : j;
-            const uint32_t w = odd ? pack_bf16x2(recv, __uint_as_float(v[j + 1]))
-                                   : pack_bf16x2(__uint_as_float(v[j]), recv);
-            st_shared_b32(box + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2, w);
-          }
-        } else {
-          __nv_bfloat16* o = outp + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nv) o[static_cast<int64_t>(j) * P.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      if (leader) mbar_arrive(tempty);  // the accumulator is free for the next tile
-      else remote_arrive(map_to_rank(smem_u32(tempty), 0));
-      named_bar(bar, 128);  // every box of the half written
-      if (issuer) {
-        for (int ch = ch0; ch < ch_end; ++ch) {
-          if (nrows - ch * 32 < 32) continue;  // written row by row above
-          uint8_t* boxes = hstage + (ch - ch0) * 8192;
-          tma_store_2d(tmOut, boxes, dcol, row0 + ch * 32);
-          tma_store_2d(tmOut, boxes + 4096, dcol + 64, row0 + ch * 32);
-        }
-        bulk_commit();
-      }
     }
-    if (issuer) bulk_wait0();  // this half's stores have landed before the CTA exits
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs, own 128 rows) ----------------
@@ -710,7 +682,7 @@ size_t mx_smem_bytes(int G, bool staged, bool swiglu_t = false) {
 
 template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st, int max_sms = 0) {
-  constexpr bool staged = (!kSwiglu || kReplay) && !kF32;
+  constexpr bool staged = (!kSwiglu || kReplay) && !kF32 && !(kT && !kSwiglu && !kReplay);
   const size_t smem = mx_smem_bytes(P.sched.G, staged, kT && kSwiglu && !kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
   auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32>;
@@ -874,8 +846,9 @@ mok_status launch_down_mx(const void* aq, const void* asc, int64_t rows, const v
   if (!out_map(&P.tmO0, y, rows, D)) return MOK_ERR_CUDA;
   P.tmO1 = P.tmO0;
   // fewer than 512 routed rows per group on average: the routed rows as the
-  // MMA's N dimension (no padding rows in the MMAs)
-  if (by_rows) return run_mx<false, false, true>(P, st, max_sms);
+  // MMA's N dimension (no padding rows in the MMAs); its stages hold two K
+  // blocks, so K = I must be a multiple of 256 (else the row-major form)
+  if (by_rows && (I / BKB) % 2 == 0) return run_mx<false, false, true>(P, st, max_sms);
   return run_mx<false>(P, st, max_sms);
 }
 

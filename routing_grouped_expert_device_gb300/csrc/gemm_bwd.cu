@@ -785,8 +785,10 @@ mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const voi
                          cudaStream_t st, int max_sms) {
   if (rows == 0) return MOK_OK;
   // fewer than 512 routed rows per group on average: the routed rows as the
-  // MMA's N dimension, one tile per expert and 256 D columns (no padding rows)
-  if (offsets && rows < static_cast<int64_t>(512) * G && D % 256 == 0 && I % 128 == 0)
+  // MMA's N dimension, one tile per expert and 256 D columns (no padding
+  // rows); the ungrouped rows of the shared expert too (tensor-bound there,
+  // where the pair MMAs keep the tensor pipe busier than 128-row tiles)
+  if ((!offsets || rows < static_cast<int64_t>(512) * G) && D % 256 == 0 && I % 128 == 0)
     return launch_dx_pair_t(dh, du, rows, w_gate, w_up, offsets, G, D, I, dx, st, max_sms);
   DxCfg::Params P;
   P.sched = sched_rows(offsets, G, rows, D / 256, 2 * (I / BK));

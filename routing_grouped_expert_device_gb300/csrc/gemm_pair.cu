@@ -1207,8 +1207,8 @@ mok_status launch_dx_pair_t_impl(const void* dh, const void* du, int64_t rows, c
 mok_status launch_dx_pair_t(const void* dh, const void* du, int64_t rows, const void* w_gate, const void* w_up,
                             const int32_t* offsets, int G, int D, int I, void* dx, cudaStream_t st, int max_sms) {
   if (rows == 0) return MOK_OK;
-  if (!offsets || G < 1 || D % 256 || I % BK) return MOK_ERR_INVALID_ARG;
-  return launch_dx_pair_t_impl(dh, du, rows, w_gate, w_up, offsets, G, D, I, dx, st, max_sms);
+  if ((offsets && G < 1) || D % 256 || I % BK) return MOK_ERR_INVALID_ARG;
+  return launch_dx_pair_t_impl(dh, du, rows, w_gate, w_up, offsets, offsets ? G : 1, D, I, dx, st, max_sms);
 }
 
 mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate, const void* w_up,

@@ -125,9 +125,9 @@ mok_status launch_bwd_dgrad_kept(const void* dyg, int64_t rows, const void* w_do
                                  int D, int I, const float* g_route, const float* act, int32_t kept_rows, void* dh,
                                  void* du, void* ag, float* dgp, cudaStream_t st, int max_sms = 0);
 // dx [rows][D] = bf16(dh W_gate + du W_up)
-//  launch_bwd_dx: routed groups averaging under 512 rows run on CTA pairs with
-//  the routed rows as the MMA's N dimension (launch_dx_pair_t, gemm_pair.cu),
-//  others on single-CTA 128-row tiles.
+//  launch_bwd_dx: routed groups averaging under 512 rows, and ungrouped rows
+//  (offsets null), run on CTA pairs with the rows as the MMA's N dimension
+//  (launch_dx_pair_t, gemm_pair.cu), others on single-CTA 128-row tiles.
 mok_status launch_dx_pair_t(const void* dh, const void* du, int64_t rows, const void* w_gate, const void* w_up,
                             const int32_t* offsets, int G, int D, int I, void* dx, cudaStream_t st, int max_sms = 0);
 mok_status launch_bwd_dx(const void* dh, const void* du, int64_t rows, const void* w_gate,

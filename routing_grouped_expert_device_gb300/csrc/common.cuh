@@ -140,38 +140,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
-// Gather of four rows (y0..y3) of a 2D tensor whose tensor map box is one row
-// high: four box rows land consecutively at dst (Blackwell tile::gather4).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
-// 16-byte asynchronous global -> shared copy (L2 only).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-// Arrive on `bar` once this thread's earlier cp.async copies have landed
-// (the barrier's expected arrival count must include this arrival).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Same with an L2 eviction-priority hint (policy from createpolicy).
-__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m, int32_t x,
-                                                 int32_t y, uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // 2D tiled store of a shared-memory box to global memory (bulk async group).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int32_t x,
                                              int32_t y) {

@@ -59,7 +59,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk-rows", type=int, default=0,
                    help="BF16 forward: gather through a ring of chunks of this many routed rows "
-                        "(512..32768; 0 = whole-batch dispatch)")
+                        "(512..32768; -1 = whole-batch dispatch; 0 = as mok_moe_fwd chooses: the ring "
+                        "with 2048-row chunks for layers of 512 or more routed rows per expert, else "
+                        "the whole-batch dispatch)")
     p.add_argument("--producer-sms", type=int, default=0,
                    help="SMs left to route, plan and the dispatch while the shared expert's up/gate "
                         "runs on the others (mok_shape.producer_sms; 0 = the shared expert takes every SM)")
@@ -371,8 +373,13 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     d = W.make_inputs(cfg, dev, seed=rank)
     T, D, I, E, K, Is, R = cfg.T, cfg.D, cfg.I, cfg.E, cfg.K, cfg.I_shared, cfg.R
-    ring = args.chunk_rows > 0 and not mx and not cfg.backward
-    shape = M.shape_of(cfg, chunk_rows=args.chunk_rows if ring else 0, producer_sms=args.producer_sms,
+    # the gather of mok_moe_fwd's automatic choice (chunk_rows 0): the ring
+    # of 2048-row chunks where the GEMMs run row-major tiles (512 or more
+    # routed rows per expert), else the whole-batch dispatch
+    ring = not mx and not cfg.backward and (args.chunk_rows > 0 or (args.chunk_rows == 0 and R >= 512 * E))
+    chunk = args.chunk_rows if args.chunk_rows > 0 else 2048
+    shape = M.shape_of(cfg, chunk_rows=chunk if ring else (args.chunk_rows if cfg.backward else -1),
+                       producer_sms=args.producer_sms,
                        bwd_shared_sms=args.bwd_shared_sms)
     i32, f32, bf, u8 = torch.int32, torch.float32, torch.bfloat16, torch.uint8
     if mx:
@@ -534,7 +541,7 @@ def run_ours(args, world, rank, local):
     ck = clk or {}
     capped = bool(ck.get("sm_mhz") and ck.get("sm_max_mhz") and ck["sm_mhz"] < 0.95 * ck["sm_max_mhz"])
     roofline, tensor_peak, burst_peak, bf16_peak = roofline_of(
-        cfg, nonempty, part_ms, peaks, capped, args.chunk_rows if ring else 0, recorded_traffic(cfg.name))
+        cfg, nonempty, part_ms, peaks, capped, chunk if ring else 0, recorded_traffic(cfg.name))
 
     # end to end through the public entry points with pinned host buffers:
     # every step copies its inputs in and reads its result back.  The copies
@@ -645,7 +652,7 @@ def run_ours(args, world, rank, local):
             "data": "synthetic (seeded; x~N(0,1), W~N(0,1/fan_in), logits~N(0,1) softmax; bf16)",
             "config": {"workload": cfg.name, "T": T, "D": D, "I": I, "E": E, "K": K, "I_shared": Is,
                        "global_batch": world * T, "parallelism": f"replicas x{world}",
-                       "chunk_rows": args.chunk_rows if ring else 0, "producer_sms": args.producer_sms,
+                       "chunk_rows": chunk if ring else 0, "producer_sms": args.producer_sms,
                        "kept_act_rows": (act_rows if cfg.backward else None),
                        "bwd_shared_sms": (M.bwd_shared_sms(shape) if cfg.backward else None),
                        "l2": "inputs larger than L2: every step streams all expert weights "

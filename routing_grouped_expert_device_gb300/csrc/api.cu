@@ -14,7 +14,7 @@ bool shape_ok(const mok_shape* s) {
   if (s->D % 256 || s->I % 128 || s->I_shared % 128) return false;
   if (static_cast<int64_t>(s->T) * s->K >= (int64_t(1) << 31)) return false;
   if (s->dtype != MOK_BF16 && s->dtype != MOK_MXFP8) return false;
-  if (s->chunk_rows != 0 && (s->chunk_rows < 512 || s->chunk_rows > 32768)) return false;
+  if (s->chunk_rows != 0 && s->chunk_rows != -1 && (s->chunk_rows < 512 || s->chunk_rows > 32768)) return false;
   if (s->producer_sms < 0 || s->producer_sms > 4096) return false;
   if (s->bwd_shared_sms < 0 || s->bwd_shared_sms > 4096) return false;
   return true;
@@ -54,8 +54,14 @@ struct FwdLayout {
       ring_counters, total;
 };
 
-// The BF16 forward with chunk_rows > 0 gathers through a ring (no xg).
-bool uses_ring(const mok_shape& s) { return s.dtype == MOK_BF16 && s.chunk_rows > 0; }
+// Whether the BF16 forward gathers through the ring (no xg): chunk_rows > 0,
+// or 0 (automatic) for layers whose GEMMs run row-major tiles, where the
+// ring measured faster than the whole-batch dispatch (the skewed 16384-token
+// layer: 3.51 vs 3.61 ms at b = 2048); -1 never.
+bool uses_ring(const mok_shape& s) {
+  if (s.dtype != MOK_BF16 || s.chunk_rows < 0) return false;
+  return s.chunk_rows > 0 || !routed_rows_as_n(static_cast<int64_t>(s.T) * s.K, s.E);
+}
 
 FwdLayout fwd_layout(const mok_shape& s) {
   const size_t T = s.T, D = s.D, I = s.I, E = s.E, K = s.K, Is = s.I_shared, R = T * K;

@@ -1220,7 +1220,7 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
   // (DSV3 forward 4.57 -> 4.51 ms).  With larger groups there is little
   // padding, and the row-major kernel's lighter epilogue measured 0.3-0.6 %
   // faster (the skewed 16384-token layer).
-  if (offsets && !(sh && sh->rows) && m_total < static_cast<int64_t>(512) * G)
+  if (offsets && !(sh && sh->rows) && routed_rows_as_n(m_total, G))
     return launch_upgate_pair_t(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st, kept);
   PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
@@ -1271,7 +1271,7 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
   // routed groups of fewer than 512 rows on average: the transposed kernel
   // (no padding rows in the MMAs), as for the up/gate
-  if (offsets && m_total < static_cast<int64_t>(512) * G)
+  if (offsets && routed_rows_as_n(m_total, G))
     return launch_down_pair_t(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st, sh);
   PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);

@@ -55,6 +55,11 @@ struct KeptAct {
   }
 };
 
+// Whether a layer of R routed rows in G groups averages fewer than 512 rows
+// per group: its forward GEMMs then take the routed rows as the MMA's N
+// dimension (no padding rows, HBM-bound), else run row-major 256-row tiles.
+inline bool routed_rows_as_n(int64_t R, int G) { return R < static_cast<int64_t>(512) * G; }
+
 // Forward grouped GEMMs (CTA pairs, gemm_pair.cu).  offsets == nullptr: one
 // group of m_total rows.
 //  up/gate: a[rows][I] = bf16(SiLU(A W_gate^T) * (A W_up^T)), A [rows][D]

@@ -59,7 +59,7 @@ def test_ring_chunk_larger_than_all_rows(m, name):
     cfg = SHAPES[name]
     inp = W.make_inputs(cfg, "cpu")
     d = {k: v.to(DEV) for k, v in inp.items()}
-    out0, _ = _fwd(m, cfg, d, chunk=0)
+    out0, _ = _fwd(m, cfg, d, chunk=-1)
     out1, _ = _fwd(m, cfg, d, chunk=32768)
     assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
 

@@ -247,7 +247,7 @@ def test_zero_tokens_is_a_noop(m):
 def test_invalid_shapes_rejected(m):
     import ctypes
     lib = m._lib_handle()
-    for bad in [dict(D=200), dict(I=100), dict(K=9), dict(E=0), dict(chunk_rows=100)]:
+    for bad in [dict(D=200), dict(I=100), dict(K=9), dict(E=0), dict(chunk_rows=100), dict(chunk_rows=-2)]:
         kw = dict(T=16, D=256, I=128, E=8, K=2, I_shared=0)
         kw.update(bad)
         sh = m.make_shape(**kw)
@@ -334,7 +334,7 @@ def test_moe_fwd_ring_matches_whole_batch_dispatch(m, name):
     ref = O.moe_forward(host(inp), cfg.K)
     d = {k: v.to(DEV) for k, v in inp.items()}
     outs = []
-    for chunk in (0, 512, 512):
+    for chunk in (-1, 512, 512):
         shape = m.shape_of(cfg, chunk_rows=chunk)
         ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
         out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
@@ -346,16 +346,46 @@ def test_moe_fwd_ring_matches_whole_batch_dispatch(m, name):
     assert_close(outs[1].float().cpu().numpy(), ref["out"], BF16_TOL, "out")
 
 
-@pytest.mark.parametrize("config,chunks", [("dsv3_bf16_fwd", (512, 2048, 32768)),
-                                           ("skewed_bf16_fwd", (512, 2048, 8192, 32768))])
+BIG_GROUPS = W.MoEConfig("big_groups", T=1100, D=256, I=256, E=2, K=1, I_shared=128)
+
+
+def test_moe_fwd_automatic_ring_for_large_groups(m):
+    """chunk_rows 0 on a layer of 550 routed rows per expert gathers through
+    the ring (b = 2048, one chunk holding every row), with the kept h, u
+    store written as by the whole-batch dispatch (chunk_rows -1): out, h and
+    u bit-identical, and out within tolerance of the oracle."""
+    cfg = BIG_GROUPS
+    inp = W.make_inputs(cfg, "cpu")
+    ref = O.moe_forward(host(inp), cfg.K)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    res = []
+    for chunk in (-1, 0):
+        shape = m.shape_of(cfg, chunk_rows=chunk)
+        ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+        out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+        saved = alloc_plan(cfg, DEV)
+        saved["act"] = torch.full((cfg.R, 2 * cfg.I), float("nan"), device=DEV)
+        m.moe_fwd(shape, m.make_weights(d), d["x"], d["s"], out, ws, m.make_plan_buf(saved))
+        m.check_device_status()
+        res.append((out, saved["act"]))
+    assert torch.equal(res[0][0].view(torch.int16), res[1][0].view(torch.int16))
+    assert torch.equal(res[0][1].view(torch.int32), res[1][1].view(torch.int32))
+    assert_close(res[1][0].float().cpu().numpy(), ref["out"], BF16_TOL, "out")
+
+
+@pytest.mark.parametrize("config,chunks", [("dsv3_bf16_fwd", (0, 512, 2048, 32768)),
+                                           ("skewed_bf16_fwd", (0, 512, 2048, 8192, 32768))])
 def test_moe_fwd_ring_full_size_bitexact(m, config, chunks):
-    """Full-size layers: every chunk size of the ring gives the whole-batch
-    dispatch's output bit for bit (including hot and empty experts)."""
+    """Full-size layers: every chunk size of the ring, and the automatic
+    choice (chunk_rows 0: the whole-batch dispatch for DSV3, the ring of
+    2048-row chunks for the skewed layer's 1024 rows per expert), give the
+    whole-batch dispatch's output bit for bit (hot and empty experts
+    included)."""
     cfg = W.CONFIGS[config]
     d = W.make_inputs(cfg, DEV)
     w = m.make_weights(d)
     outs = []
-    for chunk in (0,) + chunks:
+    for chunk in (-1,) + chunks:
         shape = m.shape_of(cfg, chunk_rows=chunk)
         ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
         out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)

@@ -37,6 +37,14 @@ def test_workspace_bytes_host_only(m):
     ring = m.make_shape(T=7168, D=7168, I=2048, E=256, K=8, I_shared=2048, chunk_rows=512)
     assert m.workspace_bytes(ring, m.OP_FWD) < fwd  # the ring replaces the R x D gathered copy
     assert m.workspace_bytes(m.make_shape(T=16, D=256, I=128, E=8, K=2, chunk_rows=100), m.OP_RING) == 0
+    # chunk_rows 0 chooses the ring (b = 2048) for 512 or more routed rows per
+    # expert: no R x D copy, as chunk_rows 2048; -1 keeps the whole-batch copy
+    skew = dict(T=16384, D=4096, I=1536, E=128, K=8)
+    auto = m.workspace_bytes(m.make_shape(**skew), m.OP_FWD)
+    assert auto == m.workspace_bytes(m.make_shape(**skew, chunk_rows=2048), m.OP_FWD)
+    whole = m.workspace_bytes(m.make_shape(**skew, chunk_rows=-1), m.OP_FWD)
+    assert whole - auto > 16384 * 8 * 4096 * 2 // 2
+    assert m.workspace_bytes(m.make_shape(**skew, chunk_rows=-2), m.OP_FWD) == 0
     assert m.workspace_bytes(m.make_shape(T=16, D=200, I=128, E=8, K=2), m.OP_FWD) == 0
     assert m.workspace_bytes(m.make_shape(T=16, D=256, I=128, E=8, K=9), m.OP_FWD) == 0
 

@@ -70,13 +70,15 @@ typedef enum {
  * arithmetic of the routed experts (the shared expert is always BF16).
  * chunk_rows: routed rows per dispatch chunk b (the overlap granularity of
  * the Mixture-of-Kittens paper note, "Granularity as a tunable"):
- * 512..32768 = the BF16 forward gathers through a ring of 4 chunks that
- * producer warps fill while the up/gate GEMM consumes it
- * (mok_expert_upgate_ring); -1 = the dispatch gathers the whole batch
- * before the expert GEMMs; 0 = automatic: the whole-batch dispatch when
- * the layer averages fewer than 512 routed rows per expert (the GEMMs then
- * take the routed rows as the MMA's N and stream weights at HBM speed),
- * else the ring with b = 2048 (measured faster there on a GB300).
+ * 512..32768 = the forward gathers through a ring of 4 chunks that producer
+ * warps fill while the up/gate GEMM consumes it (mok_expert_upgate_ring;
+ * MXFP8: the producers quantise the rows, their scales going to the grouped
+ * layout in full); -1 = the dispatch gathers the whole batch before the
+ * expert GEMMs; 0 = automatic: for BF16 the whole-batch dispatch when the
+ * layer averages fewer than 512 routed rows per expert (the GEMMs then take
+ * the routed rows as the MMA's N and stream weights at HBM speed), else the
+ * ring with b = 2048 (measured faster there on a GB300); for MXFP8 the
+ * whole-batch quantising dispatch.
  * producer_sms: the split of the GPU between the dispatch (producers) and
  * the shared expert in the first dispatch window (paper note, "The
  * production details": the shared expert fills the first dispatch window).
@@ -345,8 +347,8 @@ mok_status mok_combine(const mok_shape *shape, const void *yg, const void *ys, c
  * (nullable) receives the routing and plan for mok_moe_bwd.  With
  * shape.dtype = MOK_MXFP8 the routed experts run in MXFP8 (dispatch
  * quantises x, the up/gate epilogue quantises a) and the shared expert in
- * BF16.  BF16 gathers through the ring of mok_expert_upgate_ring instead
- * of a whole-batch dispatch as shape.chunk_rows says. */
+ * BF16.  The forward gathers through a ring instead of a whole-batch
+ * dispatch as shape.chunk_rows says. */
 mok_status mok_moe_fwd(const mok_shape *shape, const mok_weights *w, const void *x,
                        const float *s, void *out, mok_plan_buf *saved, void *ws,
                        size_t ws_bytes, void *stream);

@@ -59,7 +59,10 @@ struct FwdLayout {
 // ring measured faster than the whole-batch dispatch (the skewed 16384-token
 // layer: 3.51 vs 3.61 ms at b = 2048); -1 never.
 bool uses_ring(const mok_shape& s) {
-  if (s.dtype != MOK_BF16 || s.chunk_rows < 0) return false;
+  if (s.chunk_rows < 0) return false;
+  // MXFP8: the ring of quantised rows when asked for (its automatic choice
+  // is the whole-batch quantising dispatch)
+  if (s.dtype == MOK_MXFP8) return s.chunk_rows > 0;
   return s.chunk_rows > 0 || !routed_rows_as_n(static_cast<int64_t>(s.T) * s.K, s.E);
 }
 
@@ -77,7 +80,8 @@ FwdLayout fwd_layout(const mok_shape& s) {
   const bool ring = uses_ring(s);
   const int64_t b = ring_chunk(s.chunk_rows);
   // xg holds the ring when the forward gathers through one
-  L.xg = c.take(ring ? ring_bytes(static_cast<int64_t>(R), D, b) : R * D * (s.dtype == MOK_MXFP8 ? 1 : 2));
+  const int elem = s.dtype == MOK_MXFP8 ? 1 : 2;
+  L.xg = c.take(ring ? ring_bytes(static_cast<int64_t>(R), D, b, elem) : R * D * elem);
   L.ring_counters = c.take(ring ? ring_counter_bytes(static_cast<int64_t>(R), b) : 0);
   const bool mx = s.dtype == MOK_MXFP8;
   L.xg_scale = c.take(mx ? mx_scale_bytes(static_cast<int64_t>(R), D, s.E) : 0);
@@ -455,13 +459,22 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
                        at<int>(ws, L.hist), st)) != MOK_OK)
     return fail(r);
   if (mx) {
-    if ((r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xg,
-                                   at<uint8_t>(ws, L.xg_scale), st)) != MOK_OK)
-      return fail(r);
     void* asc = at<void>(ws, L.a_scale);
-    if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
-                              w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st, kept, w->sc_gu_pair)) != MOK_OK)
-      return fail(r);
+    if (uses_ring(s)) {
+      // the quantising dispatch runs inside the up/gate launch, through the ring in xg
+      const int64_t b = ring_chunk(s.chunk_rows);
+      if ((r = launch_upgate_mx_ring(x, pb.table, s.K, w->q_gate, w->sc_gate, w->q_up, w->sc_up, pb.offsets, s.E, R,
+                                     s.D, s.I, a, asc, at<void>(ws, L.xg_scale), xg, ring_rows_for(R, b),
+                                     static_cast<int>(b), at<int32_t>(ws, L.ring_counters), st, kept)) != MOK_OK)
+        return fail(r);
+    } else {
+      if ((r = launch_dispatch_mxfp8(x, pb.route_dst, pb.table, pb.offsets, s.T, s.K, s.D, s.E, xg,
+                                     at<uint8_t>(ws, L.xg_scale), st)) != MOK_OK)
+        return fail(r);
+      if ((r = launch_upgate_mx(xg, at<void>(ws, L.xg_scale), R, w->q_gate, w->sc_gate, w->q_up,
+                                w->sc_up, pb.offsets, s.E, s.D, s.I, a, asc, st, kept, w->sc_gu_pair)) != MOK_OK)
+        return fail(r);
+    }
     if ((r = launch_down_mx(a, asc, R, w->q_down, w->sc_down, pb.offsets, s.E, s.D, s.I, yg, st)) !=
         MOK_OK)
       return fail(r);

@@ -34,6 +34,7 @@
 
 #include "gemm_core.cuh"
 #include "kernels.h"
+#include "mx_quant.cuh"
 #include "pair.cuh"
 
 namespace mok {
@@ -91,16 +92,6 @@ __device__ __forceinline__ void mma_mx2(uint32_t d, uint64_t adesc, uint64_t bde
       : "memory");
 }
 
-// Smallest e with amax <= 448 * 2^e (same rule as the quantiser in
-// elementwise.cu): amax = 1.f * 2^E and 448 = 1.75 * 2^8.
-__device__ __forceinline__ int mx_exp(float amax) {
-  const uint32_t b = __float_as_uint(amax);
-  const int eb = static_cast<int>((b >> 23) & 0xFFu);
-  if (eb == 0) return -127;
-  const int e = eb - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-  return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
-
 struct MxParams {
   SchedArgs sched;  // bm = 256
   int* status;
@@ -131,7 +122,114 @@ struct MxParams {
   // bf16 outputs as [rows][out_ld], boxes 32 rows x 64 columns, 128-byte
   // swizzle: y (down), or h and u (replay)
   CUtensorMap tmO0, tmO1;
+  // Ring dispatch (kRing, the row-major quantising up/gate): tmA maps the
+  // ring of codes, [ring_rows + 128][D]; routed row r sits at ring row
+  // r % ring_rows (ring rows 0..127 repeated after the end, so no 128-row
+  // box wraps), and its scale words go to the grouped layout that tmSA
+  // maps (xsc, ld xs_ld), in full.
+  const uint4* x;         // [T][D] bf16, as 16-byte vectors
+  const int32_t* table;   // the plan's [R][3]
+  int32_t K, D8;          // top-k; D / 8
+  uint2* ring;            // codes, 8 per uint2
+  uint32_t* xsc;
+  int64_t xs_ld, ring_rows;
+  int32_t chunk_rows, nchunks, n_tiles;
+  int32_t* ready;         // [nchunks]: producer warps done with the chunk
+  int32_t* done;          // [nchunks]: (row, N tile) reads of the chunk completed
 };
+
+// ---------------------------------------------------------------------------
+// Ring dispatch with the quantisation in the producers (Mixture-of-Kittens
+// paper note, "The production details": MXFP8 quantisation fused into the
+// dispatch; "Granularity as a tunable": chunks of b rows signalled through
+// device counters).  Warps 2 and 3 of every CTA take chunk after chunk of b
+// routed rows in expert order: producer warp w quantises rows w, w + np, ...
+// of the chunk from x[table[r].src / K] (the dispatch's per-row rule) into
+// ring row r mod ring_rows and the row's grouped scale position, fences the
+// generic-to-async proxy and release-increments ready[c].  Before writing
+// chunk c it waits until chunk c - slots (same ring slot) has been read by
+// every N tile.  All CTAs are resident (cooperative launch); every wait is
+// bounded.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int mx_chunk_rows(const MxParams& P, int c) {
+  const int64_t r0 = static_cast<int64_t>(c) * P.chunk_rows;
+  const int64_t R = P.sched.m_total;
+  return static_cast<int>((r0 + P.chunk_rows < R ? r0 + P.chunk_rows : R) - r0);
+}
+
+__device__ void mx_ring_produce(const MxParams& P, int pw, int np, int lane, volatile int* abort) {
+  const int64_t slots = P.ring_rows / P.chunk_rows;
+  const int D8 = P.D8;
+  for (int c = 0; c < P.nchunks; ++c) {
+    if (c >= slots) {
+      bool ok = true;
+      if (lane == 0)
+        ok = wait_count(P.done + (c - slots), mx_chunk_rows(P, c - static_cast<int>(slots)) * P.n_tiles, abort,
+                        P.status, SITE_RING_SLOT);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    }
+    const int64_t r0 = static_cast<int64_t>(c) * P.chunk_rows;
+    const int64_t r1 = r0 + mx_chunk_rows(P, c);
+    for (int64_t r = r0 + pw; r < r1; r += np) {
+      const int src = __ldg(P.table + r * 3) / P.K;
+      const int e = __ldg(P.table + r * 3 + 1);
+      const int64_t off = __ldg(P.sched.offsets + e);
+      const int64_t pos = mx_scale_pos(mx_group_row0(off, e) + (r - off));
+      const uint4* in = P.x + static_cast<int64_t>(src) * D8;
+      const int64_t q = r % P.ring_rows;
+      uint2* out = P.ring + q * D8;
+      uint2* mirror = q < 128 ? P.ring + (P.ring_rows + q) * D8 : nullptr;
+#pragma unroll 1
+      for (int v0 = 0; v0 < D8; v0 += 128) {  // 4 passes of 256 columns in flight
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int vi = v0 + 32 * u + lane;
+          v[u] = vi < D8 ? ld_nc_v4(in + vi) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int vi = v0 + 32 * u + lane;
+          if (v0 + 32 * u >= D8) break;  // warp-uniform: D is a multiple of 128 (16 vectors)
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          float f[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            f[2 * j] = bf16lo(w[j]);
+            f[2 * j + 1] = bf16hi(w[j]);
+          }
+          int ex;
+          const uint2 codes = mx_codes8(f, ex);
+          const uint32_t word = mx_word16(ex, lane);
+          out[vi] = codes;
+          if (mirror) mirror[vi] = codes;
+          if ((lane & 15) == 0) P.xsc[static_cast<int64_t>(vi / 16) * P.xs_ld + pos] = word;
+        }
+      }
+    }
+    // the chunk's rows of this warp are written: visible to the consumers'
+    // TMA (async proxy) reads, then this warp is counted in
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0) red_release_add(P.ready + c, 1);
+  }
+}
+
+// Rows [max(r0, g0), min(r0 + 128, g1)) of a 128-row box that lie inside its
+// group [g0, g1): their chunks, and per chunk the count of those rows.
+template <class F>
+__device__ __forceinline__ void mx_box_chunks(const MxParams& P, int64_t r0, int64_t g0, int64_t g1, F f) {
+  const int64_t v0 = r0 > g0 ? r0 : g0;
+  const int64_t v1 = r0 + 128 < g1 ? r0 + 128 : g1;
+  for (int64_t v = v0; v < v1;) {
+    const int c = static_cast<int>(v / P.chunk_rows);
+    const int64_t e = (static_cast<int64_t>(c) + 1) * P.chunk_rows < v1 ? (static_cast<int64_t>(c) + 1) * P.chunk_rows : v1;
+    f(c, static_cast<int>(e - v));
+    v = e;
+  }
+}
 
 // kT with kSwiglu (the quantising up/gate): A is the tile's 64 W_up rows
 // (A rows 0-63) and the same 64 W_gate rows (64-127) of this CTA's half of
@@ -157,9 +255,15 @@ struct MxParams {
 // in the transposed form each warp store writes 32 consecutive columns of
 // one row (128 bytes), in the row-major form each thread 128 bytes of its
 // row.
-template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
+//
+// kRing (the row-major quantising up/gate): A's codes come from the ring
+// that warps 2 and 3 of every CTA fill (mx_ring_produce); the TMA warp waits
+// for the chunks a tile's rows lie in, and the MMA thread counts the rows
+// as read once the tile's last stage has landed.
+template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false, bool kRing = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     gemm_mx_pair_persistent(const __grid_constant__ MxParams P) {
+  static_assert(!kRing || (kSwiglu && !kReplay && !kT && !kF32), "the ring feeds the row-major up/gate");
   constexpr bool kBf16Out = !kSwiglu || kReplay;
   constexpr bool kSwigluT = kT && kSwiglu && !kReplay;
   static_assert(!kF32 || kBf16Out, "fp32 outputs replace the bf16 ones");
@@ -237,6 +341,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int sfrow = static_cast<int>(mx_group_row0(c.row0, c.g)) + local0;  // a multiple of 128
         const int brow0 = c.g * P.b_group_rows + c.nt * P.b_tile_rows;
         const int brow = brow0 + (rank ? P.b1_off : 0);
+        int ay = arow;
+        if (kRing) {
+          // this CTA's rows of the tile must be in the ring
+          mx_box_chunks(P, arow, c.row0, static_cast<int64_t>(c.row0) + c.rows, [&](int ch, int) {
+            if (ok) ok = wait_count(P.ready + ch, 2 * static_cast<int>(gridDim.x), abort_flag, P.status, SITE_RING_CHUNK);
+          });
+          if (!ok) break;
+          fence_proxy_async_global();
+          ay = static_cast<int>(arow % P.ring_rows);
+        }
         for (int kb = 0; kb < c.kblocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, P.status, SITE_PRODUCER)) {
             ok = false;
@@ -275,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tma_load_2d_pair(sf + SF_BLOCK, &P.tmSA, gb, kk, lbar);
             tma_load_2d_pair(sf + 2 * SF_BLOCK, &P.tmSA, gb + 128, kk, lbar);
           } else {
-            tma_load_2d_pair(st, &P.tmA, kk * BKB, arow, lbar);
+            tma_load_2d_pair(st, &P.tmA, kk * BKB, ay, lbar);
             tma_load_2d_pair(st + KSUB * A_BYTES, tmB, kk * BKB, brow, lbar);
             tma_load_2d_pair(sf, &P.tmSA, sfrow, kk, lbar);
             tma_load_2d_pair(sf + SF_BLOCK, &P.tmSB0, brow0, kk, lbar);
@@ -316,6 +430,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase, abort_flag, P.status, SITE_MMA));
           if (!ok) break;
           tc_fence_after();
+          if (kRing && kb == c.kblocks - 1 && lane == 0) {
+            // every load of this tile (both CTAs) has landed: its ring rows
+            // are read for this N tile
+            for (int h = 0; h < 2; ++h)
+              mx_box_chunks(P, static_cast<int64_t>(c.row0) + c.mt * 256 + h * 128, c.row0,
+                            static_cast<int64_t>(c.row0) + c.rows, [&](int ch, int n) { red_release_add(P.done + ch, n); });
+          }
           if (lane == 0) {
 #pragma unroll
             for (int sub = 0; sub < KSUB; ++sub) {
@@ -353,6 +474,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
       }
     }
+  } else if (kRing && (warp == 2 || warp == 3)) {
+    // ---------------- ring producers (every CTA: warps 2 and 3) ----------------
+    mx_ring_produce(P, static_cast<int>(blockIdx.x) * 2 + (warp - 2), 2 * static_cast<int>(gridDim.x), lane,
+                    abort_flag);
   } else if (kSwigluT && warp >= 4) {
     // ---------------- epilogue, quantising up/gate with the routed rows as N ----------------
     // Warp 4 + 4 h + q: TMEM lane quarter q, accumulator columns (routed
@@ -419,7 +544,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
               m[j] = fmaxf(keepv, __shfl_xor_sync(0xffffffffu, send, sh));
             }
           }
-          const int e = mx_exp(m[0]);
+          const int e = mx_exponent(m[0]);
           uint8_t* arow = P.aq + (row0 + ch * 32) * P.out_ld + icol;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -636,7 +761,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t words = 0;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int e = mx_exp(amax[cc]);
+          const int e = mx_exponent(amax[cc]);
           const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
           uint32_t pk[8];
 #pragma unroll
@@ -680,12 +805,12 @@ size_t mx_smem_bytes(int G, bool staged, bool swiglu_t = false) {
          (staged ? STAGING_BYTES : (swiglu_t ? XCH_BYTES : 0)) + 1024 + static_cast<size_t>(G + 1) * sizeof(int);
 }
 
-template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false>
+template <bool kSwiglu, bool kReplay = false, bool kT = false, bool kF32 = false, bool kRing = false>
 mok_status run_mx(const MxParams& P, cudaStream_t st, int max_sms = 0) {
   constexpr bool staged = (!kSwiglu || kReplay) && !kF32 && !(kT && !kSwiglu && !kReplay);
   const size_t smem = mx_smem_bytes(P.sched.G, staged, kT && kSwiglu && !kReplay);
   if (smem > 227 * 1024) return MOK_ERR_UNSUPPORTED;
-  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32>;
+  auto kern = gemm_mx_pair_persistent<kSwiglu, kReplay, kT, kF32, kRing>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return MOK_ERR_CUDA;
@@ -695,7 +820,24 @@ mok_status run_mx(const MxParams& P, cudaStream_t st, int max_sms = 0) {
   MxParams Q = P;
   Q.sched.k_blocks_fixed = P.sched.k_blocks_fixed / ksub;
   const int sms = max_sms > 0 && max_sms < num_sms() ? max_sms : num_sms();
-  kern<<<sms >= 2 ? (sms / 2) * 2 : 2, THREADS, smem, st>>>(Q);
+  const int grid = sms >= 2 ? (sms / 2) * 2 : 2;
+  if (!kRing) {
+    kern<<<grid, THREADS, smem, st>>>(Q);
+    MOK_CHECK_LAUNCH();
+    return MOK_OK;
+  }
+  // ring producers and consumers wait on each other: all CTAs must be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, Q) != cudaSuccess) return MOK_ERR_CUDA;
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }
@@ -786,6 +928,42 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
     return run_mx<true, false, true>(P, st);
   }
   return run_mx<true>(P, st);
+}
+
+mok_status launch_upgate_mx_ring(const void* x, const int32_t* table, int K, const void* qg, const void* sg,
+                                 const void* qu, const void* su, const int32_t* offsets, int G, int64_t R, int D, int I,
+                                 void* aq, void* asc, void* xsc, void* ring, int64_t ring_rows, int chunk_rows,
+                                 int32_t* counters, cudaStream_t st, KeptAct kept) {
+  if (R == 0) return MOK_OK;
+  if (!offsets || G < 1 || chunk_rows < 128 || ring_rows < chunk_rows || ring_rows % chunk_rows)
+    return MOK_ERR_INVALID_ARG;
+  const int64_t nchunks = (R + chunk_rows - 1) / chunk_rows;
+  if (nchunks > (int64_t{1} << 24)) return MOK_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(counters, 0, 2 * nchunks * sizeof(int32_t), st) != cudaSuccess) return MOK_ERR_CUDA;
+  MxParams P;
+  // tmA maps the ring (ring_rows + 128 rows of codes); tmSA the full grouped scale layout
+  mok_status r = upgate_mx_params(P, ring, xsc, R, qg, sg, qu, su, offsets, G, D, I);
+  if (r != MOK_OK) return r;
+  if (!code_map(&P.tmA, ring, ring_rows + 128, D)) return MOK_ERR_CUDA;
+  P.sched.m_outer = 1;  // rows leave the ring in order: all N tiles of an M tile before the next M tile
+  P.aq = static_cast<uint8_t*>(aq);
+  P.asc = static_cast<uint32_t*>(asc);
+  P.act = kept.act;
+  P.act_rows = kept.limit();
+  P.x = static_cast<const uint4*>(x);
+  P.table = table;
+  P.K = K;
+  P.D8 = D / 8;
+  P.ring = static_cast<uint2*>(ring);
+  P.xsc = static_cast<uint32_t*>(xsc);
+  P.xs_ld = mx_scale_ld(R, G);
+  P.ring_rows = ring_rows;
+  P.chunk_rows = chunk_rows;
+  P.nchunks = static_cast<int32_t>(nchunks);
+  P.n_tiles = I / 128;
+  P.ready = counters;
+  P.done = counters + nchunks;
+  return run_mx<true, false, false, false, true>(P, st);
 }
 
 mok_status launch_replay_mx(const void* xq, const void* xsc, int64_t rows, const void* qg, const void* sg,

@@ -107,8 +107,8 @@ inline int64_t ring_rows_for(int64_t R, int64_t b) {
   if (all < 1) all = 1;
   return (all < kRingSlots ? all : kRingSlots) * b;
 }
-inline size_t ring_bytes(int64_t R, int64_t D, int64_t b) {
-  return static_cast<size_t>(ring_rows_for(R, b) + 128) * D * 2;
+inline size_t ring_bytes(int64_t R, int64_t D, int64_t b, int elem_bytes = 2) {
+  return static_cast<size_t>(ring_rows_for(R, b) + 128) * D * elem_bytes;
 }
 inline size_t ring_counter_bytes(int64_t R, int64_t b) { return static_cast<size_t>((R + b - 1) / b) * 8; }
 mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, const int32_t* offsets, int G,
@@ -193,6 +193,15 @@ mok_status launch_upgate_mx(const void* xq, const void* xsc, int64_t rows, const
                             const void* sg, const void* qu, const void* su, const int32_t* offsets,
                             int G, int D, int I, void* aq, void* asc, cudaStream_t st, KeptAct kept = {},
                             const void* sp = nullptr);
+// The same (row-major tiles) with the quantising dispatch fused in as a ring:
+// producer warps quantise routed rows of x (bf16 [T][D], row r from
+// x[table[r].src / K]) into `ring` ([ring_rows + 128][D] codes) chunk by
+// chunk, and their scale words into xsc (the grouped layout, R rows);
+// counters: 2 * ceil(R / chunk_rows) ints.
+mok_status launch_upgate_mx_ring(const void* x, const int32_t* table, int K, const void* qg, const void* sg,
+                                 const void* qu, const void* su, const int32_t* offsets, int G, int64_t R, int D, int I,
+                                 void* aq, void* asc, void* xsc, void* ring, int64_t ring_rows, int chunk_rows,
+                                 int32_t* counters, cudaStream_t st, KeptAct kept = {});
 // Paired scale blocks of W_up / W_gate (plain-layout scale words sg, su of
 // G*I rows, K = D) for the up/gate with the routed rows as N: block
 // b = e (I / 64) + s holds the words of W_up rows e I + 64 s .. + 63, then

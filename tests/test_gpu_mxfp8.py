@@ -234,6 +234,53 @@ def test_moe_fwd_mxfp8_full_size_sampled_tokens(m):
                  "mxfp8 fwd out [full]")
 
 
+def _mx_fwd_chunk(m, cfg, d, chunk, act=False):
+    """mok_moe_fwd (MXFP8) with the given chunk_rows: out and, with act, the
+    kept h, u store."""
+    shape = m.shape_of(cfg, chunk_rows=chunk)
+    ws = torch.empty(m.workspace_bytes(shape, m.OP_FWD), dtype=torch.uint8, device=DEV)
+    out = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16, device=DEV)
+    saved = alloc_plan(cfg, DEV)
+    if act:
+        saved["act"] = torch.full((cfg.R, 2 * cfg.I), float("nan"), device=DEV)
+    m.moe_fwd(shape, m.make_weights(d), d["x"], d["s"], out, ws, m.make_plan_buf(saved))
+    m.check_device_status()
+    return out, saved.get("act")
+
+
+RING_REUSE_MX = W.MoEConfig("ring_reuse_mx", T=1024, D=256, I=128, E=16, K=4, I_shared=128, dtype="mxfp8")
+
+
+@pytest.mark.parametrize("name,chunk", [("tiny", 512), ("ragged", 512), ("skew_small", 2048), ("big_experts", 512),
+                                        ("ring_reuse", 512), ("ring_reuse", 32768)])
+def test_moe_fwd_mxfp8_ring_bitexact(m, name, chunk):
+    """The quantising dispatch fused into the up/gate as a ring (producer
+    warps quantise routed rows into 4 slots of chunk rows, reused when R >
+    4 chunks) gives the whole-batch dispatch's out and kept h, u bit for
+    bit, and the oracle within tolerance."""
+    cfg = RING_REUSE_MX if name == "ring_reuse" else SMALL[name].replace(dtype="mxfp8")
+    inp = W.make_inputs(cfg, "cpu")
+    d = mx_weights(m, {k: v.to(DEV) for k, v in inp.items()})
+    out0, act0 = _mx_fwd_chunk(m, cfg, d, -1, act=True)
+    for _ in range(2):  # the counters start from zero on every call
+        out1, act1 = _mx_fwd_chunk(m, cfg, d, chunk, act=True)
+        assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
+        assert torch.equal(act0.view(torch.int32), act1.view(torch.int32))
+    ref = O.moe_forward_mxfp8(host(inp), cfg.K)
+    assert_close(out1.float().cpu().numpy(), ref["out"], MXFP8_TOL, f"mxfp8 ring out [{name}]")
+
+
+def test_moe_fwd_mxfp8_ring_full_size_bitexact(m):
+    """DSV3 MXFP8 forward: the ring of 512- and 2048-row chunks gives the
+    whole-batch quantising dispatch's output bit for bit."""
+    cfg = W.CONFIGS["dsv3_mxfp8_fwd"]
+    d = mx_weights(m, W.make_inputs(cfg, DEV))
+    out0, _ = _mx_fwd_chunk(m, cfg, d, -1)
+    for chunk in (512, 2048):
+        out1, _ = _mx_fwd_chunk(m, cfg, d, chunk)
+        assert torch.equal(out0.view(torch.int16), out1.view(torch.int16))
+
+
 # ---------------------------------------------------------------- backward
 BWD = {
     "ragged": W.MoEConfig("ragged_bwd", T=300, D=512, I=256, E=5, K=3, I_shared=128, dtype="mxfp8"),

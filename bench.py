@@ -468,8 +468,8 @@ def run_ours(args, world, rank, local):
                 ev1.record(stream)
             return
         # the same schedule as mok_moe_fwd: the shared expert depends on x
-        # alone and runs on a side stream next to route, plan, dispatch and
-        # the routed up/gate
+        # alone and runs on a side stream next to route, plan and dispatch
+        # (and, for MXFP8, the routed up/gate)
         if Is:
             side.wait_stream(stream)
             if mx:
@@ -480,6 +480,9 @@ def run_ours(args, world, rank, local):
         M.plan(topk, E, counts, offsets, table, route_dst, pws)
         if not ring:
             M.dispatch(shape, d["x"], table, route_dst, xg, xs, offsets=offsets)
+        if Is and not mx and not ring:
+            # as mok_moe_fwd: the BF16 routed up/gate waits for the shared up/gate
+            stream.wait_stream(side)
         if ev0 is not None:
             ev0.record(stream)
         if ring:  # the dispatch runs inside the up/gate launch (producer warps, ring of chunks)

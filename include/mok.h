@@ -343,7 +343,9 @@ mok_status mok_combine(const mok_shape *shape, const void *yg, const void *ys, c
  * `stream` as one operation: the shared expert's up/gate (and, for MXFP8,
  * its down projection) runs on an internal side stream (one per device and
  * host thread, created on first use), forked from `stream` after the work
- * already queued there and joined back before its output is read.  `saved`
+ * already queued there, beside route, plan and the dispatch, and joined
+ * back before the routed up/gate (BF16 with the whole-batch dispatch) or
+ * before its output is read (otherwise).  `saved`
  * (nullable) receives the routing and plan for mok_moe_bwd.  With
  * shape.dtype = MOK_MXFP8 the routed experts run in MXFP8 (dispatch
  * quantises x, the up/gate epilogue quantises a) and the shared expert in

@@ -431,8 +431,9 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
   void* as = s.I_shared ? at<void>(ws, L.as) : nullptr;
   // The shared expert depends on x alone (paper note, "The production
   // details": it fills the first dispatch window).  Its up/gate (and for
-  // MXFP8 its down projection) runs on a side stream next to route, plan,
-  // dispatch and the routed up/gate; the stream joins back before the first
+  // MXFP8 its down projection) runs on a side stream next to route, plan and
+  // dispatch (MXFP8: and the routed up/gate); the stream joins back before
+  // the BF16 routed up/gate (whole-batch dispatch), else before the first
   // launch that reads its output.
   SideStream* side = nullptr;
   bool joined = true;
@@ -489,6 +490,14 @@ extern "C" mok_status mok_moe_fwd(const mok_shape* shape, const mok_weights* w, 
     } else {
       if ((r = launch_dispatch_bf16(x, pb.route_dst, s.T, s.K, s.D, xg, nullptr, nullptr, st)) != MOK_OK)
         return fail(r);
+      // The shared up/gate ran beside route, plan and the dispatch (its
+      // kernel leaves them room on every SM); the routed up/gate starts once
+      // it is done, on the whole GPU, instead of queueing its CTAs behind
+      // the shared expert's tail.
+      if (!joined) {
+        joined = true;
+        if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return MOK_ERR_CUDA;
+      }
       if ((r = launch_upgate_pair(xg, R, w->w_gate, w->w_up, pb.offsets, s.E, R, s.D, s.I, a, st, nullptr,
                                   kept)) != MOK_OK)
         return fail(r);

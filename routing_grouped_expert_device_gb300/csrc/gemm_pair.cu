@@ -1219,8 +1219,11 @@ mok_status launch_upgate_pair(const void* A, int64_t a_rows, const void* w_gate,
   // kernel, whose MMAs skip the padding rows of each expert's last tile
   // (DSV3 forward 4.57 -> 4.51 ms).  With larger groups there is little
   // padding, and the row-major kernel's lighter epilogue measured 0.3-0.6 %
-  // faster (the skewed 16384-token layer).
-  if (offsets && !(sh && sh->rows) && routed_rows_as_n(m_total, G))
+  // faster (the skewed 16384-token layer).  One group (the shared expert on
+  // its own stream): the transposed kernel too, whose 147 registers a thread
+  // (the row-major one takes 229) leave room on every SM for the route,
+  // plan and dispatch blocks that run beside it.
+  if (!(sh && sh->rows) && (!offsets || routed_rows_as_n(m_total, G)))
     return launch_upgate_pair_t(A, a_rows, w_gate, w_up, offsets, G, m_total, D, I, a_out, st, kept);
   PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, I / 128, D / BK);
@@ -1269,9 +1272,10 @@ mok_status launch_down_pair(const void* a, int64_t a_rows, const void* w_down, c
                             int64_t m_total, int D, int I, void* y_out, cudaStream_t st,
                             const SharedOperands* sh, int max_sms) {
   if (m_total == 0 && !(sh && sh->rows)) return MOK_OK;
-  // routed groups of fewer than 512 rows on average: the transposed kernel
-  // (no padding rows in the MMAs), as for the up/gate
-  if (offsets && routed_rows_as_n(m_total, G))
+  // routed groups of fewer than 512 rows on average, or one group: the
+  // transposed kernel (no padding rows in the MMAs, fewer registers), as
+  // for the up/gate
+  if (!offsets || routed_rows_as_n(m_total, G))
     return launch_down_pair_t(a, a_rows, w_down, offsets, G, m_total, D, I, y_out, st, sh);
   PairParams P{};
   P.sched = pair_sched(offsets, G, m_total, D / 256, I / BK);

@@ -31,7 +31,7 @@ def _mx(m, d):
     return d
 
 
-@pytest.mark.parametrize("dtype,chunk", [(None, 0), (None, 512), ("mxfp8", 0)])
+@pytest.mark.parametrize("dtype,chunk", [(None, 0), (None, 512), ("mxfp8", 0), ("mxfp8", 512)])
 def test_moe_fwd_graph_replay_matches_eager(m, dtype, chunk):
     cfg = W.MoEConfig("g", T=700, D=512, I=256, E=16, K=4, I_shared=256)
     d = {k: v.to(DEV) for k, v in W.make_inputs(cfg, "cpu").items()}

@@ -9,47 +9,6 @@
 namespace mok {
 namespace {
 
-// Dispatch (Mixture-of-Kittens blog, "Scheduling": rows land
-// expert-contiguous).  One warp per token: its row is read once, 4 vectors
-// per lane in flight, and stored at each of its K positions in expert order,
-// p = route_dst[t K + k] (lane k holds p, K <= 32).  Reading each row once
-// instead of once per route keeps x's K re-reads off DRAM while the K D-wide
-// copies stream out.  When g_route is non-null also g_route[p] = g[t K + k].
-__global__ void __launch_bounds__(256) dispatch_bf16_kernel(const uint4* __restrict__ x,
-                                                            const int32_t* __restrict__ route_dst,
-                                                            int T, int K, int D8,
-                                                            uint4* __restrict__ xg,
-                                                            const float* __restrict__ g,
-                                                            float* __restrict__ g_route) {
-  const int lane = threadIdx.x & 31;
-  const int nwarps = static_cast<int>((static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5);
-  for (int t = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5); t < T;
-       t += nwarps) {
-    const int64_t r0 = static_cast<int64_t>(t) * K;
-    const int dst = lane < K ? __ldg(route_dst + r0 + lane) : 0;
-    if (g_route && lane < K) g_route[dst] = g[r0 + lane];
-    const uint4* in = x + static_cast<int64_t>(t) * D8;
-#pragma unroll 1
-    for (int i0 = 0; i0 < D8; i0 += 128) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + 32 * u + lane;
-        v[u] = i < D8 ? ld_nc_v4(in + i) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll 1
-      for (int k = 0; k < K; ++k) {
-        uint4* out = xg + static_cast<int64_t>(__shfl_sync(0xffffffffu, dst, k)) * D8;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + 32 * u + lane;
-          if (i < D8) out[i] = v[u];
-        }
-      }
-    }
-  }
-}
-
 // One warp per row: lane l holds 8 consecutive values (16 bytes), so a
 // 1x32 block is 4 lanes (its amax: two xor shuffles) and one pass of the warp
 // covers 256 columns, two 128-column scale groups; loads and code stores are
@@ -375,12 +334,85 @@ int grid_for(int64_t work_items, int per_block) {
 
 }  // namespace
 
+// Dispatch (Mixture-of-Kittens blog, "Scheduling": rows land
+// expert-contiguous) by bulk copies, the TMA copy engine moving the bytes
+// instead of vector loads and stores by threads: a warp per CTA moves one
+// piece of P bytes of one token's row at a time, a bulk load into P bytes of
+// shared memory and then K bulk stores from there, one per route (lane k
+// stores to p = route_dst[t K + k]).  Each row is read once however many
+// routes it has.  A CTA needs one warp, a few registers and P + 8 bytes of
+// shared memory, so several fit beside a persistent GEMM that holds most of
+// an SM (the shared expert's up/gate in the first dispatch window), where a
+// warp-per-token dispatch got only the registers the GEMM leaves (DSV3
+// forward 4.52-4.55 -> 4.49-4.50 ms).  Units (token, piece) are taken in
+// token order; the next piece is loaded once every store of the current one
+// has read the buffer.  Waits are bounded.  When g_route is non-null also
+// g_route[p] = g[t K + k].
+__global__ void __launch_bounds__(32) dispatch_bulk_kernel(const uint8_t* __restrict__ x,
+                                                           const int32_t* __restrict__ route_dst, int T, int K,
+                                                           int row_bytes, int pieces, uint8_t* __restrict__ xg,
+                                                           const float* __restrict__ g, float* __restrict__ g_route,
+                                                           int* status) {
+  extern __shared__ __align__(128) uint8_t buf[];
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x;
+  const int piece = row_bytes / pieces;
+  if (lane == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  uint32_t phase = 0;
+  const int64_t units = static_cast<int64_t>(T) * pieces;
+  for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int t = static_cast<int>(u / pieces);
+    const int off = static_cast<int>(u - static_cast<int64_t>(t) * pieces) * piece;
+    // (clamped to the R rows: a plan that reported a bad route leaves no store outside xg)
+    const int dst = lane < K ? min(max(__ldg(route_dst + static_cast<int64_t>(t) * K + lane), 0), T * K - 1) : 0;
+    if (g_route && off == 0 && lane < K) g_route[dst] = __ldg(g + static_cast<int64_t>(t) * K + lane);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar, piece);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_u32(buf)),
+          "l"(x + static_cast<int64_t>(t) * row_bytes + off), "r"(piece), "r"(smem_u32(&bar))
+          : "memory");
+    }
+    const bool ok = mbar_wait(&bar, phase, reinterpret_cast<volatile int*>(&abort_flag), status, SITE_PRODUCER);
+    phase ^= 1;
+    if (!__all_sync(0xffffffffu, ok)) return;
+    if (lane < K) {
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                       xg + static_cast<int64_t>(dst) * row_bytes + off),
+                   "r"(smem_u32(buf)), "r"(piece)
+                   : "memory");
+      bulk_commit();
+      bulk_wait_read0();  // the buffer is free again once every store has read it
+    }
+    __syncwarp();
+  }
+  if (lane < K) bulk_wait0();  // the stores have landed before the CTA exits
+}
+
 mok_status launch_dispatch_bf16(const void* x, const int32_t* route_dst, int T, int K, int D, void* xg,
                                 const float* g, float* g_route, cudaStream_t st) {
   if (T == 0) return MOK_OK;
   if (K > 32) return MOK_ERR_UNSUPPORTED;
-  dispatch_bf16_kernel<<<grid_for(T, 8), 256, 0, st>>>(static_cast<const uint4*>(x), route_dst, T, K, D / 8,
-                                                        static_cast<uint4*>(xg), g, g_route);
+  // pieces of at most 4 KB that split the row evenly in 512-byte units
+  const int row_bytes = D * 2;
+  const int units = row_bytes / 512;  // D % 256 == 0
+  int pieces = 1;
+  while (units % pieces || 512 * (units / pieces) > 4096) ++pieces;
+  int* status = status_ptr();
+  if (!status) return MOK_ERR_CUDA;
+  const int64_t n = static_cast<int64_t>(T) * pieces;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+  const int grid = static_cast<int>(n < cap ? n : cap);
+  dispatch_bulk_kernel<<<grid, 32, row_bytes / pieces, st>>>(static_cast<const uint8_t*>(x), route_dst, T, K,
+                                                            row_bytes, pieces, static_cast<uint8_t*>(xg), g,
+                                                            g_route, status);
   MOK_CHECK_LAUNCH();
   return MOK_OK;
 }

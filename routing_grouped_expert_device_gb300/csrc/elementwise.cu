@@ -325,15 +325,6 @@ __global__ void __launch_bounds__(256) router_grad_kernel(
   }
 }
 
-int grid_for(int64_t work_items, int per_block) {
-  int64_t b = (work_items + per_block - 1) / per_block;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
-  if (b > cap) b = cap;
-  return b < 1 ? 1 : static_cast<int>(b);
-}
-
-}  // namespace
-
 // Dispatch (Mixture-of-Kittens blog, "Scheduling": rows land
 // expert-contiguous) by bulk copies, the TMA copy engine moving the bytes
 // instead of vector loads and stores by threads: a warp per CTA moves one
@@ -395,6 +386,15 @@ __global__ void __launch_bounds__(32) dispatch_bulk_kernel(const uint8_t* __rest
   }
   if (lane < K) bulk_wait0();  // the stores have landed before the CTA exits
 }
+
+int grid_for(int64_t work_items, int per_block) {
+  int64_t b = (work_items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  if (b > cap) b = cap;
+  return b < 1 ? 1 : static_cast<int>(b);
+}
+
+}  // namespace
 
 mok_status launch_dispatch_bf16(const void* x, const int32_t* route_dst, int T, int K, int D, void* xg,
                                 const float* g, float* g_route, cudaStream_t st) {

@@ -264,8 +264,8 @@ mok_status mok_plan_ranks(const int32_t *topk_idx, int32_t T, int32_t E, int32_t
  * copies).  xg[p] = x[table[p].src_index / K] for p < R, computed token by
  * token: row t of x is read once and stored at its K positions
  * route_dst[t*K + k] (mok_plan's inverse of the table; BF16 by bulk copies
- * through shared memory, a row piece loaded once and stored K times); x bf16 [T][D], xg
- * bf16 [R][D].  route_dst is required.  With dtype MOK_MXFP8 xg receives
+ * through shared memory, a row piece loaded once and stored K times);
+ * x bf16 [T][D], xg bf16 [R][D].  route_dst is required.  With dtype MOK_MXFP8 xg receives
  * the E4M3 codes [R][D] of the dispatched rows and xg_scale their scale
  * words in the grouped layout (quantisation fused into the dispatch, once
  * per token), for which table and offsets (mok_plan's) are required; table,

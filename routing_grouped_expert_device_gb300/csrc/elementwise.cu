@@ -372,8 +372,18 @@ __global__ void __launch_bounds__(32) dispatch_bulk_kernel(const uint8_t* __rest
           : "memory");
     }
     const bool ok = mbar_wait(&bar, phase, reinterpret_cast<volatile int*>(&abort_flag), status, SITE_PRODUCER);
+    if (!__all_sync(0xffffffffu, ok)) {
+      // the wait ran out (status set): give the load one more budget to
+      // land before the CTA's shared memory is released
+      if (lane == 0) {
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(&bar, phase) && globaltimer() - t0 < kWaitBudgetNs) {
+        }
+      }
+      __syncwarp();
+      return;
+    }
     phase ^= 1;
-    if (!__all_sync(0xffffffffu, ok)) return;
     if (lane < K) {
       asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                        xg + static_cast<int64_t>(dst) * row_bytes + off),

@@ -589,22 +589,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int ch0 = 4 * half;
       const int ch_end = min((t_ncols(c) + 31) / 32, ch0 + 4);
       if constexpr (kDirect16) {
-        // lane = output column 32 q + lane; register j = row ch * 32 + j:
-        // each warp store writes 32 neighbouring bf16 columns of one row
-#pragma unroll 1
-        for (int ch = ch0; ch < ch_end; ++ch) {
-          const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
-          uint32_t v[32];
-          tmem_ld32(taddr + ch * 32, v);
-          tmem_ld_wait();
-          __nv_bfloat16* o = P.y + static_cast<int64_t>(row0 + ch * 32) * P.out_ld + dcol + 32 * q + lane;
+        // lane = output column 32 q + lane.  The warp's chunks (at most
+        // four) are first drained into registers, rounded to bf16 (word j
+        // of chunk cc holds rows 2 j, 2 j + 1 of chunk ch0 + cc), and the
+        // accumulator is released before any store, so the next tile's MMAs
+        // do not wait for the stores; each warp store then writes 32
+        // neighbouring bf16 columns of one row.
+        uint32_t pk[4][16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nv) o[static_cast<int64_t>(j) * P.out_ld] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        for (int cc = 0; cc < 4; ++cc) {
+          if (ch0 + cc < ch_end) {
+            uint32_t v[32];
+            tmem_ld32(taddr + (ch0 + cc) * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              pk[cc][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          }
         }
         tc_fence_before();
         if (leader) mbar_arrive(tempty);  // the accumulator is free for the next tile
         else remote_arrive(map_to_rank(smem_u32(tempty), 0));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int ch = ch0 + cc;
+          if (ch < ch_end) {
+            const int nv = min(nrows - ch * 32, 32);  // valid rows of the chunk (at least 1)
+            uint16_t* o = reinterpret_cast<uint16_t*>(P.y) + static_cast<int64_t>(row0 + ch * 32) * P.out_ld +
+                          dcol + 32 * q + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nv)
+                o[static_cast<int64_t>(j) * P.out_ld] =
+                    static_cast<uint16_t>((j & 1) ? pk[cc][j >> 1] >> 16 : pk[cc][j >> 1] & 0xFFFFu);
+          }
+        }
         continue;
       }
       if constexpr (kF32) {

@@ -9,26 +9,28 @@
 namespace mok {
 namespace {
 
-// One warp per row: lane l holds 8 consecutive values (16 bytes), so a
-// 1x32 block is 4 lanes (its amax: two xor shuffles) and one pass of the warp
-// covers 256 columns, two 128-column scale groups; loads and code stores are
-// contiguous across the warp.  Each group's 4 scale bytes are gathered into
-// one 32-bit word (layout in kernels.h).  route_dst == nullptr: row r is
-// stored at row r, plain layout (the quantiser).  Else (the dispatch with
-// fused quantisation) the rows are tokens: token t is quantised once and
-// stored at each of its K positions p = route_dst[t K + k] (lane k holds p
-// and its scale position, K <= 32), with the grouped scale layout of expert
+// One warp per row: lane l holds 16 consecutive values (two 16-byte
+// vectors), so a 1x32 block is 2 lanes (its amax: one xor shuffle), one pass
+// of the warp covers 512 columns, four 128-column scale groups, and every
+// code store is 16 bytes; loads and code stores are contiguous across the
+// warp.  Each group's 4 scale bytes are gathered into one 32-bit word
+// (layout in kernels.h).  route_dst == nullptr: row r is stored at row r,
+// plain layout (the quantiser).  Else (the dispatch with fused
+// quantisation) the rows are tokens: token t is quantised once and stored
+// at each of its K positions p = route_dst[t K + k] (lane k holds p and its
+// scale position, K <= 32), with the grouped scale layout of expert
 // table[p].e.
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ src,
                                                          const int32_t* __restrict__ route_dst,
                                                          const int32_t* __restrict__ table,
                                                          const int32_t* __restrict__ offsets, int K,
                                                          int64_t rows, int64_t cols, int64_t ld,
-                                                         uint2* __restrict__ q,
+                                                         uint4* __restrict__ q,
                                                          uint32_t* __restrict__ scale) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int c8 = static_cast<int>(cols / 8);  // 16-byte vectors per row
+  const int c8 = static_cast<int>(cols / 8);  // 16-byte vectors per row (a multiple of 16)
+  const int c16 = c8 / 2;                     // 16-byte code vectors per row
   for (int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < rows;
        row += nwarps) {
     int ndst = 1;
@@ -44,33 +46,35 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     }
     const uint4* in = src + row * c8;
 #pragma unroll 1
-    for (int v0 = 0; v0 < c8; v0 += 128) {  // 4 passes of 256 columns in flight
+    for (int v0 = 0; v0 < c8; v0 += 128) {  // 2 passes of 512 columns in flight
       uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int vi = v0 + 32 * u + lane;
-        v[u] = vi < c8 ? ld_nc_v4(in + vi) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < 2; ++u) {
+        const int vi = v0 + 64 * u + 2 * lane;  // even; vi < c8 implies vi + 1 < c8
+        v[2 * u] = vi < c8 ? ld_nc_v4(in + vi) : make_uint4(0, 0, 0, 0);
+        v[2 * u + 1] = vi < c8 ? ld_nc_v4(in + vi + 1) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int vi = v0 + 32 * u + lane;
-        if (v0 + 32 * u >= c8) break;  // warp-uniform: cols is a multiple of 128 (16 vectors)
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float f[8];
+      for (int u = 0; u < 2; ++u) {
+        const int vi = v0 + 64 * u + 2 * lane;
+        if (v0 + 64 * u >= c8) break;  // warp-uniform
+        const uint32_t w[8] = {v[2 * u].x, v[2 * u].y, v[2 * u].z, v[2 * u].w,
+                               v[2 * u + 1].x, v[2 * u + 1].y, v[2 * u + 1].z, v[2 * u + 1].w};
+        float f[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           f[2 * j] = bf16lo(w[j]);
           f[2 * j + 1] = bf16hi(w[j]);
         }
         int e;
-        const uint2 codes = mx_codes8(f, e);
-        const uint32_t word = mx_word16(e, lane);
+        const uint4 codes = mx_codes16(f, e);
+        const uint32_t word = mx_word8(e, lane);
 #pragma unroll 1
         for (int k = 0; k < ndst; ++k) {
           const int64_t p = __shfl_sync(0xffffffffu, dst, k);
           const int64_t pos = __shfl_sync(0xffffffffu, dpos, k);
-          if (vi < c8) q[p * c8 + vi] = codes;
-          if ((lane & 15) == 0 && vi < c8) scale[static_cast<int64_t>(vi / 16) * ld + pos] = word;
+          if (vi < c8) q[p * c16 + vi / 2] = codes;
+          if ((lane & 7) == 0 && vi < c8) scale[static_cast<int64_t>(vi / 16) * ld + pos] = word;
         }
       }
     }
@@ -434,7 +438,7 @@ mok_status launch_dispatch_mxfp8(const void* x, const int32_t* route_dst, const 
   if (K > 32) return MOK_ERR_UNSUPPORTED;
   const int64_t R = static_cast<int64_t>(T) * K;
   quant_rows_kernel<<<grid_for(T, 8), 256, 0, st>>>(static_cast<const uint4*>(x), route_dst, table, offsets, K, T,
-                                                    D, mx_scale_ld(R, E), static_cast<uint2*>(xg_q),
+                                                    D, mx_scale_ld(R, E), static_cast<uint4*>(xg_q),
                                                     reinterpret_cast<uint32_t*>(xg_scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;
@@ -444,7 +448,7 @@ mok_status launch_quantize_mxfp8(const void* src, int64_t rows, int64_t cols, vo
                                  uint8_t* scale, cudaStream_t st) {
   if (rows == 0) return MOK_OK;
   quant_rows_kernel<<<grid_for(rows, 8), 256, 0, st>>>(static_cast<const uint4*>(src), nullptr, nullptr, nullptr, 1,
-                                                       rows, cols, mx_scale_ld(rows), static_cast<uint2*>(q),
+                                                       rows, cols, mx_scale_ld(rows), static_cast<uint4*>(q),
                                                        reinterpret_cast<uint32_t*>(scale));
   MOK_CHECK_LAUNCH();
   return MOK_OK;

@@ -81,14 +81,17 @@ def mx_weights(m, d, pair=False):
     return out
 
 
-def test_quantize_bitexact(m):
+@pytest.mark.parametrize("cols", [128, 384, 512, 640, 1024, 1152])
+def test_quantize_bitexact(m, cols):
+    """Row lengths that fill a warp pass (512 columns) exactly, partly, or
+    leave part of the warp idle (128, 384: 8 or 24 lanes of 32)."""
     gen = torch.Generator().manual_seed(9)
-    v = (torch.randn(301, 512, generator=gen) * torch.logspace(-3, 3, 512)).to(torch.bfloat16)
+    v = (torch.randn(301, cols, generator=gen) * torch.logspace(-3, 3, cols)).to(torch.bfloat16)
     v[5, :32] = 0
     v[6, 64:96] = -0.0
     q, sc = quantize(m, v.to(DEV))
     qr, sr = O.mxfp8_quantize(O.bf16_to_f32(W.bf16_bits(v)))
-    assert np.array_equal(words_to_bytes(sc, 301, 512), sr)
+    assert np.array_equal(words_to_bytes(sc, 301, cols), sr)
     assert np.array_equal(q.cpu().numpy(), qr)
 
 

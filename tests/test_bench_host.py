@@ -110,7 +110,7 @@ PEAKS = dict(hbm_gbs=6781.1, bf16=1887.9, bf16_sustained=1649.2, source="measure
 
 
 def test_roofline_bound_per_workload():
-    """The bench line's roofline is judged against the kernel's own bound:
+    """The bench line's roofline compares the kernel with its own bound:
     the skewed layer's up/gate (about 1100 FLOP per algorithmic byte) against
     the tensor peak, the DSV3 up/gate (BF16 and MXFP8) and the backward call
     against HBM; every line names both figures."""
